@@ -1,0 +1,274 @@
+"""CPU oracle for the fused MoE (sparse FFN) layer -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, the package's smoke check and the CPU-baseline leg of
+the benchmark may import this module.  The product path (the CUDA library
+and its Python binding) never calls it and shares no code with it.
+
+It is a plain, slow, obviously correct restatement of what the layer
+computes, in float64 numpy over dequantised weights:
+
+* routing alignment -- the argsort of topk_ids into per-expert, block-padded
+  groups (Xeon 6 / SGLang DeepSeek-R1 blog, section "MoE"; SGLang CPU backend
+  write-up, section "(3) FusedMoE", the moe_align_index and thread-offset
+  paragraphs);
+* the naive masked per-expert loop: for each expert, gather the tokens that
+  chose it, run GEMM-SiLU-GEMM, and add the result into each token's output
+  with its routing weight (same two sections: the "naive MoE in torch" and
+  "experts run serially" paragraphs);
+* the gate/up split of W13 as A x [B1, B2] = [C1, C2] with SiLU(C1) * C2
+  (same sections, the SiLU-fusion bullet);
+* FP8 E4M3 weights with 128x128 block scales, decoded from the OCP FP8
+  format definition and scaled per block (DeepSeek-style block quant; the
+  post-scaled FP8 GEMV of the OSDI'26 local-MoE paper summary, section "CPU
+  decode backend", is the same sum regrouped);
+* INT8 per-output-channel weights with dynamic per-token INT8 activations
+  (DA8W8; SGLang CPU backend write-up, "(3) FusedMoE", the dynamic-quant
+  fusion paragraph).
+
+Precision: float64 accumulation everywhere, except that every decision that
+turns a float into an integer code (activation quantisation) is taken in
+float32 with IEEE division and round-half-to-even, the same precision the
+GPU kernels use for that decision.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+FP8_MAX = 448.0
+INT8_MAX = 127
+QBLOCK = 128
+
+# ----------------------------------------------------------------------------
+# FP8 E4M3 codec, from the OCP 8-bit floating point format definition:
+# 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent field 0
+# holds the subnormals 2^-6 * m/8; S.1111.111 is NaN; there is no infinity;
+# the largest finite magnitude is 1.1110.110 = 448.
+# ----------------------------------------------------------------------------
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """uint8 E4M3 codes -> float64 values (NaN for the two NaN codes)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    exp = (c >> 3) & 0xF
+    man = (c & 0x7).astype(np.float64)
+    normal = np.ldexp(1.0 + man / 8.0, (exp - 7).astype(np.int64))
+    subnormal = np.ldexp(man / 8.0, -6)
+    mag = np.where(exp == 0, subnormal, normal)
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return sign * mag
+
+
+def _e4m3_positive_grid() -> np.ndarray:
+    """All 127 finite non-negative E4M3 magnitudes, ascending (codes 0x00..0x7E)."""
+    return e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+
+
+def e4m3_encode_satfinite(v) -> np.ndarray:
+    """float32 values -> E4M3 codes: round to nearest, ties to even code, clamp to +-448.
+
+    The grid is decoded from the format definition; a value is compared with
+    the midpoints between neighbouring grid points.  On a tie the code with an
+    even mantissa (even code) wins.  NaN input -> 0x7F.
+    """
+    v = np.asarray(v, dtype=np.float32).astype(np.float64)
+    grid = _e4m3_positive_grid()
+    a = np.minimum(np.abs(v), FP8_MAX)
+    lo = np.clip(np.searchsorted(grid, a, side="right") - 1, 0, 126)
+    hi = np.minimum(lo + 1, 126)
+    d_lo = a - grid[lo]
+    d_hi = grid[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0) & (hi != lo))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    code = np.where(np.signbit(v) & (code != 0), code | 0x80, code)
+    code = np.where(np.signbit(v) & (code == 0), np.uint8(0x80), code)
+    return np.where(np.isnan(v), np.uint8(0x7F), code).astype(np.uint8)
+
+
+# ----------------------------------------------------------------------------
+# Dequantisation of the stored weights.
+# ----------------------------------------------------------------------------
+
+
+def dequant_fp8_block(codes, scale) -> np.ndarray:
+    """codes uint8 [R, C], scale f32 [R/128, C/128] -> float64 W[r, c] = decode(q) * S[r//128, c//128]."""
+    codes = np.asarray(codes)
+    scale = np.asarray(scale, dtype=np.float64)
+    R, C = codes.shape
+    S = np.repeat(np.repeat(scale, QBLOCK, axis=0), QBLOCK, axis=1)[:R, :C]
+    return e4m3_decode(codes) * S
+
+
+def dequant_int8_channel(codes, scale) -> np.ndarray:
+    """codes int8 [R, C], scale f32 [R] -> float64 W[r, c] = q * s[r]."""
+    return np.asarray(codes, dtype=np.float64) * np.asarray(scale, dtype=np.float64)[:, None]
+
+
+# ----------------------------------------------------------------------------
+# Dynamic INT8 quantisation (DA8W8), one scale per row.
+# ----------------------------------------------------------------------------
+
+
+def quant_int8_per_row(a):
+    """float32 rows [R, C] -> (int8 codes, float32 scales).
+
+    s = amax(|row|) / 127 in float32 (1 when the row is all zero);
+    q = round-half-even(row / s) in float32, clamped to [-127, 127].
+    """
+    a = np.asarray(a, dtype=np.float32)
+    amax = np.max(np.abs(a), axis=-1) if a.shape[-1] else np.zeros(a.shape[:-1], np.float32)
+    s = np.where(amax > 0, amax / np.float32(INT8_MAX), np.float32(1.0)).astype(np.float32)
+    q = np.rint(np.divide(a, s[..., None], dtype=np.float32))
+    q = np.clip(q, -INT8_MAX, INT8_MAX).astype(np.int8)
+    return q, s
+
+
+# ----------------------------------------------------------------------------
+# Routing alignment.
+# ----------------------------------------------------------------------------
+
+
+def max_padded(M: int, topk: int, E: int, B: int) -> int:
+    """Capacity of sorted_ids: every expert may waste up to B-1 padding slots."""
+    n = M * topk + E * (B - 1)
+    return (n + B - 1) // B * B
+
+
+def moe_align_block_size(topk_ids, E: int, B: int):
+    """Argsort of the flat topk_ids into per-expert groups padded to multiples of B.
+
+    Flat slot i = t*topk + k.  Slots are grouped by expert in ascending expert
+    order; inside one expert they keep ascending slot order (a stable sort).
+    Slots whose id lies outside [0, E) are dropped.  Each expert's group is
+    padded with the sentinel M*topk up to a multiple of B (an expert with no
+    slots gets no block).  expert_ids[b] names the expert that owns block b;
+    blocks past the last used one hold -1.  expert_offsets is the exclusive
+    prefix sum of the padded group sizes (E+1 entries); num_post_padded its
+    last entry.
+
+    Returns (sorted_ids, expert_ids, num_post_padded, expert_offsets, counts)
+    with sorted_ids sized max_padded(...) and expert_ids sized that / B.
+    """
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    M, topk = ids.shape
+    flat = ids.reshape(-1)
+    sentinel = M * topk
+    cap = max_padded(M, topk, E, B)
+    sorted_ids = np.full(cap, sentinel, dtype=np.int32)
+    expert_ids = np.full(cap // B, -1, dtype=np.int32)
+    offsets = np.zeros(E + 1, dtype=np.int32)
+    counts = np.zeros(E, dtype=np.int32)
+    valid = np.nonzero((flat >= 0) & (flat < E))[0]
+    order = valid[np.argsort(flat[valid], kind="stable")]
+    pos = 0
+    j = 0
+    for e in range(E):
+        offsets[e] = pos
+        n = 0
+        while j < len(order) and flat[order[j]] == e:
+            sorted_ids[pos + n] = order[j]
+            n += 1
+            j += 1
+        counts[e] = n
+        padded = (n + B - 1) // B * B
+        expert_ids[pos // B:(pos + padded) // B] = e
+        pos += padded
+    offsets[E] = pos
+    return sorted_ids, expert_ids, np.int32(pos), offsets, counts
+
+
+# ----------------------------------------------------------------------------
+# The layer: naive masked per-expert loop.
+# ----------------------------------------------------------------------------
+
+
+def silu(z):
+    return z / (1.0 + np.exp(-z))
+
+
+def _as_np(t):
+    """torch tensors (bf16 included) or arrays -> numpy, exactly."""
+    if hasattr(t, "detach"):
+        t = t.detach().cpu()
+        if str(t.dtype) == "torch.bfloat16":
+            t = t.float()
+        return t.numpy()
+    return np.asarray(t)
+
+
+def fused_moe_fp8(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, experts=None):
+    """FP8 block-scaled weights, activations kept at their bf16 values (weight-only quant).
+
+    x [M, H] (bf16 values), topk_ids int [M, k], topk_weights f32 [M, k],
+    w13 uint8 [E, 2I, H] + scale [E, 2I/128, H/128], w2 uint8 [E, H, I] +
+    scale [E, H/128, I/128].  Returns float64 out [M, H].
+
+    `experts` restricts the loop to a subset (for sampling large layers);
+    contributions of other experts are then left out.
+    """
+    return _naive_moe(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, "fp8", experts)
+
+
+def fused_moe_int8(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, experts=None):
+    """INT8 per-channel weights with dynamic per-row INT8 activations (DA8W8).
+
+    The token rows are quantised once (quant_int8_per_row of x); the
+    intermediate h of each (token, expert) pair is quantised again per row
+    before the down projection.  Integer dot products are exact (int64);
+    scales are applied afterwards in float64.
+    """
+    return _naive_moe(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, "int8", experts)
+
+
+def _naive_moe(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, kind, experts):
+    x = _as_np(x).astype(np.float32)
+    ids = _as_np(topk_ids).astype(np.int64)
+    tw = _as_np(topk_weights).astype(np.float64)
+    M, H = x.shape
+    E = w13.shape[0]
+    I = w13.shape[1] // 2
+    Y = np.zeros(ids.shape + (H,), dtype=np.float64)  # Y[t, k] = expert output of slot (t, k)
+    if kind == "int8":
+        qx, sx = quant_int8_per_row(x)
+    for e in (range(E) if experts is None else experts):
+        tok, slot = np.nonzero(ids == e)  # the mask of this expert
+        if tok.size == 0:
+            continue
+        # one expert's weights at a time (they may live on a device; copy them here)
+        q13, s13, q2, s2 = (_as_np(a[e]) for a in (w13, w13_scale, w2, w2_scale))
+        if kind == "fp8":
+            W13 = dequant_fp8_block(q13, s13)                      # [2I, H]
+            W2 = dequant_fp8_block(q2, s2)                         # [H, I]
+            C = x[tok].astype(np.float64) @ W13.T                  # A x [B1, B2] = [C1, C2]
+            h = silu(C[:, :I]) * C[:, I:]                          # SiLU(C1) * C2
+            y = h @ W2.T
+        else:
+            acc = qx[tok].astype(np.int64) @ q13.astype(np.int64).T
+            C = acc * sx[tok].astype(np.float64)[:, None] * s13.astype(np.float64)[None, :]
+            h = silu(C[:, :I]) * C[:, I:]
+            qh, sh = quant_int8_per_row(h.astype(np.float32))
+            acc2 = qh.astype(np.int64) @ q2.astype(np.int64).T
+            y = acc2 * sh.astype(np.float64)[:, None] * s2.astype(np.float64)[None, :]
+        Y[tok, slot] = y
+    out = np.zeros((M, H), dtype=np.float64)
+    for k in range(ids.shape[1]):  # combine in slot order
+        valid = (ids[:, k] >= 0) & (ids[:, k] < E)
+        out += np.where(valid[:, None], tw[:, k:k + 1] * Y[:, k], 0.0)
+    return out
+
+
+def fused_moe_rows(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, kind, tokens):
+    """Oracle output for a subset of token rows only (for layers too large to run whole).
+
+    Computes exactly what the full call gives for those rows: it runs the
+    naive loop on the selected tokens alone (every token is independent once
+    routed).  Dynamic activation quantisation is per row, so it is unchanged.
+    """
+    tokens = np.asarray(tokens, dtype=np.int64)
+    x = _as_np(x)[tokens]
+    ids = _as_np(topk_ids)[tokens]
+    tw = _as_np(topk_weights)[tokens]
+    E = w13.shape[0]
+    used = sorted({int(e) for e in np.unique(ids) if 0 <= e < E})
+    fn = fused_moe_fp8 if kind == "fp8" else fused_moe_int8
+    return fn(x, ids, tw, w13, w13_scale, w2, w2_scale, experts=used)

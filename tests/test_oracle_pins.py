@@ -1,0 +1,362 @@
+"""Pins of the CPU oracle against facts fixed outside the oracle itself.
+
+Each test ties one oracle function to something independent of it: a library
+routine (torch's float8_e4m3fn conversion), a closed form, a hand-worked
+fixture, an exact integer identity stated on the pages, brute force, or a
+textbook dense FFN.  They run without a GPU.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mixture_experts_ffn_moe_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------------------- E4M3 codec
+
+def test_e4m3_decode_matches_torch_for_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert nan.sum() == 2  # 0x7F and 0xFF only
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def test_e4m3_decode_spec_values():
+    d = oracle.e4m3_decode
+    assert d(0x38) == 1.0            # 0.0111.000
+    assert d(0x7E) == 448.0          # largest finite
+    assert d(0x08) == 2.0 ** -6      # smallest normal
+    assert d(0x01) == 2.0 ** -9      # smallest subnormal
+    assert d(0x07) == 7 * 2.0 ** -9  # largest subnormal
+    assert d(0xB8) == -1.0
+    assert d(0x80) == 0.0 and math.copysign(1.0, d(0x80)) == -1.0
+
+
+def test_e4m3_encode_matches_torch_rne_in_range():
+    rng = np.random.default_rng(0)
+    v = np.concatenate([
+        rng.normal(0, 50, 20000), rng.normal(0, 0.01, 20000),
+        rng.uniform(-448, 448, 20000),
+    ]).astype(np.float32)
+    # exact midpoints between neighbouring grid values: the tie cases
+    grid = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
+    mids = ((grid[:-1] + grid[1:]) / 2).astype(np.float32)
+    assert np.array_equal(mids.astype(np.float64), (grid[:-1] + grid[1:]) / 2)
+    v = np.concatenate([v, mids, -mids, grid.astype(np.float32)])
+    ours = oracle.e4m3_encode_satfinite(v)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_e4m3_encode_saturates():
+    v = np.array([448.0, 449.0, 463.9, 464.0, 1e6, np.inf, -1e30, -np.inf], np.float32)
+    c = oracle.e4m3_encode_satfinite(v)
+    assert list(c) == [0x7E] * 6 + [0xFE] * 2
+
+
+# --------------------------------------------------------------------------- dequantisation
+
+def test_fp8_block_scale_indexing():
+    # all codes 1.0; distinct scales per 128x128 block of a 256 x 384 matrix
+    codes = np.full((256, 384), 0x38, np.uint8)
+    scale = np.array([[2.0, 3.0, 5.0], [7.0, 11.0, 13.0]], np.float32)
+    W = oracle.dequant_fp8_block(codes, scale)
+    assert W[0, 0] == 2.0 and W[127, 127] == 2.0
+    assert W[128, 0] == 7.0 and W[255, 5] == 7.0
+    assert W[5, 128] == 3.0 and W[5, 300] == 5.0
+    assert W[200, 383] == 13.0 and W[130, 200] == 11.0
+
+
+def test_int8_channel_dequant():
+    q = np.array([[1, -2], [127, -127]], np.int8)
+    s = np.array([0.5, 2.0], np.float32)
+    assert np.array_equal(oracle.dequant_int8_channel(q, s), [[0.5, -1.0], [254.0, -254.0]])
+
+
+# --------------------------------------------------------------------------- dynamic INT8 quant
+
+def test_int8_row_quant_reduces_to_rounding_when_scale_is_one():
+    # amax 127 -> s == 1 exactly, so q is plain round-half-even of x
+    row = np.array([[127.0, 2.5, 3.5, -2.5, -3.5, 0.49, -0.5, 126.5, -127.0]], np.float32)
+    q, s = oracle.quant_int8_per_row(row)
+    assert s[0] == 1.0
+    assert list(q[0]) == [127, 2, 4, -2, -4, 0, 0, 126, -127]
+
+
+def test_int8_row_quant_properties():
+    rng = np.random.default_rng(1)
+    a = (rng.normal(size=(64, 333)) * rng.uniform(0.01, 100, size=(64, 1))).astype(np.float32)
+    a[3] = 0.0
+    q, s = oracle.quant_int8_per_row(a)
+    assert s[3] == 1.0 and not q[3].any()
+    nz = np.arange(64) != 3
+    assert np.all(np.abs(q[nz]).max(axis=1) == 127)
+    err = np.abs(a[nz].astype(np.float64) / s[nz, None] - q[nz])
+    assert err.max() <= 0.5 + 1e-5
+
+
+# --------------------------------------------------------------------------- U8S8 identity (pages)
+
+def test_u8s8_compensation_identity_exact():
+    """A x B = (A + 128) x B - 128 x B in exact integers (DA8W8 on VNNI)."""
+    rng = np.random.default_rng(2)
+    A = rng.integers(-128, 128, size=(37, 300)).astype(np.int64)
+    B = rng.integers(-128, 128, size=(300, 53)).astype(np.int64)
+    U = A + 128
+    assert U.min() >= 0 and U.max() <= 255
+    comp = 128 * B.sum(axis=0, keepdims=True)
+    assert np.array_equal(U @ B - comp, A @ B)
+
+
+# --------------------------------------------------------------------------- routing alignment
+
+def _read_golden(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, *v = line.split()
+            out[k] = [int(x) for x in v]
+    return out
+
+
+def test_align_hand_worked_fixture():
+    g = _read_golden("align_tiny.txt")
+    M, k, E, B = g["M"][0], g["topk"][0], g["E"][0], g["B"][0]
+    ids = np.array(g["topk_ids"]).reshape(M, k)
+    s, eid, n, off, cnt = oracle.moe_align_block_size(ids, E, B)
+    assert list(s) == g["sorted_ids"]
+    assert list(eid) == g["expert_ids"]
+    assert int(n) == g["num_post_padded"][0]
+    assert list(off) == g["expert_offsets"]
+    assert list(cnt) == g["counts"]
+
+
+def _check_align_invariants(ids, E, B, res):
+    s, eid, n, off, cnt = res
+    M, k = ids.shape
+    flat = ids.reshape(-1)
+    sentinel = M * k
+    assert len(s) == oracle.max_padded(M, k, E, B) and len(eid) == len(s) // B
+    seen = []
+    for e in range(E):
+        assert off[e] % B == 0 and off[e + 1] >= off[e]
+        grp = s[off[e]:off[e + 1]]
+        real = [int(i) for i in grp if i != sentinel]
+        want = [i for i in range(M * k) if flat[i] == e]  # brute force: ascending slots
+        assert real == want
+        assert list(grp[:len(real)]) == real and all(i == sentinel for i in grp[len(real):])
+        assert off[e + 1] - off[e] == -(-len(want) // B) * B
+        assert all(eid[b] == e for b in range(off[e] // B, off[e + 1] // B))
+        seen += real
+    assert int(n) == off[E]
+    assert all(x == sentinel for x in s[n:]) and all(x == -1 for x in eid[n // B:])
+    assert sorted(seen) == [i for i in range(M * k) if 0 <= flat[i] < E]
+
+
+def test_align_brute_force_all_tiny_cases():
+    for M, k, E in [(1, 1, 1), (1, 2, 3), (2, 2, 3), (3, 1, 4), (3, 2, 2), (2, 2, 4)]:
+        for B in (1, 2, 4):
+            for combo in itertools.product(range(-1, E + 1), repeat=M * k):
+                ids = np.array(combo).reshape(M, k)
+                _check_align_invariants(ids, E, B, oracle.moe_align_block_size(ids, E, B))
+
+
+def test_align_random_larger():
+    rng = np.random.default_rng(3)
+    for M, k, E, B in [(100, 8, 257, 16), (37, 2, 8, 64), (513, 6, 33, 128)]:
+        ids = rng.integers(0, E, size=(M, k))
+        _check_align_invariants(ids, E, B, oracle.moe_align_block_size(ids, E, B))
+
+
+# --------------------------------------------------------------------------- layer
+
+def _torch_dequant_fp8(codes, scale):
+    """Library path: torch's float8 conversion, scales broadcast with repeat_interleave."""
+    w = torch.as_tensor(codes).view(torch.float8_e4m3fn).double()
+    s = torch.as_tensor(scale).double().repeat_interleave(128, 0).repeat_interleave(128, 1)
+    return w * s
+
+
+def _dense_swiglu(x, Wg, Wu, Wd):
+    """Textbook gated FFN: down(silu(gate(x)) * up(x)), float64 torch."""
+    g = x @ Wg.T
+    return (torch.nn.functional.silu(g) * (x @ Wu.T)) @ Wd.T
+
+
+def test_top1_weight1_equals_dense_swiglu_ffn():
+    shape = synth.LayerShape("t", 24, 256, 128, 4, 1, "fp8", "softmax")
+    d = synth.make_layer(shape, seed=5)
+    rng = np.random.default_rng(5)
+    ids = torch.from_numpy(rng.integers(0, 4, size=(24, 1)).astype(np.int32))
+    w1 = torch.ones(24, 1)
+    out = oracle.fused_moe_fp8(d["x"], ids, w1, d["w13"], d["w13_scale"], d["w2"], d["w2_scale"])
+    x = d["x"].double()
+    I = shape.I
+    for t in range(24):
+        e = int(ids[t, 0])
+        W13 = _torch_dequant_fp8(d["w13"][e], d["w13_scale"][e])
+        W2 = _torch_dequant_fp8(d["w2"][e], d["w2_scale"][e])
+        ref = _dense_swiglu(x[t:t + 1], W13[:I], W13[I:], W2)[0].numpy()
+        np.testing.assert_allclose(out[t], ref, rtol=1e-12, atol=1e-12)
+
+
+def _blocked_formulation(d, E, B, kind):
+    """The sorted/blocked form: one GEMM-SiLU-GEMM per B-row block, scattered back."""
+    x = d["x"].double().numpy()
+    ids = d["topk_ids"].numpy()
+    tw = d["topk_weights"].double().numpy()
+    M, k = ids.shape
+    s, eid, n, off, cnt = oracle.moe_align_block_size(ids, E, B)
+    I = d["w13"].shape[1] // 2
+    Y = np.zeros((M * k, x.shape[1]))
+    for b in range(int(n) // B):
+        e = int(eid[b])
+        rows = [int(i) for i in s[b * B:(b + 1) * B] if i < M * k]
+        W13 = _torch_dequant_fp8(d["w13"][e], d["w13_scale"][e]).numpy()
+        W2 = _torch_dequant_fp8(d["w2"][e], d["w2_scale"][e]).numpy()
+        A = x[[r // k for r in rows]]
+        C = A @ W13.T
+        Y[rows] = (C[:, :I] / (1 + np.exp(-C[:, :I])) * C[:, I:]) @ W2.T
+    return (Y.reshape(M, k, -1) * tw[:, :, None]).sum(axis=1)
+
+
+def test_naive_masked_loop_equals_blocked_formulation():
+    shape = synth.tiny(M=40)
+    d = synth.make_layer(shape, seed=7)
+    ref = oracle.fused_moe_fp8(d["x"], d["topk_ids"], d["topk_weights"],
+                               d["w13"], d["w13_scale"], d["w2"], d["w2_scale"])
+    for B in (1, 4, 16):
+        blk = _blocked_formulation(d, shape.E, B, "fp8")
+        np.testing.assert_allclose(ref, blk, rtol=1e-11, atol=1e-12)
+
+
+def test_silu_fusion_equals_separate_gemms():
+    rng = np.random.default_rng(8)
+    A = rng.normal(size=(5, 64))
+    B1 = rng.normal(size=(32, 64))
+    B2 = rng.normal(size=(32, 64))
+    C = A @ np.concatenate([B1, B2]).T          # A x [B1, B2] = [C1, C2]
+    fused = oracle.silu(C[:, :32]) * C[:, 32:]
+    sep = torch.nn.functional.silu(torch.from_numpy(A @ B1.T)).numpy() * (A @ B2.T)
+    np.testing.assert_allclose(fused, sep, rtol=1e-14)
+
+
+def _expert_id_layer(M, topk, E, H=256, I=128, seed=9):
+    """Weights whose expert e returns the constant row I*silu(1)*(e+1).
+
+    x[:, 0] = 1, rest 0; gate and up rows are e_0 (code 1.0, scale 1) so
+    g = u = 1 and h = silu(1) on every column; W2 codes are all 1.0 with
+    every block scale e+1, so y = I * silu(1) * (e+1) on every output.
+    """
+    x = torch.zeros(M, H, dtype=torch.bfloat16)
+    x[:, 0] = 1.0
+    w13 = torch.zeros(E, 2 * I, H, dtype=torch.uint8)
+    w13[:, :, 0] = 0x38
+    s13 = torch.ones(E, 2 * I // 128, H // 128)
+    w2 = torch.full((E, H, I), 0x38, dtype=torch.uint8)
+    s2 = (torch.arange(E, dtype=torch.float32) + 1)[:, None, None].expand(E, H // 128, I // 128).contiguous()
+    rng = np.random.default_rng(seed)
+    ids = torch.from_numpy(np.stack([rng.permutation(E)[:topk] for _ in range(M)]).astype(np.int32))
+    w = torch.from_numpy(rng.uniform(0.1, 1.0, size=(M, topk)).astype(np.float32))
+    return dict(x=x, topk_ids=ids, topk_weights=w, w13=w13, w13_scale=s13, w2=w2, w2_scale=s2)
+
+
+def expert_id_expected(d):
+    I = d["w13"].shape[1] // 2
+    silu1 = 1.0 / (1.0 + math.exp(-1.0))
+    ids = d["topk_ids"].numpy().astype(np.float64)
+    w = d["topk_weights"].numpy().astype(np.float64)
+    return I * silu1 * (w * (ids + 1)).sum(axis=1)
+
+
+def test_expert_id_weights_closed_form():
+    d = _expert_id_layer(M=11, topk=3, E=8)
+    out = oracle.fused_moe_fp8(**d)
+    want = expert_id_expected(d)
+    np.testing.assert_allclose(out, np.repeat(want[:, None], out.shape[1], axis=1), rtol=1e-13)
+
+
+def test_int8_lossless_case_closed_form():
+    """DA8W8 where every quantisation step is exact: result is a closed form.
+
+    Row t of x is [127, a_t, 0, ...] so its scale is exactly 1.  Gate rows
+    pick column 0 (g = 127, silu(127) == 127 in float64), up rows pick column
+    1 (u = a_t); h = 127*a_t on every column, so the requant scale is |a_t|
+    and every code is +-127.  Then y[m] = 127 * a_t * s2[m] * sum_j c[m, j].
+    """
+    M, H, I, E, k = 6, 128, 128, 3, 2
+    rng = np.random.default_rng(10)
+    a = rng.integers(1, 100, size=M) * rng.choice([-1, 1], size=M)
+    x = torch.zeros(M, H, dtype=torch.bfloat16)
+    x[:, 0] = 127.0
+    x[:, 1] = torch.from_numpy(a.astype(np.float32))
+    w13 = torch.zeros(E, 2 * I, H, dtype=torch.int8)
+    w13[:, :I, 0] = 1
+    w13[:, I:, 1] = 1
+    s13 = torch.ones(E, 2 * I)
+    c = torch.from_numpy(rng.integers(-127, 128, size=(E, H, I)).astype(np.int8))
+    s2 = torch.from_numpy(rng.uniform(0.5, 2.0, size=(E, H)).astype(np.float32))
+    ids = torch.from_numpy(np.stack([rng.permutation(E)[:k] for _ in range(M)]).astype(np.int32))
+    w = torch.from_numpy(rng.uniform(0.1, 1.0, size=(M, k)).astype(np.float32))
+    out = oracle.fused_moe_int8(x, ids, w, w13, s13, c, s2)
+    rows = c.double().sum(-1).numpy() * s2.double().numpy()      # [E, H]
+    want = np.zeros((M, H))
+    for t in range(M):
+        for j in range(k):
+            want[t] += float(w[t, j]) * 127.0 * a[t] * rows[int(ids[t, j])]
+    np.testing.assert_allclose(out, want, rtol=1e-12)
+
+
+def test_int8_close_to_unquantised_activations():
+    """DA8W8 differs from the float-activation layer only by 8-bit rounding of rows."""
+    shape = synth.LayerShape("q", 12, 256, 128, 6, 2, "int8", "softmax")
+    d = synth.make_layer(shape, seed=11)
+    q = oracle.fused_moe_int8(**d)
+    # same weights dequantised to float, activations unquantised
+    x = d["x"].double()
+    ref = np.zeros_like(q)
+    I = shape.I
+    for t in range(12):
+        for j in range(2):
+            e = int(d["topk_ids"][t, j])
+            W13 = d["w13"][e].double() * d["w13_scale"][e].double()[:, None]
+            W2 = d["w2"][e].double() * d["w2_scale"][e].double()[:, None]
+            ref[t] += float(d["topk_weights"][t, j]) * _dense_swiglu(x[t:t + 1], W13[:I], W13[I:], W2)[0].numpy()
+    rel = np.linalg.norm(q - ref) / np.linalg.norm(ref)
+    assert 0 < rel < 2e-2
+
+
+def test_rows_subset_equals_full_call():
+    shape = synth.tiny(M=20)
+    d = synth.make_layer(shape, seed=12)
+    full = oracle.fused_moe_fp8(**d)
+    rows = [0, 7, 19]
+    sub = oracle.fused_moe_rows(**d, kind="fp8", tokens=rows)
+    np.testing.assert_allclose(sub, full[rows], rtol=1e-11, atol=1e-15)  # BLAS blocking differs by size
+
+
+def test_ids_out_of_range_contribute_nothing():
+    shape = synth.tiny(M=10)
+    d = synth.make_layer(shape, seed=13)
+    base = oracle.fused_moe_fp8(**d)
+    ids = d["topk_ids"].clone()
+    ids[3, 1] = -1
+    ids[5, 0] = shape.E
+    d2 = dict(d, topk_ids=ids)
+    out = oracle.fused_moe_fp8(**d2)
+    keep = [0, 1, 2, 4, 6, 7, 8, 9]
+    np.testing.assert_allclose(out[keep], base[keep], rtol=1e-11, atol=1e-15)
+    assert not np.allclose(out[3], base[3]) and not np.allclose(out[5], base[5])
