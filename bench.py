@@ -1,0 +1,375 @@
+"""Benchmark of the GB300 fused MoE layer (one JSON line on stdout).
+
+A step is one call of the whole layer (routing alignment, activation
+preparation, gate/up GEMM with SiLU*mul, down projection and weighted
+combine) on one batch of synthetic, seeded input.  The default workload is a
+DeepSeek-R1-shaped MoE decode layer: 4 tokens, hidden 7168, expert
+intermediate 2048, 256 routed experts top-8 (sigmoid scores, 8 groups / top-4
+groups) plus 1 shared expert, FP8 E4M3 weights with 128x128 block scales,
+bf16 activations N(0,1).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+--impl reference times the CPU oracle (a deliberately plain float64 restatement
+of the layer) on the host cores, one bounded sample of the workload per step.
+Under torchrun (N > 1) every rank runs an independent replica of the layer on
+its own GPU (the layer is not sharded across GPUs); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mixture_experts_ffn_moe_gb300 import gbmoe, synth  # noqa: E402
+
+METRIC = "fused-MoE tokens/s per layer; decode HBM GB/s, prefill TFLOPS vs GB300 peak"
+L2_FLUSH_BYTES = 256 << 20  # twice the 129 MB L2
+
+
+def workloads():
+    return {
+        "dsr1_decode_M1": synth.deepseek_r1(1),
+        "dsr1_decode_M4": synth.deepseek_r1(4),
+        "dsr1_prefill_M2048": synth.deepseek_r1(2048, routing="deepseek_zipf"),
+        **{f"dsr1_sweep_M{m}": synth.deepseek_r1(m, routing="uniform") for m in (1, 2, 4, 8, 16, 32, 64)},
+        **{f"qwen3_M{m}": synth.qwen3_235b(m) for m in (1, 16, 256, 4096)},
+        "tiny_M16": synth.tiny(),
+    }
+
+
+DEFAULT_WORKLOAD = "dsr1_decode_M4"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "mixture_experts_ffn_moe_gb300", "csrc", "*"))):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def ncu_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    rec = d.get(workload, {}).get(kernel)
+    if not rec or rec.get("source_hash") != source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def stage_bytes(shape, ids: torch.Tensor):
+    """Algorithmic bytes per kernel of one call: distinct weights read + activations in/out."""
+    hist = synth.expert_histogram(shape, ids)
+    active = int((hist > 0).sum())
+    valid = int(hist.sum())
+    H, I, M = shape.H, shape.I, shape.M
+    if shape.weight_kind == "fp8":
+        s13 = 4 * (2 * I // 128) * (H // 128)
+        s2 = 4 * (H // 128) * (I // 128)
+        hbytes = 2
+    else:
+        s13, s2, hbytes = 4 * 2 * I, 4 * H, 2
+    return {
+        "decode_gemm1": active * (2 * I * H + s13) + M * H * 2 + valid * I * hbytes,
+        "decode_gemm2_combine": active * (H * I + s2) + valid * I * hbytes + M * H * 2,
+    }
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"gbmoe_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            self.proc.wait()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = max(smax, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def make_inputs(shape, seed=1234):
+    ids, w = synth.make_routing(shape, seed)
+    x = synth.make_x(shape, seed)
+    w13, s13, w2, s2 = synth.make_weights(shape, seed, device="cuda")
+    return x, ids, w, (w13, s13, w2, s2)
+
+
+def cpu_cores() -> int:
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        blas = [i["num_threads"] for i in info if i.get("user_api") == "blas"]
+        if blas:
+            return int(blas[0])
+    except ImportError:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_sample(shape, x, ids, w, weights):
+    """Times the oracle on one token of the batch (all of its experts); returns (tokens/s, seconds, text)."""
+    import oracle
+    w13, s13, w2, s2 = weights
+    t0 = time.perf_counter()
+    oracle.fused_moe_rows(x, ids, w, w13, s13, w2, s2, kind=shape.weight_kind, tokens=[0])
+    dt = time.perf_counter() - t0
+    return 1.0 / dt, dt, f"1 token of the {shape.M}-token batch ({int((ids[0] >= 0).sum())} experts), float64 numpy"
+
+
+def run_reference(args, shape):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    x, ids, w, weights = make_inputs(shape) if torch.cuda.is_available() else (None, None, None, None)
+    if weights is None:
+        ids, w = synth.make_routing(shape, 1234)
+        x = synth.make_x(shape, 1234)
+        weights = synth.make_weights(shape, 1234, device="cpu")
+    for _ in range(args.warmup):
+        oracle_sample(shape, x, ids, w, weights)
+    times = [oracle_sample(shape, x, ids, w, weights)[1] for _ in range(args.steps)]
+    total = sum(times)
+    value = args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(shape, args),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": oracle_sample(shape, x, ids, w, weights)[2] + " per step"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(shape, args):
+    return {"workload": args.workload, "M": shape.M, "H": shape.H, "I": shape.I, "E": shape.E_total,
+            "topk": shape.topk_total, "weights": "fp8_e4m3_block128" if shape.weight_kind == "fp8" else
+            "int8_per_channel", "routing": shape.routing, "l2": "flushed between steps (256 MiB write)",
+            "parallelism": f"replicas{args.gpus}"}
+
+
+def run_ours(args, shape):
+    world, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+    torch.cuda.set_device(local)
+    from mixture_experts_ffn_moe_gb300 import build
+    build.build()
+    gbmoe.load()
+    dev = torch.device("cuda", local)
+    x, ids, w, (w13, s13, w2, s2) = make_inputs(shape)
+    xd, idsd, wd = x.to(dev), ids.to(dev), w.to(dev)
+    kind = gbmoe.MOE_WEIGHT_FP8 if shape.weight_kind == "fp8" else gbmoe.MOE_WEIGHT_INT8
+    fn = gbmoe.fused_moe_fp8 if kind == gbmoe.MOE_WEIGHT_FP8 else gbmoe.fused_moe_int8
+    ws = gbmoe.alloc_workspace(shape.M, shape.H, shape.I, shape.E_total, shape.topk_total, kind, 0, dev)
+    out = torch.empty(shape.M, shape.H, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fn(xd, idsd, wd, w13, s13, w2, s2, out=out, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    bad, flags, st = gbmoe.moe_read_status(ws)
+    if st != 0:
+        raise SystemExit(f"device status after warm-up: bad ids {bad}, flags {flags}")
+
+    # ---- timed region: K steps, device time per step with CUDA events on the launch stream
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    gbmoe.moe_profile_enable(args.steps)
+    with ClockSampler(dev.index if world == 1 else local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        wall = time.perf_counter() - wall0
+    n_calls, stages = gbmoe.moe_profile_read()
+    gbmoe.moe_profile_enable(0)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = max_over_ranks(sum(step_ms), world)
+    ms_per_step = total_ms / args.steps
+    value = world * shape.M * args.steps / (total_ms / 1e3)
+
+    # ---- roofline of the dominant kernel
+    peaks = measured_peaks()
+    sbytes = stage_bytes(shape, ids)
+    stage_avg = {name: ms / max(n_calls, 1) for name, ms in stages}
+    dominant = max((n for n in stage_avg if n in sbytes), key=lambda n: stage_avg[n])
+    achieved = sbytes[dominant] / (stage_avg[dominant] * 1e-3) / 1e9
+    traffic = ncu_traffic(args.workload, dominant)
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                "algorithmic_bytes": sbytes[dominant], "peak_source": peaks["source"]}
+    layer_bytes = synth.distinct_weight_bytes(shape, ids)
+    flops = synth.algorithmic_flops(shape, ids)
+
+    # ---- end to end through the public API with host buffers (pinned), copies inside the timing
+    xh, idsh, wh = x.pin_memory(), ids.pin_memory(), w.pin_memory()
+    outh = torch.empty(shape.M, shape.H, dtype=torch.bfloat16).pin_memory()
+    h2d = xh.numel() * 2 + idsh.numel() * 4 + wh.numel() * 4
+    d2h = outh.numel() * 2
+    e_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        e_start[i].record(stream)
+        xd.copy_(xh, non_blocking=True)
+        idsd.copy_(idsh, non_blocking=True)
+        wd.copy_(wh, non_blocking=True)
+        step()
+        outh.copy_(out, non_blocking=True)
+        e_end[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(e_start, e_end)), world)
+    e2e_value = world * shape.M * args.steps / (e2e_ms / 1e3)
+
+    if rank != 0:
+        return
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        v, dt, text = oracle_sample(shape, x, ids, w, (w13, s13, w2, s2))
+        cpu = {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle", "sample": text,
+               "seconds": dt}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8->f16 mma, f32 acc" if kind == 0 else "int8->f16 mma, f32 acc",
+        "data": "synthetic", "config": config_of(shape, args),
+        "roofline": roofline, "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": sum(1 for _ in stages) * n_calls,
+        "clocks": clocks.summary(),
+        "layer": {"weight_gbs": layer_bytes / (ms_per_step * 1e-3) / 1e9,
+                  "weight_bytes": layer_bytes, "hbm_frac": layer_bytes / (ms_per_step * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                  "tflops": flops / (ms_per_step * 1e-3) / 1e12, "active_experts":
+                  int((synth.expert_histogram(shape, ids) > 0).sum()),
+                  "stages_ms": {n: round(v, 5) for n, v in stage_avg.items()}},
+        "wall_s": wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads()))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    shape = workloads()[args.workload]
+    if args.impl == "reference":
+        run_reference(args, shape)
+    else:
+        run_ours(args, shape)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,213 @@
+/*
+ * gbmoe.h -- C ABI of the GB300 (sm_103a) fused Mixture-of-Experts layer.
+ *
+ * The layer (one sparse FFN of a MoE transformer) as the serving pages state
+ * it (Xeon 6 / SGLang DeepSeek-R1 blog, section "MoE"; SGLang CPU backend
+ * write-up, section "(3) FusedMoE"):
+ *
+ *   1. routing alignment: argsort the flat topk_ids so that the (token, slot)
+ *      pairs of each expert are contiguous, pad every expert's group to a
+ *      multiple of a block size and record the expert of every block;
+ *   2. GEMM1 in the A x [B1, B2] = [C1, C2] form, W13 = [gate; up], with
+ *      h = SiLU(C1) * C2 computed in the epilogue;
+ *   3. GEMM2, the down projection y = h x W2^T;
+ *   4. the weighted combine out[t] = sum_k topk_weights[t,k] * y[t,k].
+ *
+ * Weights are FP8 E4M3 with one fp32 scale per 128x128 block (DeepSeek-style
+ * block quantisation) or INT8 with one fp32 scale per output channel and
+ * dynamic per-row INT8 activations (DA8W8).  Weights stay in their stored
+ * format in HBM and are expanded in registers or shared memory.
+ *
+ * Conventions shared by every entry point
+ *  - All data pointers are DEVICE pointers owned by the caller.  The library
+ *    allocates no memory and never synchronises the stream, except
+ *    moe_read_status, which waits for the stream.
+ *  - Every call is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and is ordered with the caller's other work on it.
+ *  - Matrices are row-major and contiguous.
+ *  - Host-checkable errors (bad sizes, NULL pointers, short workspace) are
+ *    returned before anything is launched.  A failed launch returns
+ *    MOE_ERR_CUDA.  Conditions only the GPU can see (expert ids outside
+ *    [0, E)) are counted in a status word inside the workspace; read it with
+ *    moe_read_status.
+ *  - A flat slot index is i = t * topk + k for token t and top-k column k.
+ *  - Calls that share a workspace must not overlap on the GPU.
+ */
+#ifndef GBMOE_H
+#define GBMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* the same type as cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* a size or pointer argument is invalid            */
+  MOE_ERR_UNSUPPORTED = 2, /* valid, but outside what the kernels implement    */
+  MOE_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than asked */
+  MOE_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed      */
+  MOE_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up               */
+  MOE_ERR_BAD_IDS = 6      /* the device saw expert ids outside [0, E)         */
+} moe_status_t;
+
+/* flags of fused_moe_fp8 / fused_moe_int8 */
+#define MOE_PATH_AUTO 0x0u    /* pick by tokens per expert                          */
+#define MOE_PATH_DECODE 0x1u  /* weight-streaming GEMV path (small token counts)    */
+#define MOE_PATH_PREFILL 0x2u /* tcgen05 grouped-GEMM path (large token counts)     */
+#define MOE_PATH_MASK 0x3u
+
+#define MOE_WEIGHT_FP8 0
+#define MOE_WEIGHT_INT8 1
+
+/* Limits of this implementation (larger sizes return MOE_ERR_UNSUPPORTED). */
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_DECODE_TOKENS 128 /* MOE_PATH_DECODE handles M <= this */
+
+/*
+ * Capacity (entries) of sorted_ids for the given routing problem:
+ * M*topk + E*(block_size-1), rounded up to a multiple of block_size.  Every
+ * expert may waste at most block_size-1 padding slots.  Returns 0 for
+ * invalid arguments.
+ */
+size_t moe_align_max_padded(int M, int topk, int num_experts, int block_size);
+
+/*
+ * Routing alignment ("moe_align_index"): the argsort of topk_ids by expert,
+ * blocked per expert (SGLang CPU backend write-up, section "(3) FusedMoE",
+ * the moe_align_index and thread-offset paragraphs; Xeon 6 / SGLang blog,
+ * section "MoE").
+ *
+ *   topk_ids        int32 [M, topk]   expert chosen by each (token, slot)
+ *   sorted_ids      int32 [cap]       out: flat slot indices grouped by
+ *                                     expert (ascending), ascending slot
+ *                                     order inside an expert, each group
+ *                                     padded to a multiple of block_size
+ *                                     with the sentinel M*topk; the tail
+ *                                     past the last group is sentinel too
+ *   expert_ids      int32 [cap/block_size]  out: expert of each block, -1
+ *                                     for blocks past the last group
+ *   num_tokens_post_padded int32 [1]  out: sum of the padded group sizes
+ *   expert_offsets  int32 [E+1]       out: start of each expert's group in
+ *                                     sorted_ids (exclusive prefix sum)
+ * cap = moe_align_max_padded(M, topk, E, block_size).  Slots whose id lies
+ * outside [0, E) are left out (as a non-local expert would be).  Experts
+ * with no slot get no block.  1 <= block_size <= 256, E <= MOE_MAX_EXPERTS.
+ * The result is deterministic and equals a stable argsort bit for bit.
+ */
+moe_status_t moe_align_block_size(const int32_t* topk_ids, int M, int topk, int num_experts,
+                                  int block_size, int32_t* sorted_ids, int32_t* expert_ids,
+                                  int32_t* num_tokens_post_padded, int32_t* expert_offsets,
+                                  moe_stream_t stream);
+
+/*
+ * Dynamic per-row INT8 quantisation of bf16 activations (the DA8W8
+ * activation side; SGLang CPU backend write-up, section "(3) FusedMoE", the
+ * dynamic-quant fusion paragraph):
+ *   scale[r] = max_c |x[r,c]| / 127 (fp32; 1 for an all-zero row)
+ *   q[r,c]   = round-half-even(x[r,c] / scale[r]) (IEEE fp32 division),
+ *              clamped to [-127, 127]
+ *   x bf16 [M, H] -> q int8 [M, H], scale fp32 [M].  M >= 0, 1 <= H.
+ * The fused INT8 layer applies exactly this function to its input rows.
+ */
+moe_status_t moe_quant_act_int8(const void* x_bf16, int M, int H, int8_t* q, float* scale,
+                                moe_stream_t stream);
+
+/*
+ * Bytes of scratch the fused layer needs for these sizes and flags
+ * (weight_kind MOE_WEIGHT_FP8 or MOE_WEIGHT_INT8).  The workspace must be
+ * 256-byte aligned.  Returns 0 for invalid or unsupported arguments.
+ */
+size_t moe_workspace_size(int M, int H, int I, int E, int topk, int weight_kind,
+                          unsigned flags);
+
+/*
+ * The whole MoE layer with FP8 E4M3 block-scaled weights; activations enter
+ * the products at their bf16 values (weight-only FP8, as in the Xeon 6 /
+ * SGLang blog, section "FP8 inference", and the SGLang CPU backend
+ * write-up, section "(4) FP8 GEMM").
+ *
+ *   x_bf16        bf16 [M, H]
+ *   topk_ids      int32 [M, topk]        ids outside [0, E) contribute 0
+ *   topk_weights  fp32 [M, topk]
+ *   w13_e4m3      uint8 [E, 2I, H]       rows 0..I-1 gate, I..2I-1 up
+ *   w13_scale     fp32 [E, 2I/128, H/128]  W13 = decode(code) * scale of its block
+ *   w2_e4m3       uint8 [E, H, I]
+ *   w2_scale      fp32 [E, H/128, I/128]
+ *   out_bf16      bf16 [M, H]            out[t] = sum_k w[t,k] * y[t,k]
+ *   workspace     moe_workspace_size(M, H, I, E, topk, MOE_WEIGHT_FP8, flags)
+ *                 bytes of device memory, 256-byte aligned
+ * H and I must be multiples of 128; 1 <= topk <= 32; M >= 0 (M == 0 is a
+ * no-op).  A shared expert is passed as one more expert with a top-k column
+ * of weight 1.0.  The products run on tensor cores with fp16 operands (the
+ * E4M3 to fp16 expansion is exact; bf16 activations are rounded to fp16,
+ * exact for magnitudes in [2^-14, 65504]) and fp32 accumulation; each
+ * 128x128 block scale is applied once per 128-deep partial sum.
+ */
+moe_status_t fused_moe_fp8(const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
+                           const void* w13_e4m3, const float* w13_scale, const void* w2_e4m3,
+                           const float* w2_scale, int M, int H, int I, int E, int topk,
+                           unsigned flags, void* out_bf16, void* workspace,
+                           size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * The whole MoE layer with INT8 per-output-channel weights and dynamic
+ * per-row INT8 activations (DA8W8; SGLang CPU backend write-up, section
+ * "(3) FusedMoE"): x rows are quantised as moe_quant_act_int8 does, and each
+ * intermediate row h of a (token, expert) pair is quantised the same way
+ * before the down projection.
+ *
+ *   w13        int8 [E, 2I, H],  w13_scale fp32 [E, 2I]
+ *   w2         int8 [E, H, I],   w2_scale  fp32 [E, H]
+ * other arguments as for fused_moe_fp8.  H and I must be multiples of 128.
+ */
+moe_status_t fused_moe_int8(const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
+                            const int8_t* w13, const float* w13_scale, const int8_t* w2,
+                            const float* w2_scale, int M, int H, int I, int E, int topk,
+                            unsigned flags, void* out_bf16, void* workspace,
+                            size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * Waits for `stream`, then copies the workspace's status words to the host:
+ *   status_out[0] = number of topk_ids entries outside [0, E) seen by the
+ *                   last fused call on this workspace
+ *   status_out[1] = bit set of device conditions (1 = a bounded wait gave up)
+ * Returns MOE_ERR_BAD_IDS / MOE_ERR_TIMEOUT when they are non-zero.
+ */
+moe_status_t moe_read_status(const void* workspace, int32_t status_out[2], moe_stream_t stream);
+
+/*
+ * Per-kernel timing of fused calls on the calling host thread (a profiling
+ * aid; it changes nothing the layer computes).
+ *
+ * moe_profile_enable(max_calls): with max_calls > 0, creates CUDA timing
+ * events on the current device for up to max_calls later fused calls and
+ * starts recording: every such call records one event before its first
+ * kernel and one after each kernel, on its own stream.  max_calls == 0 stops
+ * recording and releases the events.  Calls past the limit are not recorded.
+ *
+ * moe_profile_read(stage_ms, stage_names, max_stages, n_stages, n_calls):
+ * waits for the recorded events, writes per kernel ("stage") the summed
+ * milliseconds over all recorded calls (stage order = launch order; all
+ * recorded calls must have taken the same path) and the stage's name, then
+ * forgets the recorded calls (recording continues).
+ */
+moe_status_t moe_profile_enable(int max_calls);
+moe_status_t moe_profile_read(float* stage_ms, const char** stage_names, int max_stages, int* n_stages,
+                              int* n_calls);
+
+/* Static English text for a status code. */
+const char* moe_status_string(moe_status_t status);
+
+/* Text of the last error raised on the calling host thread ("" if none). */
+const char* moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GBMOE_H */

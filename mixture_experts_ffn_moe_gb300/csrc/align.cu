@@ -1,0 +1,211 @@
+// Routing alignment and activation preparation (the first launch of a layer call).
+//
+// Routing alignment restates the moe_align_index step of the SGLang CPU
+// backend write-up (section "(3) FusedMoE"; Xeon 6 / SGLang DeepSeek-R1 blog,
+// section "MoE"): an argsort of the flat topk_ids by expert, each expert's
+// group padded to a multiple of the block size, with the expert of every
+// block recorded.  Only group membership matters to the GEMMs, but the order
+// inside a group is fixed here (ascending slot index) so the result equals a
+// stable argsort and is deterministic.
+//
+// GB300 design: one CTA of 1024 threads does the whole alignment in three
+// passes over shared memory -- per-warp expert histograms, one block-wide
+// scan that turns them into write cursors, and a warp-ordered scatter in which
+// __match_any_sync ranks equal ids inside each 32-slot step.  The other CTAs of
+// the same launch prepare the activation rows for the expert GEMMs.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gbmoe {
+
+constexpr int kAlignThreads = 1024;
+constexpr int kAlignWarps = kAlignThreads / 32;
+
+// Block-wide exclusive scan of one int per thread (blockDim == 1024).
+__device__ int block_exclusive_scan(int v, int* warp_tot, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_tot[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    warp_tot[lane] = wi - w;  // exclusive prefix of warp totals
+    if (lane == 31) warp_tot[32] = wi;
+  }
+  __syncthreads();
+  const int res = warp_tot[warp] + incl - v;
+  total = warp_tot[32];
+  __syncthreads();
+  return res;
+}
+
+// One CTA: the full alignment.  Shared memory: kAlignWarps * E ints (per-warp
+// histograms, later per-warp write cursors) + 64 ints.
+__device__ void align_cta(const AlignArgs& a) {
+  extern __shared__ int smem[];
+  int* cur = smem;                              // [kAlignWarps][E]
+  int* scan_tmp = smem + kAlignWarps * a.E;     // [33]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = a.M * a.topk;
+  const int sentinel = n;
+  const int B = a.block;
+
+  for (int i = tid; i < kAlignWarps * a.E; i += kAlignThreads) cur[i] = 0;
+  for (int i = tid; i < a.cap; i += kAlignThreads) a.sorted_ids[i] = sentinel;
+  for (int i = tid; i < a.cap / B; i += kAlignThreads) a.expert_ids[i] = -1;
+  __syncthreads();
+
+  // pass 1: per-warp histogram over a contiguous segment of slots
+  const int seg = (n + kAlignWarps - 1) / kAlignWarps;
+  const int beg = min(n, warp * seg), end = min(n, beg + seg);
+  int bad = 0;
+  for (int i = beg + lane; i < end; i += 32) {
+    const int e = a.topk_ids[i];
+    if (e >= 0 && e < a.E) atomicAdd(&cur[warp * a.E + e], 1);
+    else ++bad;
+  }
+  bad = warp_sum_i(bad);
+  if (lane == 0 && bad && a.status) atomicAdd(&a.status->bad_ids, bad);
+  __syncthreads();
+
+  // pass 2: expert totals -> padded offsets (scan), per-warp cursors, active list
+  for (int e0 = 0; e0 < a.E; e0 += kAlignThreads) {
+    // E <= MOE_MAX_EXPERTS == kAlignThreads, so this loop runs once
+    const int e = e0 + tid;
+    int cnt = 0;
+    if (e < a.E) {
+#pragma unroll 4
+      for (int w = 0; w < kAlignWarps; ++w) cnt += cur[w * a.E + e];
+    }
+    const int padded = (cnt + B - 1) / B * B;
+    int total;
+    const int off = block_exclusive_scan(padded, scan_tmp, total);
+    int nact;
+    const int act_idx = block_exclusive_scan(cnt > 0 ? 1 : 0, scan_tmp, nact);
+    if (e < a.E) {
+      int c = off;
+      for (int w = 0; w < kAlignWarps; ++w) {
+        const int t = cur[w * a.E + e];
+        cur[w * a.E + e] = c;
+        c += t;
+      }
+      if (a.expert_offsets) a.expert_offsets[e] = off;
+      if (a.counts) a.counts[e] = cnt;
+      if (a.active && cnt > 0) a.active[act_idx] = e;
+      for (int b = off / B; b < (off + padded) / B; ++b) a.expert_ids[b] = e;
+    }
+    if (tid == 0) {
+      if (a.expert_offsets) a.expert_offsets[a.E] = total;
+      if (a.num_post) *a.num_post = total;
+      if (a.num_active) *a.num_active = nact;
+    }
+  }
+  __syncthreads();
+
+  // pass 3: stable scatter; each warp walks its segment in slot order
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base = beg; base < end; base += 32) {
+    const int i = base + lane;
+    const int e = (i < end) ? a.topk_ids[i] : -1;
+    const bool ok = (i < end) && e >= 0 && e < a.E;
+    const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : -1);
+    const int rank = __popc(peers & lt_mask);
+    if (ok) {
+      const int pos = cur[warp * a.E + e] + rank;
+      a.sorted_ids[pos] = i;
+      if (a.inv_pos) a.inv_pos[i] = pos;
+    } else if (i < end && a.inv_pos) {
+      a.inv_pos[i] = -1;
+    }
+    __syncwarp();
+    if (ok && rank == 0) cur[warp * a.E + e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// Row preparation of the activations, one CTA per row at a time.
+//   kind 1: x bf16 -> fp16 (RN)               (FP8 weight-only path)
+//   kind 2: x bf16 -> int8 codes + fp32 scale (DA8W8 path); codes stored as
+//           fp16 (exact) or int8
+template <typename QT>
+__device__ void prep_rows(const PrepArgs& p, int row0, int rstride) {
+  __shared__ float red[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  for (int r = row0; r < p.M; r += rstride) {
+    const __nv_bfloat16* xr = p.x + static_cast<size_t>(r) * p.H;
+    QT* qr = reinterpret_cast<QT*>(p.q) + static_cast<size_t>(r) * p.H;
+    if (p.kind == 1) {
+      for (int c = tid; c < p.H; c += blockDim.x) qr[c] = static_cast<QT>(__bfloat162float(xr[c]));
+      continue;
+    }
+    float m = 0.f;
+    for (int c = tid; c < p.H; c += blockDim.x) m = fmaxf(m, fabsf(__bfloat162float(xr[c])));
+    m = warp_max(m);
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+      float v = lane < nw ? red[lane] : 0.f;
+      v = warp_max(v);
+      if (lane == 0) red[0] = v;
+    }
+    __syncthreads();
+    const float amax = red[0];
+    const float s = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 1.0f;
+    if (tid == 0 && p.scale) p.scale[r] = s;
+    for (int c = tid; c < p.H; c += blockDim.x)
+      qr[c] = static_cast<QT>(quant_s8_rne(__bfloat162float(xr[c]), s));
+    __syncthreads();
+  }
+}
+
+__global__ void __launch_bounds__(kAlignThreads) prologue_kernel(AlignArgs a, PrepArgs p) {
+  if (blockIdx.x == 0) {
+    if (a.status && threadIdx.x == 0) { a.status->bad_ids = 0; a.status->flags = 0; }
+    __syncthreads();
+    align_cta(a);
+    return;
+  }
+  // zero the per-row amax words of the INT8 intermediate
+  if (p.zero_words) {
+    const int stride = (gridDim.x - 1) * blockDim.x;
+    for (int i = (blockIdx.x - 1) * blockDim.x + threadIdx.x; i < p.n_zero; i += stride) p.zero_words[i] = 0u;
+  }
+  if (p.kind != 0) prep_rows<__half>(p, blockIdx.x - 1, gridDim.x - 1);
+}
+
+__global__ void __launch_bounds__(256) quant_rows_s8_kernel(PrepArgs p) {
+  prep_rows<int8_t>(p, blockIdx.x, gridDim.x);
+}
+
+size_t align_smem_bytes(int E) { return static_cast<size_t>(kAlignWarps * E + 64) * sizeof(int); }
+
+cudaError_t launch_prologue(const AlignArgs& a, const PrepArgs& p, int prep_ctas, cudaStream_t s) {
+  const size_t smem = align_smem_bytes(a.E);
+  cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(prologue_kernel),
+                                        static_cast<int>(align_smem_bytes(MOE_MAX_EXPERTS)), 0);
+  if (err != cudaSuccess) return err;
+  prologue_kernel<<<1 + prep_ctas, kAlignThreads, smem, s>>>(a, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows_s8(const PrepArgs& p, cudaStream_t s) {
+  const int grid = p.M < 2048 ? p.M : 2048;
+  if (grid == 0) return cudaSuccess;
+  quant_rows_s8_kernel<<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace gbmoe

@@ -1,0 +1,112 @@
+// Shared device helpers of the fused MoE library (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gbmoe.h"
+
+namespace gbmoe {
+
+constexpr int kQBlock = 128;       // FP8 block-scale granularity (both dims)
+constexpr int kDecodeBlock = 8;    // align block size of the decode path (= MMA N)
+constexpr int kStatusBytes = 256;  // head of every workspace: device status words
+
+// Device status words at the start of a workspace.
+struct DeviceStatus {
+  int32_t bad_ids;  // topk_ids entries outside [0, E)
+  int32_t flags;    // bit 0: a bounded wait gave up
+};
+
+// ---------------------------------------------------------------- conversions
+
+// Four E4M3 codes (one 32-bit word, byte 0 first) -> two fp16 pairs; exact.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  __half2_raw a = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xFFFFu), __NV_E4M3);
+  __half2_raw b = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16), __NV_E4M3);
+  lo = static_cast<uint32_t>(a.x) | (static_cast<uint32_t>(a.y) << 16);
+  hi = static_cast<uint32_t>(b.x) | (static_cast<uint32_t>(b.y) << 16);
+}
+
+// Four int8 values (one word, byte 0 first) -> two fp16 pairs; exact.
+// Each byte b is biased to b+128 in [0, 255], placed as the low mantissa bits
+// of the fp16 number 1024 (0x6400), so the lane reads 1152 + b; subtracting
+// 1152 leaves b exactly (fp16 spacing is 1 on [1024, 2048)).
+__device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  uint32_t l, h;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(l) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(h) : "r"(u), "r"(0x64646464u));
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+  __half2 lh = __hsub2(*reinterpret_cast<__half2*>(&l), bias);
+  __half2 hh = __hsub2(*reinterpret_cast<__half2*>(&h), bias);
+  lo = *reinterpret_cast<uint32_t*>(&lh);
+  hi = *reinterpret_cast<uint32_t*>(&hh);
+}
+
+template <int WK>
+__device__ __forceinline__ void w8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if constexpr (WK == MOE_WEIGHT_FP8) e4m3x4_to_f16x4(w, lo, hi);
+  else s8x4_to_f16x4(w, lo, hi);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// ---------------------------------------------------------------- memory
+
+// Streaming 16-byte load that does not allocate in L1 (weights are read once).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint4 ld_v4(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// ---------------------------------------------------------------- tensor core (warp MMA)
+
+// D[16x8] += A[16x16] * B[16x8], fp16 operands, fp32 accumulate.
+// Fragment ownership (lane = 4*g + t):
+//   a[0]: A[g][2t..2t+1]   a[1]: A[g+8][2t..2t+1]
+//   a[2]: A[g][2t+8..+9]   a[3]: A[g+8][2t+8..+9]
+//   b[0]: B[2t..2t+1][g]   b[1]: B[2t+8..+9][g]
+//   d[0..1]: D[g][2t..2t+1]  d[2..3]: D[g+8][2t..2t+1]
+__device__ __forceinline__ void mma_f16_16816(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
+
+// Round-half-even of x / s in fp32 (IEEE division), clamped to +-127.
+__device__ __forceinline__ float quant_s8_rne(float x, float s) {
+  float q = rintf(__fdiv_rn(x, s));
+  return fminf(fmaxf(q, -127.0f), 127.0f);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+}  // namespace gbmoe

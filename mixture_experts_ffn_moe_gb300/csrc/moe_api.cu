@@ -1,0 +1,391 @@
+// C-ABI front end: argument checks, workspace carving, path choice, status.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gbmoe {
+
+static thread_local std::string g_last_error;
+
+static moe_status_t fail(moe_status_t st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+static moe_status_t cuda_fail(cudaError_t err, const char* where) {
+  return fail(MOE_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(err));
+}
+
+constexpr int kMaxDevices = 64;
+constexpr int kSmemSlots = 16;
+
+cudaError_t set_smem_limit_once(const void* func, int bytes, int slot) {
+  static std::mutex mu;
+  static bool done[kMaxDevices][kSmemSlots] = {};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices || slot < 0 || slot >= kSmemSlots) return cudaErrorInvalidValue;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev][slot]) return cudaSuccess;
+  err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err == cudaSuccess) done[dev][slot] = true;
+  return err;
+}
+
+static int num_sms_current() {
+  static std::mutex mu;
+  static int cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// ------------------------------------------------------------------ per-kernel timing
+struct Profiler {
+  std::vector<cudaEvent_t> events;
+  std::vector<const char*> names;  // stage name of each recorded event (nullptr = call start)
+  int max_calls = 0, calls = 0;
+  size_t used = 0;
+  bool recording_call = false;
+};
+static thread_local Profiler g_prof;
+
+static void prof_record(void*, const char* stage, cudaStream_t s) {
+  Profiler& P = g_prof;
+  if (!P.recording_call || P.used >= P.events.size()) { P.recording_call = false; return; }
+  cudaEventRecord(P.events[P.used], s);
+  P.names[P.used] = stage;
+  ++P.used;
+}
+
+static StageHook prof_begin_call(cudaStream_t s) {
+  Profiler& P = g_prof;
+  StageHook h;
+  if (P.max_calls <= 0 || P.calls >= P.max_calls) return h;
+  P.recording_call = true;
+  prof_record(nullptr, nullptr, s);
+  ++P.calls;
+  h.fn = prof_record;
+  return h;
+}
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+static size_t max_padded(int M, int topk, int E, int B) {
+  const size_t n = static_cast<size_t>(M) * topk + static_cast<size_t>(E) * (B - 1);
+  return align_up(n, static_cast<size_t>(B));
+}
+
+// Offsets (bytes) of every buffer inside a fused-call workspace.
+struct Layout {
+  int path = 0, B = 0;
+  size_t cap = 0;
+  size_t status = 0, sorted = 0, expert_ids = 0, offsets = 0, counts = 0, active = 0, scalars = 0,
+         inv_pos = 0, xq = 0, sx = 0, h = 0, hmax = 0, hq = 0, sh = 0, total = 0;
+};
+
+static int choose_path(int M, unsigned flags) {
+  const unsigned p = flags & MOE_PATH_MASK;
+  if (p == MOE_PATH_DECODE || p == MOE_PATH_PREFILL) return static_cast<int>(p);
+  return M <= MOE_MAX_DECODE_TOKENS ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
+}
+
+static Layout plan(int M, int H, int I, int E, int topk, int kind, unsigned flags) {
+  Layout L;
+  L.path = choose_path(M, flags);
+  L.B = kDecodeBlock;
+  L.cap = max_padded(M, topk, E, L.B);
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes, 256); return at; };
+  L.status = take(kStatusBytes);
+  L.sorted = take(L.cap * 4);
+  L.expert_ids = take(L.cap / L.B * 4);
+  L.offsets = take((static_cast<size_t>(E) + 1) * 4);
+  L.counts = take(static_cast<size_t>(E) * 4);
+  L.active = take(static_cast<size_t>(E) * 4);
+  L.scalars = take(16);
+  L.inv_pos = take(static_cast<size_t>(M) * topk * 4);
+  L.xq = take(static_cast<size_t>(M) * H * 2);
+  L.sx = take(static_cast<size_t>(M) * 4);
+  if (kind == MOE_WEIGHT_FP8) {
+    L.h = take(L.cap * I * 2);
+  } else {
+    L.h = take(L.cap * I * 4);
+    L.hmax = take(L.cap * 4);
+    L.hq = take(L.cap * I * 2);
+    L.sh = take(L.cap * 4);
+  }
+  L.total = o;
+  return L;
+}
+
+static moe_status_t check_layer_args(const void* x, const void* ids, const void* tw, const void* w13,
+                                     const void* s13, const void* w2, const void* s2, int M, int H, int I,
+                                     int E, int topk, unsigned flags, const void* out) {
+  if (M < 0 || H <= 0 || I <= 0 || E <= 0 || topk <= 0)
+    return fail(MOE_ERR_INVALID_ARG, "sizes must be positive (M >= 0)");
+  if (topk > 32) return fail(MOE_ERR_UNSUPPORTED, "topk > 32");
+  if (E > MOE_MAX_EXPERTS) return fail(MOE_ERR_UNSUPPORTED, "more than MOE_MAX_EXPERTS experts");
+  if (H % kQBlock || I % kQBlock) return fail(MOE_ERR_UNSUPPORTED, "H and I must be multiples of 128");
+  if (flags & ~MOE_PATH_MASK) return fail(MOE_ERR_INVALID_ARG, "unknown flag bits");
+  if ((flags & MOE_PATH_MASK) == MOE_PATH_MASK) return fail(MOE_ERR_INVALID_ARG, "both path flags set");
+  if (static_cast<long long>(M) * topk > (1LL << 30) || static_cast<long long>(M) * H > (1LL << 40))
+    return fail(MOE_ERR_UNSUPPORTED, "problem too large");
+  if (M == 0) return MOE_OK;
+  if (!x || !ids || !tw || !w13 || !s13 || !w2 || !s2 || !out) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  const int path = choose_path(M, flags);
+  if (path == MOE_PATH_DECODE && M > MOE_MAX_DECODE_TOKENS)
+    return fail(MOE_ERR_UNSUPPORTED, "decode path takes at most MOE_MAX_DECODE_TOKENS tokens");
+  if (path == MOE_PATH_PREFILL) return fail(MOE_ERR_UNSUPPORTED, "prefill path not available in this build");
+  return MOE_OK;
+}
+
+template <typename T>
+static T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, const float* tw, const void* w13,
+                               const float* s13, const void* w2, const float* s2, int M, int H, int I, int E,
+                               int topk, unsigned flags, void* out, void* ws, size_t ws_bytes,
+                               cudaStream_t stream) {
+  g_last_error.clear();
+  moe_status_t st = check_layer_args(x, ids, tw, w13, s13, w2, s2, M, H, I, E, topk, flags, out);
+  if (st != MOE_OK || M == 0) return st;
+  const Layout L = plan(M, H, I, E, topk, kind, flags);
+  if (!ws) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) % 256) return fail(MOE_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (ws_bytes < L.total) return fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_workspace_size()");
+  if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(w13) % 16 ||
+      reinterpret_cast<uintptr_t>(w2) % 16 || reinterpret_cast<uintptr_t>(out) % 4)
+    return fail(MOE_ERR_INVALID_ARG, "x, w13 and w2 must be 16-byte aligned, out 4-byte aligned");
+  const int sms = num_sms_current();
+  if (sms <= 0) return fail(MOE_ERR_CUDA, "cannot query the current device");
+
+  AlignArgs a{};
+  a.topk_ids = ids;
+  a.M = M; a.topk = topk; a.E = E; a.block = L.B; a.cap = static_cast<int>(L.cap);
+  a.sorted_ids = at<int32_t>(ws, L.sorted);
+  a.expert_ids = at<int32_t>(ws, L.expert_ids);
+  a.num_post = at<int32_t>(ws, L.scalars);
+  a.num_active = at<int32_t>(ws, L.scalars) + 1;
+  a.expert_offsets = at<int32_t>(ws, L.offsets);
+  a.counts = at<int32_t>(ws, L.counts);
+  a.active = at<int32_t>(ws, L.active);
+  a.inv_pos = at<int32_t>(ws, L.inv_pos);
+  a.status = at<DeviceStatus>(ws, L.status);
+
+  PrepArgs p{};
+  p.x = static_cast<const __nv_bfloat16*>(x);
+  p.M = M; p.H = H;
+  p.kind = kind == MOE_WEIGHT_FP8 ? 1 : 2;
+  p.q = at<__half>(ws, L.xq);
+  p.scale = at<float>(ws, L.sx);
+  if (kind == MOE_WEIGHT_INT8) { p.zero_words = at<uint32_t>(ws, L.hmax); p.n_zero = static_cast<int>(L.cap); }
+  const int prep_ctas = M < 2 * sms ? (M > 0 ? M : 1) : 2 * sms;
+  const StageHook hook = prof_begin_call(stream);
+  cudaError_t err = launch_prologue(a, p, prep_ctas, stream);
+  if (err != cudaSuccess) return cuda_fail(err, "prologue launch");
+  hook("prologue_align_prep", stream);
+
+  DecodeArgs d{};
+  d.M = M; d.H = H; d.I = I; d.E = E; d.topk = topk;
+  d.xq = at<__half>(ws, L.xq);
+  d.sx = at<float>(ws, L.sx);
+  d.w13 = static_cast<const uint8_t*>(w13);
+  d.s13 = s13;
+  d.w2 = static_cast<const uint8_t*>(w2);
+  d.s2 = s2;
+  d.topk_w = tw;
+  d.sorted_ids = a.sorted_ids;
+  d.offsets = a.expert_offsets;
+  d.counts = a.counts;
+  d.active = a.active;
+  d.num_active = a.num_active;
+  d.num_post = a.num_post;
+  d.cap = static_cast<int>(L.cap);
+  d.h = at<void>(ws, L.h);
+  if (kind == MOE_WEIGHT_INT8) {
+    d.hmax = at<uint32_t>(ws, L.hmax);
+    d.hq = at<__half>(ws, L.hq);
+    d.sh = at<float>(ws, L.sh);
+  }
+  d.out = static_cast<__nv_bfloat16*>(out);
+  err = launch_decode(d, kind, sms, stream, hook);
+  if (err != cudaSuccess) return cuda_fail(err, "decode launch");
+  return MOE_OK;
+}
+
+}  // namespace gbmoe
+
+using namespace gbmoe;
+
+extern "C" {
+
+size_t moe_align_max_padded(int M, int topk, int num_experts, int block_size) {
+  if (M < 0 || topk <= 0 || num_experts <= 0 || block_size <= 0) return 0;
+  return gbmoe::max_padded(M, topk, num_experts, block_size);
+}
+
+moe_status_t moe_align_block_size(const int32_t* topk_ids, int M, int topk, int num_experts, int block_size,
+                                  int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_tokens_post_padded,
+                                  int32_t* expert_offsets, moe_stream_t stream) {
+  g_last_error.clear();
+  if (M < 0 || topk <= 0 || num_experts <= 0 || block_size <= 0)
+    return fail(MOE_ERR_INVALID_ARG, "sizes must be positive (M >= 0)");
+  if (num_experts > MOE_MAX_EXPERTS) return fail(MOE_ERR_UNSUPPORTED, "more than MOE_MAX_EXPERTS experts");
+  if (block_size > 256) return fail(MOE_ERR_UNSUPPORTED, "block_size > 256");
+  if (static_cast<long long>(M) * topk > (1LL << 30)) return fail(MOE_ERR_UNSUPPORTED, "too many slots");
+  if ((M > 0 && !topk_ids) || !sorted_ids || !expert_ids || !num_tokens_post_padded)
+    return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  AlignArgs a{};
+  a.topk_ids = topk_ids;
+  a.M = M; a.topk = topk; a.E = num_experts; a.block = block_size;
+  a.cap = static_cast<int>(gbmoe::max_padded(M, topk, num_experts, block_size));
+  a.sorted_ids = sorted_ids;
+  a.expert_ids = expert_ids;
+  a.num_post = num_tokens_post_padded;
+  a.expert_offsets = expert_offsets;
+  PrepArgs p{};
+  cudaError_t err = launch_prologue(a, p, 0, reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_align_block_size launch");
+  return MOE_OK;
+}
+
+moe_status_t moe_quant_act_int8(const void* x_bf16, int M, int H, int8_t* q, float* scale, moe_stream_t stream) {
+  g_last_error.clear();
+  if (M < 0 || H <= 0) return fail(MOE_ERR_INVALID_ARG, "M >= 0 and H > 0 required");
+  if (M == 0) return MOE_OK;
+  if (!x_bf16 || !q || !scale) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  PrepArgs p{};
+  p.x = static_cast<const __nv_bfloat16*>(x_bf16);
+  p.M = M; p.H = H; p.kind = 2; p.q = q; p.scale = scale;
+  cudaError_t err = launch_quant_rows_s8(p, reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_quant_act_int8 launch");
+  return MOE_OK;
+}
+
+size_t moe_workspace_size(int M, int H, int I, int E, int topk, int weight_kind, unsigned flags) {
+  if (M < 0 || H <= 0 || I <= 0 || E <= 0 || topk <= 0 || E > MOE_MAX_EXPERTS) return 0;
+  if (weight_kind != MOE_WEIGHT_FP8 && weight_kind != MOE_WEIGHT_INT8) return 0;
+  if (flags & ~MOE_PATH_MASK) return 0;
+  return plan(M, H, I, E, topk, weight_kind, flags).total;
+}
+
+moe_status_t fused_moe_fp8(const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
+                           const void* w13_e4m3, const float* w13_scale, const void* w2_e4m3,
+                           const float* w2_scale, int M, int H, int I, int E, int topk, unsigned flags,
+                           void* out_bf16, void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  return fused_impl(MOE_WEIGHT_FP8, x_bf16, topk_ids, topk_weights, w13_e4m3, w13_scale, w2_e4m3, w2_scale,
+                    M, H, I, E, topk, flags, out_bf16, workspace, workspace_bytes,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t fused_moe_int8(const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
+                            const int8_t* w13, const float* w13_scale, const int8_t* w2, const float* w2_scale,
+                            int M, int H, int I, int E, int topk, unsigned flags, void* out_bf16,
+                            void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  return fused_impl(MOE_WEIGHT_INT8, x_bf16, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, M, H, I, E,
+                    topk, flags, out_bf16, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_read_status(const void* workspace, int32_t status_out[2], moe_stream_t stream) {
+  g_last_error.clear();
+  if (!workspace || !status_out) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  DeviceStatus host{};
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t err = cudaMemcpyAsync(&host, workspace, sizeof(host), cudaMemcpyDeviceToHost, s);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_read_status");
+  status_out[0] = host.bad_ids;
+  status_out[1] = host.flags;
+  if (host.flags & 1) return fail(MOE_ERR_TIMEOUT, "a bounded device wait gave up");
+  if (host.bad_ids) return fail(MOE_ERR_BAD_IDS, "topk_ids outside [0, E)");
+  return MOE_OK;
+}
+
+moe_status_t moe_profile_enable(int max_calls) {
+  g_last_error.clear();
+  Profiler& P = g_prof;
+  for (cudaEvent_t e : P.events) cudaEventDestroy(e);
+  P = Profiler{};
+  if (max_calls < 0 || max_calls > 100000) return fail(MOE_ERR_INVALID_ARG, "max_calls out of range");
+  if (max_calls == 0) return MOE_OK;
+  const size_t n = static_cast<size_t>(max_calls) * 8;  // a call records at most 8 events
+  P.events.resize(n);
+  P.names.assign(n, nullptr);
+  for (size_t i = 0; i < n; ++i) {
+    cudaError_t err = cudaEventCreate(&P.events[i]);
+    if (err != cudaSuccess) {
+      P.events.resize(i);
+      return cuda_fail(err, "moe_profile_enable");
+    }
+  }
+  P.max_calls = max_calls;
+  return MOE_OK;
+}
+
+moe_status_t moe_profile_read(float* stage_ms, const char** stage_names, int max_stages, int* n_stages,
+                              int* n_calls) {
+  g_last_error.clear();
+  Profiler& P = g_prof;
+  if (!stage_ms || !n_stages || !n_calls || max_stages <= 0) return fail(MOE_ERR_INVALID_ARG, "bad arguments");
+  *n_stages = 0;
+  *n_calls = 0;
+  if (P.used == 0) return MOE_OK;
+  cudaError_t err = cudaEventSynchronize(P.events[P.used - 1]);
+  if (err != cudaSuccess) return cuda_fail(err, "moe_profile_read");
+  std::vector<float> sums;
+  std::vector<const char*> names;
+  int calls = 0;
+  size_t stage = 0;
+  for (size_t i = 0; i < P.used; ++i) {
+    if (P.names[i] == nullptr) { ++calls; stage = 0; continue; }
+    float ms = 0.f;
+    err = cudaEventElapsedTime(&ms, P.events[i - 1], P.events[i]);
+    if (err != cudaSuccess) return cuda_fail(err, "moe_profile_read");
+    if (stage >= sums.size()) { sums.push_back(0.f); names.push_back(P.names[i]); }
+    if (names[stage] != P.names[i]) return fail(MOE_ERR_INVALID_ARG, "recorded calls took different paths");
+    sums[stage] += ms;
+    ++stage;
+  }
+  const int n = static_cast<int>(sums.size()) < max_stages ? static_cast<int>(sums.size()) : max_stages;
+  for (int i = 0; i < n; ++i) {
+    stage_ms[i] = sums[i];
+    if (stage_names) stage_names[i] = names[i];
+  }
+  *n_stages = n;
+  *n_calls = calls;
+  P.used = 0;
+  P.calls = 0;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported size or option";
+    case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "bounded device wait gave up";
+    case MOE_ERR_BAD_IDS: return "expert ids outside [0, E)";
+  }
+  return "unknown status";
+}
+
+const char* moe_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,204 @@
+"""Thin Python binding of libgbmoe.so (the C ABI declared in include/gbmoe.h).
+
+Argument marshalling only: every step of the layer runs in the library's
+CUDA kernels.  torch supplies device memory and the current CUDA stream.
+There is no fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgbmoe.so")
+
+MOE_OK = 0
+MOE_PATH_AUTO = 0x0
+MOE_PATH_DECODE = 0x1
+MOE_PATH_PREFILL = 0x2
+MOE_WEIGHT_FP8 = 0
+MOE_WEIGHT_INT8 = 1
+MOE_MAX_EXPERTS = 1024
+MOE_MAX_DECODE_TOKENS = 128
+
+_STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+                 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_BAD_IDS"}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        self.status = status
+        super().__init__(f"{where}: {_STATUS_NAMES.get(status, status)} ({detail})")
+
+
+_lib = None
+
+_vp, _i, _u, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
+_SIGS = {
+    "moe_align_max_padded": (_sz, [_i, _i, _i, _i]),
+    "moe_align_block_size": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
+    "moe_quant_act_int8": (_i, [_vp, _i, _i, _vp, _vp, _vp]),
+    "moe_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _u]),
+    "fused_moe_fp8": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp, _sz, _vp]),
+    "fused_moe_int8": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp, _sz, _vp]),
+    "moe_read_status": (_i, [_vp, _vp, _vp]),
+    "moe_profile_enable": (_i, [_i]),
+    "moe_profile_read": (_i, [_vp, _vp, _i, _vp, _vp]),
+    "moe_status_string": (ctypes.c_char_p, [_i]),
+    "moe_last_error": (ctypes.c_char_p, []),
+}
+EXPORTED = tuple(_SIGS)
+
+
+def load(path: str = LIB_PATH):
+    """Loads libgbmoe.so (built in-tree by build.py) and declares its signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m mixture_experts_ffn_moe_gb300.build` "
+                           "(the CUDA library is required; there is no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(st: int, where: str):
+    if st != MOE_OK:
+        detail = load().moe_last_error().decode() or load().moe_status_string(st).decode()
+        raise MoEError(st, where, detail)
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _need(t: torch.Tensor, dtype, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def moe_align_max_padded(M: int, topk: int, num_experts: int, block_size: int) -> int:
+    return int(load().moe_align_max_padded(M, topk, num_experts, block_size))
+
+
+def moe_align_block_size(topk_ids: torch.Tensor, num_experts: int, block_size: int, with_offsets: bool = True):
+    """Returns (sorted_ids, expert_ids, num_tokens_post_padded, expert_offsets) as device tensors."""
+    _need(topk_ids, torch.int32, "topk_ids")
+    M, topk = topk_ids.shape
+    cap = moe_align_max_padded(M, topk, num_experts, block_size)
+    dev = topk_ids.device
+    sorted_ids = torch.empty(cap, dtype=torch.int32, device=dev)
+    expert_ids = torch.empty(cap // block_size, dtype=torch.int32, device=dev)
+    npp = torch.empty(1, dtype=torch.int32, device=dev)
+    offs = torch.empty(num_experts + 1, dtype=torch.int32, device=dev) if with_offsets else None
+    st = load().moe_align_block_size(_ptr(topk_ids), M, topk, num_experts, block_size, _ptr(sorted_ids),
+                                     _ptr(expert_ids), _ptr(npp), _ptr(offs), _stream(topk_ids))
+    _check(st, "moe_align_block_size")
+    return sorted_ids, expert_ids, npp, offs
+
+
+def moe_quant_act_int8(x: torch.Tensor):
+    """bf16 [M, H] -> (int8 codes [M, H], fp32 scales [M])."""
+    _need(x, torch.bfloat16, "x")
+    M, H = x.shape
+    q = torch.empty(M, H, dtype=torch.int8, device=x.device)
+    s = torch.empty(M, dtype=torch.float32, device=x.device)
+    _check(load().moe_quant_act_int8(_ptr(x), M, H, _ptr(q), _ptr(s), _stream(x)), "moe_quant_act_int8")
+    return q, s
+
+
+def moe_workspace_size(M, H, I, E, topk, weight_kind, flags=MOE_PATH_AUTO) -> int:
+    return int(load().moe_workspace_size(M, H, I, E, topk, weight_kind, flags))
+
+
+def alloc_workspace(M, H, I, E, topk, weight_kind, flags=MOE_PATH_AUTO, device="cuda") -> torch.Tensor:
+    n = moe_workspace_size(M, H, I, E, topk, weight_kind, flags)
+    if n == 0:
+        raise MoEError(2, "moe_workspace_size", "unsupported sizes")
+    return torch.empty(n, dtype=torch.uint8, device=device)  # caching allocator blocks are 512-byte aligned
+
+
+def _fused(fn_name, kind, x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, flags, out, workspace):
+    wdt = torch.uint8 if kind == MOE_WEIGHT_FP8 else torch.int8
+    _need(x, torch.bfloat16, "x")
+    _need(topk_ids, torch.int32, "topk_ids")
+    _need(topk_weights, torch.float32, "topk_weights")
+    if w13.dtype == torch.float8_e4m3fn:
+        w13 = w13.view(torch.uint8)
+    if w2.dtype == torch.float8_e4m3fn:
+        w2 = w2.view(torch.uint8)
+    _need(w13, wdt, "w13")
+    _need(w2, wdt, "w2")
+    _need(w13_scale, torch.float32, "w13_scale")
+    _need(w2_scale, torch.float32, "w2_scale")
+    M, H = x.shape
+    E, I2, H2 = w13.shape
+    if H2 != H or tuple(w2.shape) != (E, H, I2 // 2) or topk_ids.shape[0] != M:
+        raise ValueError("inconsistent shapes")
+    if tuple(topk_weights.shape) != tuple(topk_ids.shape):
+        raise ValueError("topk_weights and topk_ids must have the same shape")
+    topk = topk_ids.shape[1]
+    I = I2 // 2
+    if out is None:
+        out = torch.empty(M, H, dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, "out")
+    if workspace is None:
+        workspace = alloc_workspace(M, H, I, E, topk, kind, flags, x.device)
+    fn = getattr(load(), fn_name)
+    st = fn(_ptr(x), _ptr(topk_ids), _ptr(topk_weights), _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale),
+            M, H, I, E, topk, flags, _ptr(out), _ptr(workspace), workspace.numel(), _stream(x))
+    _check(st, fn_name)
+    return out
+
+
+def fused_moe_fp8(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, flags=MOE_PATH_AUTO, out=None,
+                  workspace=None):
+    """The MoE layer with FP8 E4M3 128x128-block-scaled weights (see include/gbmoe.h)."""
+    return _fused("fused_moe_fp8", MOE_WEIGHT_FP8, x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale,
+                  flags, out, workspace)
+
+
+def fused_moe_int8(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, flags=MOE_PATH_AUTO, out=None,
+                   workspace=None):
+    """The MoE layer with INT8 per-channel weights and dynamic INT8 activations (see include/gbmoe.h)."""
+    return _fused("fused_moe_int8", MOE_WEIGHT_INT8, x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale,
+                  flags, out, workspace)
+
+
+def moe_read_status(workspace: torch.Tensor):
+    """(bad_id_count, flags, status) of the last fused call that used `workspace`."""
+    buf = (ctypes.c_int32 * 2)()
+    st = load().moe_read_status(_ptr(workspace), ctypes.cast(buf, ctypes.c_void_p), _stream(workspace))
+    return int(buf[0]), int(buf[1]), int(st)
+
+
+def moe_profile_enable(max_calls: int) -> None:
+    """Record per-kernel CUDA events for the next `max_calls` fused calls of this thread (0 = stop)."""
+    _check(load().moe_profile_enable(max_calls), "moe_profile_enable")
+
+
+def moe_profile_read(max_stages: int = 8):
+    """Waits for the recorded events; returns (calls, [(kernel name, summed ms), ...]) and forgets them."""
+    ms = (ctypes.c_float * max_stages)()
+    names = (ctypes.c_char_p * max_stages)()
+    n_st = ctypes.c_int(0)
+    n_calls = ctypes.c_int(0)
+    st = load().moe_profile_read(ctypes.cast(ms, ctypes.c_void_p), ctypes.cast(names, ctypes.c_void_p),
+                                 max_stages, ctypes.byref(n_st), ctypes.byref(n_calls))
+    _check(st, "moe_profile_read")
+    return n_calls.value, [(names[i].decode(), float(ms[i])) for i in range(n_st.value)]

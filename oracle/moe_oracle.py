@@ -90,13 +90,25 @@ def e4m3_encode_satfinite(v) -> np.ndarray:
 # ----------------------------------------------------------------------------
 
 
+_E4M3_TABLE = None
+
+
+def _e4m3_table() -> np.ndarray:
+    """e4m3_decode of all 256 codes, so large arrays decode by one lookup."""
+    global _E4M3_TABLE
+    if _E4M3_TABLE is None:
+        _E4M3_TABLE = e4m3_decode(np.arange(256, dtype=np.uint8))
+    return _E4M3_TABLE
+
+
 def dequant_fp8_block(codes, scale) -> np.ndarray:
     """codes uint8 [R, C], scale f32 [R/128, C/128] -> float64 W[r, c] = decode(q) * S[r//128, c//128]."""
-    codes = np.asarray(codes)
+    codes = np.asarray(codes, dtype=np.uint8)
     scale = np.asarray(scale, dtype=np.float64)
     R, C = codes.shape
-    S = np.repeat(np.repeat(scale, QBLOCK, axis=0), QBLOCK, axis=1)[:R, :C]
-    return e4m3_decode(codes) * S
+    W = _e4m3_table()[codes].reshape(R // QBLOCK, QBLOCK, C // QBLOCK, QBLOCK)
+    W *= scale[:, None, :, None]
+    return W.reshape(R, C)
 
 
 def dequant_int8_channel(codes, scale) -> np.ndarray:

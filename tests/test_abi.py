@@ -1,0 +1,80 @@
+"""The C-ABI library builds, loads and exports every entry point of include/gbmoe.h.
+
+These run without a GPU: they only call host-side functions (size queries,
+status strings) and argument checks that return before any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixture_experts_ffn_moe_gb300 import build, gbmoe
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gbmoe.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return gbmoe.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("moe_align_block_size", "fused_moe_fp8", "fused_moe_int8", "moe_workspace_size",
+              "moe_read_status", "moe_quant_act_int8"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(gbmoe.EXPORTED) == set(declared_functions())
+
+
+def test_max_padded_matches_definition(lib):
+    assert gbmoe.moe_align_max_padded(3, 2, 4, 2) == 10
+    assert gbmoe.moe_align_max_padded(2048, 9, 257, 64) == ((2048 * 9 + 257 * 63 + 63) // 64) * 64
+    assert gbmoe.moe_align_max_padded(-1, 2, 4, 2) == 0
+
+
+def test_workspace_size_queries(lib):
+    a = gbmoe.moe_workspace_size(4, 7168, 2048, 257, 9, gbmoe.MOE_WEIGHT_FP8)
+    b = gbmoe.moe_workspace_size(64, 7168, 2048, 257, 9, gbmoe.MOE_WEIGHT_FP8)
+    assert 0 < a < b
+    assert gbmoe.moe_workspace_size(4, 4096, 1536, 128, 8, gbmoe.MOE_WEIGHT_INT8) > 0
+    assert gbmoe.moe_workspace_size(4, 4096, 1536, 128, 8, 7) == 0
+    assert gbmoe.moe_workspace_size(4, 4096, 1536, 2000, 8, gbmoe.MOE_WEIGHT_FP8) == 0
+
+
+def test_status_strings(lib):
+    for st in range(7):
+        assert lib.moe_status_string(st)
+    assert lib.moe_status_string(99) == b"unknown status"
+
+
+def _call_fp8(lib, M=4, H=256, I=128, E=8, topk=2, flags=0, null=False):
+    p = None if null else ctypes.c_void_p(16)  # never dereferenced: calls fail on the host first
+    return lib.fused_moe_fp8(p, p, p, p, p, p, p, M, H, I, E, topk, flags, p, p, 0, None)
+
+
+def test_host_side_argument_errors(lib):
+    assert _call_fp8(lib, M=-1) == 1
+    assert _call_fp8(lib, H=200) == 2           # not a multiple of 128
+    assert _call_fp8(lib, E=5000) == 2           # more experts than supported
+    assert _call_fp8(lib, topk=40) == 2
+    assert _call_fp8(lib, flags=0x100) == 1      # unknown flag
+    assert _call_fp8(lib, flags=3) == 1          # both paths
+    assert _call_fp8(lib, null=True) == 1        # NULL pointers
+    assert b"NULL" in lib.moe_last_error()
+    assert _call_fp8(lib) == 3                   # workspace NULL / too small
+    assert _call_fp8(lib, M=0) == 0              # empty batch is a no-op
+    assert lib.moe_align_block_size(None, 4, 2, 8, 0, None, None, None, None, None) == 1
+    assert lib.moe_align_block_size(None, 4, 2, 8, 512, None, None, None, None, None) == 2
