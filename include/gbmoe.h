@@ -172,6 +172,35 @@ moe_status_t fused_moe_int8(const void* x_bf16, const int32_t* topk_ids, const f
                             size_t workspace_bytes, moe_stream_t stream);
 
 /*
+ * fused_moe_fp8 for callers that cannot allocate device memory.  The pages
+ * have no counterpart of this entry point; it exists for callers that hold
+ * only raw input and output pointers and may not call a device allocator (a
+ * plugin whose host framework owns all device memory, a C caller without an
+ * allocator, or a loop that must not pay for cudaMalloc / cudaFree).
+ *
+ * Same arguments, layouts and results as fused_moe_fp8, without the
+ * workspace: the scratch is a static device buffer of
+ * MOE_STATIC_SCRATCH_BYTES inside the library.  Each device on which it runs
+ * holds that buffer from its first call until the process exits.
+ *  - The first call on a device looks the buffer's address up once
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Sizes whose moe_workspace_size(..., MOE_WEIGHT_FP8, flags) exceeds
+ *    MOE_STATIC_SCRATCH_BYTES return MOE_ERR_UNSUPPORTED with a message that
+ *    names the limit; nothing is launched.
+ *  - Nothing is allocated or freed.  All calls share the buffer, which keeps
+ *    the last call's contents; the kernels clear what must start at zero.
+ *    Calls that overlap on the GPU race on it: serialise them.
+ *  - Its device status words are not readable through moe_read_status.
+ */
+#define MOE_STATIC_SCRATCH_BYTES (16u << 20)
+moe_status_t fused_moe_fp8_static_scratch(const void* x_bf16, const int32_t* topk_ids,
+                                          const float* topk_weights, const void* w13_e4m3,
+                                          const float* w13_scale, const void* w2_e4m3,
+                                          const float* w2_scale, int M, int H, int I, int E, int topk,
+                                          unsigned flags, void* out_bf16, moe_stream_t stream);
+
+/*
  * Waits for `stream`, then copies the workspace's status words to the host:
  *   status_out[0] = number of topk_ids entries outside [0, E) seen by the
  *                   last fused call on this workspace

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <string>
+
 #include "gbmoe.h"
 
 namespace gbmoe {
@@ -75,6 +77,9 @@ cudaError_t launch_prologue(const AlignArgs& a, const PrepArgs& p, int prep_ctas
 cudaError_t launch_quant_rows_s8(const PrepArgs& p, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& d, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook);
 size_t decode_gemm2_smem_bytes(int M);
+
+// Records `msg` as the calling thread's last error (moe_last_error) and returns `st`.
+moe_status_t report_error(moe_status_t st, const std::string& msg);
 
 // Sets a kernel's dynamic shared memory limit once per device.
 cudaError_t set_smem_limit_once(const void* func, int bytes, int slot);

@@ -21,6 +21,8 @@ static moe_status_t cuda_fail(cudaError_t err, const char* where) {
   return fail(MOE_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(err));
 }
 
+moe_status_t report_error(moe_status_t st, const std::string& msg) { return fail(st, msg); }
+
 constexpr int kMaxDevices = 64;
 constexpr int kSmemSlots = 16;
 

@@ -22,6 +22,7 @@ MOE_WEIGHT_FP8 = 0
 MOE_WEIGHT_INT8 = 1
 MOE_MAX_EXPERTS = 1024
 MOE_MAX_DECODE_TOKENS = 128
+MOE_STATIC_SCRATCH_BYTES = 16 << 20
 
 _STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
                  4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_BAD_IDS"}
@@ -43,6 +44,7 @@ _SIGS = {
     "moe_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _u]),
     "fused_moe_fp8": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp, _sz, _vp]),
     "fused_moe_int8": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp, _sz, _vp]),
+    "fused_moe_fp8_static_scratch": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp]),
     "moe_read_status": (_i, [_vp, _vp, _vp]),
     "moe_profile_enable": (_i, [_i]),
     "moe_profile_read": (_i, [_vp, _vp, _i, _vp, _vp]),
@@ -178,6 +180,37 @@ def fused_moe_int8(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, flag
     """The MoE layer with INT8 per-channel weights and dynamic INT8 activations (see include/gbmoe.h)."""
     return _fused("fused_moe_int8", MOE_WEIGHT_INT8, x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale,
                   flags, out, workspace)
+
+
+def fused_moe_fp8_static_scratch(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, flags=MOE_PATH_AUTO,
+                                 out=None):
+    """fused_moe_fp8 without a workspace, for callers that cannot allocate device memory.
+
+    The library runs the same kernels on a fixed static device buffer of
+    MOE_STATIC_SCRATCH_BYTES; sizes that need more are rejected.  Calls that
+    overlap on the GPU share that buffer and must be serialised.
+    """
+    _need(x, torch.bfloat16, "x")
+    _need(topk_ids, torch.int32, "topk_ids")
+    _need(topk_weights, torch.float32, "topk_weights")
+    if w13.dtype == torch.float8_e4m3fn:
+        w13 = w13.view(torch.uint8)
+    if w2.dtype == torch.float8_e4m3fn:
+        w2 = w2.view(torch.uint8)
+    for t, n in ((w13, "w13"), (w2, "w2")):
+        _need(t, torch.uint8, n)
+    _need(w13_scale, torch.float32, "w13_scale")
+    _need(w2_scale, torch.float32, "w2_scale")
+    M, H = x.shape
+    E, I2, _ = w13.shape
+    if out is None:
+        out = torch.empty(M, H, dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, "out")
+    st = load().fused_moe_fp8_static_scratch(_ptr(x), _ptr(topk_ids), _ptr(topk_weights), _ptr(w13),
+                                             _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), M, H, I2 // 2, E,
+                                             topk_ids.shape[1], flags, _ptr(out), _stream(x))
+    _check(st, "fused_moe_fp8_static_scratch")
+    return out
 
 
 def moe_read_status(workspace: torch.Tensor):
