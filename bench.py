@@ -47,6 +47,8 @@ def workloads():
         **{f"dsr1_sweep_M{m}": synth.deepseek_r1(m, routing="uniform") for m in (1, 2, 4, 8, 16, 32, 64)},
         **{f"qwen3_M{m}": synth.qwen3_235b(m) for m in (1, 16, 256, 4096)},
         "tiny_M16": synth.tiny(),
+        # same per-expert work with 32+1 experts: small enough for full ncu captures
+        "dsr1_decode_M4_E32": synth.deepseek_r1(4, E=32),
     }
 
 

@@ -66,9 +66,10 @@ def tiny(M: int = 16) -> LayerShape:
     return LayerShape(f"tiny_M{M}", M, 256, 128, 8, 2, "fp8", "softmax")
 
 
-def deepseek_r1(M: int, routing: str = "deepseek") -> LayerShape:
-    return LayerShape(f"dsr1_{routing}_M{M}", M, 7168, 2048, 256, 8, "fp8", routing,
-                      shared_expert=True, n_group=8, topk_group=4)
+def deepseek_r1(M: int, routing: str = "deepseek", E: int = 256) -> LayerShape:
+    """DeepSeek-R1 layer shapes; a smaller E keeps the per-expert work and shrinks the weight set."""
+    return LayerShape(f"dsr1_{routing}_M{M}" + ("" if E == 256 else f"_E{E}"), M, 7168, 2048, E, 8, "fp8",
+                      routing, shared_expert=True, n_group=8, topk_group=4)
 
 
 def qwen3_235b(M: int) -> LayerShape:
