@@ -95,6 +95,9 @@ __device__ void align_cta(const AlignArgs& a) {
     const int off = block_exclusive_scan(padded, scan_tmp, total);
     int nact;
     const int act_idx = block_exclusive_scan(cnt > 0 ? 1 : 0, scan_tmp, nact);
+    const int ntt = a.ttiles ? (cnt + a.tile_tokens - 1) / a.tile_tokens : 0;
+    int n_tt;
+    const int tt0 = block_exclusive_scan(ntt, scan_tmp, n_tt);
     if (e < a.E) {
       int c = off;
       for (int w = 0; w < kAlignWarps; ++w) {
@@ -106,11 +109,16 @@ __device__ void align_cta(const AlignArgs& a) {
       if (a.counts) a.counts[e] = cnt;
       if (a.active && cnt > 0) a.active[act_idx] = e;
       for (int b = off / B; b < (off + padded) / B; ++b) a.expert_ids[b] = e;
+      for (int i = 0; i < ntt; ++i) {
+        const int start = i * a.tile_tokens;
+        a.ttiles[tt0 + i] = make_int4(e, off + start, min(a.tile_tokens, cnt - start), 0);
+      }
     }
     if (tid == 0) {
       if (a.expert_offsets) a.expert_offsets[a.E] = total;
       if (a.num_post) *a.num_post = total;
       if (a.num_active) *a.num_active = nact;
+      if (a.num_ttiles) *a.num_ttiles = n_tt;
     }
   }
   __syncthreads();

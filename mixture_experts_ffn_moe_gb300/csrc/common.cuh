@@ -13,6 +13,8 @@ namespace gbmoe {
 
 constexpr int kQBlock = 128;       // FP8 block-scale granularity (both dims)
 constexpr int kDecodeBlock = 8;    // align block size of the decode path (= MMA N)
+constexpr int kPrefillBlock = 16;  // align block size of the prefill path (MMA N granularity)
+constexpr int kPrefillTileTokens = 256;  // sorted slots per prefill token tile (max MMA N)
 constexpr int kStatusBytes = 256;  // head of every workspace: device status words
 
 // Device status words at the start of a workspace.

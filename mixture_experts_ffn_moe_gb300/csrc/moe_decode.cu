@@ -185,18 +185,30 @@ __global__ void __launch_bounds__(kDecThreads) decode_gemm1_kernel(DecodeArgs d)
 }
 
 // ------------------------------------------------------------------ INT8: requantise h per row
-__global__ void __launch_bounds__(256) requant_h_kernel(DecodeArgs d) {
+// One warp per row: s = max|h| / 127, codes = RNE(h / s) clamped to +-127, stored as fp16.
+__global__ void __launch_bounds__(256) requant_h_kernel(const float* __restrict__ h, const uint32_t* __restrict__ hmax,
+                                                        const int32_t* __restrict__ num_post, int I,
+                                                        __half* __restrict__ hq, float* __restrict__ sh) {
   const int lane = threadIdx.x & 31;
-  const int rows = *d.num_post;
+  const int rows = *num_post;
   const int warps_total = gridDim.x * (blockDim.x >> 5);
   for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps_total) {
-    const float amax = __uint_as_float(d.hmax[r]);
+    const float amax = __uint_as_float(hmax[r]);
     const float s = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 1.0f;
-    const float* hr = reinterpret_cast<const float*>(d.h) + static_cast<size_t>(r) * d.I;
-    __half* qr = d.hq + static_cast<size_t>(r) * d.I;
-    for (int c = lane; c < d.I; c += 32) qr[c] = __float2half_rn(quant_s8_rne(hr[c], s));
-    if (lane == 0) d.sh[r] = s;
+    const float* hr = h + static_cast<size_t>(r) * I;
+    __half* qr = hq + static_cast<size_t>(r) * I;
+    for (int c = lane; c < I; c += 32) qr[c] = __float2half_rn(quant_s8_rne(hr[c], s));
+    if (lane == 0) sh[r] = s;
   }
+}
+
+cudaError_t launch_requant_rows(const void* h, const uint32_t* hmax, const int32_t* num_post, int cap, int I,
+                                __half* hq, float* sh, int num_sms, cudaStream_t s) {
+  int grid = (cap + 7) / 8;
+  if (grid > num_sms * 8) grid = num_sms * 8;
+  if (grid < 1) grid = 1;
+  requant_h_kernel<<<grid, 256, 0, s>>>(static_cast<const float*>(h), hmax, num_post, I, hq, sh);
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ GEMM2: down proj + weighted combine
@@ -300,10 +312,7 @@ static cudaError_t launch_decode_t(const DecodeArgs& d, int num_sms, cudaStream_
   if (err != cudaSuccess) return err;
   hook("decode_gemm1", s);
   if constexpr (WK == MOE_WEIGHT_INT8) {
-    int grid_q = (d.cap + 7) / 8;
-    if (grid_q > num_sms * 8) grid_q = num_sms * 8;
-    requant_h_kernel<<<grid_q, 256, 0, s>>>(d);
-    err = cudaGetLastError();
+    err = launch_requant_rows(d.h, d.hmax, d.num_post, d.cap, d.I, d.hq, d.sh, num_sms, s);
     if (err != cudaSuccess) return err;
     hook("requant_h", s);
   }
