@@ -50,6 +50,8 @@ def workloads():
         "tiny_M16": synth.tiny(),
         # same per-expert work with 32+1 experts: small enough for full ncu captures
         "dsr1_decode_M4_E32": synth.deepseek_r1(4, E=32),
+        "dsr1_prefill_M2048_E32": synth.deepseek_r1(2048, routing="deepseek_zipf", E=32),
+        "qwen3_M1024": synth.qwen3_235b(1024),
     }
 
 

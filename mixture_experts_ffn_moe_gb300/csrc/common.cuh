@@ -14,7 +14,7 @@ namespace gbmoe {
 constexpr int kQBlock = 128;       // FP8 block-scale granularity (both dims)
 constexpr int kDecodeBlock = 8;    // align block size of the decode path (= MMA N)
 constexpr int kPrefillBlock = 16;  // align block size of the prefill path (MMA N granularity)
-constexpr int kPrefillTileTokens = 256;  // sorted slots per prefill token tile (max MMA N)
+constexpr int kPrefillTileTokens = 128;  // sorted slots per prefill token tile (max MMA N)
 constexpr int kStatusBytes = 256;  // head of every workspace: device status words
 
 // Device status words at the start of a workspace.
@@ -26,11 +26,14 @@ struct DeviceStatus {
 // ---------------------------------------------------------------- conversions
 
 // Four E4M3 codes (one 32-bit word, byte 0 first) -> two fp16 pairs; exact.
+// One hardware conversion per 16-bit half (bytes 0,1 -> lo; bytes 2,3 -> hi).
 __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  __half2_raw a = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xFFFFu), __NV_E4M3);
-  __half2_raw b = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16), __NV_E4M3);
-  lo = static_cast<uint32_t>(a.x) | (static_cast<uint32_t>(a.y) << 16);
-  hi = static_cast<uint32_t>(b.x) | (static_cast<uint32_t>(b.y) << 16);
+  asm("{\n\t.reg .b16 l, h;\n\t"
+      "mov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 // Four int8 values (one word, byte 0 first) -> two fp16 pairs; exact.

@@ -3,6 +3,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -42,30 +43,6 @@ struct PrepArgs {
   int n_zero;
 };
 
-// Decode (weight-streaming) path.
-struct DecodeArgs {
-  int M, H, I, E, topk;
-  const __half* xq;             // [M, H] fp16 activations (or int8 codes as fp16)
-  const float* sx;              // [M] per-row activation scale (INT8 path)
-  const uint8_t* w13;           // [E, 2I, H] codes
-  const float* s13;             // FP8 [E, 2I/128, H/128]; INT8 [E, 2I]
-  const uint8_t* w2;            // [E, H, I] codes
-  const float* s2;              // FP8 [E, H/128, I/128]; INT8 [E, H]
-  const float* topk_w;          // [M, topk]
-  const int32_t* sorted_ids;    // [cap]
-  const int32_t* offsets;       // [E + 1]
-  const int32_t* counts;        // [E]
-  const int32_t* active;        // [E]
-  const int32_t* num_active;    // [1]
-  const int32_t* num_post;      // [1]
-  int cap;
-  void* h;                      // FP8: fp16 [cap, I]; INT8: fp32 [cap, I]
-  uint32_t* hmax;               // INT8: [cap] bits of max |h| per row
-  __half* hq;                   // INT8: [cap, I] requantised codes as fp16
-  float* sh;                    // INT8: [cap] per-row scale of hq
-  __nv_bfloat16* out;           // [M, H]
-};
-
 // Called after each kernel of a fused call (per-kernel timing); may be empty.
 struct StageHook {
   void (*fn)(void* ctx, const char* stage, cudaStream_t s) = nullptr;
@@ -89,14 +66,14 @@ struct PrefillArgs {
   const float* sx;       // INT8 GEMM1: per-token activation scale
   const float* sh;       // INT8 GEMM2: per-position scale of the requantised h
   const float* topk_w;   // GEMM2: routing weights per slot
-  void* out;             // GEMM1: h (fp16 FP8 path / fp32 INT8 path); GEMM2: y fp32 (weighted)
+  void* out;             // GEMM1: h by position (fp16 FP8 / fp32 INT8); GEMM2: y fp32 by slot (weighted)
   int out_ld;
   uint32_t* hmax;        // INT8 GEMM1: per-position max |h| (bits)
   DeviceStatus* status;
 };
 
-// Everything the prefill launcher needs (host view of one call).
-struct PrefillPlan {
+// Everything the path launchers need (host view of one call).
+struct LayerPlan {
   int M, H, I, E, topk, cap;
   const __half* xq;
   const float* sx;
@@ -110,22 +87,47 @@ struct PrefillPlan {
   const int32_t* inv_pos;
   const int4* ttiles;
   const int32_t* num_ttiles;
-  __half* act;           // [cap, H] gathered activations
+  __half* act;           // [cap, H] gathered activations (prefill path)
   void* h;               // [cap, I]
   uint32_t* hmax;        // INT8
   __half* hq;            // INT8
   float* sh;             // INT8
-  float* y;              // [cap, H]
+  float* y;              // [M*topk, H] weighted expert outputs by slot
   __nv_bfloat16* out;
+  DeviceStatus* status;
+};
+
+// One skinny grouped GEMM of the decode path (device view).
+struct SkinnyArgs {
+  int K;                 // reduction length: H (GEMM1) or I (GEMM2)
+  int rows_per_expert;   // weight rows of one expert: 2I (GEMM1) or H (GEMM2)
+  int up_offset;         // row offset of the up half inside an expert (GEMM1), else 0
+  int n_rt;              // 64-row tiles per expert (64 gate + 64 up rows for GEMM1)
+  const int4* ttiles;    // token tiles {expert, first position, count <= 8, 0}
+  const int32_t* num_ttiles;
+  const float* wscale;   // FP8: [E, rows/128, K/128]; INT8: [E, rows]
+  const int32_t* sorted_ids;
+  int topk;
+  const __half* b;       // B operand rows: GEMM1 prepared x [M, H] (by token); GEMM2 h [cap, I] (by position)
+  const float* sx;       // INT8 GEMM1: per-token activation scale
+  const float* sh;       // INT8 GEMM2: per-position scale of the requantised h
+  const float* topk_w;   // GEMM2: routing weights per slot
+  void* out;             // GEMM1: h by position (fp16 FP8 / fp32 INT8); GEMM2: y fp32 by slot (weighted)
+  int out_ld;
+  uint32_t* hmax;        // INT8 GEMM1: per-position max |h| (bits)
   DeviceStatus* status;
 };
 
 size_t align_smem_bytes(int E);
 cudaError_t launch_prologue(const AlignArgs& a, const PrepArgs& p, int prep_ctas, cudaStream_t s);
 cudaError_t launch_quant_rows_s8(const PrepArgs& p, cudaStream_t s);
-cudaError_t launch_decode(const DecodeArgs& d, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook);
-size_t decode_gemm2_smem_bytes(int M);
-cudaError_t launch_prefill(const PrefillPlan& P, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook);
+cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook);
+cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook);
+cudaError_t launch_combine(const float* y, const int32_t* inv_pos, int M, int topk, int H, __nv_bfloat16* out,
+                           int num_sms, cudaStream_t s);
+// 2D row-major tensor [outer, inner] of `esize`-byte elements, TMA box [box_outer, box_inner].
+bool encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner,
+                    uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
 cudaError_t launch_requant_rows(const void* h, const uint32_t* hmax, const int32_t* num_post, int cap, int I,
                                 __half* hq, float* sh, int num_sms, cudaStream_t s);
 size_t prefill_smem_bytes();

@@ -97,6 +97,7 @@ struct Layout {
   size_t status = 0, sorted = 0, expert_ids = 0, offsets = 0, counts = 0, active = 0, scalars = 0,
          inv_pos = 0, xq = 0, sx = 0, h = 0, hmax = 0, hq = 0, sh = 0, ttiles = 0, act = 0, y = 0, total = 0;
   size_t max_ttiles = 0;
+  int tile_tokens = 0;
 };
 
 static int choose_path(int M, unsigned flags) {
@@ -130,12 +131,11 @@ static Layout plan(int M, int H, int I, int E, int topk, int kind, unsigned flag
     L.hq = take(L.cap * I * 2);
     L.sh = take(L.cap * 4);
   }
-  if (L.path == MOE_PATH_PREFILL) {
-    L.max_ttiles = static_cast<size_t>(E) + static_cast<size_t>(M) * topk / kPrefillTileTokens + 1;
-    L.ttiles = take(L.max_ttiles * 16);
-    L.act = take(L.cap * H * 2);
-    L.y = take(L.cap * H * 4);
-  }
+  L.tile_tokens = L.path == MOE_PATH_PREFILL ? kPrefillTileTokens : kDecodeBlock;
+  L.max_ttiles = static_cast<size_t>(E) + static_cast<size_t>(M) * topk / L.tile_tokens + 1;
+  L.ttiles = take(L.max_ttiles * 16);
+  if (L.path == MOE_PATH_PREFILL) L.act = take(L.cap * H * 2);
+  L.y = take(static_cast<size_t>(M) * topk * H * 4);
   L.total = o;
   return L;
 }
@@ -194,11 +194,9 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
   a.active = at<int32_t>(ws, L.active);
   a.inv_pos = at<int32_t>(ws, L.inv_pos);
   a.status = at<DeviceStatus>(ws, L.status);
-  if (L.path == MOE_PATH_PREFILL) {
-    a.ttiles = at<int4>(ws, L.ttiles);
-    a.num_ttiles = at<int32_t>(ws, L.scalars) + 2;
-    a.tile_tokens = kPrefillTileTokens;
-  }
+  a.ttiles = at<int4>(ws, L.ttiles);
+  a.num_ttiles = at<int32_t>(ws, L.scalars) + 2;
+  a.tile_tokens = L.tile_tokens;
 
   PrepArgs p{};
   p.x = static_cast<const __nv_bfloat16*>(x);
@@ -213,61 +211,37 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
   if (err != cudaSuccess) return cuda_fail(err, "prologue launch");
   hook("prologue_align_prep", stream);
 
+  LayerPlan P{};
+  P.M = M; P.H = H; P.I = I; P.E = E; P.topk = topk; P.cap = static_cast<int>(L.cap);
+  P.xq = at<__half>(ws, L.xq);
+  P.sx = at<float>(ws, L.sx);
+  P.w13 = static_cast<const uint8_t*>(w13);
+  P.s13 = s13;
+  P.w2 = static_cast<const uint8_t*>(w2);
+  P.s2 = s2;
+  P.topk_w = tw;
+  P.sorted_ids = a.sorted_ids;
+  P.num_post = a.num_post;
+  P.inv_pos = a.inv_pos;
+  P.ttiles = a.ttiles;
+  P.num_ttiles = a.num_ttiles;
+  if (L.path == MOE_PATH_PREFILL) P.act = at<__half>(ws, L.act);
+  P.h = at<void>(ws, L.h);
+  if (kind == MOE_WEIGHT_INT8) {
+    P.hmax = at<uint32_t>(ws, L.hmax);
+    P.hq = at<__half>(ws, L.hq);
+    P.sh = at<float>(ws, L.sh);
+  }
+  P.y = at<float>(ws, L.y);
+  P.out = static_cast<__nv_bfloat16*>(out);
+  P.status = a.status;
   if (L.path == MOE_PATH_PREFILL) {
-    PrefillPlan P{};
-    P.M = M; P.H = H; P.I = I; P.E = E; P.topk = topk; P.cap = static_cast<int>(L.cap);
-    P.xq = at<__half>(ws, L.xq);
-    P.sx = at<float>(ws, L.sx);
-    P.w13 = static_cast<const uint8_t*>(w13);
-    P.s13 = s13;
-    P.w2 = static_cast<const uint8_t*>(w2);
-    P.s2 = s2;
-    P.topk_w = tw;
-    P.sorted_ids = a.sorted_ids;
-    P.num_post = a.num_post;
-    P.inv_pos = a.inv_pos;
-    P.ttiles = a.ttiles;
-    P.num_ttiles = a.num_ttiles;
-    P.act = at<__half>(ws, L.act);
-    P.h = at<void>(ws, L.h);
-    if (kind == MOE_WEIGHT_INT8) {
-      P.hmax = at<uint32_t>(ws, L.hmax);
-      P.hq = at<__half>(ws, L.hq);
-      P.sh = at<float>(ws, L.sh);
-    }
-    P.y = at<float>(ws, L.y);
-    P.out = static_cast<__nv_bfloat16*>(out);
-    P.status = a.status;
     err = launch_prefill(P, kind, sms, stream, hook);
     if (err != cudaSuccess) return cuda_fail(err, "prefill launch");
-    return MOE_OK;
+  } else {
+    err = launch_decode(P, kind, sms, stream, hook);
+    if (err != cudaSuccess) return cuda_fail(err, "decode launch");
   }
-
-  DecodeArgs d{};
-  d.M = M; d.H = H; d.I = I; d.E = E; d.topk = topk;
-  d.xq = at<__half>(ws, L.xq);
-  d.sx = at<float>(ws, L.sx);
-  d.w13 = static_cast<const uint8_t*>(w13);
-  d.s13 = s13;
-  d.w2 = static_cast<const uint8_t*>(w2);
-  d.s2 = s2;
-  d.topk_w = tw;
-  d.sorted_ids = a.sorted_ids;
-  d.offsets = a.expert_offsets;
-  d.counts = a.counts;
-  d.active = a.active;
-  d.num_active = a.num_active;
-  d.num_post = a.num_post;
-  d.cap = static_cast<int>(L.cap);
-  d.h = at<void>(ws, L.h);
-  if (kind == MOE_WEIGHT_INT8) {
-    d.hmax = at<uint32_t>(ws, L.hmax);
-    d.hq = at<__half>(ws, L.hq);
-    d.sh = at<float>(ws, L.sh);
-  }
-  d.out = static_cast<__nv_bfloat16*>(out);
-  err = launch_decode(d, kind, sms, stream, hook);
-  if (err != cudaSuccess) return cuda_fail(err, "decode launch");
   return MOE_OK;
 }
 

@@ -1,4 +1,4 @@
-// Decode path of the fused MoE layer: weight-streaming expert GEMV/skinny GEMMs.
+// Decode path of the fused MoE layer: weight-streaming skinny grouped GEMMs.
 //
 // At decode batch sizes each active expert sees only a few tokens, so the
 // layer is bound by reading the activated experts' weights from HBM once
@@ -6,8 +6,8 @@
 // decode backend", and the bandwidth argument of the SGLang CPU backend
 // write-up, section "(3) FusedMoE").  The math follows the pages:
 //
-//  * GEMM1 uses the A x [B1, B2] = [C1, C2] form: one work item owns 16 gate
-//    rows AND the matching 16 up rows of one expert, so h = SiLU(C1) * C2 is
+//  * GEMM1 uses the A x [B1, B2] = [C1, C2] form: one work item owns 64 gate
+//    rows AND the matching 64 up rows of one expert, so h = SiLU(C1) * C2 is
 //    finished inside the CTA and up_proj is never stored (Xeon 6 / SGLang blog,
 //    section "MoE", SiLU-fusion bullet).
 //  * FP8 weights are expanded to fp16 in registers and never stored wider; the
@@ -16,26 +16,51 @@
 //  * INT8 weights (DA8W8) multiply per-row-quantised activations; the integer
 //    products are exact in fp32 and the per-row x per-channel scales are
 //    applied once at the end.
-//  * GEMM2 owns a slice of 16 output channels for ALL tokens and walks every
-//    active expert, so the weighted top-k combine happens in shared memory in a
-//    fixed order: no atomics, no y buffer, deterministic.
+//  * GEMM2 (down projection) writes each (token, slot) row already times its
+//    routing weight, indexed by slot; a separate pass sums the top-k rows of
+//    every token in slot order (deterministic, no atomics).
 //
-// GB300 mapping: 128-bit streaming loads (L1 no-allocate) of weight rows; the
-// products run on warp-level tensor-core MMA (m16n8k16, weights as the 16-row
-// A operand, up to 8 tokens as the N operand -- a swap-AB skinny GEMM).  The
-// K order inside each 128-wide block is permuted identically for both
-// operands so that every lane's 32 consecutive weight bytes feed its MMA
-// fragments directly, with no shared-memory staging.
+// GB300 mapping.  A work item is (token tile of <= 8 slots of one expert) x
+// (a block of weight rows).  One producer warp streams the item's weight rows
+// through a deep shared-memory ring with TMA (128-byte-swizzled boxes, one
+// 128-wide K block of 128 weight rows per 16 KB stage, ~176 KB in flight per
+// SM).  Eight consumer warps take every stage in order; warp w owns 16-row
+// m-tile w, reads its MMA fragments from shared memory without bank conflicts,
+// expands E4M3 / INT8 to fp16 in registers and runs warp MMA m16n8k16 with the
+// weights as the 16-row A operand and up to 8 tokens as N (swap-AB).  Inside
+// each 128-wide K block the K order is permuted the same way for both
+// operands, so every lane's 32 consecutive weight bytes feed its fragments
+// directly.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
 #include "internal.h"
+#include "sm100_ptx.cuh"
 
 namespace gbmoe {
+namespace dec {
 
-constexpr int kDecWarps = 8;
-constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kRows = 16;  // rows of W per MMA tile
+using namespace sm100;
+
+constexpr int NCW = 8;                        // consumer warps
+constexpr int NUM_THREADS = (NCW + 1) * 32;   // + one producer warp
+constexpr int KBLK = 128;                     // K per stage (one FP8 scale block)
+constexpr int RING_BYTES = 176 * 1024;
+constexpr int BPF = 4;                        // K blocks of B fragments loaded ahead
+constexpr long long kWaitLimit = 4000000000LL;  // ~2 s of SM clocks per wait
+
+template <bool GATED> struct Cfg {
+  // One stage = one 128-wide K block of 128 weight rows (GATED: 64 gate rows and
+  // the matching 64 up rows); consumer warp w owns 16-row m-tile w of every stage.
+  static constexpr int STAGE = NCW * 16 * KBLK;            // 16 KB of weight codes
+  static constexpr int NS = RING_BYTES / STAGE;            // ring stages
+  static constexpr int OFF_RED = RING_BYTES;
+  static constexpr int RED_BYTES = 4 * 4 * 32 * 4;         // up accumulators handed to the gate warps
+  static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
+  static constexpr int SMEM = OFF_BAR + 2 * NS * 8 + 64 + 1024;
+  static constexpr int ROWS = GATED ? 64 : 128;            // output rows per item
+};
 
 __device__ __forceinline__ uint32_t word8(const uint4& a, const uint4& b, int s) {
   switch (s) {
@@ -58,8 +83,8 @@ __device__ __forceinline__ uint32_t word16(const uint4 (&x)[4], int i) {
 // (4s, 4s+1) stand at logical k = 2t, 2t+1 and (4s+2, 4s+3) at 2t+8, 2t+9,
 // and the activations follow the same map, so the sum over K is unchanged.
 template <int WK>
-__device__ __forceinline__ void tile_mma_128(float acc[4], const uint4& ra0, const uint4& ra1,
-                                             const uint4& rb0, const uint4& rb1, const uint4 (&xb)[4]) {
+__device__ __forceinline__ void tile_mma_128(float acc[4], const uint4& ra0, const uint4& ra1, const uint4& rb0,
+                                             const uint4& rb1, const uint4 (&xb)[4]) {
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
     uint32_t a[4];
@@ -69,120 +94,211 @@ __device__ __forceinline__ void tile_mma_128(float acc[4], const uint4& ra0, con
   }
 }
 
-__device__ __forceinline__ void load_x32(uint4 (&xb)[4], const __half* row, size_t kofs, bool valid) {
-  if (valid) {
-    const __half* p = row + kofs;
+__device__ __forceinline__ void load_b32(uint4 (&xb)[4], const __half* row, bool valid) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) xb[i] = ld_v4(p + 8 * i);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) xb[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
+  for (int i = 0; i < 4; ++i) xb[i] = valid ? ld_v4(row + 8 * i) : make_uint4(0u, 0u, 0u, 0u);
 }
 
-// ------------------------------------------------------------------ GEMM1: gate/up + SiLU * mul
-template <int WK>
-__global__ void __launch_bounds__(kDecThreads) decode_gemm1_kernel(DecodeArgs d) {
-  __shared__ float red[kDecWarps][2][4][32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const int tiles = d.I / kRows;
-  const int KB = d.H / kQBlock;
-  const int n_items = *d.num_active * tiles;
-  const int sblk_cols = d.H / kQBlock;
+// Consumer-warps-only barrier (named barrier 1).
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory"); }
 
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int j = item / tiles;
-    const int r0 = (item - j * tiles) * kRows;
-    const int e = d.active[j];
-    const int off = d.offsets[e], cnt = d.counts[e];
-    const uint8_t* wg = d.w13 + (static_cast<size_t>(e) * 2 * d.I + r0) * d.H;
-    const uint8_t* wu = wg + static_cast<size_t>(d.I) * d.H;
-    const uint8_t* wg_g = wg + static_cast<size_t>(g) * d.H;
-    const uint8_t* wg_g8 = wg + static_cast<size_t>(g + 8) * d.H;
-    const uint8_t* wu_g = wu + static_cast<size_t>(g) * d.H;
-    const uint8_t* wu_g8 = wu + static_cast<size_t>(g + 8) * d.H;
-    // FP8 block-scale rows of this tile (16 | 128, so one scale row per tile)
-    const float* sg = d.s13 + (static_cast<size_t>(e) * (2 * d.I / kQBlock) + r0 / kQBlock) * sblk_cols;
-    const float* su = d.s13 + (static_cast<size_t>(e) * (2 * d.I / kQBlock) + (d.I + r0) / kQBlock) * sblk_cols;
+struct Item {
+  int e, pos0, cnt, rt;
+};
 
-    for (int g0 = 0; g0 < cnt; g0 += 8) {
-      const int colg = g0 + g;
-      const int tokg = colg < cnt ? d.sorted_ids[off + colg] / d.topk : -1;
-      const __half* xrow = d.xq + static_cast<size_t>(tokg < 0 ? 0 : tokg) * d.H;
-      float tg[4] = {0.f, 0.f, 0.f, 0.f}, tu[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int kb = warp; kb < KB; kb += kDecWarps) {
-        const size_t kofs = static_cast<size_t>(kb) * kQBlock + t * 32;
-        const uint4 g0a = ld_stream_v4(wg_g + kofs), g0b = ld_stream_v4(wg_g + kofs + 16);
-        const uint4 g8a = ld_stream_v4(wg_g8 + kofs), g8b = ld_stream_v4(wg_g8 + kofs + 16);
-        const uint4 u0a = ld_stream_v4(wu_g + kofs), u0b = ld_stream_v4(wu_g + kofs + 16);
-        const uint4 u8a = ld_stream_v4(wu_g8 + kofs), u8b = ld_stream_v4(wu_g8 + kofs + 16);
-        uint4 xb[4];
-        load_x32(xb, xrow, kofs, tokg >= 0);
-        if constexpr (WK == MOE_WEIGHT_FP8) {
-          float ag[4] = {0.f, 0.f, 0.f, 0.f}, au[4] = {0.f, 0.f, 0.f, 0.f};
-          tile_mma_128<WK>(ag, g0a, g0b, g8a, g8b, xb);
-          tile_mma_128<WK>(au, u0a, u0b, u8a, u8b, xb);
-          const float scg = __ldg(sg + kb), scu = __ldg(su + kb);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) { tg[i] = fmaf(scg, ag[i], tg[i]); tu[i] = fmaf(scu, au[i], tu[i]); }
-        } else {
-          tile_mma_128<WK>(tg, g0a, g0b, g8a, g8b, xb);
-          tile_mma_128<WK>(tu, u0a, u0b, u8a, u8b, xb);
+__device__ __forceinline__ Item get_item(const SkinnyArgs& a, int it) {
+  const int tt = it / a.n_rt;
+  const int4 d = a.ttiles[tt];
+  return Item{d.x, d.y, d.z, it - tt * a.n_rt};
+}
+
+template <int WK, bool GATED>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, SkinnyArgs a) {
+  using C = Cfg<GATED>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + C::NS;
+  int* abort_flag = reinterpret_cast<int*>(empty + C::NS);
+  volatile int* abort = abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = *a.num_ttiles * a.n_rt;
+  const int KB = a.K / KBLK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], NCW);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == NCW) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmap_w);
+      long long seq = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+        const Item im = get_item(a, it);
+        const int row0 = im.e * a.rows_per_expert + im.rt * C::ROWS;
+        for (int kb = 0; kb < KB; ++kb, ++seq) {
+          const int slot = static_cast<int>(seq % C::NS);
+          const uint32_t par = static_cast<uint32_t>((seq / C::NS) & 1);
+          if (!(ok = mbar_wait(&empty[slot], par ^ 1, abort, a.status, kWaitLimit))) break;
+          mbar_arrive_expect_tx(&full[slot], C::STAGE);
+          uint8_t* dst = smem + slot * C::STAGE;
+          if (GATED) {
+            tma_load_2d(dst, &tmap_w, &full[slot], kb * KBLK, row0);
+            tma_load_2d(dst + C::STAGE / 2, &tmap_w, &full[slot], kb * KBLK, row0 + a.up_offset);
+          } else {
+            tma_load_2d(dst, &tmap_w, &full[slot], kb * KBLK, row0);
+          }
         }
       }
+      // never leave with copies in flight into this CTA's shared memory
+      const long long n_last = seq < C::NS ? seq : C::NS;
+      for (long long i = 1; i <= n_last; ++i) {
+        const long long s = seq - i;
+        int dummy = 0;
+        mbar_wait(&full[s % C::NS], static_cast<uint32_t>((s / C::NS) & 1), &dummy, nullptr, kWaitLimit);
+      }
+    }
+    return;  // the producer takes no part in the consumers' named barriers
+  }
+
+  // ------------------------------------------------------------------ consumers
+  // Every consumer warp takes part in every stage, in order (so the ring's phase
+  // parity always refers to the stage it expects); warp w owns m-tile w.
+  const int g = lane >> 2, t = lane & 3;
+  long long seq = 0;
+  bool ok = true;
+  const int kblocks = a.K / kQBlock, rblocks = a.rows_per_expert / kQBlock;
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const Item im = get_item(a, it);
+    const int r0 = im.rt * C::ROWS;  // first output row of the item inside the expert
+    // weight row (inside the expert) of this warp's m-tile
+    const int mrow = GATED ? (warp < 4 ? r0 + warp * 16 : a.up_offset + r0 + (warp - 4) * 16) : r0 + warp * 16;
+    const float* scale_row = a.wscale + (static_cast<size_t>(im.e) * rblocks + mrow / kQBlock) * kblocks;
+    // B operand row of this lane's token column g
+    const bool bvalid = g < im.cnt;
+    const __half* brow;
+    if constexpr (GATED) {
+      const int tok = bvalid ? __ldg(a.sorted_ids + im.pos0 + g) / a.topk : 0;
+      brow = a.b + static_cast<size_t>(tok) * a.K;
+    } else {
+      brow = a.b + static_cast<size_t>(im.pos0 + g) * a.K;  // rows of padded slots are readable
+    }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    // B fragments of the next BPF K blocks are loaded ahead (a ring in registers)
+    uint4 xr[BPF][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) { red[warp][0][i][lane] = tg[i]; red[warp][1][i][lane] = tu[i]; }
-      __syncthreads();
-      if (warp == 0) {
-        float G[4], U[4];
+    for (int d = 0; d < BPF; ++d)
+      if (d < KB) load_b32(xr[d], brow + static_cast<size_t>(d) * KBLK + t * 32, bvalid);
+    for (int kb0 = 0; kb0 < KB; kb0 += BPF) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float a = 0.f, b = 0.f;
+    for (int d = 0; d < BPF; ++d) {
+      const int kb = kb0 + d;
+      if (kb >= KB) break;
+      const uint4 (&xb)[4] = xr[d];
+      const int slot = static_cast<int>(seq % C::NS);
+      if (ok) ok = mbar_wait(&full[slot], static_cast<uint32_t>((seq / C::NS) & 1), abort, a.status, kWaitLimit);
+      if (ok) {
+        // rows warp*16 + g and + 8 of the stage; 16-byte chunk c of row r sits at c ^ (r % 8)
+        const uint8_t* rg = smem + slot * C::STAGE + (warp * 16 + g) * KBLK;
+        const uint8_t* rh = rg + 8 * KBLK;
+        const uint4 ra0 = *reinterpret_cast<const uint4*>(rg + (((2 * t) ^ g) << 4));
+        const uint4 ra1 = *reinterpret_cast<const uint4*>(rg + (((2 * t + 1) ^ g) << 4));
+        const uint4 rb0 = *reinterpret_cast<const uint4*>(rh + (((2 * t) ^ g) << 4));
+        const uint4 rb1 = *reinterpret_cast<const uint4*>(rh + (((2 * t + 1) ^ g) << 4));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);  // the fragments are in registers
+        if constexpr (WK == MOE_WEIGHT_FP8) {
+          float part[4] = {0.f, 0.f, 0.f, 0.f};
+          tile_mma_128<WK>(part, ra0, ra1, rb0, rb1, xb);
+          const float sc = __ldg(scale_row + kb);
 #pragma unroll
-          for (int w = 0; w < kDecWarps; ++w) { a += red[w][0][i][lane]; b += red[w][1][i][lane]; }
-          G[i] = a; U[i] = b;
+          for (int i = 0; i < 4; ++i) acc[i] = fmaf(sc, part[i], acc[i]);
+        } else {
+          tile_mma_128<WK>(acc, ra0, ra1, rb0, rb1, xb);
         }
+      }
+      if (kb + BPF < KB) load_b32(xr[d], brow + static_cast<size_t>(kb + BPF) * KBLK + t * 32, bvalid);
+      ++seq;
+    }
+    }
+
+    // ---- epilogue (fragment: rows g, g+8 x token columns 2t, 2t+1)
+    if constexpr (GATED) {
+      if (warp >= 4) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) red[((warp - 4) * 4 + i) * 32 + lane] = acc[i];
+      }
+      consumers_sync();
+      if (warp < 4) {
         float cmax[2] = {0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
+          const float G = acc[i], U = red[(warp * 4 + i) * 32 + lane];
           const int row = g + ((i & 2) ? 8 : 0);
-          const int col = g0 + 2 * t + (i & 1);
-          const bool valid = col < cnt;
-          const size_t hidx = static_cast<size_t>(off + col) * d.I + r0 + row;
+          const int col = 2 * t + (i & 1);
+          const bool valid = col < im.cnt;
+          const int pos = im.pos0 + col;
+          const int n = r0 + warp * 16 + row;
           if constexpr (WK == MOE_WEIGHT_FP8) {
-            const float h = valid ? silu_f32(G[i]) * U[i] : 0.f;
-            reinterpret_cast<__half*>(d.h)[hidx] = __float2half_rn(h);
+            if (valid) reinterpret_cast<__half*>(a.out)[static_cast<size_t>(pos) * a.out_ld + n] =
+                __float2half_rn(silu_f32(G) * U);
           } else {
             float h = 0.f;
             if (valid) {
-              const int tok = d.sorted_ids[off + col] / d.topk;
-              const float sx = d.sx[tok];
-              const float gv = G[i] * sx * __ldg(d.s13 + static_cast<size_t>(e) * 2 * d.I + r0 + row);
-              const float uv = U[i] * sx * __ldg(d.s13 + static_cast<size_t>(e) * 2 * d.I + d.I + r0 + row);
+              const float sx = __ldg(a.sx + __ldg(a.sorted_ids + pos) / a.topk);
+              const float gv = G * sx * __ldg(a.wscale + static_cast<size_t>(im.e) * a.rows_per_expert + n);
+              const float uv =
+                  U * sx * __ldg(a.wscale + static_cast<size_t>(im.e) * a.rows_per_expert + a.up_offset + n);
               h = silu_f32(gv) * uv;
+              reinterpret_cast<float*>(a.out)[static_cast<size_t>(pos) * a.out_ld + n] = h;
             }
-            reinterpret_cast<float*>(d.h)[hidx] = h;
             cmax[i & 1] = fmaxf(cmax[i & 1], fabsf(h));
           }
         }
         if constexpr (WK == MOE_WEIGHT_INT8) {
-          // max over the 16 rows of each column: reduce across g (lane bits 2..4)
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < 2; ++c) {  // max over the 16 rows of each column (lanes with equal t)
             float v = cmax[c];
             v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
             v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
             v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-            const int col = g0 + 2 * t + c;
-            if (g == 0 && col < cnt) atomicMax(d.hmax + off + col, __float_as_uint(v));
+            const int col = 2 * t + c;
+            if (g == 0 && col < im.cnt) atomicMax(a.hmax + im.pos0 + col, __float_as_uint(v));
           }
         }
       }
-      __syncthreads();
+      consumers_sync();  // red is reused by the next item
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = g + ((i & 2) ? 8 : 0);
+        const int col = 2 * t + (i & 1);
+        if (col < im.cnt) {
+          const int pos = im.pos0 + col;
+          const int n = r0 + warp * 16 + row;
+          const int slot = __ldg(a.sorted_ids + pos);
+          float wgt = __ldg(a.topk_w + slot);
+          if constexpr (WK == MOE_WEIGHT_INT8)
+            wgt *= __ldg(a.sh + pos) * __ldg(a.wscale + static_cast<size_t>(im.e) * a.rows_per_expert + n);
+          reinterpret_cast<float*>(a.out)[static_cast<size_t>(slot) * a.out_ld + n] = acc[i] * wgt;
+        }
+      }
     }
   }
 }
+
+}  // namespace dec
 
 // ------------------------------------------------------------------ INT8: requantise h per row
 // One warp per row: s = max|h| / 127, codes = RNE(h / s) clamped to +-127, stored as fp16.
@@ -211,126 +327,75 @@ cudaError_t launch_requant_rows(const void* h, const uint32_t* hmax, const int32
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------------------ GEMM2: down proj + weighted combine
-template <int WK>
-__global__ void __launch_bounds__(kDecThreads) decode_gemm2_kernel(DecodeArgs d) {
-  extern __shared__ float acc_s[];  // [kDecWarps][M][16]
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const int KB2 = d.I / kQBlock;
-  const int n_items = *d.num_active * KB2;
-  const int M = d.M;
-  const __half* hsrc = (WK == MOE_WEIGHT_FP8) ? reinterpret_cast<const __half*>(d.h) : d.hq;
-
-  for (int tile = blockIdx.x; tile < d.H / kRows; tile += gridDim.x) {
-    const int n0 = tile * kRows;
-    for (int i = threadIdx.x; i < kDecWarps * M * kRows; i += kDecThreads) acc_s[i] = 0.f;
-    __syncthreads();
-    float* my = acc_s + warp * M * kRows;
-    for (int it = warp; it < n_items; it += kDecWarps) {
-      const int j = it / KB2, kb = it - j * KB2;
-      const int e = d.active[j];
-      const int off = d.offsets[e], cnt = d.counts[e];
-      const uint8_t* w = d.w2 + (static_cast<size_t>(e) * d.H + n0) * d.I;
-      const size_t kofs = static_cast<size_t>(kb) * kQBlock + t * 32;
-      const uint4 a0 = ld_stream_v4(w + static_cast<size_t>(g) * d.I + kofs);
-      const uint4 a1 = ld_stream_v4(w + static_cast<size_t>(g) * d.I + kofs + 16);
-      const uint4 b0 = ld_stream_v4(w + static_cast<size_t>(g + 8) * d.I + kofs);
-      const uint4 b1 = ld_stream_v4(w + static_cast<size_t>(g + 8) * d.I + kofs + 16);
-      float sc = 1.f;
-      if constexpr (WK == MOE_WEIGHT_FP8)
-        sc = __ldg(d.s2 + (static_cast<size_t>(e) * (d.H / kQBlock) + n0 / kQBlock) * KB2 + kb);
-      for (int g0 = 0; g0 < cnt; g0 += 8) {
-        uint4 xb[4];
-        // h rows of padded slots are zero, so every row in [off, off + padded) is readable
-        load_x32(xb, hsrc + static_cast<size_t>(off + g0 + g) * d.I, kofs, true);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_mma_128<WK>(acc, a0, a1, b0, b1, xb);
-        float v[4];
-        int tok[2];
-        bool ok[2];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int col = g0 + 2 * t + c;
-          ok[c] = col < cnt;
-          tok[c] = 0;
-          float wgt = 0.f, srow = 1.f;
-          if (ok[c]) {
-            const int slot = d.sorted_ids[off + col];
-            tok[c] = slot / d.topk;
-            wgt = d.topk_w[slot];
-            if constexpr (WK == MOE_WEIGHT_INT8) srow = d.sh[off + col];
-          }
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int i = hh * 2 + c;
-            float s = sc * srow * wgt;
-            if constexpr (WK == MOE_WEIGHT_INT8)
-              s *= __ldg(d.s2 + static_cast<size_t>(e) * d.H + n0 + g + 8 * hh);
-            v[i] = acc[i] * s;
-          }
-        }
-        // fixed-order accumulation: lanes with equal t touch distinct rows
-#pragma unroll
-        for (int tt = 0; tt < 4; ++tt) {
-          if (t == tt) {
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              if (ok[c]) {
-                my[tok[c] * kRows + g] += v[c];
-                my[tok[c] * kRows + g + 8] += v[2 + c];
-              }
-            }
-          }
-          __syncwarp();
-        }
-      }
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < M * kRows; i += kDecThreads) {
-      float s = 0.f;
-#pragma unroll
-      for (int w = 0; w < kDecWarps; ++w) s += acc_s[w * M * kRows + i];
-      const int tok = i / kRows, row = i - tok * kRows;
-      d.out[static_cast<size_t>(tok) * d.H + n0 + row] = __float2bfloat16_rn(s);
-    }
-    __syncthreads();
-  }
+template <int WK, bool GATED>
+static cudaError_t launch_skinny(const SkinnyArgs& a, const void* w, uint64_t w_rows, int num_sms, cudaStream_t s) {
+  using C = dec::Cfg<GATED>;
+  CUtensorMap mw;
+  if (!encode_tmap_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, static_cast<uint64_t>(a.K), w_rows, dec::KBLK,
+                      C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  auto kern = dec::skinny_gemm_kernel<WK, GATED>;
+  cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM, 8 + WK * 2 + (GATED ? 1 : 0));
+  if (err != cudaSuccess) return err;
+  kern<<<num_sms, dec::NUM_THREADS, C::SMEM, s>>>(mw, a);
+  return cudaGetLastError();
 }
 
-size_t decode_gemm2_smem_bytes(int M) { return static_cast<size_t>(kDecWarps) * M * kRows * sizeof(float); }
-
-template <int WK>
-static cudaError_t launch_decode_t(const DecodeArgs& d, int num_sms, cudaStream_t s, const StageHook& hook) {
-  const int max_active = d.E < d.M * d.topk ? d.E : d.M * d.topk;
-  const int items1 = max_active * (d.I / kRows);
-  int grid1 = num_sms * 4;
-  if (items1 < grid1) grid1 = items1;
-  if (grid1 <= 0) return cudaSuccess;
-  decode_gemm1_kernel<WK><<<grid1, kDecThreads, 0, s>>>(d);
-  cudaError_t err = cudaGetLastError();
+cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook) {
+  SkinnyArgs g1{};
+  g1.K = P.H;
+  g1.rows_per_expert = 2 * P.I;
+  g1.up_offset = P.I;
+  g1.n_rt = P.I / dec::Cfg<true>::ROWS;
+  g1.ttiles = P.ttiles;
+  g1.num_ttiles = P.num_ttiles;
+  g1.wscale = P.s13;
+  g1.sorted_ids = P.sorted_ids;
+  g1.topk = P.topk;
+  g1.b = P.xq;
+  g1.sx = P.sx;
+  g1.out = P.h;
+  g1.out_ld = P.I;
+  g1.hmax = P.hmax;
+  g1.status = P.status;
+  cudaError_t err =
+      weight_kind == MOE_WEIGHT_FP8
+          ? launch_skinny<MOE_WEIGHT_FP8, true>(g1, P.w13, static_cast<uint64_t>(P.E) * 2 * P.I, num_sms, s)
+          : launch_skinny<MOE_WEIGHT_INT8, true>(g1, P.w13, static_cast<uint64_t>(P.E) * 2 * P.I, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("decode_gemm1", s);
-  if constexpr (WK == MOE_WEIGHT_INT8) {
-    err = launch_requant_rows(d.h, d.hmax, d.num_post, d.cap, d.I, d.hq, d.sh, num_sms, s);
+  const __half* b2 = static_cast<const __half*>(P.h);
+  if (weight_kind == MOE_WEIGHT_INT8) {
+    err = launch_requant_rows(P.h, P.hmax, P.num_post, P.cap, P.I, P.hq, P.sh, num_sms, s);
     if (err != cudaSuccess) return err;
     hook("requant_h", s);
+    b2 = P.hq;
   }
-  const size_t smem2 = decode_gemm2_smem_bytes(d.M);
-  err = set_smem_limit_once(reinterpret_cast<const void*>(decode_gemm2_kernel<WK>),
-                            static_cast<int>(decode_gemm2_smem_bytes(MOE_MAX_DECODE_TOKENS)), 1 + WK);
+  SkinnyArgs g2{};
+  g2.K = P.I;
+  g2.rows_per_expert = P.H;
+  g2.up_offset = 0;
+  g2.n_rt = (P.H + dec::Cfg<false>::ROWS - 1) / dec::Cfg<false>::ROWS;
+  g2.ttiles = P.ttiles;
+  g2.num_ttiles = P.num_ttiles;
+  g2.wscale = P.s2;
+  g2.sorted_ids = P.sorted_ids;
+  g2.topk = P.topk;
+  g2.b = b2;
+  g2.sh = P.sh;
+  g2.topk_w = P.topk_w;
+  g2.out = P.y;
+  g2.out_ld = P.H;
+  g2.status = P.status;
+  err = weight_kind == MOE_WEIGHT_FP8
+            ? launch_skinny<MOE_WEIGHT_FP8, false>(g2, P.w2, static_cast<uint64_t>(P.E) * P.H, num_sms, s)
+            : launch_skinny<MOE_WEIGHT_INT8, false>(g2, P.w2, static_cast<uint64_t>(P.E) * P.H, num_sms, s);
   if (err != cudaSuccess) return err;
-  decode_gemm2_kernel<WK><<<d.H / kRows, kDecThreads, smem2, s>>>(d);
-  err = cudaGetLastError();
+  hook("decode_gemm2", s);
+  err = launch_combine(P.y, P.inv_pos, P.M, P.topk, P.H, P.out, num_sms, s);
   if (err != cudaSuccess) return err;
-  hook("decode_gemm2_combine", s);
+  hook("combine", s);
   return cudaSuccess;
-}
-
-cudaError_t launch_decode(const DecodeArgs& d, int weight_kind, int num_sms, cudaStream_t s,
-                          const StageHook& hook) {
-  return weight_kind == MOE_WEIGHT_FP8 ? launch_decode_t<MOE_WEIGHT_FP8>(d, num_sms, s, hook)
-                                       : launch_decode_t<MOE_WEIGHT_INT8>(d, num_sms, s, hook);
 }
 
 }  // namespace gbmoe
