@@ -127,6 +127,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = *a.num_ttiles * a.n_rt;
   const int KB = a.K / KBLK;
+  // Item order (measured): GEMM1 items go round-robin over the CTAs; GEMM2 items
+  // go in contiguous runs per CTA, so a CTA streams adjacent weight rows.
+  const int it_begin =
+      GATED ? static_cast<int>(blockIdx.x) : static_cast<int>(static_cast<long long>(n_items) * blockIdx.x / gridDim.x);
+  const int it_end =
+      GATED ? n_items : static_cast<int>(static_cast<long long>(n_items) * (blockIdx.x + 1) / gridDim.x);
+  const int it_step = GATED ? static_cast<int>(gridDim.x) : 1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NS; ++i) {
@@ -144,7 +151,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       prefetch_tmap(&tmap_w);
       long long seq = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      for (int it = it_begin; it < it_end && ok; it += it_step) {
         const Item im = get_item(a, it);
         const int row0 = im.e * a.rows_per_expert + im.rt * C::ROWS;
         for (int kb = 0; kb < KB; ++kb, ++seq) {
@@ -179,24 +186,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   long long seq = 0;
   bool ok = true;
   const int kblocks = a.K / kQBlock, rblocks = a.rows_per_expert / kQBlock;
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+  // B operand row of this lane's token column g (GEMM1: x by token; GEMM2: h by position)
+  auto b_row = [&](const Item& x, bool& valid) -> const __half* {
+    valid = g < x.cnt;
+    if constexpr (GATED) {
+      const int tok = valid ? __ldg(a.sorted_ids + x.pos0 + g) / a.topk : 0;
+      return a.b + static_cast<size_t>(tok) * a.K;
+    } else {
+      return a.b + static_cast<size_t>(x.pos0 + g) * a.K;  // rows of padded slots are readable
+    }
+  };
+  // B fragments of the next BPF K blocks are loaded ahead (a ring in registers)
+  uint4 xr[BPF][4];
+  for (int it = it_begin; it < it_end; it += it_step) {
     const Item im = get_item(a, it);
     const int r0 = im.rt * C::ROWS;  // first output row of the item inside the expert
     // weight row (inside the expert) of this warp's m-tile
     const int mrow = GATED ? (warp < 4 ? r0 + warp * 16 : a.up_offset + r0 + (warp - 4) * 16) : r0 + warp * 16;
     const float* scale_row = a.wscale + (static_cast<size_t>(im.e) * rblocks + mrow / kQBlock) * kblocks;
-    // B operand row of this lane's token column g
-    const bool bvalid = g < im.cnt;
-    const __half* brow;
-    if constexpr (GATED) {
-      const int tok = bvalid ? __ldg(a.sorted_ids + im.pos0 + g) / a.topk : 0;
-      brow = a.b + static_cast<size_t>(tok) * a.K;
-    } else {
-      brow = a.b + static_cast<size_t>(im.pos0 + g) * a.K;  // rows of padded slots are readable
-    }
+    bool bvalid;
+    const __half* brow = b_row(im, bvalid);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    // B fragments of the next BPF K blocks are loaded ahead (a ring in registers)
-    uint4 xr[BPF][4];
 #pragma unroll
     for (int d = 0; d < BPF; ++d)
       if (d < KB) load_b32(xr[d], brow + static_cast<size_t>(d) * KBLK + t * 32, bvalid);
@@ -301,29 +311,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }  // namespace dec
 
 // ------------------------------------------------------------------ INT8: requantise h per row
-// One warp per row: s = max|h| / 127, codes = RNE(h / s) clamped to +-127, stored as fp16.
-__global__ void __launch_bounds__(256) requant_h_kernel(const float* __restrict__ h, const uint32_t* __restrict__ hmax,
+// One CTA per row: s = max|h| / 127, codes = RNE(h / s) clamped to +-127, stored as fp16.
+// I is a multiple of 128, so every thread moves whole 4-element vectors.
+__global__ void __launch_bounds__(128) requant_h_kernel(const float* __restrict__ h, const uint32_t* __restrict__ hmax,
                                                         const int32_t* __restrict__ num_post, int I,
                                                         __half* __restrict__ hq, float* __restrict__ sh) {
-  const int lane = threadIdx.x & 31;
   const int rows = *num_post;
-  const int warps_total = gridDim.x * (blockDim.x >> 5);
-  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps_total) {
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     const float amax = __uint_as_float(hmax[r]);
     const float s = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 1.0f;
-    const float* hr = h + static_cast<size_t>(r) * I;
-    __half* qr = hq + static_cast<size_t>(r) * I;
-    for (int c = lane; c < I; c += 32) qr[c] = __float2half_rn(quant_s8_rne(hr[c], s));
-    if (lane == 0) sh[r] = s;
+    const float4* hr = reinterpret_cast<const float4*>(h + static_cast<size_t>(r) * I);
+    uint2* qr = reinterpret_cast<uint2*>(hq + static_cast<size_t>(r) * I);
+    for (int c = threadIdx.x; c < I / 4; c += blockDim.x) {
+      const float4 v = __ldg(hr + c);
+      qr[c] = make_uint2(pack_half2(quant_s8_rne(v.x, s), quant_s8_rne(v.y, s)),
+                         pack_half2(quant_s8_rne(v.z, s), quant_s8_rne(v.w, s)));
+    }
+    if (threadIdx.x == 0) sh[r] = s;
   }
 }
 
 cudaError_t launch_requant_rows(const void* h, const uint32_t* hmax, const int32_t* num_post, int cap, int I,
                                 __half* hq, float* sh, int num_sms, cudaStream_t s) {
-  int grid = (cap + 7) / 8;
-  if (grid > num_sms * 8) grid = num_sms * 8;
+  int grid = cap < num_sms * 8 ? cap : num_sms * 8;
   if (grid < 1) grid = 1;
-  requant_h_kernel<<<grid, 256, 0, s>>>(static_cast<const float*>(h), hmax, num_post, I, hq, sh);
+  requant_h_kernel<<<grid, 128, 0, s>>>(static_cast<const float*>(h), hmax, num_post, I, hq, sh);
   return cudaGetLastError();
 }
 

@@ -461,11 +461,19 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const int t = static_cast<int>(i / q), c = static_cast<int>(i - static_cast<long long>(t) * q);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < topk; ++k) {
-      const int slot = t * topk + k;
-      if (__ldg(inv_pos + slot) < 0) continue;
-      const float4 v = __ldg(reinterpret_cast<const float4*>(y + static_cast<size_t>(slot) * H) + c);
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    for (int k0 = 0; k0 < topk; k0 += 8) {
+      float4 v[8];  // all loads of a group in flight together, then summed in slot order
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int k = k0 + j, slot = t * topk + k;
+        v[j] = (k < topk && __ldg(inv_pos + slot) >= 0)
+                   ? __ldg(reinterpret_cast<const float4*>(y + static_cast<size_t>(slot) * H) + c)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        acc.x += v[j].x; acc.y += v[j].y; acc.z += v[j].z; acc.w += v[j].w;
+      }
     }
     __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
     uint2 pk = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
