@@ -19,7 +19,6 @@ from __future__ import annotations
 
 import argparse
 import hashlib
-import glob
 import json
 import os
 import statistics
@@ -58,10 +57,20 @@ def workloads():
 DEFAULT_WORKLOAD = "dsr1_decode_M4"
 
 
-def source_hash() -> str:
+KERNEL_SOURCES = {  # kernel -> the source files that define it
+    "decode_gemm1": "moe_decode.cu", "decode_gemm2": "moe_decode.cu",
+    "prefill_gemm1": "moe_prefill.cu", "prefill_gemm2": "moe_prefill.cu",
+}
+
+
+def source_hash(kernel: str) -> str:
+    """Hash of the kernel's own source file and the headers it includes."""
+    csrc = os.path.join(ROOT, "mixture_experts_ffn_moe_gb300", "csrc")
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "mixture_experts_ffn_moe_gb300", "csrc", "*"))):
-        h.update(open(p, "rb").read())
+    for name in (KERNEL_SOURCES.get(kernel, ""), "common.cuh", "sm100_ptx.cuh", "internal.h"):
+        path = os.path.join(csrc, name)
+        if name and os.path.exists(path):
+            h.update(open(path, "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -81,7 +90,7 @@ def ncu_traffic(workload: str, kernel: str):
         return None
     d = json.load(open(p))
     rec = d.get(workload, {}).get(kernel)
-    if not rec or rec.get("source_hash") != source_hash():
+    if not rec or rec.get("source_hash") != source_hash(kernel):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -106,7 +115,7 @@ def stage_work(shape, ids: torch.Tensor):
     f2 = 2 * valid * H * I
     return {
         "decode_gemm1": (active * (2 * I * H + s13) + M * H * 2 + valid * I * 2, f1),
-        "decode_gemm2_combine": (active * (H * I + s2) + valid * I * 2 + M * H * 2, f2),
+        "decode_gemm2": (active * (H * I + s2) + valid * I * 2 + valid * H * 4, f2),
         "prefill_gemm1": (active * (2 * I * H + s13) + valid * H * 2 + valid * I * 2, f1),
         "prefill_gemm2": (active * (H * I + s2) + valid * I * 2 + valid * H * 4, f2),
     }

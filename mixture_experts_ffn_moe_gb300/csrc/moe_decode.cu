@@ -46,13 +46,17 @@ using namespace sm100;
 constexpr int NCW = 8;                        // consumer warps
 constexpr int NUM_THREADS = (NCW + 1) * 32;   // + one producer warp
 constexpr int KBLK = 128;                     // K per stage (one FP8 scale block)
-constexpr int RING_BYTES = 176 * 1024;
-constexpr int BPF = 4;                        // K blocks of B fragments loaded ahead
+
 constexpr long long kWaitLimit = 4000000000LL;  // ~2 s of SM clocks per wait
 
-template <bool GATED> struct Cfg {
+// OCC resident CTAs per SM (measured): 2 CTAs with an 80 KB ring each and B
+// fragments two K blocks ahead when there are few work items, 3 CTAs with
+// 48 KB rings and one block ahead otherwise -- more warps hide more latency.
+template <bool GATED, int OCC> struct Cfg {
   // One stage = one 128-wide K block of 128 weight rows (GATED: 64 gate rows and
   // the matching 64 up rows); consumer warp w owns 16-row m-tile w of every stage.
+  static constexpr int RING_BYTES = OCC == 2 ? 80 * 1024 : 48 * 1024;
+  static constexpr int BPF = OCC == 2 ? 2 : 1;             // K blocks of B fragments loaded ahead
   static constexpr int STAGE = NCW * 16 * KBLK;            // 16 KB of weight codes
   static constexpr int NS = RING_BYTES / STAGE;            // ring stages
   static constexpr int OFF_RED = RING_BYTES;
@@ -82,16 +86,29 @@ __device__ __forceinline__ uint32_t word16(const uint4 (&x)[4], int i) {
 // (xb, fp16).  MMA step s uses bytes [4s, 4s+4) of each chunk: the pairs
 // (4s, 4s+1) stand at logical k = 2t, 2t+1 and (4s+2, 4s+3) at 2t+8, 2t+9,
 // and the activations follow the same map, so the sum over K is unchanged.
+// Even and odd MMA steps accumulate into two independent chains (acc0, acc1) so
+// that consecutive tensor-core instructions do not wait on each other.
 template <int WK>
-__device__ __forceinline__ void tile_mma_128(float acc[4], const uint4& ra0, const uint4& ra1, const uint4& rb0,
-                                             const uint4& rb1, const uint4 (&xb)[4]) {
+__device__ __forceinline__ void tile_mma_128(float acc0[4], float acc1[4], const uint4& ra0, const uint4& ra1,
+                                             const uint4& rb0, const uint4& rb1, const uint4 (&xb)[4]) {
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
     uint32_t a[4];
     w8x4_to_f16x4<WK>(word8(ra0, ra1, s), a[0], a[2]);
     w8x4_to_f16x4<WK>(word8(rb0, rb1, s), a[1], a[3]);
-    mma_f16_16816(acc, a, word16(xb, 2 * s), word16(xb, 2 * s + 1));
+    mma_f16_16816((s & 1) ? acc1 : acc0, a, word16(xb, 2 * s), word16(xb, 2 * s + 1));
   }
+}
+
+// Shared-memory fragment load that the compiler may not repeat or defer: the ring
+// slot is released right after these loads.
+__device__ __forceinline__ uint4 lds_v4_once(const void* p) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p)))
+               : "memory");
+  return r;
 }
 
 __device__ __forceinline__ void load_b32(uint4 (&xb)[4], const __half* row, bool valid) {
@@ -112,10 +129,11 @@ __device__ __forceinline__ Item get_item(const SkinnyArgs& a, int it) {
   return Item{d.x, d.y, d.z, it - tt * a.n_rt};
 }
 
-template <int WK, bool GATED>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+template <int WK, bool GATED, int OCC>
+__global__ void __launch_bounds__(NUM_THREADS, OCC)
     skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, SkinnyArgs a) {
-  using C = Cfg<GATED>;
+  using C = Cfg<GATED, OCC>;
+  constexpr int BPF = C::BPF;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
@@ -150,13 +168,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       prefetch_tmap(&tmap_w);
       long long seq = 0;
+      int slot = 0;
+      uint32_t par = 0;
       bool ok = true;
       for (int it = it_begin; it < it_end && ok; it += it_step) {
         const Item im = get_item(a, it);
         const int row0 = im.e * a.rows_per_expert + im.rt * C::ROWS;
         for (int kb = 0; kb < KB; ++kb, ++seq) {
-          const int slot = static_cast<int>(seq % C::NS);
-          const uint32_t par = static_cast<uint32_t>((seq / C::NS) & 1);
           if (!(ok = mbar_wait(&empty[slot], par ^ 1, abort, a.status, kWaitLimit))) break;
           mbar_arrive_expect_tx(&full[slot], C::STAGE);
           uint8_t* dst = smem + slot * C::STAGE;
@@ -166,6 +184,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else {
             tma_load_2d(dst, &tmap_w, &full[slot], kb * KBLK, row0);
           }
+          if (++slot == C::NS) { slot = 0; par ^= 1; }
         }
       }
       // never leave with copies in flight into this CTA's shared memory
@@ -183,7 +202,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // Every consumer warp takes part in every stage, in order (so the ring's phase
   // parity always refers to the stage it expects); warp w owns m-tile w.
   const int g = lane >> 2, t = lane & 3;
-  long long seq = 0;
+  int slot = 0;          // ring slot of the next stage
+  uint32_t phase = 0;    // its phase parity
   bool ok = true;
   const int kblocks = a.K / kQBlock, rblocks = a.rows_per_expert / kQBlock;
   // B operand row of this lane's token column g (GEMM1: x by token; GEMM2: h by position)
@@ -206,43 +226,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float* scale_row = a.wscale + (static_cast<size_t>(im.e) * rblocks + mrow / kQBlock) * kblocks;
     bool bvalid;
     const __half* brow = b_row(im, bvalid);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+    float scr[BPF];  // FP8 block scales of the prefetched K blocks
 #pragma unroll
-    for (int d = 0; d < BPF; ++d)
-      if (d < KB) load_b32(xr[d], brow + static_cast<size_t>(d) * KBLK + t * 32, bvalid);
+    for (int d = 0; d < BPF; ++d) {
+      if (d < KB) {
+        load_b32(xr[d], brow + static_cast<size_t>(d) * KBLK + t * 32, bvalid);
+        if constexpr (WK == MOE_WEIGHT_FP8) scr[d] = __ldg(scale_row + d);
+      }
+    }
     for (int kb0 = 0; kb0 < KB; kb0 += BPF) {
 #pragma unroll
     for (int d = 0; d < BPF; ++d) {
       const int kb = kb0 + d;
       if (kb >= KB) break;
       const uint4 (&xb)[4] = xr[d];
-      const int slot = static_cast<int>(seq % C::NS);
-      if (ok) ok = mbar_wait(&full[slot], static_cast<uint32_t>((seq / C::NS) & 1), abort, a.status, kWaitLimit);
+      if (ok) ok = mbar_wait(&full[slot], phase, abort, a.status, kWaitLimit);
       if (ok) {
         // rows warp*16 + g and + 8 of the stage; 16-byte chunk c of row r sits at c ^ (r % 8)
         const uint8_t* rg = smem + slot * C::STAGE + (warp * 16 + g) * KBLK;
         const uint8_t* rh = rg + 8 * KBLK;
-        const uint4 ra0 = *reinterpret_cast<const uint4*>(rg + (((2 * t) ^ g) << 4));
-        const uint4 ra1 = *reinterpret_cast<const uint4*>(rg + (((2 * t + 1) ^ g) << 4));
-        const uint4 rb0 = *reinterpret_cast<const uint4*>(rh + (((2 * t) ^ g) << 4));
-        const uint4 rb1 = *reinterpret_cast<const uint4*>(rh + (((2 * t + 1) ^ g) << 4));
+        const uint4 ra0 = lds_v4_once(rg + (((2 * t) ^ g) << 4));
+        const uint4 ra1 = lds_v4_once(rg + (((2 * t + 1) ^ g) << 4));
+        const uint4 rb0 = lds_v4_once(rh + (((2 * t) ^ g) << 4));
+        const uint4 rb1 = lds_v4_once(rh + (((2 * t + 1) ^ g) << 4));
+        // the fragments are in registers; order these generic-proxy reads before the
+        // TMA (async proxy) that will overwrite the slot once every warp has released it
+        fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);  // the fragments are in registers
+        if (lane == 0) mbar_arrive(&empty[slot]);
         if constexpr (WK == MOE_WEIGHT_FP8) {
-          float part[4] = {0.f, 0.f, 0.f, 0.f};
-          tile_mma_128<WK>(part, ra0, ra1, rb0, rb1, xb);
-          const float sc = __ldg(scale_row + kb);
+          float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
+          tile_mma_128<WK>(p0, p1, ra0, ra1, rb0, rb1, xb);
+          const float sc = scr[d];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) acc[i] = fmaf(sc, part[i], acc[i]);
+          for (int i = 0; i < 4; ++i) acc[i] = fmaf(sc, p0[i] + p1[i], acc[i]);
         } else {
-          tile_mma_128<WK>(acc, ra0, ra1, rb0, rb1, xb);
+          tile_mma_128<WK>(acc, acc1, ra0, ra1, rb0, rb1, xb);
         }
       }
-      if (kb + BPF < KB) load_b32(xr[d], brow + static_cast<size_t>(kb + BPF) * KBLK + t * 32, bvalid);
-      ++seq;
+      if (kb + BPF < KB) {
+        load_b32(xr[d], brow + static_cast<size_t>(kb + BPF) * KBLK + t * 32, bvalid);
+        if constexpr (WK == MOE_WEIGHT_FP8) scr[d] = __ldg(scale_row + kb + BPF);
+      }
+      if (++slot == C::NS) { slot = 0; phase ^= 1; }
     }
     }
 
+    if constexpr (WK == MOE_WEIGHT_INT8) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] += acc1[i];
+    }
     // ---- epilogue (fragment: rows g, g+8 x token columns 2t, 2t+1)
     if constexpr (GATED) {
       if (warp >= 4) {
@@ -339,26 +373,39 @@ cudaError_t launch_requant_rows(const void* h, const uint32_t* hmax, const int32
   return cudaGetLastError();
 }
 
-template <int WK, bool GATED>
-static cudaError_t launch_skinny(const SkinnyArgs& a, const void* w, uint64_t w_rows, int num_sms, cudaStream_t s) {
-  using C = dec::Cfg<GATED>;
+template <int WK, bool GATED, int OCC>
+static cudaError_t launch_skinny_occ(const SkinnyArgs& a, const void* w, uint64_t w_rows, int num_sms,
+                                     cudaStream_t s) {
+  using C = dec::Cfg<GATED, OCC>;
   CUtensorMap mw;
   if (!encode_tmap_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, static_cast<uint64_t>(a.K), w_rows, dec::KBLK,
                       C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  auto kern = dec::skinny_gemm_kernel<WK, GATED>;
-  cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM, 8 + WK * 2 + (GATED ? 1 : 0));
+  auto kern = dec::skinny_gemm_kernel<WK, GATED, OCC>;
+  cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM,
+                                        8 + WK * 4 + (GATED ? 2 : 0) + (OCC == 3 ? 1 : 0));
   if (err != cudaSuccess) return err;
-  kern<<<num_sms, dec::NUM_THREADS, C::SMEM, s>>>(mw, a);
+  kern<<<OCC * num_sms, dec::NUM_THREADS, C::SMEM, s>>>(mw, a);
   return cudaGetLastError();
 }
 
+// max_items: an upper bound of the work items the launch can see.
+template <int WK, bool GATED>
+static cudaError_t launch_skinny(const SkinnyArgs& a, const void* w, uint64_t w_rows, long long max_items,
+                                 int num_sms, cudaStream_t s) {
+  return max_items >= 3LL * num_sms ? launch_skinny_occ<WK, GATED, 3>(a, w, w_rows, num_sms, s)
+                                    : launch_skinny_occ<WK, GATED, 2>(a, w, w_rows, num_sms, s);
+}
+
 cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook) {
+  // token tiles: at most one per (expert, 8 slots) -- bounded by min(E, slots) + slots / 8
+  const long long slots = static_cast<long long>(P.M) * P.topk;
+  const long long max_tiles = (slots < P.E ? slots : P.E) + slots / kDecodeBlock;
   SkinnyArgs g1{};
   g1.K = P.H;
   g1.rows_per_expert = 2 * P.I;
   g1.up_offset = P.I;
-  g1.n_rt = P.I / dec::Cfg<true>::ROWS;
+  g1.n_rt = P.I / dec::Cfg<true, 2>::ROWS;
   g1.ttiles = P.ttiles;
   g1.num_ttiles = P.num_ttiles;
   g1.wscale = P.s13;
@@ -372,8 +419,10 @@ cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cuda
   g1.status = P.status;
   cudaError_t err =
       weight_kind == MOE_WEIGHT_FP8
-          ? launch_skinny<MOE_WEIGHT_FP8, true>(g1, P.w13, static_cast<uint64_t>(P.E) * 2 * P.I, num_sms, s)
-          : launch_skinny<MOE_WEIGHT_INT8, true>(g1, P.w13, static_cast<uint64_t>(P.E) * 2 * P.I, num_sms, s);
+          ? launch_skinny<MOE_WEIGHT_FP8, true>(g1, P.w13, static_cast<uint64_t>(P.E) * 2 * P.I,
+                                                max_tiles * g1.n_rt, num_sms, s)
+          : launch_skinny<MOE_WEIGHT_INT8, true>(g1, P.w13, static_cast<uint64_t>(P.E) * 2 * P.I,
+                                                 max_tiles * g1.n_rt, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("decode_gemm1", s);
   const __half* b2 = static_cast<const __half*>(P.h);
@@ -387,7 +436,7 @@ cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cuda
   g2.K = P.I;
   g2.rows_per_expert = P.H;
   g2.up_offset = 0;
-  g2.n_rt = (P.H + dec::Cfg<false>::ROWS - 1) / dec::Cfg<false>::ROWS;
+  g2.n_rt = (P.H + dec::Cfg<false, 2>::ROWS - 1) / dec::Cfg<false, 2>::ROWS;
   g2.ttiles = P.ttiles;
   g2.num_ttiles = P.num_ttiles;
   g2.wscale = P.s2;
@@ -400,8 +449,10 @@ cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cuda
   g2.out_ld = P.H;
   g2.status = P.status;
   err = weight_kind == MOE_WEIGHT_FP8
-            ? launch_skinny<MOE_WEIGHT_FP8, false>(g2, P.w2, static_cast<uint64_t>(P.E) * P.H, num_sms, s)
-            : launch_skinny<MOE_WEIGHT_INT8, false>(g2, P.w2, static_cast<uint64_t>(P.E) * P.H, num_sms, s);
+            ? launch_skinny<MOE_WEIGHT_FP8, false>(g2, P.w2, static_cast<uint64_t>(P.E) * P.H,
+                                                  max_tiles * g2.n_rt, num_sms, s)
+            : launch_skinny<MOE_WEIGHT_INT8, false>(g2, P.w2, static_cast<uint64_t>(P.E) * P.H,
+                                                   max_tiles * g2.n_rt, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("decode_gemm2", s);
   err = launch_combine(P.y, P.inv_pos, P.M, P.topk, P.H, P.out, num_sms, s);
