@@ -180,6 +180,7 @@ __device__ void prep_rows(const PrepArgs& p, int row0, int rstride) {
 }
 
 __global__ void __launch_bounds__(kAlignThreads) prologue_kernel(AlignArgs a, PrepArgs p) {
+  pdl_trigger();  // the next kernel may set itself up; it waits for this grid before reading
   if (blockIdx.x == 0) {
     if (a.status && threadIdx.x == 0) { a.status->bad_ids = 0; a.status->flags = 0; }
     __syncthreads();

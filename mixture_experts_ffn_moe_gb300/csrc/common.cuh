@@ -96,6 +96,16 @@ __device__ __forceinline__ void mma_f16_16816(float d[4], const uint32_t a[4], u
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while its
+// predecessor in the stream is still running: everything it reads from the
+// predecessor must come after pdl_wait() (which returns once the predecessor has
+// completed and its writes are visible).  pdl_trigger() lets the successor start
+// launching; every kernel here triggers only after its own pdl_wait(), so data
+// written two kernels back is always complete when a kernel starts.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Round-half-even of x / s in fp32 (IEEE division), clamped to +-127.
 __device__ __forceinline__ float quant_s8_rne(float x, float s) {
   float q = rintf(__fdiv_rn(x, s));

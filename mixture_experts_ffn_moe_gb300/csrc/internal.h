@@ -9,6 +9,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <utility>
 
 #include "gbmoe.h"
 
@@ -134,6 +135,24 @@ size_t prefill_smem_bytes();
 
 // Records `msg` as the calling thread's last error (moe_last_error) and returns `st`.
 moe_status_t report_error(moe_status_t st, const std::string& msg);
+
+// Launches `kern` on `s`; with pdl the launch may overlap the previous kernel in
+// the stream (the kernel then calls pdl_wait() before reading its outputs).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                          Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Sets a kernel's dynamic shared memory limit once per device.
 cudaError_t set_smem_limit_once(const void* func, int bytes, int slot);

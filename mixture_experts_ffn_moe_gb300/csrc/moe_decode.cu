@@ -143,15 +143,7 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
   volatile int* abort = abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_items = *a.num_ttiles * a.n_rt;
   const int KB = a.K / KBLK;
-  // Item order (measured): GEMM1 items go round-robin over the CTAs; GEMM2 items
-  // go in contiguous runs per CTA, so a CTA streams adjacent weight rows.
-  const int it_begin =
-      GATED ? static_cast<int>(blockIdx.x) : static_cast<int>(static_cast<long long>(n_items) * blockIdx.x / gridDim.x);
-  const int it_end =
-      GATED ? n_items : static_cast<int>(static_cast<long long>(n_items) * (blockIdx.x + 1) / gridDim.x);
-  const int it_step = GATED ? static_cast<int>(gridDim.x) : 1;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NS; ++i) {
@@ -162,6 +154,20 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
     fence_barrier_init();
   }
   __syncthreads();
+  // GEMM1 needs the predecessor's tile list and prepared activations before anything;
+  // GEMM2's weight stream only needs the tile list (written two kernels back), so its
+  // producer starts at once and its consumers wait before reading h.
+  if (GATED || warp < NCW) pdl_wait();
+  pdl_trigger();
+
+  const int n_items = *a.num_ttiles * a.n_rt;
+  // Item order (measured): GEMM1 items go round-robin over the CTAs; GEMM2 items
+  // go in contiguous runs per CTA, so a CTA streams adjacent weight rows.
+  const int it_begin =
+      GATED ? static_cast<int>(blockIdx.x) : static_cast<int>(static_cast<long long>(n_items) * blockIdx.x / gridDim.x);
+  const int it_end =
+      GATED ? n_items : static_cast<int>(static_cast<long long>(n_items) * (blockIdx.x + 1) / gridDim.x);
+  const int it_step = GATED ? static_cast<int>(gridDim.x) : 1;
 
   if (warp == NCW) {
     // ---------------------------------------------------------------- TMA producer
@@ -350,6 +356,8 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
 __global__ void __launch_bounds__(128) requant_h_kernel(const float* __restrict__ h, const uint32_t* __restrict__ hmax,
                                                         const int32_t* __restrict__ num_post, int I,
                                                         __half* __restrict__ hq, float* __restrict__ sh) {
+  pdl_wait();
+  pdl_trigger();
   const int rows = *num_post;
   for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     const float amax = __uint_as_float(hmax[r]);
@@ -369,8 +377,8 @@ cudaError_t launch_requant_rows(const void* h, const uint32_t* hmax, const int32
                                 __half* hq, float* sh, int num_sms, cudaStream_t s) {
   int grid = cap < num_sms * 8 ? cap : num_sms * 8;
   if (grid < 1) grid = 1;
-  requant_h_kernel<<<grid, 128, 0, s>>>(static_cast<const float*>(h), hmax, num_post, I, hq, sh);
-  return cudaGetLastError();
+  return launch_kernel(requant_h_kernel, dim3(grid), dim3(128), 0, s, true, static_cast<const float*>(h), hmax,
+                       num_post, I, hq, sh);
 }
 
 template <int WK, bool GATED, int OCC>
@@ -385,8 +393,7 @@ static cudaError_t launch_skinny_occ(const SkinnyArgs& a, const void* w, uint64_
   cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM,
                                         8 + WK * 4 + (GATED ? 2 : 0) + (OCC == 3 ? 1 : 0));
   if (err != cudaSuccess) return err;
-  kern<<<OCC * num_sms, dec::NUM_THREADS, C::SMEM, s>>>(mw, a);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(OCC * num_sms), dim3(dec::NUM_THREADS), C::SMEM, s, true, mw, a);
 }
 
 // max_items: an upper bound of the work items the launch can see.

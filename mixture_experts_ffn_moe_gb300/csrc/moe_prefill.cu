@@ -164,6 +164,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = bars->tmem_base;
+  // The weight stream (raw producer, converters, MMA) needs only the tile list,
+  // written two kernels back; the activation producer and the epilogue read the
+  // predecessor's output (activations, h, h scales) and wait for it.
+  if (warp == WARP_ATMA || warp >= WARP_EPI0) pdl_wait();
+  pdl_trigger();
 
   if (warp == WARP_WTMA) {
     // ---------------------------------------------------------------- raw weight producer
@@ -438,6 +443,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __half* __restri
                                                           const int32_t* __restrict__ sorted_ids,
                                                           const int32_t* __restrict__ num_post, int n_slots,
                                                           int topk, int H, __half* __restrict__ act) {
+  pdl_wait();
+  pdl_trigger();
   const int rows = *num_post;
   const int chunks = H / 8;
   const long long total = static_cast<long long>(rows) * chunks;
@@ -455,6 +462,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __half* __restri
 // (inv_pos >= 0); y already carries the routing weight.
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ y, const int32_t* __restrict__ inv_pos,
                                                       int M, int topk, int H, __nv_bfloat16* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int q = H / 4;
   const long long total = static_cast<long long>(M) * q;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -526,16 +535,16 @@ static cudaError_t launch_gemm(const PrefillArgs& a, const void* w, uint64_t w_r
   cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(kern), pf::SMEM_BYTES,
                                         4 + WK * 2 + (GATED ? 1 : 0));
   if (err != cudaSuccess) return err;
-  kern<<<num_sms, pf::NUM_THREADS, pf::SMEM_BYTES, s>>>(mw, mb, a);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(num_sms), dim3(pf::NUM_THREADS), pf::SMEM_BYTES, s, true, mw, mb, a);
 }
 
 cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook) {
   cudaError_t err;
   {
     int grid = num_sms * 8;
-    gather_rows_kernel<<<grid, 256, 0, s>>>(P.xq, P.sorted_ids, P.num_post, P.M * P.topk, P.topk, P.H, P.act);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    err = launch_kernel(gather_rows_kernel, dim3(grid), dim3(256), 0, s, true, P.xq, P.sorted_ids, P.num_post,
+                        P.M * P.topk, P.topk, P.H, P.act);
+    if (err != cudaSuccess) return err;
     hook("prefill_gather", s);
   }
   PrefillArgs g1{};
@@ -600,8 +609,8 @@ cudaError_t launch_combine(const float* y, const int32_t* inv_pos, int M, int to
   long long grid = (work + 255) / 256;
   if (grid > num_sms * 16) grid = num_sms * 16;
   if (grid < 1) grid = 1;
-  combine_kernel<<<static_cast<int>(grid), 256, 0, s>>>(y, inv_pos, M, topk, H, out);
-  return cudaGetLastError();
+  return launch_kernel(combine_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, true, y, inv_pos, M, topk,
+                       H, out);
 }
 
 size_t prefill_smem_bytes() { return pf::SMEM_BYTES; }
