@@ -158,9 +158,12 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
   // GEMM2's weight stream only needs the tile list (written two kernels back), so its
   // producer starts at once and its consumers wait before reading h.
   if (GATED || warp < NCW) pdl_wait();
-  pdl_trigger();
-
   const int n_items = *a.num_ttiles * a.n_rt;
+  // GEMM2's grid may launch early (its CTAs set up and prefetch weights).  A long
+  // GEMM1 (more than two items per CTA) does not trigger it: GEMM2 CTAs placed one
+  // by one into the slots of finished GEMM1 CTAs made the layer slower (measured).
+  if (!GATED || n_items <= 2 * static_cast<int>(gridDim.x)) pdl_trigger();
+
   // Item order (measured): GEMM1 items go round-robin over the CTAs; GEMM2 items
   // go in contiguous runs per CTA, so a CTA streams adjacent weight rows.
   const int it_begin =
