@@ -23,7 +23,10 @@ computes, in float64 numpy over dequantised weights:
   decode backend", is the same sum regrouped);
 * INT8 per-output-channel weights with dynamic per-token INT8 activations
   (DA8W8; SGLang CPU backend write-up, "(3) FusedMoE", the dynamic-quant
-  fusion paragraph).
+  fusion paragraph);
+* the optional FP8 x FP8 ("A8") mode of the FP8 layer, in which the
+  activations and the intermediate h are quantised to E4M3 in groups of 1 x 128
+  (a reading: the pages keep FP8 activations in BF16, see quant_fp8_1x128).
 
 Precision: float64 accumulation everywhere, except that every decision that
 turns a float into an integer code (activation quantisation) is taken in
@@ -136,6 +139,48 @@ def quant_int8_per_row(a):
 
 
 # ----------------------------------------------------------------------------
+# FP8 activations in 1 x 128 groups (the optional "A8" mode of the FP8 layer).
+#
+# The pages run FP8 weights against BF16 activations (Xeon 6 / SGLang blog,
+# section "FP8 推理", the weight-only bullet; the author's write-up, section
+# "(4) FP8 GEMM").  The DeepGEMM grouped GEMMs that the news rewrite of the LMSYS
+# large-scale-EP blog integrates (section "DeepGEMM集成") multiply FP8 by FP8,
+# but no page says how the activations are quantised.  Reading: one float32
+# scale per row and per 128 consecutive columns, s = amax / 448, and codes by
+# the same E4M3 rounding the weights use -- the 128-wide group matches the
+# weights' 128 x 128 scale blocks along K.
+# ----------------------------------------------------------------------------
+
+
+def quant_fp8_1x128(a):
+    """float32 rows [R, C] (C a multiple of 128) -> (E4M3 codes uint8 [R, C], float32 scales [R, C/128]).
+
+    For every row and every group of 128 consecutive columns:
+    s = amax(|group|) / 448 in float32 (1 when the group is all zero);
+    q = e4m3_encode_satfinite(group / s), the division in float32 (IEEE).
+    """
+    a = np.asarray(a, dtype=np.float32)
+    R, C = a.shape
+    if C % QBLOCK:
+        raise ValueError("columns must be a multiple of 128")
+    g = a.reshape(R, C // QBLOCK, QBLOCK)
+    amax = np.max(np.abs(g), axis=-1) if R else np.zeros((0, C // QBLOCK), np.float32)
+    s = np.where(amax > 0, np.divide(amax, np.float32(FP8_MAX), dtype=np.float32), np.float32(1.0))
+    s = s.astype(np.float32)
+    q = e4m3_encode_satfinite(np.divide(g, s[..., None], dtype=np.float32))
+    return q.reshape(R, C), s
+
+
+def dequant_fp8_1x128(codes, scale) -> np.ndarray:
+    """codes uint8 [R, C], scale f32 [R, C/128] -> float64 a[r, c] = decode(q) * s[r, c // 128]."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    R, C = codes.shape
+    a = _e4m3_table()[codes].reshape(R, C // QBLOCK, QBLOCK)
+    a = a * np.asarray(scale, dtype=np.float64)[..., None]
+    return a.reshape(R, C)
+
+
+# ----------------------------------------------------------------------------
 # Routing alignment.
 # ----------------------------------------------------------------------------
 
@@ -208,17 +253,24 @@ def _as_np(t):
     return np.asarray(t)
 
 
-def fused_moe_fp8(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, experts=None):
-    """FP8 block-scaled weights, activations kept at their bf16 values (weight-only quant).
+def fused_moe_fp8(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, experts=None, act="a16"):
+    """FP8 block-scaled weights.
 
     x [M, H] (bf16 values), topk_ids int [M, k], topk_weights f32 [M, k],
     w13 uint8 [E, 2I, H] + scale [E, 2I/128, H/128], w2 uint8 [E, H, I] +
     scale [E, H/128, I/128].  Returns float64 out [M, H].
 
+    act="a16" (the pages' weight-only scheme): activations keep their bf16
+    values.  act="fp8_1x128": x is replaced by dequant(quant_fp8_1x128(x)), and
+    the intermediate h of every (token, expert) pair, rounded to float32, by
+    dequant(quant_fp8_1x128(h)) before the down projection.
+
     `experts` restricts the loop to a subset (for sampling large layers);
     contributions of other experts are then left out.
     """
-    return _naive_moe(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, "fp8", experts)
+    if act not in ("a16", "fp8_1x128"):
+        raise ValueError(act)
+    return _naive_moe(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, "fp8", experts, act)
 
 
 def fused_moe_int8(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, experts=None):
@@ -232,7 +284,7 @@ def fused_moe_int8(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, expe
     return _naive_moe(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, "int8", experts)
 
 
-def _naive_moe(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, kind, experts):
+def _naive_moe(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, kind, experts, act="a16"):
     x = _as_np(x).astype(np.float32)
     ids = _as_np(topk_ids).astype(np.int64)
     tw = _as_np(topk_weights).astype(np.float64)
@@ -242,6 +294,8 @@ def _naive_moe(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, kind, ex
     Y = np.zeros(ids.shape + (H,), dtype=np.float64)  # Y[t, k] = expert output of slot (t, k)
     if kind == "int8":
         qx, sx = quant_int8_per_row(x)
+    a8 = kind == "fp8" and act == "fp8_1x128"
+    xa = dequant_fp8_1x128(*quant_fp8_1x128(x)) if a8 else x.astype(np.float64)
     for e in (range(E) if experts is None else experts):
         tok, slot = np.nonzero(ids == e)  # the mask of this expert
         if tok.size == 0:
@@ -251,8 +305,10 @@ def _naive_moe(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, kind, ex
         if kind == "fp8":
             W13 = dequant_fp8_block(q13, s13)                      # [2I, H]
             W2 = dequant_fp8_block(q2, s2)                         # [H, I]
-            C = x[tok].astype(np.float64) @ W13.T                  # A x [B1, B2] = [C1, C2]
+            C = xa[tok] @ W13.T                                    # A x [B1, B2] = [C1, C2]
             h = silu(C[:, :I]) * C[:, I:]                          # SiLU(C1) * C2
+            if a8:
+                h = dequant_fp8_1x128(*quant_fp8_1x128(h.astype(np.float32)))
             y = h @ W2.T
         else:
             acc = qx[tok].astype(np.int64) @ q13.astype(np.int64).T
@@ -269,7 +325,7 @@ def _naive_moe(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, kind, ex
     return out
 
 
-def fused_moe_rows(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, kind, tokens):
+def fused_moe_rows(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, kind, tokens, act="a16"):
     """Oracle output for a subset of token rows only (for layers too large to run whole).
 
     Computes exactly what the full call gives for those rows: it runs the
@@ -282,5 +338,6 @@ def fused_moe_rows(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, kind
     tw = _as_np(topk_weights)[tokens]
     E = w13.shape[0]
     used = sorted({int(e) for e in np.unique(ids) if 0 <= e < E})
-    fn = fused_moe_fp8 if kind == "fp8" else fused_moe_int8
-    return fn(x, ids, tw, w13, w13_scale, w2, w2_scale, experts=used)
+    if kind == "fp8":
+        return fused_moe_fp8(x, ids, tw, w13, w13_scale, w2, w2_scale, experts=used, act=act)
+    return fused_moe_int8(x, ids, tw, w13, w13_scale, w2, w2_scale, experts=used)

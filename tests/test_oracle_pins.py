@@ -360,3 +360,101 @@ def test_ids_out_of_range_contribute_nothing():
     keep = [0, 1, 2, 4, 6, 7, 8, 9]
     np.testing.assert_allclose(out[keep], base[keep], rtol=1e-11, atol=1e-15)
     assert not np.allclose(out[3], base[3]) and not np.allclose(out[5], base[5])
+
+
+# --------------------------------------------------------------------------- FP8 activations, 1 x 128 groups
+
+def _finite_e4m3_codes():
+    c = np.arange(256, dtype=np.uint8)
+    return c[(c & 0x7F) != 0x7F]
+
+
+def test_fp8_1x128_exact_codes_closed_form():
+    """Groups built as 2^j * decode(code) with one +-448 element: quantisation returns those codes and s = 2^j."""
+    rng = np.random.default_rng(21)
+    R, G = 6, 5
+    codes = rng.choice(_finite_e4m3_codes(), size=(R, G, 128)).astype(np.uint8)
+    codes[:, :, 0] = np.where(rng.random((R, G)) < 0.5, 0x7E, 0xFE)  # amax = 448 * 2^j exactly
+    j = rng.integers(-20, 21, size=(R, G))
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy() * np.exp2(j)[..., None]
+    a = vals.astype(np.float32).reshape(R, G * 128)
+    assert np.array_equal(a.astype(np.float64), vals.reshape(R, -1))  # exact in float32
+    q, s = oracle.quant_fp8_1x128(a)
+    assert s.dtype == np.float32 and s.shape == (R, G)
+    assert np.array_equal(s.astype(np.float64), np.exp2(j))
+    assert np.array_equal(q, codes.reshape(R, -1))
+    np.testing.assert_array_equal(oracle.dequant_fp8_1x128(q, s), vals.reshape(R, -1))
+
+
+def test_fp8_1x128_rounding_error_bound_and_amax():
+    rng = np.random.default_rng(22)
+    R, G = 16, 4
+    a = (rng.standard_normal((R, G * 128)) * np.exp2(rng.integers(-8, 9, size=(R, 1)))).astype(np.float32)
+    a[3, 5] = 0.0
+    q, s = oracle.quant_fp8_1x128(a)
+    g = a.reshape(R, G, 128).astype(np.float64)
+    amax = np.abs(g).max(-1)
+    assert np.array_equal(s, (amax.astype(np.float32) / np.float32(448.0)).astype(np.float32))
+    deq = oracle.dequant_fp8_1x128(q, s).reshape(R, G, 128)
+    err = np.abs(deq - g)
+    sc = s.astype(np.float64)[..., None]
+    normal = np.abs(g) >= 2.0 ** -6 * sc
+    # half a unit in the last place: 2^-4 relative (3 mantissa bits), 2^-10 * s among subnormals
+    assert np.all(err[normal] <= 2.0 ** -4 * np.abs(g)[normal] * (1 + 1e-6))
+    assert np.all(err[~normal] <= 2.0 ** -10 * np.broadcast_to(sc, g.shape)[~normal] * (1 + 1e-6))
+    # the largest element of every group lands on +-448
+    idx = np.abs(g).argmax(-1)
+    top = np.take_along_axis(q.reshape(R, G, 128), idx[..., None], -1)[..., 0]
+    assert np.all((top == 0x7E) | (top == 0xFE))
+
+
+def test_fp8_1x128_zero_group_and_group_boundaries():
+    a = np.zeros((2, 384), np.float32)
+    a[0, 127] = 3.0      # last column of group 0
+    a[0, 128] = -0.5     # first column of group 1
+    q, s = oracle.quant_fp8_1x128(a)
+    assert s[0].tolist() == [np.float32(3.0) / np.float32(448.0), np.float32(0.5) / np.float32(448.0), 1.0]
+    assert s[1].tolist() == [1.0, 1.0, 1.0]
+    assert q[0, 127] == 0x7E and q[0, 128] == 0xFE
+    assert np.count_nonzero(q) == 2
+    with pytest.raises(ValueError):
+        oracle.quant_fp8_1x128(np.zeros((1, 100), np.float32))
+
+
+def test_a8_layer_top1_identity_down_projection_closed_form():
+    """Top-1 routing, weight 1, W2 = identity: out = dequant(quant(h)) of h = SiLU(a W1^T) * (a W3^T),
+    a = dequant(quant(x)) -- the quantiser is applied per token row, to x and to h."""
+    shape = synth.LayerShape("a8", 6, 256, 256, 2, 1, "fp8", "softmax")
+    d = synth.make_layer(shape, seed=23)
+    rng = np.random.default_rng(23)
+    ids = torch.from_numpy(rng.integers(0, 2, size=(6, 1)).astype(np.int32))
+    w2 = torch.zeros(2, 256, 256, dtype=torch.uint8)
+    w2[:, torch.arange(256), torch.arange(256)] = 0x38  # E4M3 1.0
+    s2 = torch.ones(2, 2, 2)
+    out = oracle.fused_moe_fp8(d["x"], ids, torch.ones(6, 1), d["w13"], d["w13_scale"], w2, s2, act="fp8_1x128")
+
+    def deq(a):
+        q, s = oracle.quant_fp8_1x128(np.asarray(a, np.float32))
+        v = torch.from_numpy(q).view(torch.float8_e4m3fn).double().numpy().reshape(len(q), -1, 128)
+        return (v * s.astype(np.float64)[..., None]).reshape(len(q), -1)
+
+    a = torch.from_numpy(deq(d["x"].float().numpy()))
+    for t in range(6):
+        e = int(ids[t, 0])
+        W13 = _torch_dequant_fp8(d["w13"][e], d["w13_scale"][e])
+        h = torch.nn.functional.silu(a[t:t + 1] @ W13[:256].T) * (a[t:t + 1] @ W13[256:].T)
+        want = deq(h.numpy())[0]
+        np.testing.assert_allclose(out[t], want, rtol=1e-12, atol=0)
+        # the h quantisation is really applied: the unquantised h differs
+        assert np.abs(h.numpy()[0] - want).max() > 0
+
+
+def test_a8_layer_close_to_a16():
+    shape = synth.LayerShape("a8", 24, 512, 256, 8, 3, "fp8", "softmax")
+    d = synth.make_layer(shape, seed=24)
+    a16 = oracle.fused_moe_fp8(**d)
+    a8 = oracle.fused_moe_fp8(**d, act="fp8_1x128")
+    rel = np.linalg.norm(a8 - a16) / np.linalg.norm(a16)
+    assert 1e-3 < rel < 6e-2
+    sub = oracle.fused_moe_rows(**d, kind="fp8", tokens=[2, 17], act="fp8_1x128")
+    np.testing.assert_allclose(sub, a8[[2, 17]], rtol=1e-11, atol=1e-15)
