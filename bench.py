@@ -44,12 +44,16 @@ def workloads():
         "dsr1_decode_M4": synth.deepseek_r1(4),
         "dsr1_prefill_M2048": synth.deepseek_r1(2048, routing="deepseek_zipf"),
         "dsr1_prefill_M16384": synth.deepseek_r1(16384, routing="deepseek_zipf"),
+        # FP8 activations in 1 x 128 groups (FP8 x FP8 tensor-core products)
+        "dsr1_prefill_M2048_a8": synth.deepseek_r1(2048, routing="deepseek_zipf", act="fp8_1x128"),
+        "dsr1_prefill_M16384_a8": synth.deepseek_r1(16384, routing="deepseek_zipf", act="fp8_1x128"),
         **{f"dsr1_sweep_M{m}": synth.deepseek_r1(m, routing="uniform") for m in (1, 2, 4, 8, 16, 32, 64)},
         **{f"qwen3_M{m}": synth.qwen3_235b(m) for m in (1, 16, 256, 4096)},
         "tiny_M16": synth.tiny(),
         # same per-expert work with 32+1 experts: small enough for full ncu captures
         "dsr1_decode_M4_E32": synth.deepseek_r1(4, E=32),
         "dsr1_prefill_M2048_E32": synth.deepseek_r1(2048, routing="deepseek_zipf", E=32),
+        "dsr1_prefill_M2048_E32_a8": synth.deepseek_r1(2048, routing="deepseek_zipf", E=32, act="fp8_1x128"),
         "qwen3_M1024": synth.qwen3_235b(1024),
     }
 
@@ -63,11 +67,12 @@ KERNEL_SOURCES = {  # kernel -> the source files that define it
 }
 
 
-def source_hash(kernel: str) -> str:
+def source_hash(kernel: str, a8: bool = False) -> str:
     """Hash of the kernel's own source file and the headers it includes."""
     csrc = os.path.join(ROOT, "mixture_experts_ffn_moe_gb300", "csrc")
     h = hashlib.sha256()
-    for name in (KERNEL_SOURCES.get(kernel, ""), "common.cuh", "sm100_ptx.cuh", "internal.h"):
+    src = "moe_prefill_a8.cu" if a8 and kernel.startswith("prefill") else KERNEL_SOURCES.get(kernel, "")
+    for name in (src, "common.cuh", "sm100_ptx.cuh", "internal.h"):
         path = os.path.join(csrc, name)
         if name and os.path.exists(path):
             h.update(open(path, "rb").read())
@@ -83,14 +88,14 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def ncu_traffic(workload: str, kernel: str):
+def ncu_traffic(workload: str, kernel: str, a8: bool = False):
     """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel sources."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
     rec = d.get(workload, {}).get(kernel)
-    if not rec or rec.get("source_hash") != source_hash(kernel):
+    if not rec or rec.get("source_hash") != source_hash(kernel, a8):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -106,6 +111,7 @@ def stage_work(shape, ids: torch.Tensor):
     active = int((hist > 0).sum())
     valid = int(hist.sum())
     H, I, M = shape.H, shape.I, shape.M
+    ab = 1 if shape.act == "fp8_1x128" else 2  # bytes per gathered activation element (E4M3 or fp16)
     if shape.weight_kind == "fp8":
         s13 = 4 * (2 * I // 128) * (H // 128)
         s2 = 4 * (H // 128) * (I // 128)
@@ -116,8 +122,8 @@ def stage_work(shape, ids: torch.Tensor):
     return {
         "decode_gemm1": (active * (2 * I * H + s13) + M * H * 2 + valid * I * 2, f1),
         "decode_gemm2": (active * (H * I + s2) + valid * I * 2 + valid * H * 4, f2),
-        "prefill_gemm1": (active * (2 * I * H + s13) + valid * H * 2 + valid * I * 2, f1),
-        "prefill_gemm2": (active * (H * I + s2) + valid * I * 2 + valid * H * 4, f2),
+        "prefill_gemm1": (active * (2 * I * H + s13) + valid * H * ab + valid * I * ab, f1),
+        "prefill_gemm2": (active * (H * I + s2) + valid * I * ab + valid * H * 4, f2),
     }
 
 
@@ -225,7 +231,7 @@ def oracle_sample(shape, x, ids, w, weights):
     import oracle
     w13, s13, w2, s2 = weights
     t0 = time.perf_counter()
-    oracle.fused_moe_rows(x, ids, w, w13, s13, w2, s2, kind=shape.weight_kind, tokens=[0])
+    oracle.fused_moe_rows(x, ids, w, w13, s13, w2, s2, kind=shape.weight_kind, tokens=[0], act=shape.act)
     dt = time.perf_counter() - t0
     return 1.0 / dt, dt, f"1 token of the {shape.M}-token batch ({int((ids[0] >= 0).sum())} experts), float64 numpy"
 
@@ -259,7 +265,9 @@ def run_reference(args, shape):
 def config_of(shape, args):
     return {"workload": args.workload, "M": shape.M, "H": shape.H, "I": shape.I, "E": shape.E_total,
             "topk": shape.topk_total, "weights": "fp8_e4m3_block128" if shape.weight_kind == "fp8" else
-            "int8_per_channel", "routing": shape.routing, "l2": "flushed between steps (256 MiB write)",
+            "int8_per_channel", "activations": "fp8_e4m3_1x128" if shape.act == "fp8_1x128" else
+            ("int8_per_row" if shape.weight_kind == "int8" else "bf16"),
+            "routing": shape.routing, "l2": "flushed between steps (256 MiB write)",
             "parallelism": f"replicas{args.gpus}"}
 
 
@@ -276,21 +284,22 @@ def run_ours(args, shape):
     xd, idsd, wd = x.to(dev), ids.to(dev), w.to(dev)
     kind = gbmoe.MOE_WEIGHT_FP8 if shape.weight_kind == "fp8" else gbmoe.MOE_WEIGHT_INT8
     fn = gbmoe.fused_moe_fp8 if kind == gbmoe.MOE_WEIGHT_FP8 else gbmoe.fused_moe_int8
-    ws = gbmoe.alloc_workspace(shape.M, shape.H, shape.I, shape.E_total, shape.topk_total, kind, 0, dev)
+    flags = gbmoe.MOE_ACT_FP8_1X128 if shape.act == "fp8_1x128" else gbmoe.MOE_PATH_AUTO
+    ws = gbmoe.alloc_workspace(shape.M, shape.H, shape.I, shape.E_total, shape.topk_total, kind, flags, dev)
     out = torch.empty(shape.M, shape.H, dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        fn(xd, idsd, wd, w13, s13, w2, s2, out=out, workspace=ws)
+        fn(xd, idsd, wd, w13, s13, w2, s2, flags=flags, out=out, workspace=ws)
 
     for _ in range(args.warmup):
         flush.zero_()
         step()
     torch.cuda.synchronize()
-    bad, flags, st = gbmoe.moe_read_status(ws)
+    bad, dev_flags, st = gbmoe.moe_read_status(ws)
     if st != 0:
-        raise SystemExit(f"device status after warm-up: bad ids {bad}, flags {flags}")
+        raise SystemExit(f"device status after warm-up: bad ids {bad}, flags {dev_flags}")
 
     # ---- timed region: K steps, device time per step with CUDA events on the launch stream.
     # The layer's kernels overlap their launches (programmatic dependent launch), so no
@@ -336,19 +345,24 @@ def run_ours(args, shape):
     dominant = max((n for n in stage_avg if n in work), key=lambda n: stage_avg[n])
     dbytes, dflops = work[dominant]
     secs = stage_avg[dominant] * 1e-3
-    # fp16 tensor-core MMA: the measured dense bf16 rate (same rate for fp16), burst figure
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    # Tensor peak of the kernel's operand type, burst figure: fp16 MMA runs at the measured dense
+    # bf16 rate; E4M3 x E4M3 at twice it (the nominal FP8:BF16 ratio, 4.5 : 2.25 PFLOP/s).
+    if shape.act == "fp8_1x128":
+        tpeak, tsrc = 2.0 * peaks["bf16_tflops"], peaks["source"] + " bf16 dense x 2 (nominal FP8:BF16 ratio)"
+    else:
+        tpeak, tsrc = peaks["bf16_tflops"], peaks["source"] + " bf16 dense (fp16 same rate)"
+    ridge = tpeak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     if dflops / dbytes > ridge:
         achieved = dflops / secs / 1e12
-        roofline = {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": peaks["bf16_tflops"],
-                    "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                    "traffic": ncu_traffic(args.workload, dominant), "algorithmic_flops": dflops,
-                    "algorithmic_bytes": dbytes, "peak_source": peaks["source"] + " bf16 dense (fp16 same rate)"}
+        roofline = {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": tpeak,
+                    "unit": "TFLOP/s", "frac": achieved / tpeak,
+                    "traffic": ncu_traffic(args.workload, dominant, shape.act == "fp8_1x128"), "algorithmic_flops": dflops,
+                    "algorithmic_bytes": dbytes, "peak_source": tsrc}
     else:
         achieved = dbytes / secs / 1e9
         roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peaks["hbm_gbs"],
                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                    "traffic": ncu_traffic(args.workload, dominant), "algorithmic_bytes": dbytes,
+                    "traffic": ncu_traffic(args.workload, dominant, shape.act == "fp8_1x128"), "algorithmic_bytes": dbytes,
                     "algorithmic_flops": dflops, "peak_source": peaks["source"]}
     layer_bytes = synth.distinct_weight_bytes(shape, ids)
     flops = synth.algorithmic_flops(shape, ids)
@@ -384,7 +398,8 @@ def run_ours(args, shape):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp8->f16 mma, f32 acc" if kind == 0 else "int8->f16 mma, f32 acc",
+        "vs_baseline": None, "dtype": ("fp8 x fp8 mma, f32 acc" if shape.act == "fp8_1x128" else
+                                       "fp8->f16 mma, f32 acc") if kind == 0 else "int8->f16 mma, f32 acc",
         "data": "synthetic", "config": config_of(shape, args),
         "roofline": roofline, "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

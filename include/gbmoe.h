@@ -60,6 +60,12 @@ typedef enum {
 #define MOE_PATH_DECODE 0x1u  /* weight-streaming GEMV path (small token counts)    */
 #define MOE_PATH_PREFILL 0x2u /* tcgen05 grouped-GEMM path (large token counts)     */
 #define MOE_PATH_MASK 0x3u
+/* fused_moe_fp8 only: FP8 x FP8 products.  x and the intermediate h are
+ * quantised to E4M3 in groups of 1 x 128 (one fp32 scale per row and 128
+ * columns, as moe_quant_act_fp8 does) before they enter the tensor cores.
+ * Runs on the tcgen05 path at every M; MOE_PATH_DECODE with it is
+ * MOE_ERR_UNSUPPORTED. */
+#define MOE_ACT_FP8_1X128 0x10u
 
 #define MOE_WEIGHT_FP8 0
 #define MOE_WEIGHT_INT8 1
@@ -118,6 +124,25 @@ moe_status_t moe_quant_act_int8(const void* x_bf16, int M, int H, int8_t* q, flo
                                 moe_stream_t stream);
 
 /*
+ * Dynamic FP8 quantisation of bf16 activations in groups of 1 x 128 (the
+ * activation side of MOE_ACT_FP8_1X128).  The pages keep FP8-weight
+ * activations in BF16 (Xeon 6 / SGLang blog, section "FP8 inference"); this
+ * is the FP8 x FP8 form of the grouped GEMMs named in the news rewrite of the
+ * LMSYS large-scale-EP blog (section "DeepGEMM integration"), with the group
+ * along H matching the weights' 128-wide scale blocks:
+ *   scale[r,g] = max over c in [128g, 128g+128) of |x[r,c]| / 448 (fp32; 1 for
+ *                an all-zero group)
+ *   q[r,c]     = E4M3(x[r,c] / scale[r, c/128]), the division in IEEE fp32,
+ *                rounded to nearest even, saturated to +-448
+ *   x bf16 [M, H] -> q uint8 E4M3 codes [M, H], scale fp32 [M, H/128].
+ * H must be a multiple of 128 (else MOE_ERR_UNSUPPORTED); M >= 0.  x 16-byte
+ * aligned, q 4-byte aligned.  The fused layer applies exactly this function
+ * to its input rows.
+ */
+moe_status_t moe_quant_act_fp8(const void* x_bf16, int M, int H, uint8_t* q, float* scale,
+                               moe_stream_t stream);
+
+/*
  * Bytes of scratch the fused layer needs for these sizes and flags
  * (weight_kind MOE_WEIGHT_FP8 or MOE_WEIGHT_INT8).  The workspace must be
  * 256-byte aligned.  Returns 0 for invalid or unsupported arguments.
@@ -147,6 +172,11 @@ size_t moe_workspace_size(int M, int H, int I, int E, int topk, int weight_kind,
  * E4M3 to fp16 expansion is exact; bf16 activations are rounded to fp16,
  * exact for magnitudes in [2^-14, 65504]) and fp32 accumulation; each
  * 128x128 block scale is applied once per 128-deep partial sum.
+ * With MOE_ACT_FP8_1X128 in flags, x is quantised as moe_quant_act_fp8 does,
+ * and so is each intermediate row h (fp32, per 128 columns of I) of a
+ * (token, expert) pair before the down projection; the products are E4M3 x
+ * E4M3 on the tensor cores, and every 128-deep partial sum is scaled by its
+ * weight block scale times its activation group scale in fp32.
  */
 moe_status_t fused_moe_fp8(const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
                            const void* w13_e4m3, const float* w13_scale, const void* w2_e4m3,

@@ -144,16 +144,42 @@ __device__ void align_cta(const AlignArgs& a) {
   }
 }
 
+// FP8 E4M3 codes of one row in groups of 128 columns: s = amax / 448 (fp32,
+// 1 for an all-zero group), q = E4M3(x / s) rounded to nearest even with
+// saturation, the division in IEEE fp32.  One warp per group, 4 columns a lane.
+__device__ void prep_row_fp8_1x128(const __nv_bfloat16* xr, uint8_t* qr, float* sr, int H) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int g = warp; g < H / kQBlock; g += nw) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(xr + g * kQBlock + lane * 4);
+    const __nv_bfloat162 b0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+    const __nv_bfloat162 b1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+    const float2 f0 = __bfloat1622float2(b0), f1 = __bfloat1622float2(b1);
+    float m = fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
+    m = warp_max(m);
+    const float s = m > 0.f ? __fdiv_rn(m, 448.0f) : 1.0f;
+    const uint32_t c0 = e4m3_code(__fdiv_rn(f0.x, s)), c1 = e4m3_code(__fdiv_rn(f0.y, s));
+    const uint32_t c2 = e4m3_code(__fdiv_rn(f1.x, s)), c3 = e4m3_code(__fdiv_rn(f1.y, s));
+    *reinterpret_cast<uint32_t*>(qr + g * kQBlock + lane * 4) = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+    if (lane == 0) sr[g] = s;
+  }
+}
+
 // Row preparation of the activations, one CTA per row at a time.
 //   kind 1: x bf16 -> fp16 (RN)               (FP8 weight-only path)
 //   kind 2: x bf16 -> int8 codes + fp32 scale (DA8W8 path); codes stored as
 //           fp16 (exact) or int8
+//   kind 3: x bf16 -> E4M3 codes + one fp32 scale per 128 columns (FP8 A8 path)
 template <typename QT>
 __device__ void prep_rows(const PrepArgs& p, int row0, int rstride) {
   __shared__ float red[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
   for (int r = row0; r < p.M; r += rstride) {
     const __nv_bfloat16* xr = p.x + static_cast<size_t>(r) * p.H;
+    if (p.kind == 3) {
+      prep_row_fp8_1x128(xr, static_cast<uint8_t*>(p.q) + static_cast<size_t>(r) * p.H,
+                         p.scale + static_cast<size_t>(r) * (p.H / kQBlock), p.H);
+      continue;
+    }
     QT* qr = reinterpret_cast<QT*>(p.q) + static_cast<size_t>(r) * p.H;
     if (p.kind == 1) {
       for (int c = tid; c < p.H; c += blockDim.x) qr[c] = static_cast<QT>(__bfloat162float(xr[c]));
@@ -195,7 +221,7 @@ __global__ void __launch_bounds__(kAlignThreads) prologue_kernel(AlignArgs a, Pr
   if (p.kind != 0) prep_rows<__half>(p, blockIdx.x - 1, gridDim.x - 1);
 }
 
-__global__ void __launch_bounds__(256) quant_rows_s8_kernel(PrepArgs p) {
+__global__ void __launch_bounds__(256) quant_rows_kernel(PrepArgs p) {
   prep_rows<int8_t>(p, blockIdx.x, gridDim.x);
 }
 
@@ -204,16 +230,16 @@ size_t align_smem_bytes(int E) { return static_cast<size_t>(kAlignWarps * E + 64
 cudaError_t launch_prologue(const AlignArgs& a, const PrepArgs& p, int prep_ctas, cudaStream_t s) {
   const size_t smem = align_smem_bytes(a.E);
   cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(prologue_kernel),
-                                        static_cast<int>(align_smem_bytes(MOE_MAX_EXPERTS)), 0);
+                                        static_cast<int>(align_smem_bytes(MOE_MAX_EXPERTS)));
   if (err != cudaSuccess) return err;
   prologue_kernel<<<1 + prep_ctas, kAlignThreads, smem, s>>>(a, p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_quant_rows_s8(const PrepArgs& p, cudaStream_t s) {
+cudaError_t launch_quant_rows(const PrepArgs& p, cudaStream_t s) {
   const int grid = p.M < 2048 ? p.M : 2048;
   if (grid == 0) return cudaSuccess;
-  quant_rows_s8_kernel<<<grid, 256, 0, s>>>(p);
+  quant_rows_kernel<<<grid, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
 

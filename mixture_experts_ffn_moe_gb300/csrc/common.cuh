@@ -58,6 +58,11 @@ __device__ __forceinline__ void w8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
   else s8x4_to_f16x4(w, lo, hi);
 }
 
+// fp32 -> E4M3 code: round to nearest, ties to even, saturating to +-448.
+__device__ __forceinline__ uint32_t e4m3_code(float v) {
+  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);

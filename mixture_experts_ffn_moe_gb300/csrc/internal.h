@@ -37,9 +37,9 @@ struct AlignArgs {
 struct PrepArgs {
   const __nv_bfloat16* x;  // [M, H]
   int M, H;
-  int kind;                // 0 none, 1 bf16 -> fp16, 2 per-row int8 quantisation
-  void* q;                 // [M, H] fp16 (kinds 1, 2 in the prologue) or int8 (quant entry)
-  float* scale;            // [M] (kind 2)
+  int kind;                // 0 none, 1 bf16 -> fp16, 2 per-row int8, 3 FP8 E4M3 per 1x128 group
+  void* q;                 // [M, H] fp16 (kinds 1, 2 in the prologue), int8 (quant entry) or E4M3 codes (kind 3)
+  float* scale;            // [M] (kind 2) or [M, H/128] (kind 3)
   uint32_t* zero_words;    // words to clear (may be null)
   int n_zero;
 };
@@ -96,6 +96,13 @@ struct LayerPlan {
   float* y;              // [M*topk, H] weighted expert outputs by slot
   __nv_bfloat16* out;
   DeviceStatus* status;
+  // FP8-activation (A8) prefill only
+  const uint8_t* xq8;    // [M, H] E4M3 codes of x
+  const float* sx8;      // [M, H/128] their scales
+  uint8_t* act8;         // [cap, H] gathered codes by position
+  float* sa8;            // [H/128, cap] gathered scales, transposed
+  uint8_t* h8;           // [cap, I] E4M3 codes of h by position
+  float* sh8;            // [I/128, cap] their scales, transposed
 };
 
 // One skinny grouped GEMM of the decode path (device view).
@@ -121,9 +128,10 @@ struct SkinnyArgs {
 
 size_t align_smem_bytes(int E);
 cudaError_t launch_prologue(const AlignArgs& a, const PrepArgs& p, int prep_ctas, cudaStream_t s);
-cudaError_t launch_quant_rows_s8(const PrepArgs& p, cudaStream_t s);
+cudaError_t launch_quant_rows(const PrepArgs& p, cudaStream_t s);
 cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook);
 cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook);
+cudaError_t launch_prefill_a8(const LayerPlan& P, int num_sms, cudaStream_t s, const StageHook& hook);
 cudaError_t launch_combine(const float* y, const int32_t* inv_pos, int M, int topk, int H, __nv_bfloat16* out,
                            int num_sms, cudaStream_t s);
 // 2D row-major tensor [outer, inner] of `esize`-byte elements, TMA box [box_outer, box_inner].
@@ -154,7 +162,7 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-// Sets a kernel's dynamic shared memory limit once per device.
-cudaError_t set_smem_limit_once(const void* func, int bytes, int slot);
+// Sets a kernel's dynamic shared memory limit once per device (and size).
+cudaError_t set_smem_limit_once(const void* func, int bytes);
 
 }  // namespace gbmoe

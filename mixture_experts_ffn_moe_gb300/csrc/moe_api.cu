@@ -2,7 +2,9 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <set>
 #include <string>
+#include <tuple>
 #include <vector>
 
 #include "common.cuh"
@@ -24,19 +26,18 @@ static moe_status_t cuda_fail(cudaError_t err, const char* where) {
 moe_status_t report_error(moe_status_t st, const std::string& msg) { return fail(st, msg); }
 
 constexpr int kMaxDevices = 64;
-constexpr int kSmemSlots = 16;
 
-cudaError_t set_smem_limit_once(const void* func, int bytes, int slot) {
+cudaError_t set_smem_limit_once(const void* func, int bytes) {
   static std::mutex mu;
-  static bool done[kMaxDevices][kSmemSlots] = {};
+  static std::set<std::tuple<int, const void*, int>> done;  // (device, kernel, bytes) already set
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= kMaxDevices || slot < 0 || slot >= kSmemSlots) return cudaErrorInvalidValue;
   std::lock_guard<std::mutex> lock(mu);
-  if (done[dev][slot]) return cudaSuccess;
+  const auto key = std::make_tuple(dev, func, bytes);
+  if (done.count(key)) return cudaSuccess;
   err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (err == cudaSuccess) done[dev][slot] = true;
+  if (err == cudaSuccess) done.insert(key);
   return err;
 }
 
@@ -95,7 +96,9 @@ struct Layout {
   int path = 0, B = 0;
   size_t cap = 0;
   size_t status = 0, sorted = 0, expert_ids = 0, offsets = 0, counts = 0, active = 0, scalars = 0,
-         inv_pos = 0, xq = 0, sx = 0, h = 0, hmax = 0, hq = 0, sh = 0, ttiles = 0, act = 0, y = 0, total = 0;
+         inv_pos = 0, xq = 0, sx = 0, h = 0, hmax = 0, hq = 0, sh = 0, ttiles = 0, act = 0, sa = 0, y = 0,
+         total = 0;
+  bool a8 = false;
   size_t max_ttiles = 0;
   int tile_tokens = 0;
 };
@@ -103,6 +106,7 @@ struct Layout {
 static int choose_path(int M, unsigned flags) {
   const unsigned p = flags & MOE_PATH_MASK;
   if (p == MOE_PATH_DECODE || p == MOE_PATH_PREFILL) return static_cast<int>(p);
+  if (flags & MOE_ACT_FP8_1X128) return MOE_PATH_PREFILL;  // the FP8 x FP8 products run on tcgen05 only
   return M <= MOE_MAX_DECODE_TOKENS ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
 }
 
@@ -121,6 +125,22 @@ static Layout plan(int M, int H, int I, int E, int topk, int kind, unsigned flag
   L.active = take(static_cast<size_t>(E) * 4);
   L.scalars = take(16);
   L.inv_pos = take(static_cast<size_t>(M) * topk * 4);
+  L.a8 = kind == MOE_WEIGHT_FP8 && (flags & MOE_ACT_FP8_1X128);
+  L.tile_tokens = L.path == MOE_PATH_PREFILL ? kPrefillTileTokens : kDecodeBlock;
+  L.max_ttiles = static_cast<size_t>(E) + static_cast<size_t>(M) * topk / L.tile_tokens + 1;
+  if (L.a8) {
+    // E4M3 codes with 1 x 128 scales; scales of gathered rows are stored transposed [K/128, cap]
+    L.xq = take(static_cast<size_t>(M) * H);
+    L.sx = take(static_cast<size_t>(M) * (H / kQBlock) * 4);
+    L.h = take(L.cap * I);
+    L.sh = take(L.cap * (I / kQBlock) * 4);
+    L.ttiles = take(L.max_ttiles * 16);
+    L.act = take(L.cap * H);
+    L.sa = take(L.cap * (H / kQBlock) * 4);
+    L.y = take(static_cast<size_t>(M) * topk * H * 4);
+    L.total = o;
+    return L;
+  }
   L.xq = take(static_cast<size_t>(M) * H * 2);
   L.sx = take(static_cast<size_t>(M) * 4);
   if (kind == MOE_WEIGHT_FP8) {
@@ -131,8 +151,6 @@ static Layout plan(int M, int H, int I, int E, int topk, int kind, unsigned flag
     L.hq = take(L.cap * I * 2);
     L.sh = take(L.cap * 4);
   }
-  L.tile_tokens = L.path == MOE_PATH_PREFILL ? kPrefillTileTokens : kDecodeBlock;
-  L.max_ttiles = static_cast<size_t>(E) + static_cast<size_t>(M) * topk / L.tile_tokens + 1;
   L.ttiles = take(L.max_ttiles * 16);
   if (L.path == MOE_PATH_PREFILL) L.act = take(L.cap * H * 2);
   L.y = take(static_cast<size_t>(M) * topk * H * 4);
@@ -140,7 +158,12 @@ static Layout plan(int M, int H, int I, int E, int topk, int kind, unsigned flag
   return L;
 }
 
-static moe_status_t check_layer_args(const void* x, const void* ids, const void* tw, const void* w13,
+static bool known_flags(int kind, unsigned flags) {
+  const unsigned allowed = MOE_PATH_MASK | (kind == MOE_WEIGHT_FP8 ? MOE_ACT_FP8_1X128 : 0u);
+  return (flags & ~allowed) == 0;
+}
+
+static moe_status_t check_layer_args(int kind, const void* x, const void* ids, const void* tw, const void* w13,
                                      const void* s13, const void* w2, const void* s2, int M, int H, int I,
                                      int E, int topk, unsigned flags, const void* out) {
   if (M < 0 || H <= 0 || I <= 0 || E <= 0 || topk <= 0)
@@ -148,8 +171,10 @@ static moe_status_t check_layer_args(const void* x, const void* ids, const void*
   if (topk > 32) return fail(MOE_ERR_UNSUPPORTED, "topk > 32");
   if (E > MOE_MAX_EXPERTS) return fail(MOE_ERR_UNSUPPORTED, "more than MOE_MAX_EXPERTS experts");
   if (H % kQBlock || I % kQBlock) return fail(MOE_ERR_UNSUPPORTED, "H and I must be multiples of 128");
-  if (flags & ~MOE_PATH_MASK) return fail(MOE_ERR_INVALID_ARG, "unknown flag bits");
+  if (!known_flags(kind, flags)) return fail(MOE_ERR_INVALID_ARG, "unknown flag bits for this weight kind");
   if ((flags & MOE_PATH_MASK) == MOE_PATH_MASK) return fail(MOE_ERR_INVALID_ARG, "both path flags set");
+  if ((flags & MOE_ACT_FP8_1X128) && (flags & MOE_PATH_MASK) == MOE_PATH_DECODE)
+    return fail(MOE_ERR_UNSUPPORTED, "MOE_ACT_FP8_1X128 runs on the tcgen05 (prefill) path only");
   if (static_cast<long long>(M) * topk > (1LL << 30) || static_cast<long long>(M) * H > (1LL << 40))
     return fail(MOE_ERR_UNSUPPORTED, "problem too large");
   if (M == 0) return MOE_OK;
@@ -170,7 +195,7 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
                                int topk, unsigned flags, void* out, void* ws, size_t ws_bytes,
                                cudaStream_t stream) {
   g_last_error.clear();
-  moe_status_t st = check_layer_args(x, ids, tw, w13, s13, w2, s2, M, H, I, E, topk, flags, out);
+  moe_status_t st = check_layer_args(kind, x, ids, tw, w13, s13, w2, s2, M, H, I, E, topk, flags, out);
   if (st != MOE_OK || M == 0) return st;
   const Layout L = plan(M, H, I, E, topk, kind, flags);
   if (!ws) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
@@ -201,8 +226,8 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
   PrepArgs p{};
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.M = M; p.H = H;
-  p.kind = kind == MOE_WEIGHT_FP8 ? 1 : 2;
-  p.q = at<__half>(ws, L.xq);
+  p.kind = L.a8 ? 3 : kind == MOE_WEIGHT_FP8 ? 1 : 2;
+  p.q = at<void>(ws, L.xq);
   p.scale = at<float>(ws, L.sx);
   if (kind == MOE_WEIGHT_INT8) { p.zero_words = at<uint32_t>(ws, L.hmax); p.n_zero = static_cast<int>(L.cap); }
   const int prep_ctas = M < 2 * sms ? (M > 0 ? M : 1) : 2 * sms;
@@ -235,6 +260,19 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
   P.y = at<float>(ws, L.y);
   P.out = static_cast<__nv_bfloat16*>(out);
   P.status = a.status;
+  if (L.a8) {
+    P.xq8 = at<uint8_t>(ws, L.xq);
+    P.sx8 = at<float>(ws, L.sx);
+    P.act8 = at<uint8_t>(ws, L.act);
+    P.sa8 = at<float>(ws, L.sa);
+    P.h8 = at<uint8_t>(ws, L.h);
+    P.sh8 = at<float>(ws, L.sh);
+    err = launch_prefill_a8(P, sms, stream, hook);
+    if (err == cudaErrorInvalidConfiguration)
+      return fail(MOE_ERR_CUDA, "FP8 x FP8 kernel was not built with its designed register count");
+    if (err != cudaSuccess) return cuda_fail(err, "prefill (FP8 activations) launch");
+    return MOE_OK;
+  }
   if (L.path == MOE_PATH_PREFILL) {
     err = launch_prefill(P, kind, sms, stream, hook);
     if (err != cudaSuccess) return cuda_fail(err, "prefill launch");
@@ -289,15 +327,31 @@ moe_status_t moe_quant_act_int8(const void* x_bf16, int M, int H, int8_t* q, flo
   PrepArgs p{};
   p.x = static_cast<const __nv_bfloat16*>(x_bf16);
   p.M = M; p.H = H; p.kind = 2; p.q = q; p.scale = scale;
-  cudaError_t err = launch_quant_rows_s8(p, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t err = launch_quant_rows(p, reinterpret_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "moe_quant_act_int8 launch");
+  return MOE_OK;
+}
+
+moe_status_t moe_quant_act_fp8(const void* x_bf16, int M, int H, uint8_t* q, float* scale, moe_stream_t stream) {
+  g_last_error.clear();
+  if (M < 0 || H <= 0) return fail(MOE_ERR_INVALID_ARG, "M >= 0 and H > 0 required");
+  if (H % kQBlock) return fail(MOE_ERR_UNSUPPORTED, "H must be a multiple of 128");
+  if (M == 0) return MOE_OK;
+  if (!x_bf16 || !q || !scale) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (reinterpret_cast<uintptr_t>(x_bf16) % 16 || reinterpret_cast<uintptr_t>(q) % 4)
+    return fail(MOE_ERR_INVALID_ARG, "x must be 16-byte aligned and q 4-byte aligned");
+  PrepArgs p{};
+  p.x = static_cast<const __nv_bfloat16*>(x_bf16);
+  p.M = M; p.H = H; p.kind = 3; p.q = q; p.scale = scale;
+  cudaError_t err = launch_quant_rows(p, reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_quant_act_fp8 launch");
   return MOE_OK;
 }
 
 size_t moe_workspace_size(int M, int H, int I, int E, int topk, int weight_kind, unsigned flags) {
   if (M < 0 || H <= 0 || I <= 0 || E <= 0 || topk <= 0 || E > MOE_MAX_EXPERTS) return 0;
   if (weight_kind != MOE_WEIGHT_FP8 && weight_kind != MOE_WEIGHT_INT8) return 0;
-  if (flags & ~MOE_PATH_MASK) return 0;
+  if (!known_flags(weight_kind, flags)) return 0;
   return plan(M, H, I, E, topk, weight_kind, flags).total;
 }
 

@@ -393,8 +393,7 @@ static cudaError_t launch_skinny_occ(const SkinnyArgs& a, const void* w, uint64_
                       C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   auto kern = dec::skinny_gemm_kernel<WK, GATED, OCC>;
-  cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM,
-                                        8 + WK * 4 + (GATED ? 2 : 0) + (OCC == 3 ? 1 : 0));
+  cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM);
   if (err != cudaSuccess) return err;
   return launch_kernel(kern, dim3(OCC * num_sms), dim3(dec::NUM_THREADS), C::SMEM, s, true, mw, a);
 }

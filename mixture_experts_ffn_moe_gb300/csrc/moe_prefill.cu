@@ -532,8 +532,7 @@ static cudaError_t launch_gemm(const PrefillArgs& a, const void* w, uint64_t w_r
                 CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   auto kern = pf::prefill_gemm_kernel<WK, GATED>;
-  cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(kern), pf::SMEM_BYTES,
-                                        4 + WK * 2 + (GATED ? 1 : 0));
+  cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(kern), pf::SMEM_BYTES);
   if (err != cudaSuccess) return err;
   return launch_kernel(kern, dim3(num_sms), dim3(pf::NUM_THREADS), pf::SMEM_BYTES, s, true, mw, mb, a);
 }

@@ -1,0 +1,547 @@
+// Prefill path with FP8 activations ("A8": E4M3 codes in 1 x 128 groups, one
+// fp32 scale per token and 128 columns): FP8 x FP8 grouped GEMMs on tcgen05
+// tensor cores (kind::f8f6f4).
+//
+// The pages run their FP8 weights against BF16 activations (Xeon 6 / SGLang
+// blog, section "FP8 推理"); this mode is the FP8 x FP8 form of the grouped
+// GEMMs that the news rewrite of the LMSYS large-scale-EP blog integrates
+// (section "DeepGEMM集成"), offered next to the weight-only path because at
+// large token counts the layer is bound by tensor-core throughput, and FP8 x FP8
+// runs at twice the fp16 rate with half the operand bytes.
+//
+// Tiles are those of the weight-only prefill kernel (a token tile of one
+// expert against two 128-row weight blocks, weights on the MMA's M side), but
+// both operands stay E4M3 in shared memory: TMA writes them in the 128-byte
+// swizzled K-major layout the MMA reads, so nothing is converted.
+//
+// Block scales.  A K block of 128 is one scale block of the weights and one
+// scale group of the activations.  Its partial sums P go to TMEM, and the
+// accumulator warps fold them into fp32 registers:
+//   acc[row, token] += P[row, token] * w_scale(row block, K block) * a_scale(token, K block)
+// (the post-scaling of the OSDI'26 local-MoE summary, section "CPU 解码后端",
+// applied per tile column).  TMEM holds the partials of two K blocks (2 buffers
+// x 2 accumulators x 128 columns), so the MMAs of one K block overlap the
+// promotion of the previous one.
+//
+// Warp roles (12 warps = 3 warpgroups, 1 CTA per SM, persistent):
+//   warp 0      TMA producer of weight tiles (2 x 16 KB per K block, ring of 4)
+//   warp 1      TMEM allocator + tcgen05.mma issuer
+//   warp 2      TMA producer of activation tiles (16 KB) and activation scale vectors (ring of 8)
+//   warp 3      scale warp: per K block, the factor vectors a_scale x w_scale of both accumulators
+//   warps 4-11  accumulators (setmaxnreg: 224 registers, the first warpgroup gives up its share)
+//               promotion, then the epilogue of the tile:
+//                 GEMM1: h = SiLU(gate) * up, quantised to E4M3 per 1 x 128 group (the tile's
+//                        128 rows are one group of I) -> h codes [cap, I] and scales [I/128, cap]
+//                 GEMM2: y[slot] = acc * routing weight
+// Every wait is bounded; a time-out sets the status flag and every role drains.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sm100_ptx.cuh"
+
+namespace gbmoe {
+namespace pfa8 {
+
+using namespace sm100;
+
+constexpr int BK = 128;                  // K per stage: one 128-deep scale block (bytes of E4M3)
+constexpr int BM = 128;                  // weight rows per accumulator (MMA M)
+constexpr int MAXN = kPrefillTileTokens; // tokens per tile (MMA N <= 128)
+constexpr int W_STAGES = 4;
+constexpr int A_STAGES = 4;
+constexpr int S_STAGES = 8;              // deeper than A_STAGES + the 2 TMEM buffers the MMA may lead by
+constexpr int W_TILE = BM * BK;          // 16 KB per accumulator
+constexpr int A_TILE = MAXN * BK;        // 16 KB
+constexpr int S_SLOT = 3 * MAXN * 4;     // activation scales, factors of accumulator 0, factors of accumulator 1
+constexpr int N_ACC_WARPS = 8;
+constexpr int WARP_WTMA = 0, WARP_MMA = 1, WARP_ATMA = 2, WARP_SCALE = 3, WARP_ACC0 = 4;
+constexpr int NUM_WARPS = WARP_ACC0 + N_ACC_WARPS;
+constexpr int NUM_THREADS = NUM_WARPS * 32;
+constexpr int REGS_AT_LAUNCH = 65536 / NUM_THREADS / 8 * 8;  // what __launch_bounds__(NUM_THREADS, 1) allows
+constexpr int REGS_SUPPORT = 56;         // warpgroup 0
+constexpr int REGS_ACC = 224;            // warpgroups 1 and 2
+static_assert(128 * REGS_SUPPORT + 256 * REGS_ACC <= NUM_THREADS * REGS_AT_LAUNCH, "register split exceeds the pool");
+constexpr uint32_t TMEM_COLS = 512;      // 2 buffers x 2 accumulators x 128 columns
+
+constexpr int OFF_W = 0;
+constexpr int OFF_A = OFF_W + W_STAGES * 2 * W_TILE;
+constexpr int OFF_S = OFF_A + A_STAGES * A_TILE;
+constexpr int OFF_RED = OFF_S + S_STAGES * S_SLOT;
+constexpr int RED_BYTES = 2 * 2 * 4 * 64 * 4;  // [tile parity][column half][lane quarter][64 columns] floats
+constexpr int OFF_BAR = OFF_RED + RED_BYTES;
+constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;  // + slack to align the base to 1024
+constexpr long long kWaitLimit = 4000000000LL;    // ~2 s of SM clocks per wait
+
+struct Bars {
+  uint64_t w_full[W_STAGES];
+  uint64_t w_empty[W_STAGES];
+  uint64_t a_full[A_STAGES];
+  uint64_t a_empty[A_STAGES];
+  uint64_t s_full[S_STAGES];   // activation scale vector landed (TMA)
+  uint64_t f_full[S_STAGES];   // factor vectors written (scale warp)
+  uint64_t s_empty[S_STAGES];  // factor vectors consumed (accumulator warps)
+  uint64_t p_full[2];          // partial sums of a K block in TMEM buffer
+  uint64_t p_empty[2];
+  uint64_t red_full[2][2];     // [tile parity][column half]: the 4 warps' column maxima are written
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(Bars) <= 512, "barrier block too large");
+
+struct Args {
+  int K;                 // H (GEMM1) or I (GEMM2)
+  int rows_per_expert;   // 2I (GEMM1) or H (GEMM2)
+  int second_rows;       // row offset of the second accumulator's block: I (GEMM1) or 128 (GEMM2)
+  int n_tiles;           // output tiles per token tile
+  int n_rows_out;        // GEMM1: I (leading dimension of h codes); GEMM2: H (of y)
+  int cap;               // positions (leading dimension of the h scale rows)
+  const int4* ttiles;
+  const int32_t* num_ttiles;
+  const float* wscale;   // [E, rows/128, K/128]
+  const int32_t* sorted_ids;
+  const float* topk_w;   // GEMM2
+  uint8_t* hq;           // GEMM1 out: h codes [cap, I]
+  float* hs;             // GEMM1 out: h scales [I/128, cap]
+  float* y;              // GEMM2 out: [M*topk, H]
+  DeviceStatus* status;
+};
+
+struct Tile {
+  int e, pos0, cnt, n0, nmma;
+  bool two;
+};
+
+template <bool GATED>
+__device__ __forceinline__ Tile get_tile(const Args& p, int t) {
+  const int tt = t / p.n_tiles;
+  const int4 d = p.ttiles[tt];
+  Tile r;
+  r.e = d.x;
+  r.pos0 = d.y;
+  r.cnt = d.z;
+  const int nt = t - tt * p.n_tiles;
+  r.n0 = nt * (GATED ? BM : 2 * BM);
+  r.nmma = (d.z + 15) & ~15;
+  r.two = GATED || (r.n0 + BM < p.rows_per_expert);
+  return r;
+}
+
+__device__ __forceinline__ void fma4(float* acc, const uint32_t* p, float4 f) {
+  acc[0] = fmaf(__uint_as_float(p[0]), f.x, acc[0]);
+  acc[1] = fmaf(__uint_as_float(p[1]), f.y, acc[1]);
+  acc[2] = fmaf(__uint_as_float(p[2]), f.z, acc[2]);
+  acc[3] = fmaf(__uint_as_float(p[3]), f.w, acc[3]);
+}
+
+// Waits (bounded) for the last min(seq, stages) fills of a ring to land: a
+// producer must not exit with copies in flight into shared memory.  Fill i
+// went to slot i % stages with phase parity (i / stages) & 1.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int stages, long long seq) {
+  const long long n = seq < stages ? seq : stages;
+  for (long long i = seq - n; i < seq; ++i) {
+    int dummy = 0;
+    mbar_wait(&full[i % stages], static_cast<uint32_t>((i / stages) & 1), &dummy, nullptr, kWaitLimit);
+  }
+}
+
+template <bool GATED>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    prefill_a8_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
+                      const __grid_constant__ CUtensorMap tmap_s, Args p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sW = smem + OFF_W;
+  uint8_t* sA = smem + OFF_A;
+  float* sS = reinterpret_cast<float*>(smem + OFF_S);
+  float* red = reinterpret_cast<float*>(smem + OFF_RED);
+  Bars* bars = reinterpret_cast<Bars*>(smem + OFF_BAR);
+  volatile int* abort = &bars->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int KC = p.K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < W_STAGES; ++i) {
+      mbar_init(&bars->w_full[i], 1);
+      mbar_init(&bars->w_empty[i], 1);
+    }
+    for (int i = 0; i < A_STAGES; ++i) {
+      mbar_init(&bars->a_full[i], 1);
+      mbar_init(&bars->a_empty[i], 1);
+    }
+    for (int i = 0; i < S_STAGES; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->f_full[i], 1);
+      mbar_init(&bars->s_empty[i], N_ACC_WARPS);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->p_full[i], 1);
+      mbar_init(&bars->p_empty[i], N_ACC_WARPS);
+      mbar_init(&bars->red_full[i][0], 4);
+      mbar_init(&bars->red_full[i][1], 4);
+    }
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(&bars->tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == WARP_WTMA && lane == 0) {
+    prefetch_tmap(&tmap_w);
+    prefetch_tmap(&tmap_b);
+    prefetch_tmap(&tmap_s);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = bars->tmem_base;
+  // The weight stream and the MMA issuer need only the tile list (written two
+  // kernels back); the activation producer, the scale warp and the accumulators
+  // read the predecessor's output and wait for it.
+  if (warp == WARP_ATMA || warp >= WARP_SCALE) pdl_wait();
+  pdl_trigger();
+  const int total_tiles = *p.num_ttiles * p.n_tiles;
+  if (warp < WARP_ACC0) {
+    // ================================================================ support warpgroup
+    regs_dec<REGS_SUPPORT>();
+    if (warp == WARP_WTMA) {
+      // ---------------------------------------------------------------- weight producer
+      if (lane == 0) {
+        int ws = 0;
+        uint32_t wph = 0;
+        long long seq = 0;  // stages issued
+        bool ok = true;
+        for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+          const Tile tl = get_tile<GATED>(p, t);
+          const int row0 = tl.e * p.rows_per_expert + tl.n0;
+          for (int kc = 0; kc < KC; ++kc) {
+            if (!(ok = mbar_wait(&bars->w_empty[ws], wph ^ 1, abort, p.status, kWaitLimit))) break;
+            mbar_arrive_expect_tx(&bars->w_full[ws], (tl.two ? 2 : 1) * W_TILE);
+            uint8_t* dst = sW + ws * 2 * W_TILE;
+            tma_load_2d(dst, &tmap_w, &bars->w_full[ws], kc * BK, row0);
+            if (tl.two) tma_load_2d(dst + W_TILE, &tmap_w, &bars->w_full[ws], kc * BK, row0 + p.second_rows);
+            ++seq;
+            if (++ws == W_STAGES) { ws = 0; wph ^= 1; }
+          }
+        }
+        drain_ring(bars->w_full, W_STAGES, seq);  // never leave with copies in flight into shared memory
+      }
+    } else if (warp == WARP_ATMA) {
+      // ---------------------------------------------------------------- activation + scale producer
+      if (lane == 0) {
+        int as = 0, ss = 0;
+        uint32_t aph = 0, sph = 0;
+        long long aseq = 0, sseq = 0;  // stages issued
+        bool ok = true;
+        for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+          const Tile tl = get_tile<GATED>(p, t);
+          for (int kc = 0; kc < KC; ++kc) {
+            if (!(ok = mbar_wait(&bars->a_empty[as], aph ^ 1, abort, p.status, kWaitLimit))) break;
+            mbar_arrive_expect_tx(&bars->a_full[as], tl.nmma * BK);
+            uint8_t* dst = sA + as * A_TILE;
+            for (int r = 0; r < tl.nmma; r += 16)
+              tma_load_2d(dst + r * BK, &tmap_b, &bars->a_full[as], kc * BK, tl.pos0 + r);
+            ++aseq;
+            if (++as == A_STAGES) { as = 0; aph ^= 1; }
+
+            if (!(ok = mbar_wait(&bars->s_empty[ss], sph ^ 1, abort, p.status, kWaitLimit))) break;
+            mbar_arrive_expect_tx(&bars->s_full[ss], MAXN * 4);
+            tma_load_2d(sS + ss * (S_SLOT / 4), &tmap_s, &bars->s_full[ss], tl.pos0, kc);
+            ++sseq;
+            if (++ss == S_STAGES) { ss = 0; sph ^= 1; }
+          }
+        }
+        drain_ring(bars->a_full, A_STAGES, aseq);
+        drain_ring(bars->s_full, S_STAGES, sseq);
+      }
+    } else if (warp == WARP_MMA) {
+      // ---------------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        int ws = 0, as = 0, buf = 0;
+        uint32_t wph = 0, aph = 0;
+        uint32_t eph[2] = {0, 0};
+        bool ok = true;
+        for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+          const Tile tl = get_tile<GATED>(p, t);
+          const uint32_t idesc = idesc_e4m3_f32(BM, tl.nmma);
+          for (int kc = 0; kc < KC; ++kc) {
+            if (!(ok = mbar_wait(&bars->p_empty[buf], eph[buf] ^ 1, abort, p.status, kWaitLimit))) break;
+            if (!(ok = mbar_wait(&bars->w_full[ws], wph, abort, p.status, kWaitLimit))) break;
+            if (!(ok = mbar_wait(&bars->a_full[as], aph, abort, p.status, kWaitLimit))) break;
+            tc_fence_after();
+            const uint32_t d0 = tbase + static_cast<uint32_t>(buf * 2 * BM);
+            const uint64_t a0 = sw128_kmajor_desc(smem_addr(sW + ws * 2 * W_TILE));
+            const uint64_t a1 = sw128_kmajor_desc(smem_addr(sW + ws * 2 * W_TILE + W_TILE));
+            const uint64_t bd = sw128_kmajor_desc(smem_addr(sA + as * A_TILE));
+  #pragma unroll
+            for (int k = 0; k < BK / 32; ++k) {  // 32 bytes (K = 32) per instruction: +2 in the encoded address
+              umma_e4m3(d0, a0 + 2 * k, bd + 2 * k, idesc, k != 0);
+              if (tl.two) umma_e4m3(d0 + BM, a1 + 2 * k, bd + 2 * k, idesc, k != 0);
+            }
+            umma_commit(&bars->w_empty[ws]);
+            umma_commit(&bars->a_empty[as]);
+            umma_commit(&bars->p_full[buf]);
+            eph[buf] ^= 1;
+            buf ^= 1;
+            if (++ws == W_STAGES) { ws = 0; wph ^= 1; }
+            if (++as == A_STAGES) { as = 0; aph ^= 1; }
+          }
+        }
+        // every issued MMA must finish before TMEM is released
+        umma_commit(&bars->mma_done);
+        int dummy = 0;
+        mbar_wait(&bars->mma_done, 0, &dummy, nullptr, kWaitLimit);
+      }
+    } else if (warp == WARP_SCALE) {
+      // ---------------------------------------------------------------- scale warp
+      const int kblocks = p.K / kQBlock, rblocks = p.rows_per_expert / kQBlock;
+      int ss = 0;
+      uint32_t sph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        const Tile tl = get_tile<GATED>(p, t);
+        const float* w0 = p.wscale + (static_cast<size_t>(tl.e) * rblocks + tl.n0 / kQBlock) * kblocks;
+        const float* w1 = p.wscale + (static_cast<size_t>(tl.e) * rblocks + (tl.n0 + p.second_rows) / kQBlock) * kblocks;
+        for (int kc = 0; kc < KC; ++kc) {
+          const float s0 = __ldg(w0 + kc);
+          const float s1 = tl.two ? __ldg(w1 + kc) : 0.f;
+          if (!(ok = mbar_wait(&bars->s_full[ss], sph, abort, p.status, kWaitLimit))) break;
+          float* slot = sS + ss * (S_SLOT / 4);
+          const float4 a = reinterpret_cast<const float4*>(slot)[lane];
+          reinterpret_cast<float4*>(slot + MAXN)[lane] = make_float4(a.x * s0, a.y * s0, a.z * s0, a.w * s0);
+          reinterpret_cast<float4*>(slot + 2 * MAXN)[lane] = make_float4(a.x * s1, a.y * s1, a.z * s1, a.w * s1);
+          // the scale vector was read by generic loads; order them before its next TMA refill
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->f_full[ss]);
+          if (++ss == S_STAGES) { ss = 0; sph ^= 1; }
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- accumulators
+    regs_inc<REGS_ACC>();
+    const int q = warp & 3;                     // TMEM lane quarter this warp may access
+    const int ch = (warp - WARP_ACC0) >> 2;     // column half: tile columns 64*ch .. 64*ch+63
+    const int row = q * 32 + lane;              // accumulator row (weight row inside the block)
+    const uint32_t lane_addr = tbase + (static_cast<uint32_t>(q * 32) << 16);
+    int ntile = 0;  // tiles this CTA has finished (selects the exchange buffer and its phase)
+    int ss = 0, buf = 0;
+    uint32_t fph = 0;
+    uint32_t pph[2] = {0, 0};
+    bool ok = true;
+    for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      const Tile tl = get_tile<GATED>(p, t);
+      float acc0[64], acc1[64];
+#pragma unroll
+      for (int j = 0; j < 64; ++j) { acc0[j] = 0.f; acc1[j] = 0.f; }
+      for (int kc = 0; kc < KC; ++kc) {
+        if (!(ok = mbar_wait(&bars->f_full[ss], fph, abort, p.status, kWaitLimit))) break;
+        if (!(ok = mbar_wait(&bars->p_full[buf], pph[buf], abort, p.status, kWaitLimit))) break;
+        tc_fence_after();
+        const float* f0 = sS + ss * (S_SLOT / 4) + MAXN;
+        const float* f1 = f0 + MAXN;
+        const uint32_t base = lane_addr + static_cast<uint32_t>(buf * 2 * BM);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int col0 = ch * 64 + c * 32;
+          if (col0 < tl.nmma) {  // warp-uniform
+            uint32_t r0[32], r1[32];
+            tmem_ld32(base + col0, r0);
+            if (tl.two) tmem_ld32(base + BM + col0, r1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              fma4(acc0 + c * 32 + j, r0 + j, *reinterpret_cast<const float4*>(f0 + col0 + j));
+            if (tl.two) {
+#pragma unroll
+              for (int j = 0; j < 32; j += 4)
+                fma4(acc1 + c * 32 + j, r1 + j, *reinterpret_cast<const float4*>(f1 + col0 + j));
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars->p_empty[buf]);
+          mbar_arrive(&bars->s_empty[ss]);
+        }
+        pph[buf] ^= 1;
+        buf ^= 1;
+        if (++ss == S_STAGES) { ss = 0; fph ^= 1; }
+      }
+      if (!ok) break;
+
+      if constexpr (GATED) {
+        // h = SiLU(gate) * up; then E4M3 codes per 1 x 128 group = the 128 rows of this tile.
+        // The four warps of a column half exchange their column maxima through a
+        // buffer that alternates between tiles (a warp cannot run two tiles ahead).
+        const int rb = ntile & 1;
+        float* my_red = red + (rb * 2 + ch) * 4 * 64;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          acc0[j] = silu_f32(acc0[j]) * acc1[j];
+          const float m = warp_max(fabsf(acc0[j]));
+          if (lane == 0) my_red[q * 64 + j] = m;
+        }
+        if (lane == 0) mbar_arrive(&bars->red_full[rb][ch]);
+        if (!(ok = mbar_wait(&bars->red_full[rb][ch], static_cast<uint32_t>((ntile >> 1) & 1), abort, p.status,
+                             kWaitLimit)))
+          break;
+        const int n = tl.n0 + row;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const int col = ch * 64 + j;
+          if (col < tl.cnt) {  // warp-uniform
+            const float amax = fmaxf(fmaxf(my_red[j], my_red[64 + j]), fmaxf(my_red[128 + j], my_red[192 + j]));
+            const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+            const int pos = tl.pos0 + col;
+            p.hq[static_cast<size_t>(pos) * p.n_rows_out + n] =
+                static_cast<uint8_t>(e4m3_code(__fdiv_rn(acc0[j], s)));
+            if (q == 0 && lane == (j & 31)) p.hs[static_cast<size_t>(tl.n0 / kQBlock) * p.cap + pos] = s;
+          }
+        }
+      } else {
+        const int n = tl.n0 + row;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const int col = ch * 64 + j;
+          if (col < tl.cnt) {  // warp-uniform
+            const int pos = tl.pos0 + col;
+            const int slot = __ldg(p.sorted_ids + pos);
+            const float wgt = __ldg(p.topk_w + slot);
+            float* yr = p.y + static_cast<size_t>(slot) * p.n_rows_out;
+            yr[n] = acc0[j] * wgt;
+            if (tl.two) yr[n + BM] = acc1[j] * wgt;
+          }
+        }
+      }
+      ++ntile;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, TMEM_COLS);
+  }
+}
+
+}  // namespace pfa8
+
+// ------------------------------------------------------------------ gather
+// E4M3 activation rows and their 1 x 128 scales in sorted (expert-contiguous)
+// order; padding rows get zero codes and zero scales.  Scales are stored
+// transposed, [H/128, cap], so a token tile's scales of one K block are
+// contiguous for the TMA.
+__global__ void __launch_bounds__(256) gather_a8_kernel(const uint8_t* __restrict__ xq, const float* __restrict__ sx,
+                                                        const int32_t* __restrict__ sorted_ids,
+                                                        const int32_t* __restrict__ num_post, int n_slots, int topk,
+                                                        int H, int cap, uint8_t* __restrict__ act,
+                                                        float* __restrict__ sa) {
+  pdl_wait();
+  pdl_trigger();
+  const int rows = *num_post;
+  const int chunks = H / 16, G = H / kQBlock;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long first = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  const long long total = static_cast<long long>(rows) * chunks;
+  for (long long i = first; i < total; i += stride) {
+    const int pos = static_cast<int>(i / chunks), c = static_cast<int>(i - static_cast<long long>(pos) * chunks);
+    const int slot = __ldg(sorted_ids + pos);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (slot < n_slots) v = ld_v4(xq + static_cast<size_t>(slot / topk) * H + c * 16);
+    *reinterpret_cast<uint4*>(act + static_cast<size_t>(pos) * H + c * 16) = v;
+  }
+  const long long total_s = static_cast<long long>(G) * rows;
+  for (long long i = first; i < total_s; i += stride) {
+    const int g = static_cast<int>(i / rows), pos = static_cast<int>(i - static_cast<long long>(g) * rows);
+    const int slot = __ldg(sorted_ids + pos);
+    sa[static_cast<size_t>(g) * cap + pos] = slot < n_slots ? __ldg(sx + static_cast<size_t>(slot / topk) * G + g) : 0.f;
+  }
+}
+
+// ------------------------------------------------------------------ host side
+template <bool GATED>
+static cudaError_t launch_a8_gemm(const pfa8::Args& a, const void* w, uint64_t w_rows, const void* b,
+                                  const float* bs, int num_sms, cudaStream_t s) {
+  using namespace pfa8;
+  auto kern = prefill_a8_kernel<GATED>;
+  // The register split (setmaxnreg) is only safe when the kernel was built with
+  // the launch-bounds register count it was designed for.
+  cudaFuncAttributes fa;
+  cudaError_t err = cudaFuncGetAttributes(&fa, reinterpret_cast<const void*>(kern));
+  if (err != cudaSuccess) return err;
+  if (fa.numRegs != REGS_AT_LAUNCH) return cudaErrorInvalidConfiguration;
+  CUtensorMap mw, mb, ms;
+  if (!encode_tmap_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, static_cast<uint64_t>(a.K), w_rows, BK, BM,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, static_cast<uint64_t>(a.K),
+                      static_cast<uint64_t>(a.cap), BK, 16, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, bs, static_cast<uint64_t>(a.cap),
+                      static_cast<uint64_t>(a.K / kQBlock), MAXN, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  err = set_smem_limit_once(reinterpret_cast<const void*>(kern), SMEM_BYTES);
+  if (err != cudaSuccess) return err;
+  return launch_kernel(kern, dim3(num_sms), dim3(NUM_THREADS), SMEM_BYTES, s, true, mw, mb, ms, a);
+}
+
+cudaError_t launch_prefill_a8(const LayerPlan& P, int num_sms, cudaStream_t s, const StageHook& hook) {
+  cudaError_t err;
+  {
+    const int grid = num_sms * 8;
+    err = launch_kernel(gather_a8_kernel, dim3(grid), dim3(256), 0, s, true, P.xq8, P.sx8, P.sorted_ids,
+                        P.num_post, P.M * P.topk, P.topk, P.H, P.cap, P.act8, P.sa8);
+    if (err != cudaSuccess) return err;
+    hook("prefill_gather", s);
+  }
+  pfa8::Args g1{};
+  g1.K = P.H;
+  g1.rows_per_expert = 2 * P.I;
+  g1.second_rows = P.I;
+  g1.n_tiles = P.I / pfa8::BM;
+  g1.n_rows_out = P.I;
+  g1.cap = P.cap;
+  g1.ttiles = P.ttiles;
+  g1.num_ttiles = P.num_ttiles;
+  g1.wscale = P.s13;
+  g1.sorted_ids = P.sorted_ids;
+  g1.hq = P.h8;
+  g1.hs = P.sh8;
+  g1.status = P.status;
+  err = launch_a8_gemm<true>(g1, P.w13, static_cast<uint64_t>(P.E) * 2 * P.I, P.act8, P.sa8, num_sms, s);
+  if (err != cudaSuccess) return err;
+  hook("prefill_gemm1", s);
+  pfa8::Args g2{};
+  g2.K = P.I;
+  g2.rows_per_expert = P.H;
+  g2.second_rows = pfa8::BM;
+  g2.n_tiles = (P.H + 2 * pfa8::BM - 1) / (2 * pfa8::BM);
+  g2.n_rows_out = P.H;
+  g2.cap = P.cap;
+  g2.ttiles = P.ttiles;
+  g2.num_ttiles = P.num_ttiles;
+  g2.wscale = P.s2;
+  g2.sorted_ids = P.sorted_ids;
+  g2.topk_w = P.topk_w;
+  g2.y = P.y;
+  g2.status = P.status;
+  err = launch_a8_gemm<false>(g2, P.w2, static_cast<uint64_t>(P.E) * P.H, P.h8, P.sh8, num_sms, s);
+  if (err != cudaSuccess) return err;
+  hook("prefill_gemm2", s);
+  err = launch_combine(P.y, P.inv_pos, P.M, P.topk, P.H, P.out, num_sms, s);
+  if (err != cudaSuccess) return err;
+  hook("combine", s);
+  return cudaSuccess;
+}
+
+}  // namespace gbmoe

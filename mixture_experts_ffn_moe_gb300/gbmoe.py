@@ -18,6 +18,7 @@ MOE_OK = 0
 MOE_PATH_AUTO = 0x0
 MOE_PATH_DECODE = 0x1
 MOE_PATH_PREFILL = 0x2
+MOE_ACT_FP8_1X128 = 0x10
 MOE_WEIGHT_FP8 = 0
 MOE_WEIGHT_INT8 = 1
 MOE_MAX_EXPERTS = 1024
@@ -41,6 +42,7 @@ _SIGS = {
     "moe_align_max_padded": (_sz, [_i, _i, _i, _i]),
     "moe_align_block_size": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
     "moe_quant_act_int8": (_i, [_vp, _i, _i, _vp, _vp, _vp]),
+    "moe_quant_act_fp8": (_i, [_vp, _i, _i, _vp, _vp, _vp]),
     "moe_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _u]),
     "fused_moe_fp8": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp, _sz, _vp]),
     "fused_moe_int8": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp, _sz, _vp]),
@@ -121,6 +123,16 @@ def moe_quant_act_int8(x: torch.Tensor):
     q = torch.empty(M, H, dtype=torch.int8, device=x.device)
     s = torch.empty(M, dtype=torch.float32, device=x.device)
     _check(load().moe_quant_act_int8(_ptr(x), M, H, _ptr(q), _ptr(s), _stream(x)), "moe_quant_act_int8")
+    return q, s
+
+
+def moe_quant_act_fp8(x: torch.Tensor):
+    """bf16 [M, H] -> (E4M3 codes uint8 [M, H], fp32 scales [M, H/128]), one scale per 1 x 128 group."""
+    _need(x, torch.bfloat16, "x")
+    M, H = x.shape
+    q = torch.empty(M, H, dtype=torch.uint8, device=x.device)
+    s = torch.empty(M, max(H // 128, 1), dtype=torch.float32, device=x.device)
+    _check(load().moe_quant_act_fp8(_ptr(x), M, H, _ptr(q), _ptr(s), _stream(x)), "moe_quant_act_fp8")
     return q, s
 
 

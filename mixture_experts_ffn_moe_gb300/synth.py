@@ -49,6 +49,7 @@ class LayerShape:
     n_group: int = 1
     topk_group: int = 1
     routed_scaling: float = 1.0
+    act: str = "a16"  # FP8 layer: "a16" (bf16 activations) | "fp8_1x128" (E4M3 activations, 1 x 128 groups)
 
     @property
     def E_total(self) -> int:
@@ -66,10 +67,10 @@ def tiny(M: int = 16) -> LayerShape:
     return LayerShape(f"tiny_M{M}", M, 256, 128, 8, 2, "fp8", "softmax")
 
 
-def deepseek_r1(M: int, routing: str = "deepseek", E: int = 256) -> LayerShape:
+def deepseek_r1(M: int, routing: str = "deepseek", E: int = 256, act: str = "a16") -> LayerShape:
     """DeepSeek-R1 layer shapes; a smaller E keeps the per-expert work and shrinks the weight set."""
-    return LayerShape(f"dsr1_{routing}_M{M}" + ("" if E == 256 else f"_E{E}"), M, 7168, 2048, E, 8, "fp8",
-                      routing, shared_expert=True, n_group=8, topk_group=4)
+    return LayerShape(f"dsr1_{routing}_M{M}" + ("" if E == 256 else f"_E{E}") + ("" if act == "a16" else "_a8"),
+                      M, 7168, 2048, E, 8, "fp8", routing, shared_expert=True, n_group=8, topk_group=4, act=act)
 
 
 def qwen3_235b(M: int) -> LayerShape:

@@ -78,3 +78,22 @@ def test_host_side_argument_errors(lib):
     assert _call_fp8(lib, M=0) == 0              # empty batch is a no-op
     assert lib.moe_align_block_size(None, 4, 2, 8, 0, None, None, None, None, None) == 1
     assert lib.moe_align_block_size(None, 4, 2, 8, 512, None, None, None, None, None) == 2
+
+
+def test_fp8_activation_flag_host_checks(lib):
+    a8 = gbmoe.MOE_ACT_FP8_1X128
+    assert _call_fp8(lib, flags=a8 | gbmoe.MOE_PATH_DECODE) == 2   # FP8 x FP8 runs on tcgen05 only
+    assert b"prefill" in lib.moe_last_error()
+    assert _call_fp8(lib, flags=a8) == 3                            # valid flags: fails on the workspace
+    assert _call_fp8(lib, flags=a8 | gbmoe.MOE_PATH_PREFILL) == 3
+    p = ctypes.c_void_p(16)
+    assert lib.fused_moe_int8(p, p, p, p, p, p, p, 4, 256, 128, 8, 2, a8, p, p, 0, None) == 1  # FP8 layer only
+    # workspace: the A8 layout holds codes (1 byte) instead of fp16 rows
+    w16 = gbmoe.moe_workspace_size(4096, 7168, 2048, 257, 9, gbmoe.MOE_WEIGHT_FP8, gbmoe.MOE_PATH_PREFILL)
+    w8 = gbmoe.moe_workspace_size(4096, 7168, 2048, 257, 9, gbmoe.MOE_WEIGHT_FP8, a8)
+    assert 0 < w8 < w16
+    assert gbmoe.moe_workspace_size(4, 4096, 1536, 128, 8, gbmoe.MOE_WEIGHT_INT8, a8) == 0
+    # the standalone quantiser
+    assert lib.moe_quant_act_fp8(p, 4, 200, p, p, None) == 2        # H not a multiple of 128
+    assert lib.moe_quant_act_fp8(None, 4, 256, p, p, None) == 1
+    assert lib.moe_quant_act_fp8(None, 0, 256, None, None, None) == 0
