@@ -9,19 +9,21 @@
 // large token counts the layer is bound by tensor-core throughput, and FP8 x FP8
 // runs at twice the fp16 rate with half the operand bytes.
 //
-// Tiles are those of the weight-only prefill kernel (a token tile of one
-// expert against two 128-row weight blocks, weights on the MMA's M side), but
-// both operands stay E4M3 in shared memory: TMA writes them in the 128-byte
-// swizzled K-major layout the MMA reads, so nothing is converted.
+// A tile is a token tile of one expert (up to 128 sorted slots) against two
+// 128-row weight blocks.  Tokens are the MMA's M side (TMEM lane = token) and
+// the weight rows its N side, so every thread owns one token.  Both operands
+// stay E4M3 in shared memory: TMA writes them in the 128-byte swizzled K-major
+// layout the MMA reads, so nothing is converted.
 //
 // Block scales.  A K block of 128 is one scale block of the weights and one
 // scale group of the activations.  Its partial sums P go to TMEM, and the
 // accumulator warps fold them into fp32 registers:
-//   acc[row, token] += P[row, token] * w_scale(row block, K block) * a_scale(token, K block)
-// (the post-scaling of the OSDI'26 local-MoE summary, section "CPU 解码后端",
-// applied per tile column).  TMEM holds the partials of two K blocks (2 buffers
-// x 2 accumulators x 128 columns), so the MMAs of one K block overlap the
-// promotion of the previous one.
+//   acc[token, row] += P[token, row] * a_scale(token, K block) * w_scale(row block, K block)
+// (the post-scaling of the OSDI'26 local-MoE summary, section "CPU 解码后端").
+// Within a tile the factor is one scalar per (token, weight block), so a thread
+// needs two factors per K block.  TMEM holds the partials of two K blocks
+// (2 buffers x 2 accumulators x 128 columns), so the MMAs of one K block
+// overlap the promotion of the previous one.
 //
 // Warp roles (12 warps = 3 warpgroups, 1 CTA per SM, persistent):
 //   warp 0      TMA producer of weight tiles (2 x 16 KB per K block, ring of 4)
@@ -47,10 +49,11 @@ namespace pfa8 {
 using namespace sm100;
 
 constexpr int BK = 128;                  // K per stage: one 128-deep scale block (bytes of E4M3)
-constexpr int BM = 128;                  // weight rows per accumulator (MMA M)
-constexpr int MAXN = kPrefillTileTokens; // tokens per tile (MMA N <= 128)
+constexpr int BM = 128;                  // weight rows per accumulator (MMA N)
+constexpr int MAXN = kPrefillTileTokens; // tokens per tile (MMA M = 128)
 constexpr int W_STAGES = 4;
-constexpr int A_STAGES = 4;
+constexpr int A_STAGES = 4;  // the weight and activation rings advance together (one K block per stage)
+static_assert(W_STAGES == A_STAGES, "one stage-empty barrier serves both rings");
 constexpr int S_STAGES = 8;              // deeper than A_STAGES + the 2 TMEM buffers the MMA may lead by
 constexpr int W_TILE = BM * BK;          // 16 KB per accumulator
 constexpr int A_TILE = MAXN * BK;        // 16 KB
@@ -69,22 +72,21 @@ constexpr int OFF_W = 0;
 constexpr int OFF_A = OFF_W + W_STAGES * 2 * W_TILE;
 constexpr int OFF_S = OFF_A + A_STAGES * A_TILE;
 constexpr int OFF_RED = OFF_S + S_STAGES * S_SLOT;
-constexpr int RED_BYTES = 2 * 2 * 4 * 64 * 4;  // [tile parity][column half][lane quarter][64 columns] floats
+constexpr int RED_BYTES = 2 * 2 * MAXN * 4;  // [tile parity][column half][token] floats
 constexpr int OFF_BAR = OFF_RED + RED_BYTES;
 constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;  // + slack to align the base to 1024
 constexpr long long kWaitLimit = 4000000000LL;    // ~2 s of SM clocks per wait
 
 struct Bars {
   uint64_t w_full[W_STAGES];
-  uint64_t w_empty[W_STAGES];
   uint64_t a_full[A_STAGES];
-  uint64_t a_empty[A_STAGES];
+  uint64_t st_empty[W_STAGES];  // the MMAs of a K block have read its weight and activation stages
   uint64_t s_full[S_STAGES];   // activation scale vector landed (TMA)
   uint64_t f_full[S_STAGES];   // factor vectors written (scale warp)
   uint64_t s_empty[S_STAGES];  // factor vectors consumed (accumulator warps)
   uint64_t p_full[2];          // partial sums of a K block in TMEM buffer
   uint64_t p_empty[2];
-  uint64_t red_full[2][2];     // [tile parity][column half]: the 4 warps' column maxima are written
+  uint64_t red_full[2][4];     // [tile parity][lane quarter]: both column halves wrote their token maxima
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -129,12 +131,7 @@ __device__ __forceinline__ Tile get_tile(const Args& p, int t) {
   return r;
 }
 
-__device__ __forceinline__ void fma4(float* acc, const uint32_t* p, float4 f) {
-  acc[0] = fmaf(__uint_as_float(p[0]), f.x, acc[0]);
-  acc[1] = fmaf(__uint_as_float(p[1]), f.y, acc[1]);
-  acc[2] = fmaf(__uint_as_float(p[2]), f.z, acc[2]);
-  acc[3] = fmaf(__uint_as_float(p[3]), f.w, acc[3]);
-}
+__device__ __forceinline__ float elem(const float2* a, int j) { return (j & 1) ? a[j >> 1].y : a[j >> 1].x; }
 
 // Waits (bounded) for the last min(seq, stages) fills of a ring to land: a
 // producer must not exit with copies in flight into shared memory.  Fill i
@@ -166,11 +163,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < W_STAGES; ++i) {
       mbar_init(&bars->w_full[i], 1);
-      mbar_init(&bars->w_empty[i], 1);
-    }
-    for (int i = 0; i < A_STAGES; ++i) {
       mbar_init(&bars->a_full[i], 1);
-      mbar_init(&bars->a_empty[i], 1);
+      mbar_init(&bars->st_empty[i], 1);
     }
     for (int i = 0; i < S_STAGES; ++i) {
       mbar_init(&bars->s_full[i], 1);
@@ -180,8 +174,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->p_full[i], 1);
       mbar_init(&bars->p_empty[i], N_ACC_WARPS);
-      mbar_init(&bars->red_full[i][0], 4);
-      mbar_init(&bars->red_full[i][1], 4);
+      for (int j = 0; j < 4; ++j) mbar_init(&bars->red_full[i][j], 64);
     }
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
@@ -220,7 +213,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const Tile tl = get_tile<GATED>(p, t);
           const int row0 = tl.e * p.rows_per_expert + tl.n0;
           for (int kc = 0; kc < KC; ++kc) {
-            if (!(ok = mbar_wait(&bars->w_empty[ws], wph ^ 1, abort, p.status, kWaitLimit))) break;
+            if (!(ok = mbar_wait(&bars->st_empty[ws], wph ^ 1, abort, p.status, kWaitLimit))) break;
             mbar_arrive_expect_tx(&bars->w_full[ws], (tl.two ? 2 : 1) * W_TILE);
             uint8_t* dst = sW + ws * 2 * W_TILE;
             tma_load_2d(dst, &tmap_w, &bars->w_full[ws], kc * BK, row0);
@@ -241,7 +234,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
           const Tile tl = get_tile<GATED>(p, t);
           for (int kc = 0; kc < KC; ++kc) {
-            if (!(ok = mbar_wait(&bars->a_empty[as], aph ^ 1, abort, p.status, kWaitLimit))) break;
+            if (!(ok = mbar_wait(&bars->st_empty[as], aph ^ 1, abort, p.status, kWaitLimit))) break;
             mbar_arrive_expect_tx(&bars->a_full[as], tl.nmma * BK);
             uint8_t* dst = sA + as * A_TILE;
             for (int r = 0; r < tl.nmma; r += 16)
@@ -268,23 +261,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
           const Tile tl = get_tile<GATED>(p, t);
-          const uint32_t idesc = idesc_e4m3_f32(BM, tl.nmma);
+          const uint32_t idesc = idesc_e4m3_f32(MAXN, BM);  // M = 128 tokens, N = 128 weight rows
           for (int kc = 0; kc < KC; ++kc) {
             if (!(ok = mbar_wait(&bars->p_empty[buf], eph[buf] ^ 1, abort, p.status, kWaitLimit))) break;
             if (!(ok = mbar_wait(&bars->w_full[ws], wph, abort, p.status, kWaitLimit))) break;
             if (!(ok = mbar_wait(&bars->a_full[as], aph, abort, p.status, kWaitLimit))) break;
             tc_fence_after();
             const uint32_t d0 = tbase + static_cast<uint32_t>(buf * 2 * BM);
-            const uint64_t a0 = sw128_kmajor_desc(smem_addr(sW + ws * 2 * W_TILE));
-            const uint64_t a1 = sw128_kmajor_desc(smem_addr(sW + ws * 2 * W_TILE + W_TILE));
-            const uint64_t bd = sw128_kmajor_desc(smem_addr(sA + as * A_TILE));
+            const uint64_t ad = sw128_kmajor_desc(smem_addr(sA + as * A_TILE));           // tokens
+            const uint64_t b0 = sw128_kmajor_desc(smem_addr(sW + ws * 2 * W_TILE));        // weight block 0
+            const uint64_t b1 = sw128_kmajor_desc(smem_addr(sW + ws * 2 * W_TILE + W_TILE));  // block 1
   #pragma unroll
             for (int k = 0; k < BK / 32; ++k) {  // 32 bytes (K = 32) per instruction: +2 in the encoded address
-              umma_e4m3(d0, a0 + 2 * k, bd + 2 * k, idesc, k != 0);
-              if (tl.two) umma_e4m3(d0 + BM, a1 + 2 * k, bd + 2 * k, idesc, k != 0);
+              umma_e4m3(d0, ad + 2 * k, b0 + 2 * k, idesc, k != 0);
+              if (tl.two) umma_e4m3(d0 + BM, ad + 2 * k, b1 + 2 * k, idesc, k != 0);
             }
-            umma_commit(&bars->w_empty[ws]);
-            umma_commit(&bars->a_empty[as]);
+            umma_commit(&bars->st_empty[ws]);  // == as: both rings advance one stage per K block
             umma_commit(&bars->p_full[buf]);
             eph[buf] ^= 1;
             buf ^= 1;
@@ -307,9 +299,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const Tile tl = get_tile<GATED>(p, t);
         const float* w0 = p.wscale + (static_cast<size_t>(tl.e) * rblocks + tl.n0 / kQBlock) * kblocks;
         const float* w1 = p.wscale + (static_cast<size_t>(tl.e) * rblocks + (tl.n0 + p.second_rows) / kQBlock) * kblocks;
+        // weight block scales of 64 K blocks at a time, one load per lane (K block kc sits
+        // in lane kc % 32 of register kc / 32 % 2): the latency is paid once per 64 K blocks
+        float w0r[2] = {0.f, 0.f}, w1r[2] = {0.f, 0.f};
         for (int kc = 0; kc < KC; ++kc) {
-          const float s0 = __ldg(w0 + kc);
-          const float s1 = tl.two ? __ldg(w1 + kc) : 0.f;
+          if ((kc & 63) == 0) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int k = kc + h * 32 + lane;
+              w0r[h] = k < KC ? __ldg(w0 + k) : 0.f;
+              w1r[h] = (k < KC && tl.two) ? __ldg(w1 + k) : 0.f;
+            }
+          }
+          const int hsel = (kc >> 5) & 1;
+          const float s0 = __shfl_sync(0xffffffffu, hsel ? w0r[1] : w0r[0], kc & 31);
+          const float s1 = __shfl_sync(0xffffffffu, hsel ? w1r[1] : w1r[0], kc & 31);
           if (!(ok = mbar_wait(&bars->s_full[ss], sph, abort, p.status, kWaitLimit))) break;
           float* slot = sS + ss * (S_SLOT / 4);
           const float4 a = reinterpret_cast<const float4*>(slot)[lane];
@@ -327,8 +331,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ---------------------------------------------------------------- accumulators
     regs_inc<REGS_ACC>();
     const int q = warp & 3;                     // TMEM lane quarter this warp may access
-    const int ch = (warp - WARP_ACC0) >> 2;     // column half: tile columns 64*ch .. 64*ch+63
-    const int row = q * 32 + lane;              // accumulator row (weight row inside the block)
+    const int ch = (warp - WARP_ACC0) >> 2;     // column half: outputs 64*ch .. 64*ch+63 of each block
+    const int tok = q * 32 + lane;              // token (TMEM lane) inside the tile
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(q * 32) << 16);
     int ntile = 0;  // tiles this CTA has finished (selects the exchange buffer and its phase)
     int ss = 0, buf = 0;
@@ -337,31 +341,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
       const Tile tl = get_tile<GATED>(p, t);
-      float acc0[64], acc1[64];
+      const bool quarter_live = q * 32 < tl.cnt;  // warp-uniform: this quarter holds real tokens
+      const bool live = tok < tl.cnt;
+      float2 acc0[32], acc1[32];  // outputs 2i, 2i+1 of this thread's 64 in block 0 / block 1
 #pragma unroll
-      for (int j = 0; j < 64; ++j) { acc0[j] = 0.f; acc1[j] = 0.f; }
+      for (int j = 0; j < 32; ++j) { acc0[j] = make_float2(0.f, 0.f); acc1[j] = make_float2(0.f, 0.f); }
+      // GEMM2: the token's slot now, its routing weight after the first K block (off the critical path)
+      int slot = 0;
+      float wgt = 0.f;
+      if constexpr (!GATED) {
+        if (live) slot = __ldg(p.sorted_ids + tl.pos0 + tok);
+      }
       for (int kc = 0; kc < KC; ++kc) {
         if (!(ok = mbar_wait(&bars->f_full[ss], fph, abort, p.status, kWaitLimit))) break;
         if (!(ok = mbar_wait(&bars->p_full[buf], pph[buf], abort, p.status, kWaitLimit))) break;
         tc_fence_after();
-        const float* f0 = sS + ss * (S_SLOT / 4) + MAXN;
-        const float* f1 = f0 + MAXN;
-        const uint32_t base = lane_addr + static_cast<uint32_t>(buf * 2 * BM);
+        if (quarter_live) {
+          const float* fs = sS + ss * (S_SLOT / 4);
+          const float2 fa = make_float2(fs[MAXN + tok], fs[MAXN + tok]);          // a_scale x w_scale, block 0
+          const float2 fb = make_float2(fs[2 * MAXN + tok], fs[2 * MAXN + tok]);  // block 1
+          const uint32_t base = lane_addr + static_cast<uint32_t>(buf * 2 * BM + ch * 64);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int col0 = ch * 64 + c * 32;
-          if (col0 < tl.nmma) {  // warp-uniform
+          for (int c = 0; c < 2; ++c) {
             uint32_t r0[32], r1[32];
-            tmem_ld32(base + col0, r0);
-            if (tl.two) tmem_ld32(base + BM + col0, r1);
+            tmem_ld32(base + c * 32, r0);
+            if (tl.two) tmem_ld32(base + BM + c * 32, r1);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-              fma4(acc0 + c * 32 + j, r0 + j, *reinterpret_cast<const float4*>(f0 + col0 + j));
+            for (int j = 0; j < 32; j += 2)
+              acc0[(c * 32 + j) / 2] =
+                  __ffma2_rn(make_float2(__uint_as_float(r0[j]), __uint_as_float(r0[j + 1])), fa, acc0[(c * 32 + j) / 2]);
             if (tl.two) {
 #pragma unroll
-              for (int j = 0; j < 32; j += 4)
-                fma4(acc1 + c * 32 + j, r1 + j, *reinterpret_cast<const float4*>(f1 + col0 + j));
+              for (int j = 0; j < 32; j += 2)
+                acc1[(c * 32 + j) / 2] = __ffma2_rn(make_float2(__uint_as_float(r1[j]), __uint_as_float(r1[j + 1])),
+                                                    fb, acc1[(c * 32 + j) / 2]);
             }
           }
         }
@@ -371,6 +385,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_arrive(&bars->p_empty[buf]);
           mbar_arrive(&bars->s_empty[ss]);
         }
+        if constexpr (!GATED) {
+          if (kc == 0 && live) wgt = __ldg(p.topk_w + slot);  // the slot has arrived by now
+        }
         pph[buf] ^= 1;
         buf ^= 1;
         if (++ss == S_STAGES) { ss = 0; fph ^= 1; }
@@ -378,46 +395,58 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
 
       if constexpr (GATED) {
-        // h = SiLU(gate) * up; then E4M3 codes per 1 x 128 group = the 128 rows of this tile.
-        // The four warps of a column half exchange their column maxima through a
-        // buffer that alternates between tiles (a warp cannot run two tiles ahead).
-        const int rb = ntile & 1;
-        float* my_red = red + (rb * 2 + ch) * 4 * 64;
+        // h = SiLU(gate) * up for this token's 64 outputs; its 1 x 128 group (the tile's 128
+        // outputs) is split between this warp and the warp of the other column half, which
+        // exchange their maxima through a buffer that alternates between tiles.
+        float hv[64];
+        float m = 0.f;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          acc0[j] = silu_f32(acc0[j]) * acc1[j];
-          const float m = warp_max(fabsf(acc0[j]));
-          if (lane == 0) my_red[q * 64 + j] = m;
+          const float g = elem(acc0, j);
+          hv[j] = g * __frcp_rn(1.0f + __expf(-g)) * elem(acc1, j);
+          m = fmaxf(m, fabsf(hv[j]));
         }
-        if (lane == 0) mbar_arrive(&bars->red_full[rb][ch]);
-        if (!(ok = mbar_wait(&bars->red_full[rb][ch], static_cast<uint32_t>((ntile >> 1) & 1), abort, p.status,
+        const int rb = ntile & 1;
+        red[(rb * 2 + ch) * MAXN + tok] = m;
+        mbar_arrive(&bars->red_full[rb][q]);
+        if (!(ok = mbar_wait(&bars->red_full[rb][q], static_cast<uint32_t>((ntile >> 1) & 1), abort, p.status,
                              kWaitLimit)))
           break;
-        const int n = tl.n0 + row;
+        const float amax = fmaxf(m, red[(rb * 2 + (ch ^ 1)) * MAXN + tok]);
+        if (live) {
+          // s = amax / 448 and codes of h / s, by reciprocals (h codes are covered by the layer tolerance)
+          const float s = amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f;
+          const float inv = amax > 0.f ? 448.0f * __frcp_rn(amax) : 1.0f;
+          const int pos = tl.pos0 + tok;
+          uint4* dst = reinterpret_cast<uint4*>(p.hq + static_cast<size_t>(pos) * p.n_rows_out + tl.n0 + ch * 64);
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int col = ch * 64 + j;
-          if (col < tl.cnt) {  // warp-uniform
-            const float amax = fmaxf(fmaxf(my_red[j], my_red[64 + j]), fmaxf(my_red[128 + j], my_red[192 + j]));
-            const float s = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-            const int pos = tl.pos0 + col;
-            p.hq[static_cast<size_t>(pos) * p.n_rows_out + n] =
-                static_cast<uint8_t>(e4m3_code(__fdiv_rn(acc0[j], s)));
-            if (q == 0 && lane == (j & 31)) p.hs[static_cast<size_t>(tl.n0 / kQBlock) * p.cap + pos] = s;
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int j = v * 16 + u * 4;
+              const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(hv[j] * inv, hv[j + 1] * inv), __NV_SATFINITE,
+                                                           __NV_E4M3);
+              const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(hv[j + 2] * inv, hv[j + 3] * inv),
+                                                           __NV_SATFINITE, __NV_E4M3);
+              w[u] = lo | (hi << 16);
+            }
+            dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
           }
+          if (ch == 0) p.hs[static_cast<size_t>(tl.n0 / kQBlock) * p.cap + pos] = s;
         }
       } else {
-        const int n = tl.n0 + row;
+        if (live) {
+          float4* yr = reinterpret_cast<float4*>(p.y + static_cast<size_t>(slot) * p.n_rows_out + tl.n0 + ch * 64);
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int col = ch * 64 + j;
-          if (col < tl.cnt) {  // warp-uniform
-            const int pos = tl.pos0 + col;
-            const int slot = __ldg(p.sorted_ids + pos);
-            const float wgt = __ldg(p.topk_w + slot);
-            float* yr = p.y + static_cast<size_t>(slot) * p.n_rows_out;
-            yr[n] = acc0[j] * wgt;
-            if (tl.two) yr[n + BM] = acc1[j] * wgt;
+          for (int v = 0; v < 16; ++v)
+            yr[v] = make_float4(acc0[2 * v].x * wgt, acc0[2 * v].y * wgt, acc0[2 * v + 1].x * wgt,
+                                acc0[2 * v + 1].y * wgt);
+          if (tl.two) {
+#pragma unroll
+            for (int v = 0; v < 16; ++v)
+              yr[BM / 4 + v] = make_float4(acc1[2 * v].x * wgt, acc1[2 * v].y * wgt, acc1[2 * v + 1].x * wgt,
+                                           acc1[2 * v + 1].y * wgt);
           }
         }
       }
