@@ -8,16 +8,20 @@
 // The expert-contiguous row layout is the "contiguous" grouped-GEMM layout of
 // the LMSYS large-scale-EP news rewrite (section "DeepGEMM integration").
 //
-// Swap-AB: weights are the MMA's M = 128 side, tokens its N side (16..128,
-// a multiple of 16), so a tile with few tokens wastes little tensor work.
-// Each tile keeps two TMEM accumulators against one activation tile:
+// Each tile pairs two 128-row weight blocks with one activation tile:
 //  * GEMM1: 128 gate rows and the matching 128 up rows, A x [B1, B2] =
 //    [C1, C2], and the epilogue computes SiLU(C1) * C2 (Xeon 6 / SGLang blog,
 //    section "MoE");
 //  * GEMM2: two consecutive 128-row blocks of W2, so every activation byte
 //    fetched feeds 256 output rows.
-// TMEM holds two such accumulator pairs (4 x 128 columns), so the epilogue of
-// one tile overlaps the MMAs of the next.
+// Orientation (measured per GEMM).  GEMM1, and GEMM2 with INT8 weights, put
+// the tokens on the MMA's M = 128 side and both converted weight blocks,
+// adjacent in shared memory, on its N = 256 side: one MMA per K step instead
+// of two, and an epilogue in which each thread finishes one token.  The FP8
+// GEMM2 keeps weights on the M side and tokens as N (16..128, a multiple of
+// 16, swap-AB), where short token tiles read less activation data.
+// TMEM holds two accumulators of 256 columns, so the epilogue of one tile
+// overlaps the MMAs of the next.
 //
 // Weights stay FP8 E4M3 (or INT8) in HBM.  TMA brings raw 128x64-byte weight
 // tiles into shared memory; converter warps expand them to fp16 in registers
@@ -128,6 +132,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total_tiles = *p.num_ttiles * p.n_tiles;
+  // Orientation (measured per GEMM): tokens on the MMA's M side and both weight blocks as one N = 256
+  // operand for GEMM1 and for INT8; weights on the M side (two MMAs of N = tokens) for the FP8 down
+  // projection, whose 128-token padding of the M side cost more shared-memory bandwidth than it saved.
+  constexpr bool TOKM = GATED || WK == MOE_WEIGHT_INT8;
   const int KC = p.K / BK;
   const int second_rows = GATED ? p.up_offset : BM;  // row offset of the second accumulator's block
 
@@ -242,7 +250,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
         const Tile tl = get_tile<GATED>(p, t);
-        const uint32_t idesc = idesc_f16_f32(BM, tl.nmma);
+        // TOKM: M = 128 tokens, N = both weight blocks at once (256 rows; 128 when the second is absent);
+        // else M = 128 weight rows per block, N = the tile's tokens
+        const uint32_t idesc = TOKM ? idesc_f16_f32(MAXN, tl.two ? 2 * BM : BM) : idesc_f16_f32(BM, tl.nmma);
         const uint32_t d0 = tbase + static_cast<uint32_t>(buf * 2 * BM);
         if (!(ok = mbar_wait(&bars->acc_empty[buf], eph[buf] ^ 1, abort, p.status, kWaitLimit))) break;
         tc_fence_after();
@@ -250,14 +260,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!(ok = mbar_wait(&bars->conv_full[cs], cph, abort, p.status, kWaitLimit))) break;
           if (!(ok = mbar_wait(&bars->act_full[as], aph, abort, p.status, kWaitLimit))) break;
           tc_fence_after();
-          const uint64_t a0 = sw128_kmajor_desc(smem_addr(sA + cs * 2 * A_TILE));
-          const uint64_t a1 = sw128_kmajor_desc(smem_addr(sA + cs * 2 * A_TILE + A_TILE));
-          const uint64_t bd = sw128_kmajor_desc(smem_addr(sB + as * B_TILE));
+          const uint64_t xd = sw128_kmajor_desc(smem_addr(sB + as * B_TILE));       // tokens
+          const uint64_t wd = sw128_kmajor_desc(smem_addr(sA + cs * 2 * A_TILE));  // converted weight blocks
+          const uint64_t wd1 = sw128_kmajor_desc(smem_addr(sA + cs * 2 * A_TILE + A_TILE));  // second block alone
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
+          for (int k = 0; k < BK / 16; ++k) {  // +32 bytes along K per step
             const uint32_t acc = (kc | k) != 0;
-            umma_f16(d0, a0 + 2 * k, bd + 2 * k, idesc, acc);  // +32 bytes along K per step
-            if (tl.two) umma_f16(d0 + BM, a1 + 2 * k, bd + 2 * k, idesc, acc);
+            if constexpr (TOKM) {
+              // tokens (A, M side) x the two weight blocks, adjacent in shared memory (B, N side)
+              umma_f16(d0, xd + 2 * k, wd + 2 * k, idesc, acc);
+            } else {
+              umma_f16(d0, wd + 2 * k, xd + 2 * k, idesc, acc);
+              if (tl.two) umma_f16(d0 + BM, wd1 + 2 * k, xd + 2 * k, idesc, acc);
+            }
           }
           umma_commit(&bars->conv_empty[cs]);
           umma_commit(&bars->act_empty[as]);
@@ -352,48 +367,92 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // ---------------------------------------------------------------- epilogue
+    // TMEM lane = token: every thread finishes one token's outputs of the tile
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int row = q * 32 + lane;
+    const int tok = q * 32 + lane;
     uint32_t fph[2] = {0, 0};
     int buf = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
       const Tile tl = get_tile<GATED>(p, t);
+      const bool live = tok < tl.cnt;
+      const int pos = tl.pos0 + tok;
       if (!(ok = mbar_wait(&bars->acc_full[buf], fph[buf], abort, p.status, kWaitLimit))) break;
       tc_fence_after();
       const uint32_t lane_addr = tbase + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * 2 * BM);
+      const float* chs = p.wscale + static_cast<size_t>(tl.e) * p.rows_per_expert;  // INT8 channel scales
       if constexpr (GATED) {
-        const int n = tl.n0 + row;
-        float swg = 1.f, swu = 1.f;
-        if constexpr (WK == MOE_WEIGHT_INT8) {
-          swg = __ldg(p.wscale + static_cast<size_t>(tl.e) * p.rows_per_expert + n);
-          swu = __ldg(p.wscale + static_cast<size_t>(tl.e) * p.rows_per_expert + p.up_offset + n);
-        }
-        for (int c0 = 0; c0 < tl.nmma; c0 += 32) {
+        float sx = 1.f, hmax = 0.f;
+        if constexpr (WK == MOE_WEIGHT_INT8) sx = live ? __ldg(p.sx + __ldg(p.sorted_ids + pos) / p.topk) : 0.f;
+        for (int c0 = 0; c0 < BM; c0 += 32) {  // gate columns c0.., up columns BM + c0..
           uint32_t g[32], u[32];
-          __syncwarp();
           tmem_ld32(lane_addr + c0, g);
           tmem_ld32(lane_addr + BM + c0, u);
           tmem_ld_wait();
+          const int n = tl.n0 + c0;
+          if constexpr (WK == MOE_WEIGHT_FP8) {
+            uint32_t hw[16];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int col = c0 + j;
-            if (col >= tl.cnt) continue;  // warp-uniform
-            const int pos = tl.pos0 + col;
-            const float gv = __uint_as_float(g[j]), uv = __uint_as_float(u[j]);
-            if constexpr (WK == MOE_WEIGHT_FP8) {
-              reinterpret_cast<__half*>(p.out)[static_cast<size_t>(pos) * p.out_ld + n] =
-                  __float2half_rn(silu_f32(gv) * uv);
-            } else {
-              const float sx = __ldg(p.sx + __ldg(p.sorted_ids + pos) / p.topk);
-              const float h = silu_f32(gv * sx * swg) * (uv * sx * swu);
-              reinterpret_cast<float*>(p.out)[static_cast<size_t>(pos) * p.out_ld + n] = h;
-              const float m = warp_max(fabsf(h));
-              if (lane == 0) atomicMax(p.hmax + pos, __float_as_uint(m));
+            for (int j = 0; j < 16; ++j) {
+              const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
+              hw[j] = pack_half2(silu_f32(g0) * __uint_as_float(u[2 * j]), silu_f32(g1) * __uint_as_float(u[2 * j + 1]));
+            }
+            if (live) {
+              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(p.out) + static_cast<size_t>(pos) * p.out_ld + n);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) dst[v] = make_uint4(hw[4 * v], hw[4 * v + 1], hw[4 * v + 2], hw[4 * v + 3]);
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + static_cast<size_t>(pos) * p.out_ld + n);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const float4 sg = __ldg(reinterpret_cast<const float4*>(chs + n) + v);
+              const float4 su = __ldg(reinterpret_cast<const float4*>(chs + p.up_offset + n) + v);
+              float h[4];
+              const float sgv[4] = {sg.x, sg.y, sg.z, sg.w}, suv[4] = {su.x, su.y, su.z, su.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int j = 4 * v + i;
+                h[i] = silu_f32(__uint_as_float(g[j]) * sx * sgv[i]) * (__uint_as_float(u[j]) * sx * suv[i]);
+                hmax = fmaxf(hmax, fabsf(h[i]));
+              }
+              if (live) dst[v] = make_float4(h[0], h[1], h[2], h[3]);
             }
           }
         }
+        if constexpr (WK == MOE_WEIGHT_INT8) {
+          if (live) atomicMax(p.hmax + pos, __float_as_uint(hmax));
+        }
+      } else if constexpr (TOKM) {
+        int slot = 0;
+        float wgt = 0.f;
+        if (live) {
+          slot = __ldg(p.sorted_ids + pos);
+          wgt = __ldg(p.topk_w + slot);
+          if constexpr (WK == MOE_WEIGHT_INT8) wgt *= __ldg(p.sh + pos);
+        }
+#pragma unroll 1
+        for (int c0 = 0; c0 < (tl.two ? 2 * BM : BM); c0 += 32) {  // output rows n0 + c0..
+          uint32_t g[32];
+          tmem_ld32(lane_addr + c0, g);
+          tmem_ld_wait();
+          const int n = tl.n0 + c0;
+          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + static_cast<size_t>(slot) * p.out_ld + n);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            float4 sc = make_float4(wgt, wgt, wgt, wgt);
+            if constexpr (WK == MOE_WEIGHT_INT8) {
+              const float4 cs = __ldg(reinterpret_cast<const float4*>(chs + n) + v);
+              sc = make_float4(wgt * cs.x, wgt * cs.y, wgt * cs.z, wgt * cs.w);
+            }
+            if (live)
+              dst[v] = make_float4(__uint_as_float(g[4 * v]) * sc.x, __uint_as_float(g[4 * v + 1]) * sc.y,
+                                   __uint_as_float(g[4 * v + 2]) * sc.z, __uint_as_float(g[4 * v + 3]) * sc.w);
+          }
+        }
       } else {
+        // weights on the M side: TMEM lane = output row, columns = tokens
+        const int row = tok;
 #pragma unroll 1
         for (int a = 0; a < 2; ++a) {
           if (a == 1 && !tl.two) break;
