@@ -88,6 +88,36 @@ def _stable_topk_desc(score: torch.Tensor, k: int) -> torch.Tensor:
     return torch.argsort(-score, dim=-1, stable=True)[:, :k]
 
 
+def _router_logits(shape: LayerShape, g: torch.Generator) -> torch.Tensor:
+    """Router logits [M, E] in float64 for the softmax / deepseek / deepseek_zipf recipes."""
+    M, E = shape.M, shape.E
+    if shape.routing in ("softmax", "deepseek"):
+        return torch.randn(M, E, generator=g, dtype=torch.float32).double()
+    if shape.routing == "deepseek_zipf":
+        perm = torch.randperm(E, generator=g)
+        ranks = torch.arange(1, E + 1, dtype=torch.float64)
+        p = ranks.pow(-1.1)
+        p = p / p.sum()
+        u = torch.rand(M, E, generator=g, dtype=torch.float64).clamp_(1e-300, 1.0 - 1e-16)
+        gumbel = -torch.log(-torch.log(u))
+        return torch.log(p[perm])[None, :] + gumbel
+    raise ValueError(f"routing {shape.routing!r} draws no logits")
+
+
+def make_router_logits(shape: LayerShape, seed: int) -> torch.Tensor:
+    """The router logits make_routing draws for (shape, seed), rounded to fp32 [M, E].
+
+    For the softmax and deepseek recipes the logits are fp32 draws, so this is
+    exactly what make_routing ranks; the Zipf recipe's float64 logits are rounded.
+    """
+    return _router_logits(shape, _cpu_gen(seed, 1)).float().contiguous()
+
+
+def make_router_bias(E: int, seed: int, std: float = 0.05) -> torch.Tensor:
+    """A selection bias per expert (fp32 [E], N(0, std)), standing in for a learnt load-balancing correction."""
+    return (torch.randn(E, generator=_cpu_gen(seed, 5), dtype=torch.float32) * std).contiguous()
+
+
 def make_routing(shape: LayerShape, seed: int):
     """Router choices (topk_ids int32 [M, topk_total], topk_weights fp32) on the CPU.
 
@@ -112,22 +142,13 @@ def make_routing(shape: LayerShape, seed: int):
         w = torch.sigmoid(torch.randn(M, k, generator=g, dtype=torch.float64))
         w = w / w.sum(-1, keepdim=True)
     elif shape.routing == "softmax":
-        logits = torch.randn(M, E, generator=g, dtype=torch.float32)
-        p = torch.softmax(logits.double(), dim=-1)
+        logits = _router_logits(shape, g)
+        p = torch.softmax(logits, dim=-1)
         ids = _stable_topk_desc(p, k)
         w = p.gather(1, ids)
         w = w / w.sum(-1, keepdim=True)
     elif shape.routing in ("deepseek", "deepseek_zipf"):
-        if shape.routing == "deepseek":
-            logits = torch.randn(M, E, generator=g, dtype=torch.float32).double()
-        else:
-            perm = torch.randperm(E, generator=g)
-            ranks = torch.arange(1, E + 1, dtype=torch.float64)
-            p = ranks.pow(-1.1)
-            p = p / p.sum()
-            u = torch.rand(M, E, generator=g, dtype=torch.float64).clamp_(1e-300, 1.0 - 1e-16)
-            gumbel = -torch.log(-torch.log(u))
-            logits = torch.log(p[perm])[None, :] + gumbel
+        logits = _router_logits(shape, g)
         s = torch.sigmoid(logits)
         gs = E // shape.n_group
         grouped = s.view(M, shape.n_group, gs)

@@ -26,12 +26,18 @@ computes, in float64 numpy over dequantised weights:
   fusion paragraph);
 * the optional FP8 x FP8 ("A8") mode of the FP8 layer, in which the
   activations and the intermediate h are quantised to E4M3 in groups of 1 x 128
-  (a reading: the pages keep FP8 activations in BF16, see quant_fp8_1x128).
+  (a reading: the pages keep FP8 activations in BF16, see quant_fp8_1x128);
+* the router's gating functions that produce topk_ids / topk_weights from
+  logits (softmax top-k renormalised; sigmoid with a selection bias and
+  group-limited top-k).  The pages take the router's output as given; these
+  follow the measured layers' model configurations.
 
 Precision: float64 accumulation everywhere, except that every decision that
 turns a float into an integer code (activation quantisation) is taken in
 float32 with IEEE division and round-half-to-even, the same precision the
-GPU kernels use for that decision.
+GPU kernels use for that decision.  The gating functions rank in float64:
+their results are exact rankings, and the GPU gate (which ranks in float32)
+is compared with them only where the ranking margin exceeds float32 error.
 """
 from __future__ import annotations
 
@@ -178,6 +184,57 @@ def dequant_fp8_1x128(codes, scale) -> np.ndarray:
     a = _e4m3_table()[codes].reshape(R, C // QBLOCK, QBLOCK)
     a = a * np.asarray(scale, dtype=np.float64)[..., None]
     return a.reshape(R, C)
+
+
+# ----------------------------------------------------------------------------
+# Gating: router logits -> (topk_ids, topk_weights).  Not on the pages (they
+# take the router's choices as given); the two functions follow the layer
+# configurations the hot path is measured on: softmax top-k renormalised
+# (Qwen3-style) and sigmoid scores with bias-corrected group-limited top-k
+# (DeepSeek-style).  Ties always go to the lower index.
+# ----------------------------------------------------------------------------
+
+
+def _stable_desc(v, axis=-1):
+    """Indices sorting v in descending order; equal values keep ascending index order."""
+    return np.argsort(-v, axis=axis, kind="stable")
+
+
+def gate_softmax_topk(logits, k: int):
+    """logits [M, E] -> (ids int32 [M, k], weights float64 [M, k]).
+
+    p = softmax(logits) in float64; the k largest p (ties to the lower index);
+    weights p_sel / sum(p_sel).
+    """
+    l = np.asarray(logits, dtype=np.float64)
+    p = np.exp(l - l.max(axis=-1, keepdims=True))
+    p /= p.sum(axis=-1, keepdims=True)
+    ids = _stable_desc(p)[:, :k]
+    w = np.take_along_axis(p, ids, axis=-1)
+    return ids.astype(np.int32), w / w.sum(axis=-1, keepdims=True)
+
+
+def gate_grouped_sigmoid_topk(logits, k: int, n_group: int, topk_group: int, bias=None, routed_scaling=1.0):
+    """logits [M, E] -> (ids int32 [M, k], weights float64 [M, k]).
+
+    s = sigmoid(logits) in float64 and b = s + bias (selection only).  The E
+    experts form n_group consecutive groups; a group's score is the sum of its
+    two largest b; the topk_group best groups are kept; the k largest b inside
+    them are chosen.  Weights are s_sel / sum(s_sel) times routed_scaling.
+    """
+    l = np.asarray(logits, dtype=np.float64)
+    M, E = l.shape
+    s = 1.0 / (1.0 + np.exp(-l))
+    b = s + (0.0 if bias is None else np.asarray(bias, dtype=np.float64)[None, :])
+    grouped = b.reshape(M, n_group, E // n_group)
+    gscore = -np.sort(-grouped, axis=-1)[..., :2].sum(axis=-1)
+    keep = _stable_desc(gscore)[:, :topk_group]
+    in_kept = np.zeros((M, n_group), dtype=bool)
+    np.put_along_axis(in_kept, keep, True, axis=-1)
+    masked = np.where(np.repeat(in_kept, E // n_group, axis=-1), b, -np.inf)
+    ids = _stable_desc(masked)[:, :k]
+    w = np.take_along_axis(s, ids, axis=-1)
+    return ids.astype(np.int32), w / w.sum(axis=-1, keepdims=True) * routed_scaling
 
 
 # ----------------------------------------------------------------------------

@@ -458,3 +458,155 @@ def test_a8_layer_close_to_a16():
     assert 1e-3 < rel < 6e-2
     sub = oracle.fused_moe_rows(**d, kind="fp8", tokens=[2, 17], act="fp8_1x128")
     np.testing.assert_allclose(sub, a8[[2, 17]], rtol=1e-11, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------
+# Gating.  Pins: the selection against exhaustive search over expert subsets on
+# integer-valued logits (exact sums, planted ties), torch.topk on tie-free
+# inputs, closed forms of the weights, and the group rule checked as an
+# invariant rather than re-executed.
+# ----------------------------------------------------------------------------
+
+
+def _best_subset_lexmin(score, k):
+    """Exhaustive: the k-subset of maximal total score; among equal totals the
+    lexicographically smallest index tuple (lower indices win ties)."""
+    best = None
+    for c in itertools.combinations(range(len(score)), k):
+        tot = sum(score[i] for i in c)
+        if best is None or tot > best[0]:
+            best = (tot, c)
+    return best[1]
+
+
+def test_gate_softmax_selection_brute_force_with_ties():
+    rng = np.random.default_rng(31)
+    for trial in range(300):
+        E = int(rng.integers(2, 8))
+        k = int(rng.integers(1, E + 1))
+        lg = rng.integers(-3, 4, size=E).astype(np.float64)  # small integers: many exact ties
+        ids, w = oracle.gate_softmax_topk(lg[None, :], k)
+        want = _best_subset_lexmin(lg, k)
+        assert tuple(sorted(ids[0].tolist())) == want
+        # output order: descending score, equal scores by ascending index
+        order = sorted(want, key=lambda i: (-lg[i], i))
+        assert ids[0].tolist() == order
+
+
+def test_gate_softmax_weights_closed_form():
+    rng = np.random.default_rng(32)
+    lg = rng.standard_normal((50, 16)).astype(np.float32)
+    # k = E: the weights are the softmax itself (computed here with scipy)
+    from scipy.special import softmax
+    ids, w = oracle.gate_softmax_topk(lg, 16)
+    np.testing.assert_allclose(w, np.take_along_axis(softmax(lg.astype(np.float64), axis=-1), ids, -1),
+                               rtol=1e-13)
+    # k = 1: weight 1; general k: ratios exp(l_i - l_j) and unit sum
+    _, w1 = oracle.gate_softmax_topk(lg, 1)
+    np.testing.assert_array_equal(w1, 1.0)
+    ids, w = oracle.gate_softmax_topk(lg, 4)
+    l_sel = np.take_along_axis(lg.astype(np.float64), ids, -1)
+    np.testing.assert_allclose(w[:, 1:] / w[:, :1], np.exp(l_sel[:, 1:] - l_sel[:, :1]), rtol=1e-13)
+    np.testing.assert_allclose(w.sum(-1), 1.0, rtol=1e-14)
+    # tie-free input: the same set and order as torch.topk
+    tv, ti = torch.topk(torch.from_numpy(lg.astype(np.float64)), 4, dim=-1)
+    np.testing.assert_array_equal(ids, ti.numpy())
+
+
+def test_gate_grouped_single_group_is_plain_sigmoid_topk():
+    rng = np.random.default_rng(33)
+    lg = rng.standard_normal((40, 64)).astype(np.float32)
+    ids, w = oracle.gate_grouped_sigmoid_topk(lg, 6, n_group=1, topk_group=1, routed_scaling=2.5)
+    s = torch.sigmoid(torch.from_numpy(lg.astype(np.float64)))
+    tv, ti = torch.topk(s, 6, dim=-1)
+    np.testing.assert_array_equal(ids, ti.numpy())
+    np.testing.assert_allclose(w, (tv / tv.sum(-1, keepdim=True) * 2.5).numpy(), rtol=1e-14)
+    # keeping every group changes nothing either
+    ids8, w8 = oracle.gate_grouped_sigmoid_topk(lg, 6, n_group=8, topk_group=8, routed_scaling=2.5)
+    np.testing.assert_array_equal(ids8, ids)
+    np.testing.assert_allclose(w8, w, rtol=0)
+
+
+def _check_grouped_invariants(lg, bias, ids, w, k, n_group, topk_group, scale):
+    """The group rule stated as properties of the answer."""
+    M, E = lg.shape
+    gs = E // n_group
+    s = 1.0 / (1.0 + np.exp(-lg.astype(np.float64)))
+    b = s + bias[None, :]
+    for t in range(M):
+        gscore = np.array([np.sort(b[t, g * gs:(g + 1) * gs])[-2:].sum() for g in range(n_group)])
+        chosen = set(ids[t].tolist())
+        assert len(chosen) == k
+        groups = {i // gs for i in chosen}
+        assert len(groups) <= topk_group
+        # some kept set of topk_group groups contains them all, and no group outside
+        # a kept set scores higher than one inside it: the chosen groups are among
+        # the topk_group best (lower index on equal scores)
+        rank = sorted(range(n_group), key=lambda g: (-gscore[g], g))
+        kept = set(rank[:topk_group])
+        assert groups <= kept
+        # within the kept groups nothing unchosen beats a chosen expert
+        cand = [i for i in range(E) if i // gs in kept]
+        worst = min(b[t, i] for i in chosen)
+        for i in cand:
+            if i not in chosen:
+                assert b[t, i] < worst or (b[t, i] == worst and i > max(j for j in chosen if b[t, j] == worst))
+        # weights: unbiased scores, renormalised, scaled
+        ss = s[t, ids[t]]
+        np.testing.assert_allclose(w[t], ss / ss.sum() * scale, rtol=1e-14)
+
+
+def test_gate_grouped_invariants_random_and_tied():
+    rng = np.random.default_rng(34)
+    for trial in range(60):
+        n_group = int(rng.choice([2, 4, 8]))
+        gs = int(rng.choice([2, 4, 8]))
+        E = n_group * gs
+        topk_group = int(rng.integers(1, n_group + 1))
+        k = int(rng.integers(1, min(8, topk_group * gs) + 1))
+        if trial % 2:
+            lg = rng.integers(-2, 3, size=(5, E)).astype(np.float32)  # ties inside and across groups
+            bias = np.zeros(E)
+        else:
+            lg = rng.standard_normal((5, E)).astype(np.float32)
+            bias = rng.standard_normal(E) * 0.1
+        scale = float(rng.choice([1.0, 2.5]))
+        ids, w = oracle.gate_grouped_sigmoid_topk(lg, k, n_group, topk_group, bias=bias, routed_scaling=scale)
+        _check_grouped_invariants(lg, bias, ids, w, k, n_group, topk_group, scale)
+
+
+def test_gate_grouped_hand_worked_case():
+    # 8 experts in 4 groups of 2, keep 2 groups, pick 2.  Sigmoid is monotone, so
+    # ranks follow the logits:  group scores (top-2 sums of s) order the groups
+    # 3 > 0 > 1 > 2; the best expert overall (5, group 2) is excluded.
+    lg = np.array([[1.0, 0.5, 0.2, 0.6, -3.0, 2.0, 0.9, 0.8]])
+    ids, w = oracle.gate_grouped_sigmoid_topk(lg, 2, n_group=4, topk_group=2)
+    assert ids.tolist() == [[0, 6]]
+    s = 1 / (1 + np.exp(-np.array([1.0, 0.9])))
+    np.testing.assert_allclose(w[0], s / s.sum(), rtol=1e-14)
+    # a bias moves the selection but not the weights
+    bias = np.zeros(8)
+    bias[4] = 5.0  # group 2 now scores highest and expert 4 is the best biased score
+    ids_b, w_b = oracle.gate_grouped_sigmoid_topk(lg, 2, n_group=4, topk_group=2, bias=bias)
+    assert ids_b.tolist() == [[4, 5]]
+    s4, s5 = 1 / (1 + np.exp(3.0)), 1 / (1 + np.exp(-2.0))
+    np.testing.assert_allclose(w_b[0], [s4 / (s4 + s5), s5 / (s4 + s5)], rtol=1e-14)
+
+
+def test_gate_matches_the_torch_routing_generator():
+    # two implementations of the same rules (numpy here, torch in the input
+    # generator) agree on the generator's own logits
+    for routing, E, k in (("softmax", 128, 8), ("deepseek", 256, 8)):
+        shape = synth.LayerShape("g", 200, 256, 128, E, k, "fp8", routing, shared_expert=False,
+                                 n_group=8 if routing == "deepseek" else 1,
+                                 topk_group=4 if routing == "deepseek" else 1,
+                                 routed_scaling=2.5 if routing == "deepseek" else 1.0)
+        ids_ref, w_ref = synth.make_routing(shape, 11)
+        lg = synth.make_router_logits(shape, 11).numpy()
+        if routing == "softmax":
+            ids, w = oracle.gate_softmax_topk(lg, k)
+        else:
+            ids, w = oracle.gate_grouped_sigmoid_topk(lg, k, shape.n_group, shape.topk_group,
+                                                      routed_scaling=shape.routed_scaling)
+        np.testing.assert_array_equal(ids, ids_ref.numpy())
+        np.testing.assert_allclose(w, w_ref.numpy(), rtol=1e-6)
