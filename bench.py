@@ -60,6 +60,23 @@ def workloads():
 
 DEFAULT_WORKLOAD = "dsr1_decode_M4"
 
+# Workloads whose step starts from router logits: GPU gating, then the layer (fused_moe_gated).
+GATED = {f"{n}_gated": n for n in ("dsr1_decode_M1", "dsr1_decode_M4", "dsr1_prefill_M2048", "dsr1_prefill_M16384",
+                                   "qwen3_M16", "qwen3_M4096")}
+
+
+def all_workloads():
+    w = workloads()
+    return {**w, **{g: w[base] for g, base in GATED.items()}}
+
+
+def gate_config_of(shape):
+    """The router of the workload's model configuration."""
+    if shape.routing.startswith("deepseek"):
+        return gbmoe.gate_config(gbmoe.MOE_GATE_SIGMOID_GROUPED, shape.n_group, shape.topk_group,
+                                 shape.routed_scaling, None, shape.shared_expert)
+    return gbmoe.gate_config(shared_expert=shape.shared_expert)
+
 
 KERNEL_SOURCES = {  # kernel -> the source files that define it
     "decode_gemm1": "moe_decode.cu", "decode_gemm2": "moe_decode.cu",
@@ -267,7 +284,8 @@ def config_of(shape, args):
             "topk": shape.topk_total, "weights": "fp8_e4m3_block128" if shape.weight_kind == "fp8" else
             "int8_per_channel", "activations": "fp8_e4m3_1x128" if shape.act == "fp8_1x128" else
             ("int8_per_row" if shape.weight_kind == "int8" else "bf16"),
-            "routing": shape.routing, "l2": "flushed between steps (256 MiB write)",
+            "routing": shape.routing + (" (gated on the GPU from router logits)" if args.workload in GATED else ""),
+            "l2": "flushed between steps (256 MiB write)",
             "parallelism": f"replicas{args.gpus}"}
 
 
@@ -290,8 +308,18 @@ def run_ours(args, shape):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        fn(xd, idsd, wd, w13, s13, w2, s2, flags=flags, out=out, workspace=ws)
+    gated = args.workload in GATED
+    if gated:
+        lg = synth.make_router_logits(shape, 1234)
+        lgd = lg.to(dev)
+        gcfg = gate_config_of(shape)
+
+        def step():
+            gbmoe.fused_moe_gated(kind, xd, lgd, gcfg, shape.topk, w13, s13, w2, s2, flags=flags, out=out,
+                                  workspace=ws, topk_ids=idsd, topk_weights=wd)
+    else:
+        def step():
+            fn(xd, idsd, wd, w13, s13, w2, s2, flags=flags, out=out, workspace=ws)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -368,9 +396,11 @@ def run_ours(args, shape):
     flops = synth.algorithmic_flops(shape, ids)
 
     # ---- end to end through the public API with host buffers (pinned), copies inside the timing
+    # (gated workloads copy the router logits instead of the routing)
     xh, idsh, wh = x.pin_memory(), ids.pin_memory(), w.pin_memory()
+    lgh = lg.pin_memory() if gated else None
     outh = torch.empty(shape.M, shape.H, dtype=torch.bfloat16).pin_memory()
-    h2d = xh.numel() * 2 + idsh.numel() * 4 + wh.numel() * 4
+    h2d = xh.numel() * 2 + (lgh.numel() * 4 if gated else idsh.numel() * 4 + wh.numel() * 4)
     d2h = outh.numel() * 2
     e_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     e_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -378,8 +408,11 @@ def run_ours(args, shape):
         flush.zero_()
         e_start[i].record(stream)
         xd.copy_(xh, non_blocking=True)
-        idsd.copy_(idsh, non_blocking=True)
-        wd.copy_(wh, non_blocking=True)
+        if gated:
+            lgd.copy_(lgh, non_blocking=True)
+        else:
+            idsd.copy_(idsh, non_blocking=True)
+            wd.copy_(wh, non_blocking=True)
         step()
         outh.copy_(out, non_blocking=True)
         e_end[i].record(stream)
@@ -422,12 +455,12 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads()))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(all_workloads()))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    shape = workloads()[args.workload]
+    shape = all_workloads()[args.workload]
     if args.impl == "reference":
         run_reference(args, shape)
     else:

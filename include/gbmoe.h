@@ -111,6 +111,53 @@ moe_status_t moe_align_block_size(const int32_t* topk_ids, int M, int topk, int 
                                   moe_stream_t stream);
 
 /*
+ * Router gating: each token's experts and routing weights from its router
+ * logits.  The pages take topk_ids / topk_weights as the router's given
+ * output; the two gating functions here are those of the model
+ * configurations the layer serves (softmax top-k as in Qwen3-MoE, and the
+ * DeepSeek-V3/R1 sigmoid router with group-limited selection).  Equal scores
+ * go to the lower expert index.
+ *
+ *  MOE_GATE_SOFTMAX: p = softmax(logits[t]); topk_ids[t] = the topk largest p
+ *    in descending order; topk_weights[t,j] = p_j / (sum of the chosen p).
+ *    Ranking p is ranking the logits, so only the chosen terms are formed:
+ *    w_j = exp(l_j - l_max) / sum over chosen of exp(l_i - l_max).
+ *  MOE_GATE_SIGMOID_GROUPED: s = sigmoid(logits[t]) and b = s + bias (the
+ *    bias only ranks).  The E experts form n_group consecutive groups of
+ *    E / n_group; a group's score is the sum of its two largest b (its only b
+ *    in a group of one); the topk_group best groups are kept and
+ *    topk_ids[t] = the topk largest b inside them, descending;
+ *    topk_weights[t,j] = s_j / (sum of the chosen s) * routed_scaling.
+ * Arithmetic is fp32 (expf, IEEE division); rankings compare fp32 scores, so
+ * scores closer than a few fp32 ulps may rank either way.  Whatever the
+ * logits (NaN included), every written id lies in [0, E).
+ */
+#define MOE_GATE_SOFTMAX 0
+#define MOE_GATE_SIGMOID_GROUPED 1
+typedef struct moe_gate_config {
+  int scoring;          /* MOE_GATE_SOFTMAX or MOE_GATE_SIGMOID_GROUPED                      */
+  int n_group;          /* SIGMOID_GROUPED: 1..32, divides E.  SOFTMAX: must be 1              */
+  int topk_group;       /* SIGMOID_GROUPED: 1..n_group, topk <= topk_group * E / n_group.
+                           SOFTMAX: must be 1                                                  */
+  float routed_scaling; /* SIGMOID_GROUPED: > 0.  SOFTMAX: must be 1.0                         */
+  const float* bias;    /* SIGMOID_GROUPED: fp32 [E] device pointer, or NULL for none.
+                           SOFTMAX: must be NULL                                               */
+  int shared_expert;    /* 0 or 1: also write column topk of every row as (id E, weight 1.0)   */
+} moe_gate_config_t;
+
+/*
+ *   logits        fp32 [M, E]                     router logits
+ *   topk_ids      int32 [M, topk + shared_expert] out
+ *   topk_weights  fp32  [M, topk + shared_expert] out
+ * 1 <= topk <= min(E, 32), E <= MOE_MAX_EXPERTS, M >= 0.  One warp ranks one
+ * token.  Launched with programmatic dependent launch: the kernel waits for
+ * the stream's previous kernel before it reads or writes anything, and the
+ * next kernel of the library may be scheduled while it runs.
+ */
+moe_status_t moe_gate_topk(const float* logits, int M, int E, int topk, const moe_gate_config_t* gate,
+                           int32_t* topk_ids, float* topk_weights, moe_stream_t stream);
+
+/*
  * Dynamic per-row INT8 quantisation of bf16 activations (the DA8W8
  * activation side; SGLang CPU backend write-up, section "(3) FusedMoE", the
  * dynamic-quant fusion paragraph):
@@ -200,6 +247,32 @@ moe_status_t fused_moe_int8(const void* x_bf16, const int32_t* topk_ids, const f
                             const float* w2_scale, int M, int H, int I, int E, int topk,
                             unsigned flags, void* out_bf16, void* workspace,
                             size_t workspace_bytes, moe_stream_t stream);
+
+/*
+ * The whole layer from router logits: moe_gate_topk, then fused_moe_fp8
+ * (weight_kind MOE_WEIGHT_FP8) or fused_moe_int8 (MOE_WEIGHT_INT8) on its
+ * result, with no host step between them.
+ *
+ *   router_logits  fp32 [M, E]   E = routed experts
+ *   gate           gating function and options, as for moe_gate_topk
+ *   w13, w2 (+ scales)  hold E + gate->shared_expert experts; a shared
+ *                  expert is the last one
+ *   topk_ids, topk_weights  out, [M, topk + gate->shared_expert], as
+ *                  moe_gate_topk writes them (the routing the layer used)
+ *   workspace      moe_workspace_size(M, H, I, E + shared_expert,
+ *                  topk + shared_expert, weight_kind, flags) bytes
+ * other arguments as for fused_moe_fp8 / fused_moe_int8 (flags must suit the
+ * weight kind).  When M <= MOE_GATE_INLINE_TOKENS and E <= 256 the ranking
+ * runs inside the layer's first kernel, ahead of the routing alignment (one
+ * launch fewer); otherwise it is one more launch, chained to the layer by
+ * programmatic dependent launch.  Results are the same either way.
+ */
+#define MOE_GATE_INLINE_TOKENS 64
+moe_status_t fused_moe_gated(int weight_kind, const void* x_bf16, const float* router_logits,
+                             const moe_gate_config_t* gate, const void* w13, const float* w13_scale,
+                             const void* w2, const float* w2_scale, int M, int H, int I, int E, int topk,
+                             unsigned flags, int32_t* topk_ids, float* topk_weights, void* out_bf16,
+                             void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /*
  * fused_moe_fp8 for callers that cannot allocate device memory.  The pages

@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "gate.cuh"
 #include "internal.h"
 
 namespace gbmoe {
@@ -205,11 +206,18 @@ __device__ void prep_rows(const PrepArgs& p, int row0, int rstride) {
   }
 }
 
-__global__ void __launch_bounds__(kAlignThreads) prologue_kernel(AlignArgs a, PrepArgs p) {
+// GV > 0: the alignment CTA first ranks every token's experts (router gating,
+// GV experts per lane) and writes topk_ids / topk_weights, then aligns them.
+template <int GV>
+__global__ void __launch_bounds__(kAlignThreads) prologue_kernel(AlignArgs a, PrepArgs p, GateArgs g) {
   pdl_trigger();  // the next kernel may set itself up; it waits for this grid before reading
+  pdl_wait();     // inputs (and this workspace's previous readers) belong to earlier kernels
   if (blockIdx.x == 0) {
     if (a.status && threadIdx.x == 0) { a.status->bad_ids = 0; a.status->flags = 0; }
-    __syncthreads();
+    if constexpr (GV > 0) {
+      for (int t = threadIdx.x >> 5; t < g.M; t += kAlignWarps) gate_token<GV>(g, t, threadIdx.x & 31);
+    }
+    __syncthreads();  // the ids written above are read by the whole CTA below
     align_cta(a);
     return;
   }
@@ -227,13 +235,26 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(PrepArgs p) {
 
 size_t align_smem_bytes(int E) { return static_cast<size_t>(kAlignWarps * E + 64) * sizeof(int); }
 
-cudaError_t launch_prologue(const AlignArgs& a, const PrepArgs& p, int prep_ctas, cudaStream_t s) {
+template <int GV>
+static cudaError_t launch_prologue_t(const AlignArgs& a, const PrepArgs& p, const GateArgs& g, int prep_ctas,
+                                     cudaStream_t s) {
   const size_t smem = align_smem_bytes(a.E);
-  cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(prologue_kernel),
+  cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(prologue_kernel<GV>),
                                         static_cast<int>(align_smem_bytes(MOE_MAX_EXPERTS)));
   if (err != cudaSuccess) return err;
-  prologue_kernel<<<1 + prep_ctas, kAlignThreads, smem, s>>>(a, p);
-  return cudaGetLastError();
+  return launch_kernel(prologue_kernel<GV>, dim3(1 + prep_ctas), dim3(kAlignThreads), smem, s, true, a, p, g);
+}
+
+cudaError_t launch_prologue(const AlignArgs& a, const PrepArgs& p, int prep_ctas, cudaStream_t s,
+                            const GateArgs* inline_gate) {
+  if (!inline_gate) return launch_prologue_t<0>(a, p, GateArgs{}, prep_ctas, s);
+  switch (gate_vpl(inline_gate->E)) {
+    case 1: return launch_prologue_t<1>(a, p, *inline_gate, prep_ctas, s);
+    case 2: return launch_prologue_t<2>(a, p, *inline_gate, prep_ctas, s);
+    case 4: return launch_prologue_t<4>(a, p, *inline_gate, prep_ctas, s);
+    case 8: return launch_prologue_t<8>(a, p, *inline_gate, prep_ctas, s);
+  }
+  return cudaErrorInvalidValue;  // the caller ranks more than 256 experts in its own launch
 }
 
 cudaError_t launch_quant_rows(const PrepArgs& p, cudaStream_t s) {

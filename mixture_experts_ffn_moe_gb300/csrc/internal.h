@@ -16,6 +16,7 @@
 namespace gbmoe {
 
 struct DeviceStatus;
+struct GateArgs;
 
 struct AlignArgs {
   const int32_t* topk_ids;
@@ -127,7 +128,11 @@ struct SkinnyArgs {
 };
 
 size_t align_smem_bytes(int E);
-cudaError_t launch_prologue(const AlignArgs& a, const PrepArgs& p, int prep_ctas, cudaStream_t s);
+// inline_gate (may be null; at most 256 experts): rank the tokens' experts in
+// the alignment CTA before aligning; a.topk_ids must then be inline_gate->ids.
+cudaError_t launch_prologue(const AlignArgs& a, const PrepArgs& p, int prep_ctas, cudaStream_t s,
+                            const GateArgs* inline_gate = nullptr);
+cudaError_t launch_gate(const GateArgs& g, int num_sms, cudaStream_t s);
 cudaError_t launch_quant_rows(const PrepArgs& p, cudaStream_t s);
 cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook);
 cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook);

@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "gate.cuh"
 #include "internal.h"
 
 namespace gbmoe {
@@ -190,11 +191,52 @@ static T* at(void* base, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(base) + off);
 }
 
+// Checks a gating request over E routed experts and fills the kernel arguments
+// (all but ids / w).
+static moe_status_t check_gate(const float* logits, int M, int E, int topk, const moe_gate_config_t* gate,
+                               GateArgs& g) {
+  if (!gate) return fail(MOE_ERR_INVALID_ARG, "gate config is NULL");
+  if (M < 0 || E <= 0 || topk <= 0) return fail(MOE_ERR_INVALID_ARG, "sizes must be positive (M >= 0)");
+  if (E > MOE_MAX_EXPERTS) return fail(MOE_ERR_UNSUPPORTED, "more than MOE_MAX_EXPERTS experts");
+  if (gate->shared_expert != 0 && gate->shared_expert != 1)
+    return fail(MOE_ERR_INVALID_ARG, "shared_expert must be 0 or 1");
+  if (topk > E) return fail(MOE_ERR_INVALID_ARG, "topk > E");
+  if (topk + gate->shared_expert > 32) return fail(MOE_ERR_UNSUPPORTED, "topk + shared_expert > 32");
+  if (gate->scoring == MOE_GATE_SOFTMAX) {
+    if (gate->n_group != 1 || gate->topk_group != 1 || gate->routed_scaling != 1.0f || gate->bias)
+      return fail(MOE_ERR_INVALID_ARG, "softmax gating takes n_group = topk_group = 1, scaling 1, no bias");
+  } else if (gate->scoring == MOE_GATE_SIGMOID_GROUPED) {
+    if (gate->n_group < 1 || gate->n_group > 32 || E % gate->n_group)
+      return fail(MOE_ERR_INVALID_ARG, "n_group must lie in 1..32 and divide E");
+    if (gate->topk_group < 1 || gate->topk_group > gate->n_group)
+      return fail(MOE_ERR_INVALID_ARG, "topk_group must lie in 1..n_group");
+    if (topk > gate->topk_group * (E / gate->n_group))
+      return fail(MOE_ERR_INVALID_ARG, "topk exceeds the experts of the kept groups");
+    if (!(gate->routed_scaling > 0.0f) || gate->routed_scaling > 3.0e38f)
+      return fail(MOE_ERR_INVALID_ARG, "routed_scaling must be positive and finite");
+  } else {
+    return fail(MOE_ERR_INVALID_ARG, "unknown gate scoring");
+  }
+  if (M > 0 && !logits) return fail(MOE_ERR_INVALID_ARG, "NULL logits");
+  g = GateArgs{};
+  g.logits = logits;
+  g.bias = gate->bias;
+  g.M = M; g.E = E; g.topk = topk; g.ld = topk + gate->shared_expert;
+  g.scoring = gate->scoring;
+  g.n_group = gate->n_group; g.topk_group = gate->topk_group;
+  g.scale = gate->routed_scaling;
+  g.shared = gate->shared_expert;
+  g.vec_ok = (E % 4 == 0 && reinterpret_cast<uintptr_t>(logits) % 16 == 0) ? 1 : 0;
+  return MOE_OK;
+}
+
+// gate (may be null): the ids / weights are first written by the router gating
+// (gate->ids == ids, gate->w == tw), inside the prologue for small calls.
 static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, const float* tw, const void* w13,
                                const float* s13, const void* w2, const float* s2, int M, int H, int I, int E,
                                int topk, unsigned flags, void* out, void* ws, size_t ws_bytes,
-                               cudaStream_t stream) {
-  g_last_error.clear();
+                               cudaStream_t stream, const GateArgs* gate = nullptr) {
+  if (!gate) g_last_error.clear();
   moe_status_t st = check_layer_args(kind, x, ids, tw, w13, s13, w2, s2, M, H, I, E, topk, flags, out);
   if (st != MOE_OK || M == 0) return st;
   const Layout L = plan(M, H, I, E, topk, kind, flags);
@@ -232,9 +274,16 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
   if (kind == MOE_WEIGHT_INT8) { p.zero_words = at<uint32_t>(ws, L.hmax); p.n_zero = static_cast<int>(L.cap); }
   const int prep_ctas = M < 2 * sms ? (M > 0 ? M : 1) : 2 * sms;
   const StageHook hook = prof_begin_call(stream);
-  cudaError_t err = launch_prologue(a, p, prep_ctas, stream);
+  const bool gate_inline = gate && M <= MOE_GATE_INLINE_TOKENS && gate->E <= 256;
+  cudaError_t err;
+  if (gate && !gate_inline) {
+    err = launch_gate(*gate, sms, stream);
+    if (err != cudaSuccess) return cuda_fail(err, "gate launch");
+    hook("gate", stream);
+  }
+  err = launch_prologue(a, p, prep_ctas, stream, gate_inline ? gate : nullptr);
   if (err != cudaSuccess) return cuda_fail(err, "prologue launch");
-  hook("prologue_align_prep", stream);
+  hook(gate_inline ? "prologue_gate_align_prep" : "prologue_align_prep", stream);
 
   LayerPlan P{};
   P.M = M; P.H = H; P.I = I; P.E = E; P.topk = topk; P.cap = static_cast<int>(L.cap);
@@ -317,6 +366,42 @@ moe_status_t moe_align_block_size(const int32_t* topk_ids, int M, int topk, int 
   cudaError_t err = launch_prologue(a, p, 0, reinterpret_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_fail(err, "moe_align_block_size launch");
   return MOE_OK;
+}
+
+moe_status_t moe_gate_topk(const float* logits, int M, int E, int topk, const moe_gate_config_t* gate,
+                           int32_t* topk_ids, float* topk_weights, moe_stream_t stream) {
+  g_last_error.clear();
+  GateArgs g;
+  moe_status_t st = check_gate(logits, M, E, topk, gate, g);
+  if (st != MOE_OK || M == 0) return st;
+  if (!topk_ids || !topk_weights) return fail(MOE_ERR_INVALID_ARG, "NULL output pointer");
+  g.ids = topk_ids;
+  g.w = topk_weights;
+  const int sms = num_sms_current();
+  if (sms <= 0) return fail(MOE_ERR_CUDA, "cannot query the current device");
+  cudaError_t err = launch_gate(g, sms, reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_gate_topk launch");
+  return MOE_OK;
+}
+
+moe_status_t fused_moe_gated(int weight_kind, const void* x_bf16, const float* router_logits,
+                             const moe_gate_config_t* gate, const void* w13, const float* w13_scale,
+                             const void* w2, const float* w2_scale, int M, int H, int I, int E, int topk,
+                             unsigned flags, int32_t* topk_ids, float* topk_weights, void* out_bf16,
+                             void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  g_last_error.clear();
+  if (weight_kind != MOE_WEIGHT_FP8 && weight_kind != MOE_WEIGHT_INT8)
+    return fail(MOE_ERR_INVALID_ARG, "unknown weight kind");
+  GateArgs g;
+  moe_status_t st = check_gate(router_logits, M, E, topk, gate, g);
+  if (st != MOE_OK) return st;
+  g.ids = topk_ids;
+  g.w = topk_weights;
+  const int sh = gate->shared_expert;
+  if (M > 0 && E + sh > MOE_MAX_EXPERTS) return fail(MOE_ERR_UNSUPPORTED, "more than MOE_MAX_EXPERTS experts");
+  return fused_impl(weight_kind, x_bf16, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, M, H, I, E + sh,
+                    topk + sh, flags, out_bf16, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream),
+                    &g);
 }
 
 moe_status_t moe_quant_act_int8(const void* x_bf16, int M, int H, int8_t* q, float* scale, moe_stream_t stream) {

@@ -24,6 +24,15 @@ MOE_WEIGHT_INT8 = 1
 MOE_MAX_EXPERTS = 1024
 MOE_MAX_DECODE_TOKENS = 128
 MOE_STATIC_SCRATCH_BYTES = 16 << 20
+MOE_GATE_SOFTMAX = 0
+MOE_GATE_SIGMOID_GROUPED = 1
+MOE_GATE_INLINE_TOKENS = 64
+
+
+class GateConfig(ctypes.Structure):
+    """moe_gate_config_t."""
+    _fields_ = [("scoring", ctypes.c_int), ("n_group", ctypes.c_int), ("topk_group", ctypes.c_int),
+                ("routed_scaling", ctypes.c_float), ("bias", ctypes.c_void_p), ("shared_expert", ctypes.c_int)]
 
 _STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
                  4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_BAD_IDS"}
@@ -41,6 +50,8 @@ _vp, _i, _u, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
 _SIGS = {
     "moe_align_max_padded": (_sz, [_i, _i, _i, _i]),
     "moe_align_block_size": (_i, [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
+    "moe_gate_topk": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp, _vp]),
+    "fused_moe_gated": (_i, [_i] + [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_quant_act_int8": (_i, [_vp, _i, _i, _vp, _vp, _vp]),
     "moe_quant_act_fp8": (_i, [_vp, _i, _i, _vp, _vp, _vp]),
     "moe_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _u]),
@@ -114,6 +125,72 @@ def moe_align_block_size(topk_ids: torch.Tensor, num_experts: int, block_size: i
                                      _ptr(expert_ids), _ptr(npp), _ptr(offs), _stream(topk_ids))
     _check(st, "moe_align_block_size")
     return sorted_ids, expert_ids, npp, offs
+
+
+def gate_config(scoring=MOE_GATE_SOFTMAX, n_group=1, topk_group=1, routed_scaling=1.0, bias=None,
+                shared_expert=False):
+    """A moe_gate_config_t.  `bias` (fp32 [E] CUDA tensor or None) is kept alive by the config."""
+    if bias is not None:
+        _need(bias, torch.float32, "bias")
+    cfg = GateConfig(scoring, n_group, topk_group, routed_scaling,
+                     bias.data_ptr() if bias is not None else None, 1 if shared_expert else 0)
+    cfg.bias_tensor = bias  # the struct holds a raw pointer into this tensor
+    return cfg
+
+
+def moe_gate_topk(logits: torch.Tensor, topk: int, gate: GateConfig):
+    """fp32 router logits [M, E] -> (topk_ids int32, topk_weights fp32), both [M, topk + shared_expert]."""
+    _need(logits, torch.float32, "logits")
+    M, E = logits.shape
+    ld = topk + gate.shared_expert
+    ids = torch.empty(M, ld, dtype=torch.int32, device=logits.device)
+    w = torch.empty(M, ld, dtype=torch.float32, device=logits.device)
+    st = load().moe_gate_topk(_ptr(logits), M, E, topk, ctypes.byref(gate), _ptr(ids), _ptr(w), _stream(logits))
+    _check(st, "moe_gate_topk")
+    return ids, w
+
+
+def fused_moe_gated(weight_kind, x, router_logits, gate: GateConfig, topk, w13, w13_scale, w2, w2_scale,
+                    flags=MOE_PATH_AUTO, out=None, workspace=None, topk_ids=None, topk_weights=None):
+    """The layer from router logits: gating, then the fused layer (see include/gbmoe.h).
+
+    Returns (out, topk_ids, topk_weights); the weights hold E + gate.shared_expert experts.
+    """
+    wdt = torch.uint8 if weight_kind == MOE_WEIGHT_FP8 else torch.int8
+    _need(x, torch.bfloat16, "x")
+    _need(router_logits, torch.float32, "router_logits")
+    if w13.dtype == torch.float8_e4m3fn:
+        w13 = w13.view(torch.uint8)
+    if w2.dtype == torch.float8_e4m3fn:
+        w2 = w2.view(torch.uint8)
+    _need(w13, wdt, "w13")
+    _need(w2, wdt, "w2")
+    _need(w13_scale, torch.float32, "w13_scale")
+    _need(w2_scale, torch.float32, "w2_scale")
+    M, H = x.shape
+    E = router_logits.shape[1]
+    sh = gate.shared_expert
+    Et, I2, H2 = w13.shape
+    if router_logits.shape[0] != M or Et != E + sh or H2 != H or tuple(w2.shape) != (Et, H, I2 // 2):
+        raise ValueError("inconsistent shapes")
+    I = I2 // 2
+    ids = topk_ids if topk_ids is not None else torch.empty(M, topk + sh, dtype=torch.int32, device=x.device)
+    w = topk_weights if topk_weights is not None else torch.empty(M, topk + sh, dtype=torch.float32,
+                                                                  device=x.device)
+    _need(ids, torch.int32, "topk_ids")
+    _need(w, torch.float32, "topk_weights")
+    if tuple(ids.shape) != (M, topk + sh) or tuple(w.shape) != (M, topk + sh):
+        raise ValueError("topk_ids / topk_weights must be [M, topk + shared_expert]")
+    if out is None:
+        out = torch.empty(M, H, dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, "out")
+    if workspace is None:
+        workspace = alloc_workspace(M, H, I, Et, topk + sh, weight_kind, flags, x.device)
+    st = load().fused_moe_gated(weight_kind, _ptr(x), _ptr(router_logits), ctypes.byref(gate), _ptr(w13),
+                                _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), M, H, I, E, topk, flags, _ptr(ids),
+                                _ptr(w), _ptr(out), _ptr(workspace), workspace.numel(), _stream(x))
+    _check(st, "fused_moe_gated")
+    return out, ids, w
 
 
 def moe_quant_act_int8(x: torch.Tensor):

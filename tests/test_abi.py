@@ -97,3 +97,45 @@ def test_fp8_activation_flag_host_checks(lib):
     assert lib.moe_quant_act_fp8(p, 4, 200, p, p, None) == 2        # H not a multiple of 128
     assert lib.moe_quant_act_fp8(None, 4, 256, p, p, None) == 1
     assert lib.moe_quant_act_fp8(None, 0, 256, None, None, None) == 0
+
+
+def test_gate_host_checks(lib):
+    p = ctypes.c_void_p(16)  # never dereferenced: every call below returns on the host
+    G = gbmoe.gate_config
+
+    def gate(M=4, E=8, topk=2, cfg=None):
+        cfg = cfg if cfg is not None else G()
+        return lib.moe_gate_topk(p, M, E, topk, ctypes.byref(cfg), p, p, None)
+
+    assert lib.moe_gate_topk(p, 4, 8, 2, None, p, p, None) == 1                    # no config
+    assert gate(M=0) == 0                                                          # empty batch
+    assert gate(topk=9) == 1                                                       # topk > E
+    assert gate(E=2000) == 2                                                       # too many experts
+    assert gate(E=64, topk=32, cfg=G(shared_expert=True)) == 2                     # 33 columns
+    assert gate(cfg=G(n_group=2)) == 1                                             # softmax takes no groups
+    assert gate(cfg=G(routed_scaling=2.0)) == 1
+    assert gate(cfg=GateCfg_bias()) == 1
+    sig = gbmoe.MOE_GATE_SIGMOID_GROUPED
+    assert gate(E=12, cfg=G(sig, n_group=8, topk_group=4)) == 1                    # 8 does not divide 12
+    assert gate(E=256, cfg=G(sig, n_group=64, topk_group=4)) == 1                  # more than 32 groups
+    assert gate(E=256, cfg=G(sig, n_group=8, topk_group=9)) == 1
+    assert gate(E=16, topk=5, cfg=G(sig, n_group=8, topk_group=2)) == 1            # 2 groups of 2 hold 4
+    assert gate(E=16, topk=4, cfg=G(sig, n_group=8, topk_group=2, routed_scaling=0.0)) == 1
+    assert gate(M=0, E=16, topk=4, cfg=G(sig, n_group=8, topk_group=2)) == 0
+    assert gate(cfg=G(scoring=7)) == 1
+    cfg = G()
+    assert lib.moe_gate_topk(None, 4, 8, 2, ctypes.byref(cfg), p, p, None) == 1   # NULL logits
+    # the gated layer: weight kind and the layer's own checks
+    assert lib.fused_moe_gated(5, p, p, ctypes.byref(cfg), p, p, p, p, 4, 256, 128, 8, 2, 0, p, p, p, p, 0,
+                               None) == 1
+    assert lib.fused_moe_gated(0, p, p, ctypes.byref(cfg), p, p, p, p, 4, 200, 128, 8, 2, 0, p, p, p, p, 0,
+                               None) == 2                                          # H not a multiple of 128
+    assert lib.fused_moe_gated(0, p, p, ctypes.byref(cfg), p, p, p, p, 4, 256, 128, 8, 2, 0, p, p, p, p, 0,
+                               None) == 3                                          # no workspace
+
+
+class GateCfg_bias(gbmoe.GateConfig):
+    """A softmax config that carries a bias pointer (invalid)."""
+
+    def __init__(self):
+        super().__init__(gbmoe.MOE_GATE_SOFTMAX, 1, 1, 1.0, 16, 0)
