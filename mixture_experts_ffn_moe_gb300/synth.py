@@ -27,6 +27,7 @@ import torch
 
 FP8_MAX = 448.0
 INT8_MAX = 127.0
+INT4_QMAX = 7.0
 QBLOCK = 128
 
 
@@ -43,7 +44,7 @@ class LayerShape:
     I: int
     E: int
     topk: int
-    weight_kind: str  # "fp8" | "int8"
+    weight_kind: str  # "fp8" | "int8" | "int4"
     routing: str      # "softmax" | "deepseek" | "deepseek_zipf" | "uniform"
     shared_expert: bool = False
     n_group: int = 1
@@ -199,6 +200,26 @@ def quantize_int8_channel(w: torch.Tensor):
     return q, scale
 
 
+def pack_int4(q: torch.Tensor) -> torch.Tensor:
+    """int values in [-8, 7], [..., C] -> uint8 [..., C/2]: column 2j in the low nibble, 2j+1 in the high one."""
+    n = (q.to(torch.int16) & 0xF).to(torch.uint8)
+    return (n[..., 0::2] | (n[..., 1::2] << 4)).contiguous()
+
+
+def quantize_int4_group(w: torch.Tensor):
+    """Weights [..., R, C] -> (packed int4 codes uint8 [..., R, C/2], fp32 scales [..., R, C/128]).
+
+    Per row and 128 columns: s = amax / 7 (1 when the group is all zero),
+    q = round-half-even(w / s), which lies in [-7, 7] (the format also holds -8).
+    """
+    *lead, R, C = w.shape
+    wg = w.reshape(*lead, R, C // QBLOCK, QBLOCK)
+    amax = wg.abs().amax(dim=-1)
+    scale = torch.where(amax > 0, amax / INT4_QMAX, torch.ones_like(amax)).float()
+    q = torch.round(wg / scale[..., None]).clamp(-8, 7).reshape(*lead, R, C)
+    return pack_int4(q), scale
+
+
 def make_weights(shape: LayerShape, seed: int, device="cpu", std: float = 0.02):
     """Expert weights, one expert at a time (so full-size layers fit), on `device`.
 
@@ -207,6 +228,8 @@ def make_weights(shape: LayerShape, seed: int, device="cpu", std: float = 0.02):
             w2  uint8 [E, H, I],  w2_scale  f32 [E, H/128, I/128]
       int8: w13 int8 [E, 2I, H], w13_scale f32 [E, 2I],
             w2  int8 [E, H, I],  w2_scale  f32 [E, H]
+      int4: w13 uint8 [E, 2I, H/2] (two codes a byte), w13_scale f32 [E, 2I, H/128],
+            w2  uint8 [E, H, I/2],  w2_scale  f32 [E, H, I/128]
     Rows 0..I-1 of w13 are the gate projection, rows I..2I-1 the up projection.
     """
     E, H, I = shape.E_total, shape.H, shape.I
@@ -223,6 +246,12 @@ def make_weights(shape: LayerShape, seed: int, device="cpu", std: float = 0.02):
         w2 = torch.empty(E, H, I, dtype=torch.int8, device=device)
         s2 = torch.empty(E, H, dtype=torch.float32, device=device)
         quant = quantize_int8_channel
+    elif shape.weight_kind == "int4":
+        w13 = torch.empty(E, 2 * I, H // 2, dtype=torch.uint8, device=device)
+        s13 = torch.empty(E, 2 * I, H // QBLOCK, dtype=torch.float32, device=device)
+        w2 = torch.empty(E, H, I // 2, dtype=torch.uint8, device=device)
+        s2 = torch.empty(E, H, I // QBLOCK, dtype=torch.float32, device=device)
+        quant = quantize_int4_group
     else:
         raise ValueError(shape.weight_kind)
     g = torch.Generator(device=device)
@@ -250,6 +279,8 @@ def distinct_weight_bytes(shape: LayerShape, topk_ids: torch.Tensor) -> int:
     H, I = shape.H, shape.I
     if shape.weight_kind == "fp8":
         per = 3 * H * I + 4 * (2 * I // QBLOCK) * (H // QBLOCK) + 4 * (H // QBLOCK) * (I // QBLOCK)
+    elif shape.weight_kind == "int4":
+        per = 3 * H * I // 2 + 4 * (2 * I * (H // QBLOCK) + H * (I // QBLOCK))
     else:
         per = 3 * H * I + 4 * (2 * I + H)
     return active * per

@@ -8,4 +8,5 @@ from .moe_oracle import (  # noqa: F401
     e4m3_decode, e4m3_encode_satfinite, dequant_fp8_block, dequant_int8_channel,
     quant_int8_per_row, max_padded, moe_align_block_size, fused_moe_fp8,
     fused_moe_int8, fused_moe_rows, silu, gate_softmax_topk, gate_grouped_sigmoid_topk,
+    unpack_int4, dequant_int4_group, fused_moe_int4,
 )

@@ -24,6 +24,9 @@ computes, in float64 numpy over dequantised weights:
 * INT8 per-output-channel weights with dynamic per-token INT8 activations
   (DA8W8; SGLang CPU backend write-up, "(3) FusedMoE", the dynamic-quant
   fusion paragraph);
+* INT4 weights with one scale per row and 128 columns, activations at their
+  bf16 values (a reading: the pages name INT4 without a layout, see
+  unpack_int4);
 * the optional FP8 x FP8 ("A8") mode of the FP8 layer, in which the
   activations and the intermediate h are quantised to E4M3 in groups of 1 x 128
   (a reading: the pages keep FP8 activations in BF16, see quant_fp8_1x128);
@@ -123,6 +126,30 @@ def dequant_fp8_block(codes, scale) -> np.ndarray:
 def dequant_int8_channel(codes, scale) -> np.ndarray:
     """codes int8 [R, C], scale f32 [R] -> float64 W[r, c] = q * s[r]."""
     return np.asarray(codes, dtype=np.float64) * np.asarray(scale, dtype=np.float64)[:, None]
+
+
+# ----------------------------------------------------------------------------
+# INT4 weights with one scale per row and 128 columns (group-wise W4A16).
+# The pages name INT4 as the quantised alternative to native FP8 (SGLang CPU
+# backend write-up, closing section; OSDI'26 local-MoE summary, evaluation of
+# the INT4 decode baseline) without fixing a layout.  Reading: two's-complement
+# nibbles in [-8, 7], two per byte (column 2j in the low nibble, 2j+1 in the
+# high one), and w = q * s with one fp32 scale per row and 128 columns, the
+# same 128-wide K grouping as the FP8 block scales.
+# ----------------------------------------------------------------------------
+
+
+def unpack_int4(packed) -> np.ndarray:
+    """uint8 [..., C/2] -> int8 [..., C]: byte j = column 2j (low nibble) and 2j+1 (high nibble)."""
+    b = np.asarray(packed, dtype=np.uint8).astype(np.int16)
+    nib = np.stack([b & 0x0F, b >> 4], axis=-1).reshape(*b.shape[:-1], 2 * b.shape[-1])
+    return np.where(nib >= 8, nib - 16, nib).astype(np.int8)
+
+
+def dequant_int4_group(packed, scale) -> np.ndarray:
+    """packed uint8 [R, C/2], scale f32 [R, C/128] -> float64 W[r, c] = q[r, c] * s[r, c // 128]."""
+    q = unpack_int4(packed).astype(np.float64)
+    return q * np.repeat(np.asarray(scale, dtype=np.float64), QBLOCK, axis=-1)
 
 
 # ----------------------------------------------------------------------------
@@ -330,6 +357,12 @@ def fused_moe_fp8(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, exper
     return _naive_moe(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, "fp8", experts, act)
 
 
+def fused_moe_int4(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, experts=None):
+    """The layer with group-wise INT4 weights (w13 uint8 [E, 2I, H/2], w13_scale f32 [E, 2I, H/128],
+    w2 uint8 [E, H, I/2], w2_scale f32 [E, H, I/128]); activations enter at their bf16 values."""
+    return _naive_moe(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, "int4", experts)
+
+
 def fused_moe_int8(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, experts=None):
     """INT8 per-channel weights with dynamic per-row INT8 activations (DA8W8).
 
@@ -359,9 +392,10 @@ def _naive_moe(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, kind, ex
             continue
         # one expert's weights at a time (they may live on a device; copy them here)
         q13, s13, q2, s2 = (_as_np(a[e]) for a in (w13, w13_scale, w2, w2_scale))
-        if kind == "fp8":
-            W13 = dequant_fp8_block(q13, s13)                      # [2I, H]
-            W2 = dequant_fp8_block(q2, s2)                         # [H, I]
+        if kind in ("fp8", "int4"):
+            deq = dequant_fp8_block if kind == "fp8" else dequant_int4_group
+            W13 = deq(q13, s13)                                    # [2I, H]
+            W2 = deq(q2, s2)                                       # [H, I]
             C = xa[tok] @ W13.T                                    # A x [B1, B2] = [C1, C2]
             h = silu(C[:, :I]) * C[:, I:]                          # SiLU(C1) * C2
             if a8:

@@ -610,3 +610,70 @@ def test_gate_matches_the_torch_routing_generator():
                                                       routed_scaling=shape.routed_scaling)
         np.testing.assert_array_equal(ids, ids_ref.numpy())
         np.testing.assert_allclose(w, w_ref.numpy(), rtol=1e-6)
+
+
+# ----------------------------------------------------------------------------
+# INT4 weights (group-wise, one scale per row and 128 columns).  Pins: the
+# nibble decoder against sign extension by arithmetic shifts (a different
+# route to the same bits) on all 256 bytes and a hand-worked table, the group
+# scale indexing in closed form, and the layer against a textbook dense SwiGLU
+# on weights unpacked independently.
+# ----------------------------------------------------------------------------
+
+
+def test_int4_unpack_all_bytes_by_arithmetic_shifts():
+    b = np.arange(256, dtype=np.uint8)
+    lo = (b.astype(np.uint8) << 4).view(np.int8) >> 4        # low nibble, sign-extended
+    hi = b.view(np.int8) >> 4                                 # high nibble, sign-extended
+    q = oracle.unpack_int4(b[None, :])[0]
+    np.testing.assert_array_equal(q[0::2], lo)
+    np.testing.assert_array_equal(q[1::2], hi)
+    # hand-worked: 0x8F = (-1, -8), 0x70 = (0, 7), 0x19 = (-7, 1)
+    np.testing.assert_array_equal(oracle.unpack_int4(np.array([[0x8F, 0x70, 0x19]], dtype=np.uint8)),
+                                  [[-1, -8, 0, 7, -7, 1]])
+
+
+def test_int4_pack_roundtrip_and_group_scale_indexing():
+    rng = np.random.default_rng(41)
+    q = rng.integers(-8, 8, size=(6, 512))
+    packed = synth.pack_int4(torch.from_numpy(q)).numpy()
+    assert packed.shape == (6, 256)
+    np.testing.assert_array_equal(oracle.unpack_int4(packed), q)
+    scale = np.array([[10.0 ** g * (r + 1) for g in range(4)] for r in range(6)], dtype=np.float32)
+    W = oracle.dequant_int4_group(packed, scale)
+    for r, c in [(0, 0), (0, 127), (0, 128), (3, 300), (5, 511)]:
+        assert W[r, c] == q[r, c] * 10.0 ** (c // 128) * (r + 1)
+
+
+def test_int4_quantiser_bound():
+    w = torch.randn(4, 384, generator=torch.Generator().manual_seed(5)) * 0.02
+    packed, s = synth.quantize_int4_group(w)
+    W = oracle.dequant_int4_group(packed.numpy(), s.numpy())
+    err = np.abs(W - w.double().numpy())
+    # half a step of each group, and the group maximum lands on +-7 steps exactly
+    assert (err <= 0.5 * np.repeat(s.double().numpy(), 128, axis=1) * (1 + 1e-6)).all()
+    q = oracle.unpack_int4(packed.numpy()).reshape(4, 3, 128)
+    assert (np.abs(q).max(axis=-1) == 7).all()
+
+
+def test_int4_layer_top1_equals_dense_swiglu():
+    shape = synth.LayerShape("i4", 5, 256, 256, 4, 1, "int4", "uniform")
+    d = synth.make_layer(shape, seed=43)
+    d["topk_weights"] = torch.ones_like(d["topk_weights"])
+    out = oracle.fused_moe_int4(**d)
+
+    def unpack(p):  # independent route: arithmetic shifts
+        p = p.numpy()
+        lo = (p << 4).view(np.int8) >> 4
+        hi = p.view(np.int8) >> 4
+        q = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.float64)
+        q[..., 0::2], q[..., 1::2] = lo, hi
+        return q
+
+    x = d["x"].double()
+    for t in range(5):
+        e = int(d["topk_ids"][t, 0])
+        W13 = torch.from_numpy(unpack(d["w13"][e]) * np.repeat(d["w13_scale"][e].double().numpy(), 128, axis=1))
+        W2 = torch.from_numpy(unpack(d["w2"][e]) * np.repeat(d["w2_scale"][e].double().numpy(), 128, axis=1))
+        np.testing.assert_allclose(out[t], _dense_swiglu(x[t:t + 1], W13[:256], W13[256:], W2)[0].numpy(),
+                                   rtol=1e-10, atol=1e-12)
