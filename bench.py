@@ -55,6 +55,12 @@ def workloads():
         "dsr1_prefill_M2048_E32": synth.deepseek_r1(2048, routing="deepseek_zipf", E=32),
         "dsr1_prefill_M2048_E32_a8": synth.deepseek_r1(2048, routing="deepseek_zipf", E=32, act="fp8_1x128"),
         "qwen3_M1024": synth.qwen3_235b(1024),
+        # group-wise INT4 weights (one scale per row and 128 columns), bf16 activations
+        "dsr1_decode_M1_int4": synth.deepseek_r1(1, weight_kind="int4"),
+        "dsr1_decode_M4_int4": synth.deepseek_r1(4, weight_kind="int4"),
+        "dsr1_sweep_M64_int4": synth.deepseek_r1(64, routing="uniform", weight_kind="int4"),
+        "qwen3_M1_int4": synth.qwen3_235b(1, weight_kind="int4"),
+        "qwen3_M16_int4": synth.qwen3_235b(16, weight_kind="int4"),
     }
 
 
@@ -129,16 +135,19 @@ def stage_work(shape, ids: torch.Tensor):
     valid = int(hist.sum())
     H, I, M = shape.H, shape.I, shape.M
     ab = 1 if shape.act == "fp8_1x128" else 2  # bytes per gathered activation element (E4M3 or fp16)
+    wb = 0.5 if shape.weight_kind == "int4" else 1  # bytes per weight code
     if shape.weight_kind == "fp8":
         s13 = 4 * (2 * I // 128) * (H // 128)
         s2 = 4 * (H // 128) * (I // 128)
+    elif shape.weight_kind == "int4":
+        s13, s2 = 4 * 2 * I * (H // 128), 4 * H * (I // 128)
     else:
         s13, s2 = 4 * 2 * I, 4 * H
     f1 = 2 * valid * 2 * I * H
     f2 = 2 * valid * H * I
     return {
-        "decode_gemm1": (active * (2 * I * H + s13) + M * H * 2 + valid * I * 2, f1),
-        "decode_gemm2": (active * (H * I + s2) + valid * I * 2 + valid * H * 4, f2),
+        "decode_gemm1": (int(active * (2 * I * H * wb + s13)) + M * H * 2 + valid * I * 2, f1),
+        "decode_gemm2": (int(active * (H * I * wb + s2)) + valid * I * 2 + valid * H * 4, f2),
         "prefill_gemm1": (active * (2 * I * H + s13) + valid * H * ab + valid * I * ab, f1),
         "prefill_gemm2": (active * (H * I + s2) + valid * I * ab + valid * H * 4, f2),
     }
@@ -281,8 +290,9 @@ def run_reference(args, shape):
 
 def config_of(shape, args):
     return {"workload": args.workload, "M": shape.M, "H": shape.H, "I": shape.I, "E": shape.E_total,
-            "topk": shape.topk_total, "weights": "fp8_e4m3_block128" if shape.weight_kind == "fp8" else
-            "int8_per_channel", "activations": "fp8_e4m3_1x128" if shape.act == "fp8_1x128" else
+            "topk": shape.topk_total, "weights": {"fp8": "fp8_e4m3_block128", "int8": "int8_per_channel",
+                                                  "int4": "int4_group128"}[shape.weight_kind],
+            "activations": "fp8_e4m3_1x128" if shape.act == "fp8_1x128" else
             ("int8_per_row" if shape.weight_kind == "int8" else "bf16"),
             "routing": shape.routing + (" (gated on the GPU from router logits)" if args.workload in GATED else ""),
             "l2": "flushed between steps (256 MiB write)",
@@ -300,8 +310,9 @@ def run_ours(args, shape):
     dev = torch.device("cuda", local)
     x, ids, w, (w13, s13, w2, s2) = make_inputs(shape)
     xd, idsd, wd = x.to(dev), ids.to(dev), w.to(dev)
-    kind = gbmoe.MOE_WEIGHT_FP8 if shape.weight_kind == "fp8" else gbmoe.MOE_WEIGHT_INT8
-    fn = gbmoe.fused_moe_fp8 if kind == gbmoe.MOE_WEIGHT_FP8 else gbmoe.fused_moe_int8
+    kind = {"fp8": gbmoe.MOE_WEIGHT_FP8, "int8": gbmoe.MOE_WEIGHT_INT8, "int4": gbmoe.MOE_WEIGHT_INT4}[shape.weight_kind]
+    fn = {gbmoe.MOE_WEIGHT_FP8: gbmoe.fused_moe_fp8, gbmoe.MOE_WEIGHT_INT8: gbmoe.fused_moe_int8,
+          gbmoe.MOE_WEIGHT_INT4: gbmoe.fused_moe_int4}[kind]
     flags = gbmoe.MOE_ACT_FP8_1X128 if shape.act == "fp8_1x128" else gbmoe.MOE_PATH_AUTO
     ws = gbmoe.alloc_workspace(shape.M, shape.H, shape.I, shape.E_total, shape.topk_total, kind, flags, dev)
     out = torch.empty(shape.M, shape.H, dtype=torch.bfloat16, device=dev)
@@ -432,7 +443,8 @@ def run_ours(args, shape):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": ("fp8 x fp8 mma, f32 acc" if shape.act == "fp8_1x128" else
-                                       "fp8->f16 mma, f32 acc") if kind == 0 else "int8->f16 mma, f32 acc",
+                                       "fp8->f16 mma, f32 acc") if kind == 0 else
+                                      ("int8->f16 mma, f32 acc" if kind == 1 else "int4->f16 mma, f32 acc"),
         "data": "synthetic", "config": config_of(shape, args),
         "roofline": roofline, "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

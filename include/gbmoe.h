@@ -14,9 +14,10 @@
  *   4. the weighted combine out[t] = sum_k topk_weights[t,k] * y[t,k].
  *
  * Weights are FP8 E4M3 with one fp32 scale per 128x128 block (DeepSeek-style
- * block quantisation) or INT8 with one fp32 scale per output channel and
- * dynamic per-row INT8 activations (DA8W8).  Weights stay in their stored
- * format in HBM and are expanded in registers or shared memory.
+ * block quantisation), INT8 with one fp32 scale per output channel and
+ * dynamic per-row INT8 activations (DA8W8), or INT4 with one fp32 scale per
+ * row and 128 columns.  Weights stay in their stored format in HBM and are
+ * expanded in registers or shared memory.
  *
  * Conventions shared by every entry point
  *  - All data pointers are DEVICE pointers owned by the caller.  The library
@@ -55,7 +56,7 @@ typedef enum {
   MOE_ERR_BAD_IDS = 6      /* the device saw expert ids outside [0, E)         */
 } moe_status_t;
 
-/* flags of fused_moe_fp8 / fused_moe_int8 */
+/* flags of fused_moe_fp8 / fused_moe_int8 / fused_moe_int4 / fused_moe_gated */
 #define MOE_PATH_AUTO 0x0u    /* pick by tokens per expert                          */
 #define MOE_PATH_DECODE 0x1u  /* weight-streaming GEMV path (small token counts)    */
 #define MOE_PATH_PREFILL 0x2u /* tcgen05 grouped-GEMM path (large token counts)     */
@@ -69,6 +70,7 @@ typedef enum {
 
 #define MOE_WEIGHT_FP8 0
 #define MOE_WEIGHT_INT8 1
+#define MOE_WEIGHT_INT4 2
 
 /* Limits of this implementation (larger sizes return MOE_ERR_UNSUPPORTED). */
 #define MOE_MAX_EXPERTS 1024
@@ -191,7 +193,7 @@ moe_status_t moe_quant_act_fp8(const void* x_bf16, int M, int H, uint8_t* q, flo
 
 /*
  * Bytes of scratch the fused layer needs for these sizes and flags
- * (weight_kind MOE_WEIGHT_FP8 or MOE_WEIGHT_INT8).  The workspace must be
+ * (weight_kind MOE_WEIGHT_FP8, MOE_WEIGHT_INT8 or MOE_WEIGHT_INT4).  The workspace must be
  * 256-byte aligned.  Returns 0 for invalid or unsupported arguments.
  */
 size_t moe_workspace_size(int M, int H, int I, int E, int topk, int weight_kind,
@@ -249,9 +251,35 @@ moe_status_t fused_moe_int8(const void* x_bf16, const int32_t* topk_ids, const f
                             size_t workspace_bytes, moe_stream_t stream);
 
 /*
+ * The whole MoE layer with group-wise INT4 weights (W4A16).  The pages name
+ * INT4 as the quantised alternative to native FP8 (SGLang CPU backend
+ * write-up, closing section; OSDI'26 local-MoE summary, the INT4 decode
+ * baseline of its evaluation) but fix no layout; this one is:
+ *
+ *   w13        uint8 [E, 2I, H/2]   two's-complement int4 codes in [-8, 7],
+ *                                   column 2j in the low nibble of byte j,
+ *                                   column 2j+1 in its high nibble
+ *   w13_scale  fp32 [E, 2I, H/128]  W13[e,n,k] = q * w13_scale[e, n, k/128]
+ *   w2         uint8 [E, H, I/2],   w2_scale fp32 [E, H, I/128]
+ * other arguments as for fused_moe_fp8.  Activations enter the products at
+ * their bf16 values (rounded to fp16, as on the FP8 weight-only path) and
+ * each 128-deep partial sum is scaled by its row's group scale in fp32.
+ * H and I must be multiples of 128.  The layer runs on the weight-streaming
+ * (decode) kernels at every M; MOE_PATH_PREFILL is MOE_ERR_UNSUPPORTED and
+ * MOE_ACT_FP8_1X128 is MOE_ERR_INVALID_ARG.  Workspace:
+ * moe_workspace_size(..., MOE_WEIGHT_INT4, flags).
+ */
+moe_status_t fused_moe_int4(const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
+                            const uint8_t* w13, const float* w13_scale, const uint8_t* w2,
+                            const float* w2_scale, int M, int H, int I, int E, int topk,
+                            unsigned flags, void* out_bf16, void* workspace,
+                            size_t workspace_bytes, moe_stream_t stream);
+
+/*
  * The whole layer from router logits: moe_gate_topk, then fused_moe_fp8
- * (weight_kind MOE_WEIGHT_FP8) or fused_moe_int8 (MOE_WEIGHT_INT8) on its
- * result, with no host step between them.
+ * (weight_kind MOE_WEIGHT_FP8), fused_moe_int8 (MOE_WEIGHT_INT8) or
+ * fused_moe_int4 (MOE_WEIGHT_INT4) on its result, with no host step between
+ * them.
  *
  *   router_logits  fp32 [M, E]   E = routed experts
  *   gate           gating function and options, as for moe_gate_topk
@@ -261,7 +289,7 @@ moe_status_t fused_moe_int8(const void* x_bf16, const int32_t* topk_ids, const f
  *                  moe_gate_topk writes them (the routing the layer used)
  *   workspace      moe_workspace_size(M, H, I, E + shared_expert,
  *                  topk + shared_expert, weight_kind, flags) bytes
- * other arguments as for fused_moe_fp8 / fused_moe_int8 (flags must suit the
+ * other arguments as for fused_moe_fp8 / _int8 / _int4 (flags must suit the
  * weight kind).  When M <= MOE_GATE_INLINE_TOKENS and E <= 256 the ranking
  * runs inside the layer's first kernel, ahead of the routing alignment (one
  * launch fewer); otherwise it is one more launch, chained to the layer by

@@ -170,6 +170,8 @@ __device__ void prep_row_fp8_1x128(const __nv_bfloat16* xr, uint8_t* qr, float* 
 //   kind 2: x bf16 -> int8 codes + fp32 scale (DA8W8 path); codes stored as
 //           fp16 (exact) or int8
 //   kind 3: x bf16 -> E4M3 codes + one fp32 scale per 128 columns (FP8 A8 path)
+//   kind 4: x bf16 -> fp16 (RN), each group of 8 columns stored in the order
+//           0 4 1 5 2 6 3 7 (INT4 path: the order its weights expand in)
 template <typename QT>
 __device__ void prep_rows(const PrepArgs& p, int row0, int rstride) {
   __shared__ float red[32];
@@ -179,6 +181,19 @@ __device__ void prep_rows(const PrepArgs& p, int row0, int rstride) {
     if (p.kind == 3) {
       prep_row_fp8_1x128(xr, static_cast<uint8_t*>(p.q) + static_cast<size_t>(r) * p.H,
                          p.scale + static_cast<size_t>(r) * (p.H / kQBlock), p.H);
+      continue;
+    }
+    if (p.kind == 4) {
+      uint4* qr4 = reinterpret_cast<uint4*>(static_cast<__half*>(p.q) + static_cast<size_t>(r) * p.H);
+      for (int c = tid; c < p.H / 8; c += blockDim.x) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(xr + 8 * c);
+        const float2 f01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+        const float2 f23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+        const float2 f45 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.z));
+        const float2 f67 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.w));
+        qr4[c] = make_uint4(pack_half2(f01.x, f45.x), pack_half2(f01.y, f45.y), pack_half2(f23.x, f67.x),
+                            pack_half2(f23.y, f67.y));
+      }
       continue;
     }
     QT* qr = reinterpret_cast<QT*>(p.q) + static_cast<size_t>(r) * p.H;

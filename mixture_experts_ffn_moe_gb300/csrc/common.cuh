@@ -52,6 +52,37 @@ __device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
   hi = *reinterpret_cast<uint32_t*>(&hh);
 }
 
+// Eight two's-complement int4 values (one word, nibble i = value k_i) -> four
+// fp16 pairs, exact: r[0] = (k0, k4), r[1] = (k1, k5), r[2] = (k2, k6),
+// r[3] = (k3, k7).  Each nibble is biased to k+8 in [0, 15] and becomes mantissa
+// bits of the fp16 number 1024 (0x6400): at bit 0 the half reads 1024 + (k+8),
+// at bit 4 it reads 1024 + 16 (k+8).  One subtraction of 1032, or one fused
+// multiply-add by 1/16 and -72, leaves k exactly.
+__device__ __forceinline__ void s4x8_to_f16x8(uint32_t w, uint32_t r[4]) {
+  const uint32_t u = w ^ 0x88888888u, v = u >> 8;
+  const uint32_t l0 = (u & 0x000f000fu) | 0x64006400u, h0 = (u & 0x00f000f0u) | 0x64006400u;
+  const uint32_t l1 = (v & 0x000f000fu) | 0x64006400u, h1 = (v & 0x00f000f0u) | 0x64006400u;
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
+  const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));  // 1/16
+  const __half2 m72 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));    // -72
+  __half2 q0 = __hsub2(*reinterpret_cast<const __half2*>(&l0), bias);
+  __half2 q1 = __hfma2(*reinterpret_cast<const __half2*>(&h0), sixteenth, m72);
+  __half2 q2 = __hsub2(*reinterpret_cast<const __half2*>(&l1), bias);
+  __half2 q3 = __hfma2(*reinterpret_cast<const __half2*>(&h1), sixteenth, m72);
+  r[0] = *reinterpret_cast<uint32_t*>(&q0);
+  r[1] = *reinterpret_cast<uint32_t*>(&q1);
+  r[2] = *reinterpret_cast<uint32_t*>(&q2);
+  r[3] = *reinterpret_cast<uint32_t*>(&q3);
+}
+
+// INT4 layer: activations (x, and h between the GEMMs) are stored as fp16 with
+// every group of 8 consecutive K values in the order k0 k4 k1 k5 k2 k6 k3 k7, the
+// order in which s4x8_to_f16x8 yields the weights.  Stored position of K index n:
+__device__ __forceinline__ int int4_kperm(int n) {
+  const int i = n & 7;
+  return (n & ~7) | (i < 4 ? 2 * i : 2 * (i - 4) + 1);
+}
+
 template <int WK>
 __device__ __forceinline__ void w8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
   if constexpr (WK == MOE_WEIGHT_FP8) e4m3x4_to_f16x4(w, lo, hi);

@@ -38,7 +38,8 @@ struct AlignArgs {
 struct PrepArgs {
   const __nv_bfloat16* x;  // [M, H]
   int M, H;
-  int kind;                // 0 none, 1 bf16 -> fp16, 2 per-row int8, 3 FP8 E4M3 per 1x128 group
+  int kind;                // 0 none, 1 bf16 -> fp16, 2 per-row int8, 3 FP8 E4M3 per 1x128 group,
+                           // 4 bf16 -> fp16 in the INT4 K order
   void* q;                 // [M, H] fp16 (kinds 1, 2 in the prologue), int8 (quant entry) or E4M3 codes (kind 3)
   float* scale;            // [M] (kind 2) or [M, H/128] (kind 3)
   uint32_t* zero_words;    // words to clear (may be null)

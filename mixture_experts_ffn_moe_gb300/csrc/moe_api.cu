@@ -104,8 +104,9 @@ struct Layout {
   int tile_tokens = 0;
 };
 
-static int choose_path(int M, unsigned flags) {
+static int choose_path(int M, int kind, unsigned flags) {
   const unsigned p = flags & MOE_PATH_MASK;
+  if (kind == MOE_WEIGHT_INT4) return MOE_PATH_DECODE;  // INT4 runs on the weight-streaming kernels only
   if (p == MOE_PATH_DECODE || p == MOE_PATH_PREFILL) return static_cast<int>(p);
   if (flags & MOE_ACT_FP8_1X128) return MOE_PATH_PREFILL;  // the FP8 x FP8 products run on tcgen05 only
   return M <= MOE_MAX_DECODE_TOKENS ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
@@ -113,7 +114,7 @@ static int choose_path(int M, unsigned flags) {
 
 static Layout plan(int M, int H, int I, int E, int topk, int kind, unsigned flags) {
   Layout L;
-  L.path = choose_path(M, flags);
+  L.path = choose_path(M, kind, flags);
   L.B = L.path == MOE_PATH_PREFILL ? kPrefillBlock : kDecodeBlock;
   L.cap = max_padded(M, topk, E, L.B);
   size_t o = 0;
@@ -144,8 +145,8 @@ static Layout plan(int M, int H, int I, int E, int topk, int kind, unsigned flag
   }
   L.xq = take(static_cast<size_t>(M) * H * 2);
   L.sx = take(static_cast<size_t>(M) * 4);
-  if (kind == MOE_WEIGHT_FP8) {
-    L.h = take(L.cap * I * 2);
+  if (kind != MOE_WEIGHT_INT8) {
+    L.h = take(L.cap * I * 2);  // fp16 h (FP8, INT4)
   } else {
     L.h = take(L.cap * I * 4);
     L.hmax = take(L.cap * 4);
@@ -157,6 +158,10 @@ static Layout plan(int M, int H, int I, int E, int topk, int kind, unsigned flag
   L.y = take(static_cast<size_t>(M) * topk * H * 4);
   L.total = o;
   return L;
+}
+
+static bool known_kind(int kind) {
+  return kind == MOE_WEIGHT_FP8 || kind == MOE_WEIGHT_INT8 || kind == MOE_WEIGHT_INT4;
 }
 
 static bool known_flags(int kind, unsigned flags) {
@@ -176,12 +181,14 @@ static moe_status_t check_layer_args(int kind, const void* x, const void* ids, c
   if ((flags & MOE_PATH_MASK) == MOE_PATH_MASK) return fail(MOE_ERR_INVALID_ARG, "both path flags set");
   if ((flags & MOE_ACT_FP8_1X128) && (flags & MOE_PATH_MASK) == MOE_PATH_DECODE)
     return fail(MOE_ERR_UNSUPPORTED, "MOE_ACT_FP8_1X128 runs on the tcgen05 (prefill) path only");
+  if (kind == MOE_WEIGHT_INT4 && (flags & MOE_PATH_MASK) == MOE_PATH_PREFILL)
+    return fail(MOE_ERR_UNSUPPORTED, "INT4 weights run on the weight-streaming (decode) kernels only");
   if (static_cast<long long>(M) * topk > (1LL << 30) || static_cast<long long>(M) * H > (1LL << 40))
     return fail(MOE_ERR_UNSUPPORTED, "problem too large");
   if (M == 0) return MOE_OK;
   if (!x || !ids || !tw || !w13 || !s13 || !w2 || !s2 || !out) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
-  const int path = choose_path(M, flags);
-  if (path == MOE_PATH_DECODE && M > MOE_MAX_DECODE_TOKENS)
+  const int path = choose_path(M, kind, flags);
+  if (path == MOE_PATH_DECODE && M > MOE_MAX_DECODE_TOKENS && kind != MOE_WEIGHT_INT4)
     return fail(MOE_ERR_UNSUPPORTED, "decode path takes at most MOE_MAX_DECODE_TOKENS tokens");
   return MOE_OK;
 }
@@ -268,7 +275,7 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
   PrepArgs p{};
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.M = M; p.H = H;
-  p.kind = L.a8 ? 3 : kind == MOE_WEIGHT_FP8 ? 1 : 2;
+  p.kind = L.a8 ? 3 : kind == MOE_WEIGHT_FP8 ? 1 : kind == MOE_WEIGHT_INT4 ? 4 : 2;
   p.q = at<void>(ws, L.xq);
   p.scale = at<float>(ws, L.sx);
   if (kind == MOE_WEIGHT_INT8) { p.zero_words = at<uint32_t>(ws, L.hmax); p.n_zero = static_cast<int>(L.cap); }
@@ -390,8 +397,7 @@ moe_status_t fused_moe_gated(int weight_kind, const void* x_bf16, const float* r
                              unsigned flags, int32_t* topk_ids, float* topk_weights, void* out_bf16,
                              void* workspace, size_t workspace_bytes, moe_stream_t stream) {
   g_last_error.clear();
-  if (weight_kind != MOE_WEIGHT_FP8 && weight_kind != MOE_WEIGHT_INT8)
-    return fail(MOE_ERR_INVALID_ARG, "unknown weight kind");
+  if (!known_kind(weight_kind)) return fail(MOE_ERR_INVALID_ARG, "unknown weight kind");
   GateArgs g;
   moe_status_t st = check_gate(router_logits, M, E, topk, gate, g);
   if (st != MOE_OK) return st;
@@ -435,7 +441,7 @@ moe_status_t moe_quant_act_fp8(const void* x_bf16, int M, int H, uint8_t* q, flo
 
 size_t moe_workspace_size(int M, int H, int I, int E, int topk, int weight_kind, unsigned flags) {
   if (M < 0 || H <= 0 || I <= 0 || E <= 0 || topk <= 0 || E > MOE_MAX_EXPERTS) return 0;
-  if (weight_kind != MOE_WEIGHT_FP8 && weight_kind != MOE_WEIGHT_INT8) return 0;
+  if (!known_kind(weight_kind)) return 0;
   if (!known_flags(weight_kind, flags)) return 0;
   return plan(M, H, I, E, topk, weight_kind, flags).total;
 }
@@ -454,6 +460,14 @@ moe_status_t fused_moe_int8(const void* x_bf16, const int32_t* topk_ids, const f
                             int M, int H, int I, int E, int topk, unsigned flags, void* out_bf16,
                             void* workspace, size_t workspace_bytes, moe_stream_t stream) {
   return fused_impl(MOE_WEIGHT_INT8, x_bf16, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, M, H, I, E,
+                    topk, flags, out_bf16, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t fused_moe_int4(const void* x_bf16, const int32_t* topk_ids, const float* topk_weights,
+                            const uint8_t* w13, const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                            int M, int H, int I, int E, int topk, unsigned flags, void* out_bf16,
+                            void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  return fused_impl(MOE_WEIGHT_INT4, x_bf16, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, M, H, I, E,
                     topk, flags, out_bf16, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -16,6 +16,10 @@
 //  * INT8 weights (DA8W8) multiply per-row-quantised activations; the integer
 //    products are exact in fp32 and the per-row x per-channel scales are
 //    applied once at the end.
+//  * INT4 weights (two per byte, one scale per row and 128 columns) expand to
+//    fp16 in registers like FP8; each 128-deep partial sum is scaled by its
+//    row's group scale.  A stage holds the same 128 bytes of every row, which
+//    are 256 K values (two scale groups).
 //  * GEMM2 (down projection) writes each (token, slot) row already times its
 //    routing weight, indexed by slot; a separate pass sums the top-k rows of
 //    every token in slot order (deterministic, no atomics).
@@ -53,10 +57,11 @@ constexpr long long kWaitLimit = 4000000000LL;  // ~2 s of SM clocks per wait
 // fragments two K blocks ahead when there are few work items, 3 CTAs with
 // 48 KB rings and one block ahead otherwise -- more warps hide more latency.
 template <bool GATED, int OCC> struct Cfg {
-  // One stage = one 128-wide K block of 128 weight rows (GATED: 64 gate rows and
-  // the matching 64 up rows); consumer warp w owns 16-row m-tile w of every stage.
+  // One stage = 128 bytes of 128 weight rows (GATED: 64 gate rows and the matching
+  // 64 up rows): one 128-wide K block of 8-bit codes or 256 K values of INT4.
+  // Consumer warp w owns 16-row m-tile w of every stage.
   static constexpr int RING_BYTES = OCC == 2 ? 80 * 1024 : 48 * 1024;
-  static constexpr int BPF = OCC == 2 ? 2 : 1;             // K blocks of B fragments loaded ahead
+  static constexpr int BPF = OCC == 2 ? 2 : 1;             // stages of B fragments loaded ahead
   static constexpr int STAGE = NCW * 16 * KBLK;            // 16 KB of weight codes
   static constexpr int NS = RING_BYTES / STAGE;            // ring stages
   static constexpr int OFF_RED = RING_BYTES;
@@ -73,7 +78,7 @@ __device__ __forceinline__ uint32_t word8(const uint4& a, const uint4& b, int s)
   }
 }
 
-__device__ __forceinline__ uint32_t word16(const uint4 (&x)[4], int i) {
+__device__ __forceinline__ uint32_t word16(const uint4* x, int i) {
   const uint4& v = x[i >> 2];
   switch (i & 3) {
     case 0: return v.x; case 1: return v.y; case 2: return v.z; default: return v.w;
@@ -90,13 +95,35 @@ __device__ __forceinline__ uint32_t word16(const uint4 (&x)[4], int i) {
 // that consecutive tensor-core instructions do not wait on each other.
 template <int WK>
 __device__ __forceinline__ void tile_mma_128(float acc0[4], float acc1[4], const uint4& ra0, const uint4& ra1,
-                                             const uint4& rb0, const uint4& rb1, const uint4 (&xb)[4]) {
+                                             const uint4& rb0, const uint4& rb1, const uint4* xb) {
 #pragma unroll
   for (int s = 0; s < 8; ++s) {
     uint32_t a[4];
     w8x4_to_f16x4<WK>(word8(ra0, ra1, s), a[0], a[2]);
     w8x4_to_f16x4<WK>(word8(rb0, rb1, s), a[1], a[3]);
     mma_f16_16816((s & 1) ? acc1 : acc0, a, word16(xb, 2 * s), word16(xb, 2 * s + 1));
+  }
+}
+
+// INT4: 16 rows x 128 K.  Lane (g, t) holds 16 consecutive bytes (32 values) of
+// rows g and g+8 from column 32t (ra, rb) and the 32 matching activations of
+// token column g, stored in the INT4 K order (xb).  Word w of ra expands to the
+// pairs (k0,k4) (k1,k5) (k2,k6) (k3,k7) of K values 32t+8w..32t+8w+7: the first
+// two pairs feed one MMA step, the last two the next, and xb[w] holds the
+// activations of the same K values in the same order.
+__device__ __forceinline__ void tile_mma_int4(float acc0[4], float acc1[4], const uint4& ra, const uint4& rb,
+                                              const uint4* xb) {
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const uint32_t wa = w == 0 ? ra.x : w == 1 ? ra.y : w == 2 ? ra.z : ra.w;
+    const uint32_t wb = w == 0 ? rb.x : w == 1 ? rb.y : w == 2 ? rb.z : rb.w;
+    uint32_t fa[4], fb[4];
+    s4x8_to_f16x8(wa, fa);
+    s4x8_to_f16x8(wb, fb);
+    const uint32_t a0[4] = {fa[0], fb[0], fa[1], fb[1]};
+    mma_f16_16816(acc0, a0, xb[w].x, xb[w].y);
+    const uint32_t a1[4] = {fa[2], fb[2], fa[3], fb[3]};
+    mma_f16_16816(acc1, a1, xb[w].z, xb[w].w);
   }
 }
 
@@ -111,7 +138,7 @@ __device__ __forceinline__ uint4 lds_v4_once(const void* p) {
   return r;
 }
 
-__device__ __forceinline__ void load_b32(uint4 (&xb)[4], const __half* row, bool valid) {
+__device__ __forceinline__ void load_b32(uint4* xb, const __half* row, bool valid) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) xb[i] = valid ? ld_v4(row + 8 * i) : make_uint4(0u, 0u, 0u, 0u);
 }
@@ -133,7 +160,10 @@ template <int WK, bool GATED, int OCC>
 __global__ void __launch_bounds__(NUM_THREADS, OCC)
     skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, SkinnyArgs a) {
   using C = Cfg<GATED, OCC>;
-  constexpr int BPF = C::BPF;
+  constexpr bool I4 = WK == MOE_WEIGHT_INT4;
+  constexpr int KST = I4 ? 2 * KBLK : KBLK;  // K values per stage
+  constexpr int XB = I4 ? 8 : 4;             // 16-byte B fragments per stage and lane
+  constexpr int BPF = I4 ? 1 : C::BPF;       // an INT4 stage already carries twice the B fragments
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* red = reinterpret_cast<float*>(smem + C::OFF_RED);
@@ -143,7 +173,7 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
   volatile int* abort = abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int KB = a.K / KBLK;
+  const int KB = (a.K + KST - 1) / KST;  // stages per item (INT4: the last may hold one group)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NS; ++i) {
@@ -187,6 +217,7 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
           if (!(ok = mbar_wait(&empty[slot], par ^ 1, abort, a.status, kWaitLimit))) break;
           mbar_arrive_expect_tx(&full[slot], C::STAGE);
           uint8_t* dst = smem + slot * C::STAGE;
+          // (INT4 with K % 256 == 128: the last box reaches past the row end and is zero-filled)
           if (GATED) {
             tma_load_2d(dst, &tmap_w, &full[slot], kb * KBLK, row0);
             tma_load_2d(dst + C::STAGE / 2, &tmap_w, &full[slot], kb * KBLK, row0 + a.up_offset);
@@ -225,23 +256,42 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
       return a.b + static_cast<size_t>(x.pos0 + g) * a.K;  // rows of padded slots are readable
     }
   };
-  // B fragments of the next BPF K blocks are loaded ahead (a ring in registers)
-  uint4 xr[BPF][4];
+  // B fragments of the next BPF stages are loaded ahead (a ring in registers).  INT4:
+  // the two groups of a stage, the second absent past K.
+  uint4 xr[BPF][XB];
+  auto load_stage = [&](uint4* xb, const __half* brow, int kb, bool valid) {
+    load_b32(xb, brow + static_cast<size_t>(kb) * KST + t * 32, valid);
+    if constexpr (I4) load_b32(xb + 4, brow + static_cast<size_t>(kb) * KST + KBLK + t * 32,
+                               valid && kb * KST + KBLK < a.K);
+  };
   for (int it = it_begin; it < it_end; it += it_step) {
     const Item im = get_item(a, it);
     const int r0 = im.rt * C::ROWS;  // first output row of the item inside the expert
     // weight row (inside the expert) of this warp's m-tile
     const int mrow = GATED ? (warp < 4 ? r0 + warp * 16 : a.up_offset + r0 + (warp - 4) * 16) : r0 + warp * 16;
     const float* scale_row = a.wscale + (static_cast<size_t>(im.e) * rblocks + mrow / kQBlock) * kblocks;
+    // INT4: group scales of this lane's rows g and g+8, [E, rows, K/128]
+    const float* sg_row = a.wscale + (static_cast<size_t>(im.e) * a.rows_per_expert + mrow + g) * kblocks;
     bool bvalid;
     const __half* brow = b_row(im, bvalid);
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-    float scr[BPF];  // FP8 block scales of the prefetched K blocks
+    float scr[BPF];     // FP8 block scales of the prefetched stages
+    float sgs[BPF][4];  // INT4: group scales of rows g, g+8 (group 0) and g, g+8 (group 1)
+    auto load_scales = [&](int d, int kb) {
+      if constexpr (WK == MOE_WEIGHT_FP8) scr[d] = __ldg(scale_row + kb);
+      if constexpr (I4) {
+        const bool two = 2 * kb + 1 < kblocks;
+        sgs[d][0] = __ldg(sg_row + 2 * kb);
+        sgs[d][1] = __ldg(sg_row + 8 * kblocks + 2 * kb);
+        sgs[d][2] = two ? __ldg(sg_row + 2 * kb + 1) : 0.f;
+        sgs[d][3] = two ? __ldg(sg_row + 8 * kblocks + 2 * kb + 1) : 0.f;
+      }
+    };
 #pragma unroll
     for (int d = 0; d < BPF; ++d) {
       if (d < KB) {
-        load_b32(xr[d], brow + static_cast<size_t>(d) * KBLK + t * 32, bvalid);
-        if constexpr (WK == MOE_WEIGHT_FP8) scr[d] = __ldg(scale_row + d);
+        load_stage(xr[d], brow, d, bvalid);
+        load_scales(d, d);
       }
     }
     for (int kb0 = 0; kb0 < KB; kb0 += BPF) {
@@ -249,9 +299,31 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
     for (int d = 0; d < BPF; ++d) {
       const int kb = kb0 + d;
       if (kb >= KB) break;
-      const uint4 (&xb)[4] = xr[d];
+      const uint4* xb = xr[d];
       if (ok) ok = mbar_wait(&full[slot], phase, abort, a.status, kWaitLimit);
-      if (ok) {
+      if (!ok) {
+      } else if constexpr (I4) {
+        // rows warp*16 + g and + 8 of the stage; 16-byte chunk c of row r sits at c ^ (r % 8);
+        // chunks 0-3 are group 0, chunks 4-7 group 1, and lane t takes chunk t of each
+        const uint8_t* rg = smem + slot * C::STAGE + (warp * 16 + g) * KBLK;
+        const uint8_t* rh = rg + 8 * KBLK;
+        const uint4 ra0 = lds_v4_once(rg + ((t ^ g) << 4));
+        const uint4 ra1 = lds_v4_once(rg + (((t + 4) ^ g) << 4));
+        const uint4 rb0 = lds_v4_once(rh + ((t ^ g) << 4));
+        const uint4 rb1 = lds_v4_once(rh + (((t + 4) ^ g) << 4));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
+        float q0[4] = {0.f, 0.f, 0.f, 0.f}, q1[4] = {0.f, 0.f, 0.f, 0.f};
+        tile_mma_int4(p0, p1, ra0, rb0, xb);
+        tile_mma_int4(q0, q1, ra1, rb1, xb + 4);  // zero codes and activations past K
+        const float* sc = sgs[d];
+        acc[0] = fmaf(sc[0], p0[0] + p1[0], fmaf(sc[2], q0[0] + q1[0], acc[0]));
+        acc[1] = fmaf(sc[0], p0[1] + p1[1], fmaf(sc[2], q0[1] + q1[1], acc[1]));
+        acc[2] = fmaf(sc[1], p0[2] + p1[2], fmaf(sc[3], q0[2] + q1[2], acc[2]));
+        acc[3] = fmaf(sc[1], p0[3] + p1[3], fmaf(sc[3], q0[3] + q1[3], acc[3]));
+      } else {
         // rows warp*16 + g and + 8 of the stage; 16-byte chunk c of row r sits at c ^ (r % 8)
         const uint8_t* rg = smem + slot * C::STAGE + (warp * 16 + g) * KBLK;
         const uint8_t* rh = rg + 8 * KBLK;
@@ -275,8 +347,8 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
         }
       }
       if (kb + BPF < KB) {
-        load_b32(xr[d], brow + static_cast<size_t>(kb + BPF) * KBLK + t * 32, bvalid);
-        if constexpr (WK == MOE_WEIGHT_FP8) scr[d] = __ldg(scale_row + kb + BPF);
+        load_stage(xr[d], brow, kb + BPF, bvalid);
+        load_scales(d, kb + BPF);
       }
       if (++slot == C::NS) { slot = 0; phase ^= 1; }
     }
@@ -305,6 +377,10 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
           const int n = r0 + warp * 16 + row;
           if constexpr (WK == MOE_WEIGHT_FP8) {
             if (valid) reinterpret_cast<__half*>(a.out)[static_cast<size_t>(pos) * a.out_ld + n] =
+                __float2half_rn(silu_f32(G) * U);
+          } else if constexpr (WK == MOE_WEIGHT_INT4) {
+            // h feeds GEMM2's activations: stored in the INT4 K order
+            if (valid) reinterpret_cast<__half*>(a.out)[static_cast<size_t>(pos) * a.out_ld + int4_kperm(n)] =
                 __float2half_rn(silu_f32(G) * U);
           } else {
             float h = 0.f;
@@ -389,8 +465,10 @@ static cudaError_t launch_skinny_occ(const SkinnyArgs& a, const void* w, uint64_
                                      cudaStream_t s) {
   using C = dec::Cfg<GATED, OCC>;
   CUtensorMap mw;
-  if (!encode_tmap_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, static_cast<uint64_t>(a.K), w_rows, dec::KBLK,
-                      C::ROWS, CU_TENSOR_MAP_SWIZZLE_128B))
+  // a row holds K bytes of 8-bit codes or K/2 bytes of INT4; a stage takes 128 of them
+  const uint64_t row_bytes = WK == MOE_WEIGHT_INT4 ? a.K / 2 : a.K;
+  if (!encode_tmap_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, row_bytes, w_rows, dec::KBLK, C::ROWS,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   auto kern = dec::skinny_gemm_kernel<WK, GATED, OCC>;
   cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM);
@@ -402,8 +480,14 @@ static cudaError_t launch_skinny_occ(const SkinnyArgs& a, const void* w, uint64_
 template <int WK, bool GATED>
 static cudaError_t launch_skinny(const SkinnyArgs& a, const void* w, uint64_t w_rows, long long max_items,
                                  int num_sms, cudaStream_t s) {
-  return max_items >= 3LL * num_sms ? launch_skinny_occ<WK, GATED, 3>(a, w, w_rows, num_sms, s)
-                                    : launch_skinny_occ<WK, GATED, 2>(a, w, w_rows, num_sms, s);
+  // INT4 keeps two CTAs per SM: at three, its B fragments of two groups do not fit the registers
+  if constexpr (WK == MOE_WEIGHT_INT4) {
+    (void)max_items;
+    return launch_skinny_occ<WK, GATED, 2>(a, w, w_rows, num_sms, s);
+  } else {
+    return max_items >= 3LL * num_sms ? launch_skinny_occ<WK, GATED, 3>(a, w, w_rows, num_sms, s)
+                                      : launch_skinny_occ<WK, GATED, 2>(a, w, w_rows, num_sms, s);
+  }
 }
 
 cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook) {
@@ -426,12 +510,13 @@ cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cuda
   g1.out_ld = P.I;
   g1.hmax = P.hmax;
   g1.status = P.status;
+  const uint64_t rows1 = static_cast<uint64_t>(P.E) * 2 * P.I;
   cudaError_t err =
       weight_kind == MOE_WEIGHT_FP8
-          ? launch_skinny<MOE_WEIGHT_FP8, true>(g1, P.w13, static_cast<uint64_t>(P.E) * 2 * P.I,
-                                                max_tiles * g1.n_rt, num_sms, s)
-          : launch_skinny<MOE_WEIGHT_INT8, true>(g1, P.w13, static_cast<uint64_t>(P.E) * 2 * P.I,
-                                                 max_tiles * g1.n_rt, num_sms, s);
+          ? launch_skinny<MOE_WEIGHT_FP8, true>(g1, P.w13, rows1, max_tiles * g1.n_rt, num_sms, s)
+      : weight_kind == MOE_WEIGHT_INT4
+          ? launch_skinny<MOE_WEIGHT_INT4, true>(g1, P.w13, rows1, max_tiles * g1.n_rt, num_sms, s)
+          : launch_skinny<MOE_WEIGHT_INT8, true>(g1, P.w13, rows1, max_tiles * g1.n_rt, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("decode_gemm1", s);
   const __half* b2 = static_cast<const __half*>(P.h);
@@ -457,11 +542,12 @@ cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cuda
   g2.out = P.y;
   g2.out_ld = P.H;
   g2.status = P.status;
+  const uint64_t rows2 = static_cast<uint64_t>(P.E) * P.H;
   err = weight_kind == MOE_WEIGHT_FP8
-            ? launch_skinny<MOE_WEIGHT_FP8, false>(g2, P.w2, static_cast<uint64_t>(P.E) * P.H,
-                                                  max_tiles * g2.n_rt, num_sms, s)
-            : launch_skinny<MOE_WEIGHT_INT8, false>(g2, P.w2, static_cast<uint64_t>(P.E) * P.H,
-                                                   max_tiles * g2.n_rt, num_sms, s);
+            ? launch_skinny<MOE_WEIGHT_FP8, false>(g2, P.w2, rows2, max_tiles * g2.n_rt, num_sms, s)
+        : weight_kind == MOE_WEIGHT_INT4
+            ? launch_skinny<MOE_WEIGHT_INT4, false>(g2, P.w2, rows2, max_tiles * g2.n_rt, num_sms, s)
+            : launch_skinny<MOE_WEIGHT_INT8, false>(g2, P.w2, rows2, max_tiles * g2.n_rt, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("decode_gemm2", s);
   err = launch_combine(P.y, P.inv_pos, P.M, P.topk, P.H, P.out, num_sms, s);

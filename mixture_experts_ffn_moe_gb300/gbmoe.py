@@ -21,6 +21,7 @@ MOE_PATH_PREFILL = 0x2
 MOE_ACT_FP8_1X128 = 0x10
 MOE_WEIGHT_FP8 = 0
 MOE_WEIGHT_INT8 = 1
+MOE_WEIGHT_INT4 = 2
 MOE_MAX_EXPERTS = 1024
 MOE_MAX_DECODE_TOKENS = 128
 MOE_STATIC_SCRATCH_BYTES = 16 << 20
@@ -57,6 +58,7 @@ _SIGS = {
     "moe_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i, _u]),
     "fused_moe_fp8": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp, _sz, _vp]),
     "fused_moe_int8": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp, _sz, _vp]),
+    "fused_moe_int4": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp, _sz, _vp]),
     "fused_moe_fp8_static_scratch": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp]),
     "moe_read_status": (_i, [_vp, _vp, _vp]),
     "moe_profile_enable": (_i, [_i]),
@@ -156,7 +158,7 @@ def fused_moe_gated(weight_kind, x, router_logits, gate: GateConfig, topk, w13, 
 
     Returns (out, topk_ids, topk_weights); the weights hold E + gate.shared_expert experts.
     """
-    wdt = torch.uint8 if weight_kind == MOE_WEIGHT_FP8 else torch.int8
+    wdt = torch.int8 if weight_kind == MOE_WEIGHT_INT8 else torch.uint8
     _need(x, torch.bfloat16, "x")
     _need(router_logits, torch.float32, "router_logits")
     if w13.dtype == torch.float8_e4m3fn:
@@ -170,10 +172,9 @@ def fused_moe_gated(weight_kind, x, router_logits, gate: GateConfig, topk, w13, 
     M, H = x.shape
     E = router_logits.shape[1]
     sh = gate.shared_expert
-    Et, I2, H2 = w13.shape
-    if router_logits.shape[0] != M or Et != E + sh or H2 != H or tuple(w2.shape) != (Et, H, I2 // 2):
+    Et, I = _weight_dims(weight_kind, x, w13, w2)
+    if router_logits.shape[0] != M or Et != E + sh:
         raise ValueError("inconsistent shapes")
-    I = I2 // 2
     ids = topk_ids if topk_ids is not None else torch.empty(M, topk + sh, dtype=torch.int32, device=x.device)
     w = topk_weights if topk_weights is not None else torch.empty(M, topk + sh, dtype=torch.float32,
                                                                   device=x.device)
@@ -224,8 +225,18 @@ def alloc_workspace(M, H, I, E, topk, weight_kind, flags=MOE_PATH_AUTO, device="
     return torch.empty(n, dtype=torch.uint8, device=device)  # caching allocator blocks are 512-byte aligned
 
 
+def _weight_dims(kind, x, w13, w2):
+    """(E, I) of the stored weights; checks their shapes against x [M, H]."""
+    H = x.shape[1]
+    E, I2, Hs = w13.shape
+    pack = 2 if kind == MOE_WEIGHT_INT4 else 1  # INT4 stores two codes per byte along K
+    if Hs * pack != H or tuple(w2.shape) != (E, H, I2 // 2 // pack):
+        raise ValueError("inconsistent shapes")
+    return E, I2 // 2
+
+
 def _fused(fn_name, kind, x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, flags, out, workspace):
-    wdt = torch.uint8 if kind == MOE_WEIGHT_FP8 else torch.int8
+    wdt = torch.int8 if kind == MOE_WEIGHT_INT8 else torch.uint8
     _need(x, torch.bfloat16, "x")
     _need(topk_ids, torch.int32, "topk_ids")
     _need(topk_weights, torch.float32, "topk_weights")
@@ -238,13 +249,12 @@ def _fused(fn_name, kind, x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scal
     _need(w13_scale, torch.float32, "w13_scale")
     _need(w2_scale, torch.float32, "w2_scale")
     M, H = x.shape
-    E, I2, H2 = w13.shape
-    if H2 != H or tuple(w2.shape) != (E, H, I2 // 2) or topk_ids.shape[0] != M:
+    E, I = _weight_dims(kind, x, w13, w2)
+    if topk_ids.shape[0] != M:
         raise ValueError("inconsistent shapes")
     if tuple(topk_weights.shape) != tuple(topk_ids.shape):
         raise ValueError("topk_weights and topk_ids must have the same shape")
     topk = topk_ids.shape[1]
-    I = I2 // 2
     if out is None:
         out = torch.empty(M, H, dtype=torch.bfloat16, device=x.device)
     _need(out, torch.bfloat16, "out")
@@ -268,6 +278,14 @@ def fused_moe_int8(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, flag
                    workspace=None):
     """The MoE layer with INT8 per-channel weights and dynamic INT8 activations (see include/gbmoe.h)."""
     return _fused("fused_moe_int8", MOE_WEIGHT_INT8, x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale,
+                  flags, out, workspace)
+
+
+def fused_moe_int4(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, flags=MOE_PATH_AUTO, out=None,
+                   workspace=None):
+    """The MoE layer with group-wise INT4 weights: w13 uint8 [E, 2I, H/2] + scales [E, 2I, H/128],
+    w2 uint8 [E, H, I/2] + scales [E, H, I/128] (see include/gbmoe.h)."""
+    return _fused("fused_moe_int4", MOE_WEIGHT_INT4, x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale,
                   flags, out, workspace)
 
 

@@ -68,14 +68,17 @@ def tiny(M: int = 16) -> LayerShape:
     return LayerShape(f"tiny_M{M}", M, 256, 128, 8, 2, "fp8", "softmax")
 
 
-def deepseek_r1(M: int, routing: str = "deepseek", E: int = 256, act: str = "a16") -> LayerShape:
+def deepseek_r1(M: int, routing: str = "deepseek", E: int = 256, act: str = "a16",
+                weight_kind: str = "fp8") -> LayerShape:
     """DeepSeek-R1 layer shapes; a smaller E keeps the per-expert work and shrinks the weight set."""
-    return LayerShape(f"dsr1_{routing}_M{M}" + ("" if E == 256 else f"_E{E}") + ("" if act == "a16" else "_a8"),
-                      M, 7168, 2048, E, 8, "fp8", routing, shared_expert=True, n_group=8, topk_group=4, act=act)
+    return LayerShape(f"dsr1_{routing}_M{M}" + ("" if E == 256 else f"_E{E}") + ("" if act == "a16" else "_a8")
+                      + ("" if weight_kind == "fp8" else f"_{weight_kind}"),
+                      M, 7168, 2048, E, 8, weight_kind, routing, shared_expert=True, n_group=8, topk_group=4, act=act)
 
 
-def qwen3_235b(M: int) -> LayerShape:
-    return LayerShape(f"qwen3_M{M}", M, 4096, 1536, 128, 8, "int8", "softmax")
+def qwen3_235b(M: int, weight_kind: str = "int8") -> LayerShape:
+    return LayerShape(f"qwen3_M{M}" + ("" if weight_kind == "int8" else f"_{weight_kind}"), M, 4096, 1536, 128, 8,
+                      weight_kind, "softmax")
 
 
 def _cpu_gen(seed: int, stream: int) -> torch.Generator:

@@ -431,4 +431,8 @@ def fused_moe_rows(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, kind
     used = sorted({int(e) for e in np.unique(ids) if 0 <= e < E})
     if kind == "fp8":
         return fused_moe_fp8(x, ids, tw, w13, w13_scale, w2, w2_scale, experts=used, act=act)
+    if kind == "int4":
+        return fused_moe_int4(x, ids, tw, w13, w13_scale, w2, w2_scale, experts=used)
+    if kind != "int8":
+        raise ValueError(f"unknown weight kind {kind!r}")
     return fused_moe_int8(x, ids, tw, w13, w13_scale, w2, w2_scale, experts=used)

@@ -139,3 +139,19 @@ class GateCfg_bias(gbmoe.GateConfig):
 
     def __init__(self):
         super().__init__(gbmoe.MOE_GATE_SOFTMAX, 1, 1, 1.0, 16, 0)
+
+
+def test_int4_host_checks(lib):
+    p = ctypes.c_void_p(16)
+
+    def call(M=4, H=256, I=128, flags=0):
+        return lib.fused_moe_int4(p, p, p, p, p, p, p, M, H, I, 8, 2, flags, p, p, 0, None)
+
+    assert call(flags=gbmoe.MOE_PATH_PREFILL) == 2          # INT4 runs on the weight-streaming kernels
+    assert call(flags=gbmoe.MOE_ACT_FP8_1X128) == 1         # FP8 layer only
+    assert call(H=200) == 2
+    assert call() == 3                                      # valid: fails on the workspace
+    assert call(M=5000) == 3                                # any M (no decode-path token limit for INT4)
+    assert gbmoe.moe_workspace_size(4, 7168, 2048, 257, 9, gbmoe.MOE_WEIGHT_INT4) > 0
+    assert gbmoe.moe_workspace_size(4, 7168, 2048, 257, 9, gbmoe.MOE_WEIGHT_INT4, gbmoe.MOE_ACT_FP8_1X128) == 0
+    assert gbmoe.moe_workspace_size(4, 7168, 2048, 257, 9, 3) == 0

@@ -677,3 +677,11 @@ def test_int4_layer_top1_equals_dense_swiglu():
         W2 = torch.from_numpy(unpack(d["w2"][e]) * np.repeat(d["w2_scale"][e].double().numpy(), 128, axis=1))
         np.testing.assert_allclose(out[t], _dense_swiglu(x[t:t + 1], W13[:256], W13[256:], W2)[0].numpy(),
                                    rtol=1e-10, atol=1e-12)
+
+
+def test_int4_rows_subset_equals_full_call():
+    shape = synth.LayerShape("i4", 9, 256, 128, 6, 3, "int4", "softmax")
+    d = synth.make_layer(shape, seed=44)
+    full = oracle.fused_moe_int4(**d)
+    sub = oracle.fused_moe_rows(**d, kind="int4", tokens=[1, 7])
+    np.testing.assert_allclose(sub, full[[1, 7]], rtol=1e-12, atol=1e-15)
