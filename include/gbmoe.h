@@ -276,6 +276,39 @@ moe_status_t fused_moe_int4(const void* x_bf16, const int32_t* topk_ids, const f
                             size_t workspace_bytes, moe_stream_t stream);
 
 /*
+ * The experts of the layer on the masked, fixed-capacity layout of
+ * expert-parallel low-latency dispatch (the "masked" grouped GEMM of the
+ * DeepGEMM integration in the news rewrite of the LMSYS large-scale-EP blog,
+ * section "DeepGEMM集成"): tokens arrive already grouped by expert, each expert
+ * holding up to `cap` rows, and only a device-side count says how many are real.
+ * Nothing in the call depends on host knowledge of the counts, so it can be
+ * captured in a CUDA graph and replayed with new counts.
+ *
+ *   x_bf16     bf16 [E, cap, H]   row (e, i) is the i-th token sent to expert e
+ *   masked_m   int32 [E]          rows held by expert e (device memory, read by
+ *                                 the kernels); values are clamped to [0, cap]
+ *   w13, w2 (+ scales)            as for fused_moe_fp8 (weight_kind
+ *                                 MOE_WEIGHT_FP8) or fused_moe_int4
+ *                                 (MOE_WEIGHT_INT4); MOE_WEIGHT_INT8 is
+ *                                 MOE_ERR_UNSUPPORTED
+ *   out_bf16   bf16 [E, cap, H]   out[e, i] = W2_e (SiLU(W1_e x) * (W3_e x)) for
+ *                                 i < masked_m[e]; rows past the count are left
+ *                                 untouched.  No routing weight is applied (the
+ *                                 combine of the dispatch applies it).
+ *   workspace  moe_workspace_size_masked(E, cap, H, I, weight_kind) bytes,
+ *              256-byte aligned
+ * H and I multiples of 128, E <= MOE_MAX_EXPERTS, cap >= 1.  The products
+ * run on the weight-streaming (decode) kernels, with the arithmetic of the
+ * weight kind's layer entry point.  Every kernel of the call is enqueued on
+ * `stream`; flags: MOE_PATH_AUTO or MOE_PATH_DECODE only.
+ */
+size_t moe_workspace_size_masked(int E, int cap, int H, int I, int weight_kind);
+moe_status_t fused_moe_masked(int weight_kind, const void* x_bf16, const int32_t* masked_m, const void* w13,
+                              const float* w13_scale, const void* w2, const float* w2_scale, int E, int cap,
+                              int H, int I, unsigned flags, void* out_bf16, void* workspace,
+                              size_t workspace_bytes, moe_stream_t stream);
+
+/*
  * The whole layer from router logits: moe_gate_topk, then fused_moe_fp8
  * (weight_kind MOE_WEIGHT_FP8), fused_moe_int8 (MOE_WEIGHT_INT8) or
  * fused_moe_int4 (MOE_WEIGHT_INT4) on its result, with no host step between

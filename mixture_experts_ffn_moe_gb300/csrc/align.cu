@@ -24,35 +24,6 @@ namespace gbmoe {
 constexpr int kAlignThreads = 1024;
 constexpr int kAlignWarps = kAlignThreads / 32;
 
-// Block-wide exclusive scan of one int per thread (blockDim == 1024).
-__device__ int block_exclusive_scan(int v, int* warp_tot, int& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int n = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += n;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int w = warp_tot[lane];
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int n = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += n;
-    }
-    warp_tot[lane] = wi - w;  // exclusive prefix of warp totals
-    if (lane == 31) warp_tot[32] = wi;
-  }
-  __syncthreads();
-  const int res = warp_tot[warp] + incl - v;
-  total = warp_tot[32];
-  __syncthreads();
-  return res;
-}
-
 // One CTA: the full alignment.  Shared memory: kAlignWarps * E ints (per-warp
 // histograms, later per-warp write cursors) + 64 ints.
 __device__ void align_cta(const AlignArgs& a) {

@@ -89,6 +89,35 @@ __device__ __forceinline__ void w8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
   else s8x4_to_f16x4(w, lo, hi);
 }
 
+// Block-wide exclusive scan of one int per thread (blockDim == 1024).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_tot[lane];
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    warp_tot[lane] = wi - w;  // exclusive prefix of warp totals
+    if (lane == 31) warp_tot[32] = wi;
+  }
+  __syncthreads();
+  const int res = warp_tot[warp] + incl - v;
+  total = warp_tot[32];
+  __syncthreads();
+  return res;
+}
+
 // fp32 -> E4M3 code: round to nearest, ties to even, saturating to +-448.
 __device__ __forceinline__ uint32_t e4m3_code(float v) {
   return static_cast<uint32_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
@@ -137,8 +166,10 @@ __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)
 // predecessor in the stream is still running: everything it reads from the
 // predecessor must come after pdl_wait() (which returns once the predecessor has
 // completed and its writes are visible).  pdl_trigger() lets the successor start
-// launching; every kernel here triggers only after its own pdl_wait(), so data
-// written two kernels back is always complete when a kernel starts.
+// launching.  The first kernel of a call (routing prologue, router gating) triggers
+// at once, and every kernel that follows it waits before it reads anything.  Every
+// other kernel triggers only after its own pdl_wait(), so a kernel placed behind
+// one of those may read data written two kernels back without waiting.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

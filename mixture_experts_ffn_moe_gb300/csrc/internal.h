@@ -105,6 +105,10 @@ struct LayerPlan {
   float* sa8;            // [H/128, cap] gathered scales, transposed
   uint8_t* h8;           // [cap, I] E4M3 codes of h by position
   float* sh8;            // [I/128, cap] their scales, transposed
+  // masked layout: GEMM1 reads its activations by position (xq holds them in position
+  // order) and GEMM2 writes bf16 rows straight to out_direct[sorted_ids[pos]], unweighted;
+  // there is no combine
+  __nv_bfloat16* out_direct;
 };
 
 // One skinny grouped GEMM of the decode path (device view).
@@ -126,6 +130,8 @@ struct SkinnyArgs {
   int out_ld;
   uint32_t* hmax;        // INT8 GEMM1: per-position max |h| (bits)
   DeviceStatus* status;
+  int b_by_pos;          // GEMM1: activation rows by position (masked layout), not by token
+  __nv_bfloat16* out_bf16;  // GEMM2: if set, bf16 output rows out_bf16[slot] (unweighted), not y
 };
 
 size_t align_smem_bytes(int E);
@@ -134,6 +140,23 @@ size_t align_smem_bytes(int E);
 cudaError_t launch_prologue(const AlignArgs& a, const PrepArgs& p, int prep_ctas, cudaStream_t s,
                             const GateArgs* inline_gate = nullptr);
 cudaError_t launch_gate(const GateArgs& g, int num_sms, cudaStream_t s);
+
+// Masked layout: from masked_m [E] (clamped to [0, cap]) builds the token tiles of
+// every expert's rows (positions: each expert's rows padded to a multiple of 8),
+// sorted_ids[pos] = e * cap + i, and the prepared activations xq [positions, H]
+// (kind 1: fp16; kind 4: fp16 in the INT4 K order).
+struct MaskedArgs {
+  const __nv_bfloat16* x;   // [E * cap, H]
+  const int32_t* masked_m;  // [E]
+  int E, cap, H, kind;
+  __half* xq;               // [E * round8(cap), H]
+  int32_t* sorted_ids;      // [E * round8(cap)]
+  int4* ttiles;             // [E * ceil(cap / 8)]
+  int32_t* num_ttiles;
+  int32_t* num_post;
+  DeviceStatus* status;
+};
+cudaError_t launch_masked_prologue(const MaskedArgs& m, int num_sms, cudaStream_t s);
 cudaError_t launch_quant_rows(const PrepArgs& p, cudaStream_t s);
 cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook);
 cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook);

@@ -1,0 +1,94 @@
+// Masked (fixed-capacity) layout: the first kernel of fused_moe_masked.
+//
+// Expert-parallel low-latency dispatch hands the MoE layer its tokens already
+// grouped by expert, E blocks of `cap` rows, with a device-side count of the
+// real rows per expert (the masked grouped GEMM of the DeepGEMM integration in
+// the news rewrite of the LMSYS large-scale-EP blog, section "DeepGEMM集成").
+// Nothing needs sorting: this kernel turns the counts into the decode GEMMs'
+// work description and prepares the activation rows.
+//
+// Positions: expert e's real rows take positions off[e] .. off[e] + m_e - 1,
+// with off[] the exclusive prefix sum of the counts rounded up to 8, so a token
+// tile (<= 8 rows of one expert) never reaches past the buffers.  Every CTA
+// computes the prefix sum itself (E <= 1024 counts, one scan); CTA 0 writes the
+// tile list and sorted_ids[pos] = e * cap + i (the output row), the others copy
+// the real rows of x into position order, converted to fp16.
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace gbmoe {
+
+constexpr int kMaskedThreads = 1024;
+
+__global__ void __launch_bounds__(kMaskedThreads) masked_prologue_kernel(MaskedArgs m) {
+  __shared__ int off[MOE_MAX_EXPERTS + 1];
+  __shared__ int cnt[MOE_MAX_EXPERTS];
+  __shared__ int scan_tmp[33];
+  pdl_trigger();  // the next kernel may set itself up; it waits for this grid before reading
+  pdl_wait();     // the counts and x may come from the previous kernel (the dispatch)
+  const int tid = threadIdx.x;
+  int c = 0;
+  if (tid < m.E) {
+    c = __ldg(m.masked_m + tid);
+    c = c < 0 ? 0 : (c > m.cap ? m.cap : c);
+    cnt[tid] = c;
+  }
+  int total;
+  const int o = block_exclusive_scan((c + 7) & ~7, scan_tmp, total);
+  if (tid < m.E) off[tid] = o;
+  if (tid == 0) off[m.E] = total;
+  if (blockIdx.x == 0) {
+    int ntiles;
+    const int t0 = block_exclusive_scan((c + 7) / 8, scan_tmp, ntiles);
+    if (tid < m.E) {
+      for (int j = 0; j * 8 < c; ++j) m.ttiles[t0 + j] = make_int4(tid, o + 8 * j, min(8, c - 8 * j), 0);
+    }
+    if (tid == 0) {
+      *m.num_ttiles = ntiles;
+      *m.num_post = total;
+      if (m.status) { m.status->bad_ids = 0; m.status->flags = 0; }
+    }
+    __syncthreads();
+    // sorted_ids: one warp per expert
+    for (int e = tid >> 5; e < m.E; e += kMaskedThreads / 32)
+      for (int i = tid & 31; i < cnt[e]; i += 32) m.sorted_ids[off[e] + i] = e * m.cap + i;
+    return;
+  }
+  __syncthreads();
+  // activation rows, one warp per row; H is a multiple of 128, so a lane moves whole 8-column groups
+  const int warp = tid >> 5, lane = tid & 31;
+  const int nw = kMaskedThreads / 32;
+  const long long rows = static_cast<long long>(m.E) * m.cap;
+  for (long long r = (blockIdx.x - 1) * static_cast<long long>(nw) + warp; r < rows;
+       r += static_cast<long long>(gridDim.x - 1) * nw) {
+    const int e = static_cast<int>(r / m.cap), i = static_cast<int>(r - static_cast<long long>(e) * m.cap);
+    if (i >= cnt[e]) continue;
+    const uint4* src = reinterpret_cast<const uint4*>(m.x + r * m.H);
+    uint4* dst = reinterpret_cast<uint4*>(m.xq + static_cast<size_t>(off[e] + i) * m.H);
+    for (int g = lane; g < m.H / 8; g += 32) {
+      const uint4 raw = __ldg(src + g);
+      const float2 f01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
+      const float2 f23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
+      const float2 f45 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.z));
+      const float2 f67 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.w));
+      dst[g] = m.kind == 4 ? make_uint4(pack_half2(f01.x, f45.x), pack_half2(f01.y, f45.y),
+                                        pack_half2(f23.x, f67.x), pack_half2(f23.y, f67.y))
+                           : make_uint4(pack_half2(f01.x, f01.y), pack_half2(f23.x, f23.y),
+                                        pack_half2(f45.x, f45.y), pack_half2(f67.x, f67.y));
+    }
+  }
+}
+
+cudaError_t launch_masked_prologue(const MaskedArgs& m, int num_sms, cudaStream_t s) {
+  const long long rows = static_cast<long long>(m.E) * m.cap;
+  const long long per_cta = kMaskedThreads / 32;
+  long long prep = (rows + per_cta - 1) / per_cta;
+  if (prep > 2LL * num_sms) prep = 2LL * num_sms;
+  if (prep < 1) prep = 1;
+  return launch_kernel(masked_prologue_kernel, dim3(static_cast<unsigned>(1 + prep)), dim3(kMaskedThreads), 0, s,
+                       true, m);
+}
+
+}  // namespace gbmoe

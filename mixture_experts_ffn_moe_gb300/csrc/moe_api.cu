@@ -339,6 +339,87 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
   return MOE_OK;
 }
 
+// ------------------------------------------------------------------ masked layout
+struct MaskedLayout {
+  size_t status = 0, sorted = 0, ttiles = 0, scalars = 0, xq = 0, h = 0, total = 0;
+};
+
+static MaskedLayout plan_masked(int E, int cap, int H, int I) {
+  MaskedLayout L;
+  const size_t positions = static_cast<size_t>(E) * ((static_cast<size_t>(cap) + 7) / 8 * 8);
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes, 256); return at; };
+  L.status = take(kStatusBytes);
+  L.sorted = take(positions * 4);
+  L.ttiles = take(static_cast<size_t>(E) * ((cap + 7) / 8) * 16);
+  L.scalars = take(16);
+  L.xq = take(positions * H * 2);
+  L.h = take(positions * I * 2);
+  L.total = o;
+  return L;
+}
+
+static moe_status_t masked_impl(int kind, const void* x, const int32_t* masked_m, const void* w13,
+                                const float* s13, const void* w2, const float* s2, int E, int cap, int H, int I,
+                                unsigned flags, void* out, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  g_last_error.clear();
+  if (!known_kind(kind)) return fail(MOE_ERR_INVALID_ARG, "unknown weight kind");
+  if (kind == MOE_WEIGHT_INT8)
+    return fail(MOE_ERR_UNSUPPORTED, "the masked layout takes FP8 or INT4 weights (INT8 needs per-token scales)");
+  if (E <= 0 || cap <= 0 || H <= 0 || I <= 0) return fail(MOE_ERR_INVALID_ARG, "sizes must be positive");
+  if (E > MOE_MAX_EXPERTS) return fail(MOE_ERR_UNSUPPORTED, "more than MOE_MAX_EXPERTS experts");
+  if (H % kQBlock || I % kQBlock) return fail(MOE_ERR_UNSUPPORTED, "H and I must be multiples of 128");
+  if (flags & ~MOE_PATH_MASK) return fail(MOE_ERR_INVALID_ARG, "unknown flag bits for the masked layout");
+  if ((flags & MOE_PATH_MASK) == MOE_PATH_PREFILL || (flags & MOE_PATH_MASK) == MOE_PATH_MASK)
+    return fail(MOE_ERR_UNSUPPORTED, "the masked layout runs on the weight-streaming (decode) kernels");
+  if (static_cast<long long>(E) * cap > (1LL << 28)) return fail(MOE_ERR_UNSUPPORTED, "problem too large");
+  if (!x || !masked_m || !w13 || !s13 || !w2 || !s2 || !out) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(w13) % 16 ||
+      reinterpret_cast<uintptr_t>(w2) % 16 || reinterpret_cast<uintptr_t>(out) % 2)
+    return fail(MOE_ERR_INVALID_ARG, "x, w13 and w2 must be 16-byte aligned, out 2-byte aligned");
+  const MaskedLayout L = plan_masked(E, cap, H, I);
+  if (!ws) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) % 256) return fail(MOE_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (ws_bytes < L.total) return fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_workspace_size_masked()");
+  const int sms = num_sms_current();
+  if (sms <= 0) return fail(MOE_ERR_CUDA, "cannot query the current device");
+
+  MaskedArgs m{};
+  m.x = static_cast<const __nv_bfloat16*>(x);
+  m.masked_m = masked_m;
+  m.E = E; m.cap = cap; m.H = H;
+  m.kind = kind == MOE_WEIGHT_INT4 ? 4 : 1;
+  m.xq = at<__half>(ws, L.xq);
+  m.sorted_ids = at<int32_t>(ws, L.sorted);
+  m.ttiles = at<int4>(ws, L.ttiles);
+  m.num_ttiles = at<int32_t>(ws, L.scalars);
+  m.num_post = at<int32_t>(ws, L.scalars) + 1;
+  m.status = at<DeviceStatus>(ws, L.status);
+  const StageHook hook = prof_begin_call(stream);
+  cudaError_t err = launch_masked_prologue(m, sms, stream);
+  if (err != cudaSuccess) return cuda_fail(err, "masked prologue launch");
+  hook("masked_prologue", stream);
+
+  LayerPlan P{};
+  P.M = E * cap; P.H = H; P.I = I; P.E = E; P.topk = 1;
+  P.cap = static_cast<int>(static_cast<size_t>(E) * ((cap + 7) / 8 * 8));
+  P.xq = m.xq;
+  P.w13 = static_cast<const uint8_t*>(w13);
+  P.s13 = s13;
+  P.w2 = static_cast<const uint8_t*>(w2);
+  P.s2 = s2;
+  P.sorted_ids = m.sorted_ids;
+  P.num_post = m.num_post;
+  P.ttiles = m.ttiles;
+  P.num_ttiles = m.num_ttiles;
+  P.h = at<void>(ws, L.h);
+  P.status = m.status;
+  P.out_direct = static_cast<__nv_bfloat16*>(out);
+  err = launch_decode(P, kind, sms, stream, hook);
+  if (err != cudaSuccess) return cuda_fail(err, "masked decode launch");
+  return MOE_OK;
+}
+
 }  // namespace gbmoe
 
 using namespace gbmoe;
@@ -469,6 +550,21 @@ moe_status_t fused_moe_int4(const void* x_bf16, const int32_t* topk_ids, const f
                             void* workspace, size_t workspace_bytes, moe_stream_t stream) {
   return fused_impl(MOE_WEIGHT_INT4, x_bf16, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, M, H, I, E,
                     topk, flags, out_bf16, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t moe_workspace_size_masked(int E, int cap, int H, int I, int weight_kind) {
+  if (E <= 0 || cap <= 0 || H <= 0 || I <= 0 || E > MOE_MAX_EXPERTS) return 0;
+  if (weight_kind != MOE_WEIGHT_FP8 && weight_kind != MOE_WEIGHT_INT4) return 0;
+  if (static_cast<long long>(E) * cap > (1LL << 28)) return 0;
+  return plan_masked(E, cap, H, I).total;
+}
+
+moe_status_t fused_moe_masked(int weight_kind, const void* x_bf16, const int32_t* masked_m, const void* w13,
+                              const float* w13_scale, const void* w2, const float* w2_scale, int E, int cap,
+                              int H, int I, unsigned flags, void* out_bf16, void* workspace,
+                              size_t workspace_bytes, moe_stream_t stream) {
+  return masked_impl(weight_kind, x_bf16, masked_m, w13, w13_scale, w2, w2_scale, E, cap, H, I, flags, out_bf16,
+                     workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_read_status(const void* workspace, int32_t status_out[2], moe_stream_t stream) {

@@ -250,6 +250,7 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
   auto b_row = [&](const Item& x, bool& valid) -> const __half* {
     valid = g < x.cnt;
     if constexpr (GATED) {
+      if (a.b_by_pos) return a.b + static_cast<size_t>(x.pos0 + (valid ? g : 0)) * a.K;  // masked layout
       const int tok = valid ? __ldg(a.sorted_ids + x.pos0 + g) / a.topk : 0;
       return a.b + static_cast<size_t>(tok) * a.K;
     } else {
@@ -417,6 +418,10 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
           const int pos = im.pos0 + col;
           const int n = r0 + warp * 16 + row;
           const int slot = __ldg(a.sorted_ids + pos);
+          if (a.out_bf16) {  // masked layout: the output row itself, unweighted
+            a.out_bf16[static_cast<size_t>(slot) * a.out_ld + n] = __float2bfloat16_rn(acc[i]);
+            continue;
+          }
           float wgt = __ldg(a.topk_w + slot);
           if constexpr (WK == MOE_WEIGHT_INT8)
             wgt *= __ldg(a.sh + pos) * __ldg(a.wscale + static_cast<size_t>(im.e) * a.rows_per_expert + n);
@@ -510,6 +515,7 @@ cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cuda
   g1.out_ld = P.I;
   g1.hmax = P.hmax;
   g1.status = P.status;
+  g1.b_by_pos = P.out_direct ? 1 : 0;
   const uint64_t rows1 = static_cast<uint64_t>(P.E) * 2 * P.I;
   cudaError_t err =
       weight_kind == MOE_WEIGHT_FP8
@@ -542,6 +548,7 @@ cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cuda
   g2.out = P.y;
   g2.out_ld = P.H;
   g2.status = P.status;
+  g2.out_bf16 = P.out_direct;
   const uint64_t rows2 = static_cast<uint64_t>(P.E) * P.H;
   err = weight_kind == MOE_WEIGHT_FP8
             ? launch_skinny<MOE_WEIGHT_FP8, false>(g2, P.w2, rows2, max_tiles * g2.n_rt, num_sms, s)
@@ -550,6 +557,7 @@ cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cuda
             : launch_skinny<MOE_WEIGHT_INT8, false>(g2, P.w2, rows2, max_tiles * g2.n_rt, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("decode_gemm2", s);
+  if (P.out_direct) return cudaSuccess;  // masked layout: GEMM2 wrote the output rows
   err = launch_combine(P.y, P.inv_pos, P.M, P.topk, P.H, P.out, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("combine", s);

@@ -59,6 +59,8 @@ _SIGS = {
     "fused_moe_fp8": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp, _sz, _vp]),
     "fused_moe_int8": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp, _sz, _vp]),
     "fused_moe_int4": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp, _sz, _vp]),
+    "moe_workspace_size_masked": (_sz, [_i, _i, _i, _i, _i]),
+    "fused_moe_masked": (_i, [_i] + [_vp] * 6 + [_i] * 4 + [_u, _vp, _vp, _sz, _vp]),
     "fused_moe_fp8_static_scratch": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp]),
     "moe_read_status": (_i, [_vp, _vp, _vp]),
     "moe_profile_enable": (_i, [_i]),
@@ -287,6 +289,45 @@ def fused_moe_int4(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, flag
     w2 uint8 [E, H, I/2] + scales [E, H, I/128] (see include/gbmoe.h)."""
     return _fused("fused_moe_int4", MOE_WEIGHT_INT4, x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale,
                   flags, out, workspace)
+
+
+def moe_workspace_size_masked(E, cap, H, I, weight_kind) -> int:
+    return int(load().moe_workspace_size_masked(E, cap, H, I, weight_kind))
+
+
+def fused_moe_masked(weight_kind, x, masked_m, w13, w13_scale, w2, w2_scale, flags=MOE_PATH_AUTO, out=None,
+                     workspace=None):
+    """Expert FFNs on the masked layout: x bf16 [E, cap, H], masked_m int32 [E] (device) -> out bf16 [E, cap, H].
+
+    Rows i >= masked_m[e] of `out` are left untouched (see include/gbmoe.h).
+    """
+    _need(x, torch.bfloat16, "x")
+    _need(masked_m, torch.int32, "masked_m")
+    if w13.dtype == torch.float8_e4m3fn:
+        w13 = w13.view(torch.uint8)
+    if w2.dtype == torch.float8_e4m3fn:
+        w2 = w2.view(torch.uint8)
+    _need(w13, torch.uint8, "w13")
+    _need(w2, torch.uint8, "w2")
+    _need(w13_scale, torch.float32, "w13_scale")
+    _need(w2_scale, torch.float32, "w2_scale")
+    E, cap, H = x.shape
+    Ew, I = _weight_dims(weight_kind, x.view(E * cap, H), w13, w2)
+    if Ew != E or tuple(masked_m.shape) != (E,):
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.zeros(E, cap, H, dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, "out")
+    if workspace is None:
+        n = moe_workspace_size_masked(E, cap, H, I, weight_kind)
+        if n == 0:
+            raise MoEError(2, "moe_workspace_size_masked", "unsupported sizes or weight kind")
+        workspace = torch.empty(n, dtype=torch.uint8, device=x.device)
+    st = load().fused_moe_masked(weight_kind, _ptr(x), _ptr(masked_m), _ptr(w13), _ptr(w13_scale), _ptr(w2),
+                                 _ptr(w2_scale), E, cap, H, I, flags, _ptr(out), _ptr(workspace), workspace.numel(),
+                                 _stream(x))
+    _check(st, "fused_moe_masked")
+    return out
 
 
 def fused_moe_fp8_static_scratch(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, flags=MOE_PATH_AUTO,

@@ -155,3 +155,25 @@ def test_int4_host_checks(lib):
     assert gbmoe.moe_workspace_size(4, 7168, 2048, 257, 9, gbmoe.MOE_WEIGHT_INT4) > 0
     assert gbmoe.moe_workspace_size(4, 7168, 2048, 257, 9, gbmoe.MOE_WEIGHT_INT4, gbmoe.MOE_ACT_FP8_1X128) == 0
     assert gbmoe.moe_workspace_size(4, 7168, 2048, 257, 9, 3) == 0
+
+
+def test_masked_host_checks(lib):
+    p = ctypes.c_void_p(16)
+
+    def call(kind=0, E=8, cap=16, H=256, I=128, flags=0, null=False):
+        q = None if null else p
+        return lib.fused_moe_masked(kind, q, q, q, q, q, q, E, cap, H, I, flags, q, q, 0, None)
+
+    assert call(kind=1) == 2                      # INT8 needs per-token scales
+    assert call(kind=7) == 1
+    assert call(cap=0) == 1
+    assert call(E=5000) == 2
+    assert call(H=200) == 2
+    assert call(flags=gbmoe.MOE_PATH_PREFILL) == 2
+    assert call(flags=gbmoe.MOE_ACT_FP8_1X128) == 1
+    assert call(null=True) == 1
+    assert call() == 3                            # valid: fails on the workspace
+    assert call(kind=2) == 3
+    a = gbmoe.moe_workspace_size_masked(32, 128, 7168, 2048, gbmoe.MOE_WEIGHT_FP8)
+    assert a > 32 * 128 * (7168 + 2048) * 2
+    assert gbmoe.moe_workspace_size_masked(32, 128, 7168, 2048, gbmoe.MOE_WEIGHT_INT8) == 0
