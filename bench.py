@@ -18,6 +18,7 @@ its own GPU (the layer is not sharded across GPUs); rank 0 prints.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -71,9 +72,31 @@ GATED = {f"{n}_gated": n for n in ("dsr1_decode_M1", "dsr1_decode_M4", "dsr1_pre
                                    "qwen3_M16", "qwen3_M4096")}
 
 
+# Masked fixed-capacity layout of expert-parallel low-latency decode: the 32 local experts of
+# one of 8 ranks of a DeepSeek-R1 layer, 128 rows each; the counts are the rows the
+# DeepSeek router sends to experts 0..31 from a global batch of M tokens.
+MASKED = {"dsr1_masked_ep8_M64": (32, 128, 64), "dsr1_masked_ep8_M512": (32, 128, 512)}
+
+
+def masked_problem(name, seed=1234):
+    """(local layer shape [M = E*cap rows, topk 1], x [E*cap, H], flat ids [E*cap, 1] with -1 on
+    padding rows, unit weights, counts [E])."""
+    E, cap, M = MASKED[name]
+    full = synth.deepseek_r1(M)
+    ids, _ = synth.make_routing(full, seed)
+    counts = torch.bincount(ids[:, :full.topk].reshape(-1).long(), minlength=full.E)[:E].clamp(max=cap)
+    shape = synth.LayerShape(name, E * cap, full.H, full.I, E, 1, "fp8", "uniform")
+    x = synth.make_x(shape, seed)
+    flat = torch.full((E * cap, 1), -1, dtype=torch.int32)
+    for e in range(E):
+        flat[e * cap:e * cap + int(counts[e]), 0] = e
+    return shape, x, flat, torch.ones(E * cap, 1), counts.to(torch.int32)
+
+
 def all_workloads():
     w = workloads()
-    return {**w, **{g: w[base] for g, base in GATED.items()}}
+    masked = {n: synth.LayerShape(n, E * cap, 7168, 2048, E, 1, "fp8", "uniform") for n, (E, cap, _) in MASKED.items()}
+    return {**w, **{g: w[base] for g, base in GATED.items()}, **masked}
 
 
 def gate_config_of(shape):
@@ -252,28 +275,32 @@ def cpu_cores() -> int:
     return os.cpu_count() or 1
 
 
-def oracle_sample(shape, x, ids, w, weights):
+def oracle_sample(shape, x, ids, w, weights, token=0):
     """Times the oracle on one token of the batch (all of its experts); returns (tokens/s, seconds, text)."""
     import oracle
     w13, s13, w2, s2 = weights
     t0 = time.perf_counter()
-    oracle.fused_moe_rows(x, ids, w, w13, s13, w2, s2, kind=shape.weight_kind, tokens=[0], act=shape.act)
+    oracle.fused_moe_rows(x, ids, w, w13, s13, w2, s2, kind=shape.weight_kind, tokens=[token], act=shape.act)
     dt = time.perf_counter() - t0
-    return 1.0 / dt, dt, f"1 token of the {shape.M}-token batch ({int((ids[0] >= 0).sum())} experts), float64 numpy"
+    return 1.0 / dt, dt, (f"1 token of the {shape.M}-token batch ({int((ids[token] >= 0).sum())} experts), "
+                          "float64 numpy")
 
 
 def run_reference(args, shape):
     world, rank, _ = dist_setup()
     if rank != 0:
         return
-    x, ids, w, weights = make_inputs(shape) if torch.cuda.is_available() else (None, None, None, None)
-    if weights is None:
+    wdev = "cuda" if torch.cuda.is_available() else "cpu"
+    if args.workload in MASKED:
+        shape, x, ids, w, _ = masked_problem(args.workload)
+    else:
         ids, w = synth.make_routing(shape, 1234)
         x = synth.make_x(shape, 1234)
-        weights = synth.make_weights(shape, 1234, device="cpu")
+    weights = synth.make_weights(shape, 1234, device=wdev)
+    tok = int((ids[:, 0] >= 0).nonzero()[0])
     for _ in range(args.warmup):
-        oracle_sample(shape, x, ids, w, weights)
-    times = [oracle_sample(shape, x, ids, w, weights)[1] for _ in range(args.steps)]
+        oracle_sample(shape, x, ids, w, weights, tok)
+    times = [oracle_sample(shape, x, ids, w, weights, tok)[1] for _ in range(args.steps)]
     total = sum(times)
     value = args.steps / total
     line = {
@@ -282,13 +309,19 @@ def run_reference(args, shape):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(shape, args),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": oracle_sample(shape, x, ids, w, weights)[2] + " per step"},
+                         "sample": oracle_sample(shape, x, ids, w, weights, tok)[2] + " per step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
 def config_of(shape, args):
+    if args.workload in MASKED:
+        E, cap, M = MASKED[args.workload]
+        return {"workload": args.workload, "layout": f"masked: {E} local experts x {cap} rows (rank 0 of 8)",
+                "global_tokens": M, "H": shape.H, "I": shape.I, "weights": "fp8_e4m3_block128",
+                "activations": "bf16", "unit": "a token is one dispatched (token, local expert) row",
+                "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas{args.gpus}"}
     return {"workload": args.workload, "M": shape.M, "H": shape.H, "I": shape.I, "E": shape.E_total,
             "topk": shape.topk_total, "weights": {"fp8": "fp8_e4m3_block128", "int8": "int8_per_channel",
                                                   "int4": "int4_group128"}[shape.weight_kind],
@@ -308,13 +341,26 @@ def run_ours(args, shape):
     build.build()
     gbmoe.load()
     dev = torch.device("cuda", local)
-    x, ids, w, (w13, s13, w2, s2) = make_inputs(shape)
+    masked = args.workload in MASKED
+    if masked:
+        shape, x, ids, w, counts = masked_problem(args.workload)
+        w13, s13, w2, s2 = synth.make_weights(shape, 1234, device="cuda")
+        units = int(counts.sum())  # dispatched rows processed per step
+    else:
+        x, ids, w, (w13, s13, w2, s2) = make_inputs(shape)
+        units = shape.M
     xd, idsd, wd = x.to(dev), ids.to(dev), w.to(dev)
     kind = {"fp8": gbmoe.MOE_WEIGHT_FP8, "int8": gbmoe.MOE_WEIGHT_INT8, "int4": gbmoe.MOE_WEIGHT_INT4}[shape.weight_kind]
     fn = {gbmoe.MOE_WEIGHT_FP8: gbmoe.fused_moe_fp8, gbmoe.MOE_WEIGHT_INT8: gbmoe.fused_moe_int8,
           gbmoe.MOE_WEIGHT_INT4: gbmoe.fused_moe_int4}[kind]
     flags = gbmoe.MOE_ACT_FP8_1X128 if shape.act == "fp8_1x128" else gbmoe.MOE_PATH_AUTO
-    ws = gbmoe.alloc_workspace(shape.M, shape.H, shape.I, shape.E_total, shape.topk_total, kind, flags, dev)
+    if masked:
+        E_loc, cap = shape.E, shape.M // shape.E
+        ws = torch.empty(gbmoe.moe_workspace_size_masked(E_loc, cap, shape.H, shape.I, kind), dtype=torch.uint8,
+                         device=dev)
+        md = counts.to(dev)
+    else:
+        ws = gbmoe.alloc_workspace(shape.M, shape.H, shape.I, shape.E_total, shape.topk_total, kind, flags, dev)
     out = torch.empty(shape.M, shape.H, dtype=torch.bfloat16, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -328,6 +374,10 @@ def run_ours(args, shape):
         def step():
             gbmoe.fused_moe_gated(kind, xd, lgd, gcfg, shape.topk, w13, s13, w2, s2, flags=flags, out=out,
                                   workspace=ws, topk_ids=idsd, topk_weights=wd)
+    elif masked:
+        def step():
+            gbmoe.fused_moe_masked(kind, xd.view(E_loc, cap, shape.H), md, w13, s13, w2, s2,
+                                   out=out.view(E_loc, cap, shape.H), workspace=ws)
     else:
         def step():
             fn(xd, idsd, wd, w13, s13, w2, s2, flags=flags, out=out, workspace=ws)
@@ -375,11 +425,12 @@ def run_ours(args, shape):
     gbmoe.moe_profile_enable(0)
     total_ms = max_over_ranks(sum(step_ms), world)
     ms_per_step = total_ms / args.steps
-    value = world * shape.M * args.steps / (total_ms / 1e3)
+    value = world * units * args.steps / (total_ms / 1e3)
 
     # ---- roofline of the dominant kernel
     peaks = measured_peaks()
-    work = stage_work(shape, ids)
+    # (masked: the activation terms count the real rows only)
+    work = stage_work(dataclasses.replace(shape, M=units) if masked else shape, ids)
     stage_avg = {name: ms / max(n_calls, 1) for name, ms in stages}
     dominant = max((n for n in stage_avg if n in work), key=lambda n: stage_avg[n])
     dbytes, dflops = work[dominant]
@@ -410,8 +461,10 @@ def run_ours(args, shape):
     # (gated workloads copy the router logits instead of the routing)
     xh, idsh, wh = x.pin_memory(), ids.pin_memory(), w.pin_memory()
     lgh = lg.pin_memory() if gated else None
+    mh = counts.pin_memory() if masked else None
     outh = torch.empty(shape.M, shape.H, dtype=torch.bfloat16).pin_memory()
-    h2d = xh.numel() * 2 + (lgh.numel() * 4 if gated else idsh.numel() * 4 + wh.numel() * 4)
+    h2d = xh.numel() * 2 + (lgh.numel() * 4 if gated else mh.numel() * 4 if masked else
+                            idsh.numel() * 4 + wh.numel() * 4)
     d2h = outh.numel() * 2
     e_start = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     e_end = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -421,6 +474,8 @@ def run_ours(args, shape):
         xd.copy_(xh, non_blocking=True)
         if gated:
             lgd.copy_(lgh, non_blocking=True)
+        elif masked:
+            md.copy_(mh, non_blocking=True)
         else:
             idsd.copy_(idsh, non_blocking=True)
             wd.copy_(wh, non_blocking=True)
@@ -429,14 +484,14 @@ def run_ours(args, shape):
         e_end[i].record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(e_start, e_end)), world)
-    e2e_value = world * shape.M * args.steps / (e2e_ms / 1e3)
+    e2e_value = world * units * args.steps / (e2e_ms / 1e3)
 
     if rank != 0:
         return
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        v, dt, text = oracle_sample(shape, x, ids, w, (w13, s13, w2, s2))
+        v, dt, text = oracle_sample(shape, x, ids, w, (w13, s13, w2, s2), token=int((ids[:, 0] >= 0).nonzero()[0]))
         cpu = {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle", "sample": text,
                "seconds": dt}
     line = {
