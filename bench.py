@@ -62,6 +62,7 @@ def workloads():
         "dsr1_sweep_M64_int4": synth.deepseek_r1(64, routing="uniform", weight_kind="int4"),
         "qwen3_M1_int4": synth.qwen3_235b(1, weight_kind="int4"),
         "qwen3_M16_int4": synth.qwen3_235b(16, weight_kind="int4"),
+        "dsr1_decode_M4_E32_int4": synth.deepseek_r1(4, E=32, weight_kind="int4"),
     }
 
 

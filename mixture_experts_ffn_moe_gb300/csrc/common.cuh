@@ -52,16 +52,25 @@ __device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
   hi = *reinterpret_cast<uint32_t*>(&hh);
 }
 
+// f(w, a, b) = a ? (w ^ b) : b, bit by bit (one LOP3): where a is set the bit of
+// w passes, inverted where b is set; elsewhere the bit of b is the result.
+__device__ __forceinline__ uint32_t lop3_sel_xor(uint32_t w, uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(r) : "r"(w), "r"(a), "r"(b));
+  return r;
+}
+
 // Eight two's-complement int4 values (one word, nibble i = value k_i) -> four
 // fp16 pairs, exact: r[0] = (k0, k4), r[1] = (k1, k5), r[2] = (k2, k6),
-// r[3] = (k3, k7).  Each nibble is biased to k+8 in [0, 15] and becomes mantissa
-// bits of the fp16 number 1024 (0x6400): at bit 0 the half reads 1024 + (k+8),
-// at bit 4 it reads 1024 + 16 (k+8).  One subtraction of 1032, or one fused
-// multiply-add by 1/16 and -72, leaves k exactly.
+// r[3] = (k3, k7).  Each nibble is biased to k+8 in [0, 15] (its top bit
+// inverted) and becomes mantissa bits of the fp16 number 1024 (0x6400): at bit
+// 0 the half reads 1024 + (k+8), at bit 4 it reads 1024 + 16 (k+8).  One LOP3
+// per pair selects the nibbles, inverts their top bit and sets the exponent; one
+// subtraction of 1032, or one fused multiply-add by 1/16 and -72, leaves k exactly.
 __device__ __forceinline__ void s4x8_to_f16x8(uint32_t w, uint32_t r[4]) {
-  const uint32_t u = w ^ 0x88888888u, v = u >> 8;
-  const uint32_t l0 = (u & 0x000f000fu) | 0x64006400u, h0 = (u & 0x00f000f0u) | 0x64006400u;
-  const uint32_t l1 = (v & 0x000f000fu) | 0x64006400u, h1 = (v & 0x00f000f0u) | 0x64006400u;
+  const uint32_t v = w >> 8;
+  const uint32_t l0 = lop3_sel_xor(w, 0x000f000fu, 0x64086408u), h0 = lop3_sel_xor(w, 0x00f000f0u, 0x64806480u);
+  const uint32_t l1 = lop3_sel_xor(v, 0x000f000fu, 0x64086408u), h1 = lop3_sel_xor(v, 0x00f000f0u, 0x64806480u);
   const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
   const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));  // 1/16
   const __half2 m72 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));    // -72
