@@ -76,13 +76,16 @@ GATED = {f"{n}_gated": n for n in ("dsr1_decode_M1", "dsr1_decode_M4", "dsr1_pre
 # Masked fixed-capacity layout of expert-parallel low-latency decode: the 32 local experts of
 # one of 8 ranks of a DeepSeek-R1 layer, 128 rows each; the counts are the rows the
 # DeepSeek router sends to experts 0..31 from a global batch of M tokens.
-MASKED = {"dsr1_masked_ep8_M64": (32, 128, 64), "dsr1_masked_ep8_M512": (32, 128, 512)}
+# (local experts, rows per expert, global tokens, path flag: the caller picks the path, since the counts
+# live on the device)
+MASKED = {"dsr1_masked_ep8_M64": (32, 128, 64, 0), "dsr1_masked_ep8_M512": (32, 128, 512, 0),
+          "dsr1_masked_ep8_M512_tc": (32, 128, 512, 2), "dsr1_masked_ep8_M4096_tc": (32, 1024, 4096, 2)}
 
 
 def masked_problem(name, seed=1234):
     """(local layer shape [M = E*cap rows, topk 1], x [E*cap, H], flat ids [E*cap, 1] with -1 on
     padding rows, unit weights, counts [E])."""
-    E, cap, M = MASKED[name]
+    E, cap, M, _ = MASKED[name]
     full = synth.deepseek_r1(M)
     ids, _ = synth.make_routing(full, seed)
     counts = torch.bincount(ids[:, :full.topk].reshape(-1).long(), minlength=full.E)[:E].clamp(max=cap)
@@ -96,7 +99,7 @@ def masked_problem(name, seed=1234):
 
 def all_workloads():
     w = workloads()
-    masked = {n: synth.LayerShape(n, E * cap, 7168, 2048, E, 1, "fp8", "uniform") for n, (E, cap, _) in MASKED.items()}
+    masked = {n: synth.LayerShape(n, E * cap, 7168, 2048, E, 1, "fp8", "uniform") for n, (E, cap, _, _) in MASKED.items()}
     return {**w, **{g: w[base] for g, base in GATED.items()}, **masked}
 
 
@@ -318,8 +321,9 @@ def run_reference(args, shape):
 
 def config_of(shape, args):
     if args.workload in MASKED:
-        E, cap, M = MASKED[args.workload]
+        E, cap, M, path = MASKED[args.workload]
         return {"workload": args.workload, "layout": f"masked: {E} local experts x {cap} rows (rank 0 of 8)",
+                "path": "tcgen05 (MOE_PATH_PREFILL)" if path == 2 else "weight-streaming",
                 "global_tokens": M, "H": shape.H, "I": shape.I, "weights": "fp8_e4m3_block128",
                 "activations": "bf16", "unit": "a token is one dispatched (token, local expert) row",
                 "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas{args.gpus}"}
@@ -378,7 +382,7 @@ def run_ours(args, shape):
     elif masked:
         def step():
             gbmoe.fused_moe_masked(kind, xd.view(E_loc, cap, shape.H), md, w13, s13, w2, s2,
-                                   out=out.view(E_loc, cap, shape.H), workspace=ws)
+                                   out=out.view(E_loc, cap, shape.H), workspace=ws, flags=MASKED[args.workload][3])
     else:
         def step():
             fn(xd, idsd, wd, w13, s13, w2, s2, flags=flags, out=out, workspace=ws)

@@ -73,6 +73,7 @@ struct PrefillArgs {
   int out_ld;
   uint32_t* hmax;        // INT8 GEMM1: per-position max |h| (bits)
   DeviceStatus* status;
+  __nv_bfloat16* out_bf16;  // GEMM2 (FP8): if set, bf16 output rows out_bf16[slot] (unweighted), not y
 };
 
 // Everything the path launchers need (host view of one call).
@@ -142,16 +143,17 @@ cudaError_t launch_prologue(const AlignArgs& a, const PrepArgs& p, int prep_ctas
 cudaError_t launch_gate(const GateArgs& g, int num_sms, cudaStream_t s);
 
 // Masked layout: from masked_m [E] (clamped to [0, cap]) builds the token tiles of
-// every expert's rows (positions: each expert's rows padded to a multiple of 8),
-// sorted_ids[pos] = e * cap + i, and the prepared activations xq [positions, H]
-// (kind 1: fp16; kind 4: fp16 in the INT4 K order).
+// every expert's rows (positions: each expert's rows padded to a multiple of
+// `block`; tiles of up to `tile` rows), sorted_ids[pos] = e * cap + i, and the
+// prepared activations xq [positions, H] (kind 1: fp16; kind 4: fp16 in the INT4
+// K order).  Decode path: block = tile = 8; tcgen05 path: block 16, tile 128.
 struct MaskedArgs {
   const __nv_bfloat16* x;   // [E * cap, H]
   const int32_t* masked_m;  // [E]
-  int E, cap, H, kind;
-  __half* xq;               // [E * round8(cap), H]
-  int32_t* sorted_ids;      // [E * round8(cap)]
-  int4* ttiles;             // [E * ceil(cap / 8)]
+  int E, cap, H, kind, block, tile;
+  __half* xq;               // [E * round16(cap), H]
+  int32_t* sorted_ids;      // [E * round16(cap)]
+  int4* ttiles;             // [E * ceil(cap / tile)]
   int32_t* num_ttiles;
   int32_t* num_post;
   DeviceStatus* status;

@@ -4,14 +4,15 @@
 // grouped by expert, E blocks of `cap` rows, with a device-side count of the
 // real rows per expert (the masked grouped GEMM of the DeepGEMM integration in
 // the news rewrite of the LMSYS large-scale-EP blog, section "DeepGEMM集成").
-// Nothing needs sorting: this kernel turns the counts into the decode GEMMs'
-// work description and prepares the activation rows.
+// Nothing needs sorting: this kernel turns the counts into the GEMMs' work
+// description and prepares the activation rows.
 //
 // Positions: expert e's real rows take positions off[e] .. off[e] + m_e - 1,
-// with off[] the exclusive prefix sum of the counts rounded up to 8, so a token
-// tile (<= 8 rows of one expert) never reaches past the buffers.  Every CTA
-// computes the prefix sum itself (E <= 1024 counts, one scan); CTA 0 writes the
-// tile list and sorted_ids[pos] = e * cap + i (the output row), the others copy
+// with off[] the exclusive prefix sum of the counts rounded up to the block (8
+// for the decode kernels, 16 for the tcgen05 ones), so a token tile never reads
+// past the buffers and starts where the tcgen05 path's 16-row loads need it.
+// Every CTA computes the prefix sum itself (E <= 1024 counts, one scan); CTA 0
+// writes the tile list and sorted_ids[pos] = e * cap + i (the output row), the others copy
 // the real rows of x into position order, converted to fp16.
 #include <cuda_runtime.h>
 
@@ -36,14 +37,15 @@ __global__ void __launch_bounds__(kMaskedThreads) masked_prologue_kernel(MaskedA
     cnt[tid] = c;
   }
   int total;
-  const int o = block_exclusive_scan((c + 7) & ~7, scan_tmp, total);
+  const int o = block_exclusive_scan((c + m.block - 1) / m.block * m.block, scan_tmp, total);
   if (tid < m.E) off[tid] = o;
   if (tid == 0) off[m.E] = total;
   if (blockIdx.x == 0) {
     int ntiles;
-    const int t0 = block_exclusive_scan((c + 7) / 8, scan_tmp, ntiles);
+    const int t0 = block_exclusive_scan((c + m.tile - 1) / m.tile, scan_tmp, ntiles);
     if (tid < m.E) {
-      for (int j = 0; j * 8 < c; ++j) m.ttiles[t0 + j] = make_int4(tid, o + 8 * j, min(8, c - 8 * j), 0);
+      for (int j = 0; j * m.tile < c; ++j)
+        m.ttiles[t0 + j] = make_int4(tid, o + m.tile * j, min(m.tile, c - m.tile * j), 0);
     }
     if (tid == 0) {
       *m.num_ttiles = ntiles;

@@ -346,12 +346,13 @@ struct MaskedLayout {
 
 static MaskedLayout plan_masked(int E, int cap, int H, int I) {
   MaskedLayout L;
-  const size_t positions = static_cast<size_t>(E) * ((static_cast<size_t>(cap) + 7) / 8 * 8);
+  // positions for either path: rows padded to 16 per expert (8 suffice for the decode kernels)
+  const size_t positions = static_cast<size_t>(E) * ((static_cast<size_t>(cap) + 15) / 16 * 16);
   size_t o = 0;
   auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes, 256); return at; };
   L.status = take(kStatusBytes);
   L.sorted = take(positions * 4);
-  L.ttiles = take(static_cast<size_t>(E) * ((cap + 7) / 8) * 16);
+  L.ttiles = take(static_cast<size_t>(E) * ((cap + 7) / 8) * 16);  // decode tiles (8 rows) outnumber tcgen05 ones
   L.scalars = take(16);
   L.xq = take(positions * H * 2);
   L.h = take(positions * I * 2);
@@ -370,8 +371,12 @@ static moe_status_t masked_impl(int kind, const void* x, const int32_t* masked_m
   if (E > MOE_MAX_EXPERTS) return fail(MOE_ERR_UNSUPPORTED, "more than MOE_MAX_EXPERTS experts");
   if (H % kQBlock || I % kQBlock) return fail(MOE_ERR_UNSUPPORTED, "H and I must be multiples of 128");
   if (flags & ~MOE_PATH_MASK) return fail(MOE_ERR_INVALID_ARG, "unknown flag bits for the masked layout");
-  if ((flags & MOE_PATH_MASK) == MOE_PATH_PREFILL || (flags & MOE_PATH_MASK) == MOE_PATH_MASK)
-    return fail(MOE_ERR_UNSUPPORTED, "the masked layout runs on the weight-streaming (decode) kernels");
+  if ((flags & MOE_PATH_MASK) == MOE_PATH_MASK) return fail(MOE_ERR_INVALID_ARG, "both path flags set");
+  // The counts are on the device, so the path is the caller's choice: the weight-streaming kernels
+  // (default) suit a few rows per expert, the tcgen05 kernels (MOE_PATH_PREFILL) many.
+  const bool tc = (flags & MOE_PATH_MASK) == MOE_PATH_PREFILL;
+  if (tc && kind == MOE_WEIGHT_INT4)
+    return fail(MOE_ERR_UNSUPPORTED, "INT4 weights run on the weight-streaming (decode) kernels only");
   if (static_cast<long long>(E) * cap > (1LL << 28)) return fail(MOE_ERR_UNSUPPORTED, "problem too large");
   if (!x || !masked_m || !w13 || !s13 || !w2 || !s2 || !out) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
   if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(w13) % 16 ||
@@ -389,6 +394,8 @@ static moe_status_t masked_impl(int kind, const void* x, const int32_t* masked_m
   m.masked_m = masked_m;
   m.E = E; m.cap = cap; m.H = H;
   m.kind = kind == MOE_WEIGHT_INT4 ? 4 : 1;
+  m.block = tc ? kPrefillBlock : kDecodeBlock;
+  m.tile = tc ? kPrefillTileTokens : kDecodeBlock;
   m.xq = at<__half>(ws, L.xq);
   m.sorted_ids = at<int32_t>(ws, L.sorted);
   m.ttiles = at<int4>(ws, L.ttiles);
@@ -402,8 +409,9 @@ static moe_status_t masked_impl(int kind, const void* x, const int32_t* masked_m
 
   LayerPlan P{};
   P.M = E * cap; P.H = H; P.I = I; P.E = E; P.topk = 1;
-  P.cap = static_cast<int>(static_cast<size_t>(E) * ((cap + 7) / 8 * 8));
+  P.cap = static_cast<int>(static_cast<size_t>(E) * ((cap + 15) / 16 * 16));
   P.xq = m.xq;
+  P.act = m.xq;  // tcgen05 path: the activation rows, already in position order
   P.w13 = static_cast<const uint8_t*>(w13);
   P.s13 = s13;
   P.w2 = static_cast<const uint8_t*>(w2);
@@ -415,8 +423,8 @@ static moe_status_t masked_impl(int kind, const void* x, const int32_t* masked_m
   P.h = at<void>(ws, L.h);
   P.status = m.status;
   P.out_direct = static_cast<__nv_bfloat16*>(out);
-  err = launch_decode(P, kind, sms, stream, hook);
-  if (err != cudaSuccess) return cuda_fail(err, "masked decode launch");
+  err = tc ? launch_prefill(P, kind, sms, stream, hook) : launch_decode(P, kind, sms, stream, hook);
+  if (err != cudaSuccess) return cuda_fail(err, "masked layout launch");
   return MOE_OK;
 }
 

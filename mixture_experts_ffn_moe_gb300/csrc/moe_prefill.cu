@@ -470,6 +470,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (col >= tl.cnt) continue;  // warp-uniform
               const int pos = tl.pos0 + col;
               const int slot = __ldg(p.sorted_ids + pos);
+              if (p.out_bf16) {  // masked layout: the output row itself, unweighted
+                p.out_bf16[static_cast<size_t>(slot) * p.out_ld + n] = __float2bfloat16_rn(__uint_as_float(g[j]));
+                continue;
+              }
               float s = __ldg(p.topk_w + slot);
               if constexpr (WK == MOE_WEIGHT_INT8) s *= __ldg(p.sh + pos) * sw;
               reinterpret_cast<float*>(p.out)[static_cast<size_t>(slot) * p.out_ld + n] = __uint_as_float(g[j]) * s;
@@ -598,7 +602,7 @@ static cudaError_t launch_gemm(const PrefillArgs& a, const void* w, uint64_t w_r
 
 cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook) {
   cudaError_t err;
-  {
+  if (!P.out_direct) {  // (the masked layout's prologue already wrote the rows in position order)
     int grid = num_sms * 8;
     err = launch_kernel(gather_rows_kernel, dim3(grid), dim3(256), 0, s, true, P.xq, P.sorted_ids, P.num_post,
                         P.M * P.topk, P.topk, P.H, P.act);
@@ -649,12 +653,14 @@ cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cud
   g2.out = P.y;
   g2.out_ld = P.H;
   g2.status = P.status;
+  g2.out_bf16 = P.out_direct;
   err = weight_kind == MOE_WEIGHT_FP8
             ? launch_gemm<MOE_WEIGHT_FP8, false>(g2, P.w2, static_cast<uint64_t>(P.E) * P.H, b2, P.cap, num_sms, s)
             : launch_gemm<MOE_WEIGHT_INT8, false>(g2, P.w2, static_cast<uint64_t>(P.E) * P.H, b2, P.cap, num_sms,
                                                   s);
   if (err != cudaSuccess) return err;
   hook("prefill_gemm2", s);
+  if (P.out_direct) return cudaSuccess;  // masked layout: GEMM2 wrote the output rows
   err = launch_combine(P.y, P.inv_pos, P.M, P.topk, P.H, P.out, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("combine", s);

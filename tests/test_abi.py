@@ -169,7 +169,9 @@ def test_masked_host_checks(lib):
     assert call(cap=0) == 1
     assert call(E=5000) == 2
     assert call(H=200) == 2
-    assert call(flags=gbmoe.MOE_PATH_PREFILL) == 2
+    assert call(flags=gbmoe.MOE_PATH_PREFILL) == 3          # FP8 on the tcgen05 kernels: valid
+    assert call(kind=2, flags=gbmoe.MOE_PATH_PREFILL) == 2  # INT4 has no tcgen05 path
+    assert call(flags=3) == 1
     assert call(flags=gbmoe.MOE_ACT_FP8_1X128) == 1
     assert call(null=True) == 1
     assert call() == 3                            # valid: fails on the workspace

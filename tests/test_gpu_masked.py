@@ -50,12 +50,12 @@ def _oracle_masked(x, m, weights, kind, rows=None):
     return fn(xf, ids_t, w, *weights), mc
 
 
-def _run(x, m, weights, kind, out=None):
+def _run(x, m, weights, kind, out=None, flags=gbmoe.MOE_PATH_AUTO):
     kd = gbmoe.MOE_WEIGHT_FP8 if kind == "fp8" else gbmoe.MOE_WEIGHT_INT4
     w = [t.cuda() for t in weights]
     if out is None:
         out = torch.full(x.shape, SENTINEL, dtype=torch.bfloat16, device="cuda")
-    gbmoe.fused_moe_masked(kd, x.cuda(), m.cuda(), *w, out=out)
+    gbmoe.fused_moe_masked(kd, x.cuda(), m.cuda(), *w, out=out, flags=flags)
     torch.cuda.synchronize()
     return out.float().cpu().numpy()
 
@@ -82,6 +82,17 @@ def test_masked_layout(kind, E, cap, H, I, counts):
     x, m, weights = _masked_inputs(E, cap, H, I, kind, seed=E * cap + H, counts=counts)
     ref, mc = _oracle_masked(x, m, weights, kind)
     _check(_run(x, m, weights, kind), ref, mc, f"masked {kind} E{E} cap{cap}")
+
+
+@pytest.mark.parametrize("E,cap,H,I,counts", [
+    (4, 300, 256, 256, [300, 0, 129, 17]),        # several 128-row tiles, an empty expert, ragged tails
+    (8, 16, 256, 128, None),
+    (2, 40, 7168, 512, [40, 33]),                 # long K
+])
+def test_masked_layout_tcgen05_path(E, cap, H, I, counts):
+    x, m, weights = _masked_inputs(E, cap, H, I, "fp8", seed=E + cap + I, counts=counts)
+    ref, mc = _oracle_masked(x, m, weights, "fp8")
+    _check(_run(x, m, weights, "fp8", flags=gbmoe.MOE_PATH_PREFILL), ref, mc, f"masked tcgen05 E{E} cap{cap}")
 
 
 def test_masked_deepseek_local_experts_full_size():
