@@ -298,9 +298,12 @@ moe_status_t fused_moe_int4(const void* x_bf16, const int32_t* topk_ids, const f
  *   workspace  moe_workspace_size_masked(E, cap, H, I, weight_kind) bytes,
  *              256-byte aligned
  * H and I multiples of 128, E <= MOE_MAX_EXPERTS, cap >= 1.  The products
- * run on the weight-streaming (decode) kernels, with the arithmetic of the
- * weight kind's layer entry point.  Every kernel of the call is enqueued on
- * `stream`; flags: MOE_PATH_AUTO or MOE_PATH_DECODE only.
+ * use the arithmetic of the weight kind's layer entry point.  Since the counts
+ * are on the device the caller picks the kernels: MOE_PATH_AUTO or
+ * MOE_PATH_DECODE runs the weight-streaming kernels (best for a few rows per
+ * expert); MOE_PATH_PREFILL runs the tcgen05 kernels (FP8 only; best for many
+ * rows per expert; INT4 with it is MOE_ERR_UNSUPPORTED).  Every kernel of the
+ * call is enqueued on `stream`.
  */
 size_t moe_workspace_size_masked(int E, int cap, int H, int I, int weight_kind);
 moe_status_t fused_moe_masked(int weight_kind, const void* x_bf16, const int32_t* masked_m, const void* w13,
