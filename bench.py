@@ -63,6 +63,8 @@ def workloads():
         "qwen3_M1_int4": synth.qwen3_235b(1, weight_kind="int4"),
         "qwen3_M16_int4": synth.qwen3_235b(16, weight_kind="int4"),
         "dsr1_decode_M4_E32_int4": synth.deepseek_r1(4, E=32, weight_kind="int4"),
+        "qwen3_M4096_int4": synth.qwen3_235b(4096, weight_kind="int4"),
+        "dsr1_prefill_M2048_int4": synth.deepseek_r1(2048, routing="deepseek_zipf", weight_kind="int4"),
     }
 
 

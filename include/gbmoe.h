@@ -264,8 +264,9 @@ moe_status_t fused_moe_int8(const void* x_bf16, const int32_t* topk_ids, const f
  * other arguments as for fused_moe_fp8.  Activations enter the products at
  * their bf16 values (rounded to fp16, as on the FP8 weight-only path) and
  * each 128-deep partial sum is scaled by its row's group scale in fp32.
- * H and I must be multiples of 128.  The layer runs on the weight-streaming
- * (decode) kernels at every M; MOE_PATH_PREFILL is MOE_ERR_UNSUPPORTED and
+ * H and I must be multiples of 128.  Paths as for fused_moe_fp8 (the
+ * weight-streaming kernels up to MOE_MAX_DECODE_TOKENS tokens, the tcgen05
+ * grouped GEMMs above; MOE_PATH_DECODE is accepted at any M for INT4);
  * MOE_ACT_FP8_1X128 is MOE_ERR_INVALID_ARG.  Workspace:
  * moe_workspace_size(..., MOE_WEIGHT_INT4, flags).
  */
@@ -301,9 +302,8 @@ moe_status_t fused_moe_int4(const void* x_bf16, const int32_t* topk_ids, const f
  * use the arithmetic of the weight kind's layer entry point.  Since the counts
  * are on the device the caller picks the kernels: MOE_PATH_AUTO or
  * MOE_PATH_DECODE runs the weight-streaming kernels (best for a few rows per
- * expert); MOE_PATH_PREFILL runs the tcgen05 kernels (FP8 only; best for many
- * rows per expert; INT4 with it is MOE_ERR_UNSUPPORTED).  Every kernel of the
- * call is enqueued on `stream`.
+ * expert); MOE_PATH_PREFILL runs the tcgen05 kernels (best for many rows per
+ * expert).  Every kernel of the call is enqueued on `stream`.
  */
 size_t moe_workspace_size_masked(int E, int cap, int H, int I, int weight_kind);
 moe_status_t fused_moe_masked(int weight_kind, const void* x_bf16, const int32_t* masked_m, const void* w13,

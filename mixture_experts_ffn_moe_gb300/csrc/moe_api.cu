@@ -106,7 +106,6 @@ struct Layout {
 
 static int choose_path(int M, int kind, unsigned flags) {
   const unsigned p = flags & MOE_PATH_MASK;
-  if (kind == MOE_WEIGHT_INT4) return MOE_PATH_DECODE;  // INT4 runs on the weight-streaming kernels only
   if (p == MOE_PATH_DECODE || p == MOE_PATH_PREFILL) return static_cast<int>(p);
   if (flags & MOE_ACT_FP8_1X128) return MOE_PATH_PREFILL;  // the FP8 x FP8 products run on tcgen05 only
   return M <= MOE_MAX_DECODE_TOKENS ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
@@ -181,8 +180,6 @@ static moe_status_t check_layer_args(int kind, const void* x, const void* ids, c
   if ((flags & MOE_PATH_MASK) == MOE_PATH_MASK) return fail(MOE_ERR_INVALID_ARG, "both path flags set");
   if ((flags & MOE_ACT_FP8_1X128) && (flags & MOE_PATH_MASK) == MOE_PATH_DECODE)
     return fail(MOE_ERR_UNSUPPORTED, "MOE_ACT_FP8_1X128 runs on the tcgen05 (prefill) path only");
-  if (kind == MOE_WEIGHT_INT4 && (flags & MOE_PATH_MASK) == MOE_PATH_PREFILL)
-    return fail(MOE_ERR_UNSUPPORTED, "INT4 weights run on the weight-streaming (decode) kernels only");
   if (static_cast<long long>(M) * topk > (1LL << 30) || static_cast<long long>(M) * H > (1LL << 40))
     return fail(MOE_ERR_UNSUPPORTED, "problem too large");
   if (M == 0) return MOE_OK;
@@ -375,8 +372,6 @@ static moe_status_t masked_impl(int kind, const void* x, const int32_t* masked_m
   // The counts are on the device, so the path is the caller's choice: the weight-streaming kernels
   // (default) suit a few rows per expert, the tcgen05 kernels (MOE_PATH_PREFILL) many.
   const bool tc = (flags & MOE_PATH_MASK) == MOE_PATH_PREFILL;
-  if (tc && kind == MOE_WEIGHT_INT4)
-    return fail(MOE_ERR_UNSUPPORTED, "INT4 weights run on the weight-streaming (decode) kernels only");
   if (static_cast<long long>(E) * cap > (1LL << 28)) return fail(MOE_ERR_UNSUPPORTED, "problem too large");
   if (!x || !masked_m || !w13 || !s13 || !w2 || !s2 || !out) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
   if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(w13) % 16 ||

@@ -14,7 +14,7 @@
 //    section "MoE");
 //  * GEMM2: two consecutive 128-row blocks of W2, so every activation byte
 //    fetched feeds 256 output rows.
-// Orientation (measured per GEMM).  GEMM1, and GEMM2 with INT8 weights, put
+// Orientation (measured per GEMM).  GEMM1, and GEMM2 with INT8 or INT4 weights, put
 // the tokens on the MMA's M = 128 side and both converted weight blocks,
 // adjacent in shared memory, on its N = 256 side: one MMA per K step instead
 // of two, and an epilogue in which each thread finishes one token.  The FP8
@@ -31,6 +31,10 @@
 // lies outside the fp16 normal range), because a tensor-core accumulator
 // cannot be rescaled per K block without a second TMEM pass.  INT8 weights convert
 // exactly and the per-row x per-channel scales are applied in the epilogue.
+// INT4 weights (two per byte, one scale per row and 128 columns) arrive as
+// 32-byte rows per stage, expand to fp16 in the INT4 K order (pairs k0,k4 /
+// k1,k5 / ...; the activations and h are stored in that order too) and take
+// their row's group scale in the same fp16 multiply.
 //
 // Warp roles (15 warps, 1 CTA per SM, persistent; rings sized so that about a
 // microsecond of loads is in flight):
@@ -73,6 +77,8 @@ constexpr int CONV_THREADS = N_CONV_WARPS * 32;
 constexpr int EPI_THREADS = N_EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;    // 2 buffers x 2 accumulators x 128 columns
 constexpr int CHUNKS_PER_ACC = BM * BK / 16;  // 16-byte raw chunks per accumulator and stage
+constexpr int RAW_TILE_I4 = BM * BK / 2;      // INT4: 4 KB of codes per accumulator and stage
+constexpr int CHUNKS_PER_ACC_I4 = RAW_TILE_I4 / 16;
 
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + CONV_STAGES * 2 * A_TILE;
@@ -133,9 +139,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total_tiles = *p.num_ttiles * p.n_tiles;
   // Orientation (measured per GEMM): tokens on the MMA's M side and both weight blocks as one N = 256
-  // operand for GEMM1 and for INT8; weights on the M side (two MMAs of N = tokens) for the FP8 down
+  // operand for GEMM1 and for INT8 / INT4; weights on the M side (two MMAs of N = tokens) for the FP8 down
   // projection, whose 128-token padding of the M side cost more shared-memory bandwidth than it saved.
-  constexpr bool TOKM = GATED || WK == MOE_WEIGHT_INT8;
+  constexpr bool TOKM = GATED || WK != MOE_WEIGHT_FP8;
+  constexpr bool I4 = WK == MOE_WEIGHT_INT4;
+  constexpr int RAWB = I4 ? RAW_TILE_I4 : RAW_TILE;  // raw bytes per accumulator and stage
   const int KC = p.K / BK;
   const int second_rows = GATED ? p.up_offset : BM;  // row offset of the second accumulator's block
 
@@ -192,10 +200,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row0 = tl.e * p.rows_per_expert + tl.n0;
         for (int kc = 0; kc < KC; ++kc) {
           if (!(ok = mbar_wait(&bars->raw_empty[rs], rph ^ 1, abort, p.status, kWaitLimit))) break;
-          mbar_arrive_expect_tx(&bars->raw_full[rs], (tl.two ? 2 : 1) * RAW_TILE);
+          mbar_arrive_expect_tx(&bars->raw_full[rs], (tl.two ? 2 : 1) * RAWB);
           uint8_t* dst = sRaw + rs * 2 * RAW_TILE;
-          tma_load_2d(dst, &tmap_w, &bars->raw_full[rs], kc * BK, row0);
-          if (tl.two) tma_load_2d(dst + RAW_TILE, &tmap_w, &bars->raw_full[rs], kc * BK, row0 + second_rows);
+          const int kx = I4 ? kc * (BK / 2) : kc * BK;  // K offset in bytes of the stored rows
+          tma_load_2d(dst, &tmap_w, &bars->raw_full[rs], kx, row0);
+          if (tl.two) tma_load_2d(dst + RAW_TILE, &tmap_w, &bars->raw_full[rs], kx, row0 + second_rows);
 #pragma unroll
           for (int i = 0; i < RAW_STAGES; ++i)
             if (i == rs) last_par[i] = static_cast<int>(rph);
@@ -299,8 +308,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int rblocks = p.rows_per_expert / kQBlock;
     for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
       const Tile tl = get_tile<GATED>(p, t);
-      const int nchunks = (tl.two ? 2 : 1) * CHUNKS_PER_ACC;
+      const int nchunks = (tl.two ? 2 : 1) * (I4 ? CHUNKS_PER_ACC_I4 : CHUNKS_PER_ACC);
+      // INT4: this thread expands row ct/2 of each weight block in every stage; its group scales
+      // (one per 128 K, i.e. per two stages) are loaded one group ahead
+      const int i4row = ct >> 1;
+      const float* i4s0 = p.wscale + (static_cast<size_t>(tl.e) * p.rows_per_expert + tl.n0 + i4row) * kblocks;
+      const float* i4s1 = i4s0 + static_cast<size_t>(second_rows) * kblocks;
+      float i4cur[2] = {0.f, 0.f}, i4nxt[2] = {0.f, 0.f};
+      if constexpr (I4) {
+        i4nxt[0] = __ldg(i4s0);
+        i4nxt[1] = tl.two ? __ldg(i4s1) : 0.f;
+      }
       for (int kc = 0; kc < KC; ++kc) {
+        if constexpr (I4) {
+          if ((kc & 1) == 0) {  // a new 128-wide group: take the prefetched scales, fetch the next ones
+            i4cur[0] = i4nxt[0];
+            i4cur[1] = i4nxt[1];
+            const int g = kc / 2 + 1;
+            if (g < kblocks) {
+              i4nxt[0] = __ldg(i4s0 + g);
+              i4nxt[1] = tl.two ? __ldg(i4s1 + g) : 0.f;
+            }
+          }
+        }
         if (!(ok = mbar_wait(&bars->raw_full[rs], rph, abort, p.status, kWaitLimit))) break;
         if (!(ok = mbar_wait(&bars->conv_empty[cs], cph ^ 1, abort, p.status, kWaitLimit))) break;
         float sc[2] = {1.f, 1.f};
@@ -317,6 +347,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         const uint8_t* raw = sRaw + rs * 2 * RAW_TILE;
         uint8_t* dstA = sA + cs * 2 * A_TILE;
+        if constexpr (I4) {
+          // a 16-byte chunk holds 32 K values of one row and expands to four 16-byte fp16 chunks
+#pragma unroll
+          for (int s = 0; s < 2 * CHUNKS_PER_ACC_I4 / CONV_THREADS; ++s) {
+            const int j = ct + s * CONV_THREADS;
+            if (j < nchunks) {
+              const int acc = j / CHUNKS_PER_ACC_I4;
+              const int idx = j - acc * CHUNKS_PER_ACC_I4;
+              const int row = idx >> 1, c16 = idx & 1;  // row == i4row
+              const uint4 v = *reinterpret_cast<const uint4*>(raw + acc * RAW_TILE + row * (BK / 2) + c16 * 16);
+              uint32_t o[16];
+              s4x8_to_f16x8(v.x, o);
+              s4x8_to_f16x8(v.y, o + 4);
+              s4x8_to_f16x8(v.z, o + 8);
+              s4x8_to_f16x8(v.w, o + 12);
+              const float s2 = i4cur[acc];
+              const float m = fabsf(s2);
+              if (m >= 6.103515625e-05f && m * 8.f <= 65504.f) {
+                const __half2 sh2 = __half2half2(__float2half_rn(s2));
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  __half2 v2 = __hmul2(*reinterpret_cast<const __half2*>(&o[i]), sh2);
+                  o[i] = *reinterpret_cast<uint32_t*>(&v2);
+                }
+              } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&o[i]));
+                  o[i] = pack_half2(f.x * s2, f.y * s2);
+                }
+              }
+              uint8_t* rowp = dstA + acc * A_TILE + row * 128;
+              const int r8 = row & 7;
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<uint4*>(rowp + (((4 * c16 + i) ^ r8) << 4)) =
+                    make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            }
+          }
+        } else {
 #pragma unroll
         for (int s = 0; s < 2 * CHUNKS_PER_ACC / CONV_THREADS; ++s) {
           const int j = ct + s * CONV_THREADS;  // 16-byte chunk of the raw stage
@@ -355,6 +425,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             *reinterpret_cast<uint4*>(rowp + (((2 * c16 + 1) ^ r8) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
           }
         }
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -390,12 +461,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld32(lane_addr + BM + c0, u);
           tmem_ld_wait();
           const int n = tl.n0 + c0;
-          if constexpr (WK == MOE_WEIGHT_FP8) {
+          if constexpr (WK == MOE_WEIGHT_FP8 || I4) {
             uint32_t hw[16];
+            if constexpr (I4) {  // h feeds GEMM2's activations: INT4 K order within each 8 columns
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int a = 8 * (j >> 2) + (j & 3), b = a + 4;
+                hw[j] = pack_half2(silu_f32(__uint_as_float(g[a])) * __uint_as_float(u[a]),
+                                   silu_f32(__uint_as_float(g[b])) * __uint_as_float(u[b]));
+              }
+            } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
               hw[j] = pack_half2(silu_f32(g0) * __uint_as_float(u[2 * j]), silu_f32(g1) * __uint_as_float(u[2 * j + 1]));
+            }
             }
             if (live) {
               uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(p.out) + static_cast<size_t>(pos) * p.out_ld + n);
@@ -428,7 +508,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float wgt = 0.f;
         if (live) {
           slot = __ldg(p.sorted_ids + pos);
-          wgt = __ldg(p.topk_w + slot);
+          wgt = p.out_bf16 ? 1.f : __ldg(p.topk_w + slot);  // masked layout: unweighted bf16 rows
           if constexpr (WK == MOE_WEIGHT_INT8) wgt *= __ldg(p.sh + pos);
         }
 #pragma unroll 1
@@ -438,6 +518,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld_wait();
           const int n = tl.n0 + c0;
           float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + static_cast<size_t>(slot) * p.out_ld + n);
+          uint2* dstb = reinterpret_cast<uint2*>(p.out_bf16 + static_cast<size_t>(slot) * p.out_ld + n);
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
             float4 sc = make_float4(wgt, wgt, wgt, wgt);
@@ -445,38 +526,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const float4 cs = __ldg(reinterpret_cast<const float4*>(chs + n) + v);
               sc = make_float4(wgt * cs.x, wgt * cs.y, wgt * cs.z, wgt * cs.w);
             }
-            if (live)
-              dst[v] = make_float4(__uint_as_float(g[4 * v]) * sc.x, __uint_as_float(g[4 * v + 1]) * sc.y,
-                                   __uint_as_float(g[4 * v + 2]) * sc.z, __uint_as_float(g[4 * v + 3]) * sc.w);
+            const float4 r = make_float4(__uint_as_float(g[4 * v]) * sc.x, __uint_as_float(g[4 * v + 1]) * sc.y,
+                                         __uint_as_float(g[4 * v + 2]) * sc.z, __uint_as_float(g[4 * v + 3]) * sc.w);
+            if (live && p.out_bf16) {
+              const __nv_bfloat162 lo = __floats2bfloat162_rn(r.x, r.y), hi = __floats2bfloat162_rn(r.z, r.w);
+              dstb[v] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+            } else if (live) {
+              dst[v] = r;
+            }
           }
         }
       } else {
         // weights on the M side: TMEM lane = output row, columns = tokens
         const int row = tok;
+        if (p.out_bf16) {
+          // masked layout: the output rows themselves, unweighted
 #pragma unroll 1
-        for (int a = 0; a < 2; ++a) {
-          if (a == 1 && !tl.two) break;
-          const int n = tl.n0 + a * BM + row;
-          float sw = 1.f;
-          if constexpr (WK == MOE_WEIGHT_INT8) sw = __ldg(p.wscale + static_cast<size_t>(tl.e) * p.rows_per_expert + n);
-          for (int c0 = 0; c0 < tl.nmma; c0 += 32) {
-            uint32_t g[32];
-            __syncwarp();
-            tmem_ld32(lane_addr + a * BM + c0, g);
-            tmem_ld_wait();
+          for (int a = 0; a < 2; ++a) {
+            if (a == 1 && !tl.two) break;
+            const int n = tl.n0 + a * BM + row;
+            for (int c0 = 0; c0 < tl.nmma; c0 += 32) {
+              uint32_t g[32];
+              __syncwarp();
+              tmem_ld32(lane_addr + a * BM + c0, g);
+              tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int col = c0 + j;
-              if (col >= tl.cnt) continue;  // warp-uniform
-              const int pos = tl.pos0 + col;
-              const int slot = __ldg(p.sorted_ids + pos);
-              if (p.out_bf16) {  // masked layout: the output row itself, unweighted
+              for (int j = 0; j < 32; ++j) {
+                const int col = c0 + j;
+                if (col >= tl.cnt) continue;  // warp-uniform
+                const int slot = __ldg(p.sorted_ids + tl.pos0 + col);
                 p.out_bf16[static_cast<size_t>(slot) * p.out_ld + n] = __float2bfloat16_rn(__uint_as_float(g[j]));
-                continue;
               }
-              float s = __ldg(p.topk_w + slot);
-              if constexpr (WK == MOE_WEIGHT_INT8) s *= __ldg(p.sh + pos) * sw;
-              reinterpret_cast<float*>(p.out)[static_cast<size_t>(slot) * p.out_ld + n] = __uint_as_float(g[j]) * s;
+            }
+          }
+        } else {
+#pragma unroll 1
+          for (int a = 0; a < 2; ++a) {
+            if (a == 1 && !tl.two) break;
+            const int n = tl.n0 + a * BM + row;
+            float sw = 1.f;
+            if constexpr (WK == MOE_WEIGHT_INT8) sw = __ldg(p.wscale + static_cast<size_t>(tl.e) * p.rows_per_expert + n);
+            for (int c0 = 0; c0 < tl.nmma; c0 += 32) {
+              uint32_t g[32];
+              __syncwarp();
+              tmem_ld32(lane_addr + a * BM + c0, g);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const int col = c0 + j;
+                if (col >= tl.cnt) continue;  // warp-uniform
+                const int pos = tl.pos0 + col;
+                const int slot = __ldg(p.sorted_ids + pos);
+                float s = __ldg(p.topk_w + slot);
+                if constexpr (WK == MOE_WEIGHT_INT8) s *= __ldg(p.sh + pos) * sw;
+                reinterpret_cast<float*>(p.out)[static_cast<size_t>(slot) * p.out_ld + n] = __uint_as_float(g[j]) * s;
+              }
             }
           }
         }
@@ -588,8 +692,9 @@ template <int WK, bool GATED>
 static cudaError_t launch_gemm(const PrefillArgs& a, const void* w, uint64_t w_rows, const void* b, uint64_t b_rows,
                                int num_sms, cudaStream_t s) {
   CUtensorMap mw, mb;
-  if (!encode_tmap_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, static_cast<uint64_t>(a.K), w_rows, pf::BK, pf::BM,
-                CU_TENSOR_MAP_SWIZZLE_NONE))
+  constexpr bool I4 = WK == MOE_WEIGHT_INT4;  // rows of K/2 bytes, 32 of them per stage
+  if (!encode_tmap_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, static_cast<uint64_t>(I4 ? a.K / 2 : a.K), w_rows,
+                      I4 ? pf::BK / 2 : pf::BK, pf::BM, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, b, static_cast<uint64_t>(a.K), b_rows, pf::BK, 16,
                 CU_TENSOR_MAP_SWIZZLE_128B))
@@ -624,11 +729,11 @@ cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cud
   g1.out_ld = P.I;
   g1.hmax = P.hmax;
   g1.status = P.status;
-  err = weight_kind == MOE_WEIGHT_FP8
-            ? launch_gemm<MOE_WEIGHT_FP8, true>(g1, P.w13, static_cast<uint64_t>(P.E) * 2 * P.I, P.act, P.cap,
-                                                num_sms, s)
-            : launch_gemm<MOE_WEIGHT_INT8, true>(g1, P.w13, static_cast<uint64_t>(P.E) * 2 * P.I, P.act, P.cap,
-                                                 num_sms, s);
+  const uint64_t rows1 = static_cast<uint64_t>(P.E) * 2 * P.I;
+  err = weight_kind == MOE_WEIGHT_FP8 ? launch_gemm<MOE_WEIGHT_FP8, true>(g1, P.w13, rows1, P.act, P.cap, num_sms, s)
+        : weight_kind == MOE_WEIGHT_INT4
+            ? launch_gemm<MOE_WEIGHT_INT4, true>(g1, P.w13, rows1, P.act, P.cap, num_sms, s)
+            : launch_gemm<MOE_WEIGHT_INT8, true>(g1, P.w13, rows1, P.act, P.cap, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("prefill_gemm1", s);
   const __half* b2 = reinterpret_cast<const __half*>(P.h);
@@ -654,10 +759,11 @@ cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cud
   g2.out_ld = P.H;
   g2.status = P.status;
   g2.out_bf16 = P.out_direct;
-  err = weight_kind == MOE_WEIGHT_FP8
-            ? launch_gemm<MOE_WEIGHT_FP8, false>(g2, P.w2, static_cast<uint64_t>(P.E) * P.H, b2, P.cap, num_sms, s)
-            : launch_gemm<MOE_WEIGHT_INT8, false>(g2, P.w2, static_cast<uint64_t>(P.E) * P.H, b2, P.cap, num_sms,
-                                                  s);
+  const uint64_t rows2 = static_cast<uint64_t>(P.E) * P.H;
+  err = weight_kind == MOE_WEIGHT_FP8 ? launch_gemm<MOE_WEIGHT_FP8, false>(g2, P.w2, rows2, b2, P.cap, num_sms, s)
+        : weight_kind == MOE_WEIGHT_INT4
+            ? launch_gemm<MOE_WEIGHT_INT4, false>(g2, P.w2, rows2, b2, P.cap, num_sms, s)
+            : launch_gemm<MOE_WEIGHT_INT8, false>(g2, P.w2, rows2, b2, P.cap, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("prefill_gemm2", s);
   if (P.out_direct) return cudaSuccess;  // masked layout: GEMM2 wrote the output rows

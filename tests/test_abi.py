@@ -147,7 +147,7 @@ def test_int4_host_checks(lib):
     def call(M=4, H=256, I=128, flags=0):
         return lib.fused_moe_int4(p, p, p, p, p, p, p, M, H, I, 8, 2, flags, p, p, 0, None)
 
-    assert call(flags=gbmoe.MOE_PATH_PREFILL) == 2          # INT4 runs on the weight-streaming kernels
+    assert call(flags=gbmoe.MOE_PATH_PREFILL) == 3          # INT4 on the tcgen05 kernels: valid
     assert call(flags=gbmoe.MOE_ACT_FP8_1X128) == 1         # FP8 layer only
     assert call(H=200) == 2
     assert call() == 3                                      # valid: fails on the workspace
@@ -170,7 +170,7 @@ def test_masked_host_checks(lib):
     assert call(E=5000) == 2
     assert call(H=200) == 2
     assert call(flags=gbmoe.MOE_PATH_PREFILL) == 3          # FP8 on the tcgen05 kernels: valid
-    assert call(kind=2, flags=gbmoe.MOE_PATH_PREFILL) == 2  # INT4 has no tcgen05 path
+    assert call(kind=2, flags=gbmoe.MOE_PATH_PREFILL) == 3
     assert call(flags=3) == 1
     assert call(flags=gbmoe.MOE_ACT_FP8_1X128) == 1
     assert call(null=True) == 1

@@ -44,6 +44,23 @@ def test_int4_shapes(M, H, I, E, k):
     assert_layer_close(_run(d), oracle.fused_moe_int4(**d), f"INT4 {M}x{H}x{I} E{E} k{k}")
 
 
+@pytest.mark.parametrize("M,H,I,E,k", [
+    (300, 256, 256, 8, 2),     # ~75 slots per expert: partial token tiles
+    (600, 512, 384, 4, 2),     # several token tiles per expert, three GEMM1 row blocks
+    (129, 640, 1024, 33, 5),   # ragged: many experts with few slots
+    (4, 7168, 256, 16, 3),     # long K, tiny M on the tcgen05 path
+])
+def test_int4_tcgen05_path(M, H, I, E, k):
+    shape = synth.LayerShape("i4", M, H, I, E, k, "int4", "softmax")
+    d = synth.make_layer(shape, seed=M + H + I + 7)
+    assert_layer_close(_run(d, flags=gbmoe.MOE_PATH_PREFILL), oracle.fused_moe_int4(**d),
+                       f"INT4 tcgen05 {M}x{H}x{I} E{E} k{k}")
+
+
+def test_int4_qwen3_shape_prefill_4096():
+    _full_size(synth.qwen3_235b(4096, weight_kind="int4"), seed=23, rows=[0, 2047, 4095])
+
+
 def test_int4_every_code_and_extreme_group_scales():
     # random bytes use all 16 codes (-8 included); scales span 2^-20 .. 2^4 across groups
     shape = synth.LayerShape("i4", 24, 512, 256, 4, 2, "int4", "uniform")
@@ -54,7 +71,9 @@ def test_int4_every_code_and_extreme_group_scales():
         d[sk] = (torch.exp2(torch.randint(-20, 5, tuple(d[sk].shape), generator=g).float()) * 0.01).contiguous()
     q = oracle.unpack_int4(d["w13"][0].numpy())
     assert q.min() == -8 and q.max() == 7
-    assert_layer_close(_run(d), oracle.fused_moe_int4(**d), "INT4 all codes")
+    ref = oracle.fused_moe_int4(**d)
+    assert_layer_close(_run(d), ref, "INT4 all codes")
+    assert_layer_close(_run(d, flags=gbmoe.MOE_PATH_PREFILL), ref, "INT4 all codes, tcgen05 path")
 
 
 def test_int4_expert_id_closed_form():
@@ -82,9 +101,6 @@ def test_int4_flags_and_status():
     shape = synth.LayerShape("i4", 8, 256, 128, 8, 2, "int4", "softmax")
     d = synth.make_layer(shape, seed=5)
     ws = gbmoe.alloc_workspace(8, 256, 128, 8, 2, gbmoe.MOE_WEIGHT_INT4)
-    with pytest.raises(gbmoe.MoEError) as e:
-        _run(d, flags=gbmoe.MOE_PATH_PREFILL, ws=ws)
-    assert e.value.status == 2
     with pytest.raises(gbmoe.MoEError) as e:
         _run(d, flags=gbmoe.MOE_ACT_FP8_1X128, ws=ws)
     assert e.value.status == 1

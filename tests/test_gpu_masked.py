@@ -89,10 +89,11 @@ def test_masked_layout(kind, E, cap, H, I, counts):
     (8, 16, 256, 128, None),
     (2, 40, 7168, 512, [40, 33]),                 # long K
 ])
-def test_masked_layout_tcgen05_path(E, cap, H, I, counts):
-    x, m, weights = _masked_inputs(E, cap, H, I, "fp8", seed=E + cap + I, counts=counts)
-    ref, mc = _oracle_masked(x, m, weights, "fp8")
-    _check(_run(x, m, weights, "fp8", flags=gbmoe.MOE_PATH_PREFILL), ref, mc, f"masked tcgen05 E{E} cap{cap}")
+@pytest.mark.parametrize("kind", ["fp8", "int4"])
+def test_masked_layout_tcgen05_path(kind, E, cap, H, I, counts):
+    x, m, weights = _masked_inputs(E, cap, H, I, kind, seed=E + cap + I, counts=counts)
+    ref, mc = _oracle_masked(x, m, weights, kind)
+    _check(_run(x, m, weights, kind, flags=gbmoe.MOE_PATH_PREFILL), ref, mc, f"masked {kind} tcgen05 E{E} cap{cap}")
 
 
 def test_masked_deepseek_local_experts_full_size():
