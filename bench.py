@@ -514,7 +514,11 @@ def run_ours(args, shape):
         "clocks": clocks.summary(),
         "layer": {"weight_gbs": layer_bytes / (ms_per_step * 1e-3) / 1e9,
                   "weight_bytes": layer_bytes, "hbm_frac": layer_bytes / (ms_per_step * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                  "tflops": flops / (ms_per_step * 1e-3) / 1e12, "active_experts":
+                  "tflops": flops / (ms_per_step * 1e-3) / 1e12,
+                  # context: the layer's rate against the dense bf16 peak and the FP8 peak (2x bf16, nominal ratio)
+                  "tflops_frac_bf16": flops / (ms_per_step * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                  "tflops_frac_fp8": flops / (ms_per_step * 1e-3) / 1e12 / (2.0 * peaks["bf16_tflops"]),
+                  "active_experts":
                   int((synth.expert_histogram(shape, ids) > 0).sum()),
                   "stages_ms": {n: round(v, 5) for n, v in stage_avg.items()},
                   "ms_per_step_with_kernel_events": prof_ms / args.steps},
