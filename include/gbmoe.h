@@ -377,6 +377,21 @@ moe_status_t fused_moe_fp8_static_scratch(const void* x_bf16, const int32_t* top
 moe_status_t moe_read_status(const void* workspace, int32_t status_out[2], moe_stream_t stream);
 
 /*
+ * Self-test of the failure path of the bounded device waits.  Launches one
+ * small kernel whose waits can never complete: one gives up after
+ * limit_cycles SM clocks (1000 <= limit_cycles <= 2^31, about a second at
+ * most), sets bit 0 of the workspace's status words and the shared abort
+ * flag; the other leaves through that flag, as every role of a GEMM kernel
+ * does when one of them times out.  *gave_up (device int32) receives the
+ * number of waits that gave up (2).  moe_read_status(workspace) then returns
+ * MOE_ERR_TIMEOUT.  Only the status words (the first 8 bytes of any
+ * workspace, at least 256 bytes, 256-byte aligned) and *gave_up are written;
+ * nothing faults and the context stays usable.
+ */
+moe_status_t moe_selftest_wait_timeout(void* workspace, long long limit_cycles, int32_t* gave_up,
+                                       moe_stream_t stream);
+
+/*
  * Per-kernel timing of fused calls on the calling host thread (a profiling
  * aid; it changes nothing the layer computes).
  *

@@ -159,6 +159,7 @@ struct MaskedArgs {
   DeviceStatus* status;
 };
 cudaError_t launch_masked_prologue(const MaskedArgs& m, int num_sms, cudaStream_t s);
+cudaError_t launch_wait_timeout(DeviceStatus* status, long long limit, int32_t* gave_up, cudaStream_t s);
 cudaError_t launch_quant_rows(const PrepArgs& p, cudaStream_t s);
 cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook);
 cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook);

@@ -570,6 +570,19 @@ moe_status_t fused_moe_masked(int weight_kind, const void* x_bf16, const int32_t
                      workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+moe_status_t moe_selftest_wait_timeout(void* workspace, long long limit_cycles, int32_t* gave_up,
+                                       moe_stream_t stream) {
+  g_last_error.clear();
+  if (!workspace || !gave_up) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256) return fail(MOE_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (limit_cycles < 1000 || limit_cycles > (1LL << 31))
+    return fail(MOE_ERR_INVALID_ARG, "limit_cycles must lie in [1000, 2^31]");
+  cudaError_t err = launch_wait_timeout(static_cast<DeviceStatus*>(workspace), limit_cycles, gave_up,
+                                        reinterpret_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_fail(err, "moe_selftest_wait_timeout launch");
+  return MOE_OK;
+}
+
 moe_status_t moe_read_status(const void* workspace, int32_t status_out[2], moe_stream_t stream) {
   g_last_error.clear();
   if (!workspace || !status_out) return fail(MOE_ERR_INVALID_ARG, "NULL pointer");

@@ -63,6 +63,7 @@ _SIGS = {
     "fused_moe_masked": (_i, [_i] + [_vp] * 6 + [_i] * 4 + [_u, _vp, _vp, _sz, _vp]),
     "fused_moe_fp8_static_scratch": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp]),
     "moe_read_status": (_i, [_vp, _vp, _vp]),
+    "moe_selftest_wait_timeout": (_i, [_vp, ctypes.c_longlong, _vp, _vp]),
     "moe_profile_enable": (_i, [_i]),
     "moe_profile_read": (_i, [_vp, _vp, _i, _vp, _vp]),
     "moe_status_string": (ctypes.c_char_p, [_i]),
@@ -366,6 +367,14 @@ def moe_read_status(workspace: torch.Tensor):
     buf = (ctypes.c_int32 * 2)()
     st = load().moe_read_status(_ptr(workspace), ctypes.cast(buf, ctypes.c_void_p), _stream(workspace))
     return int(buf[0]), int(buf[1]), int(st)
+
+
+def moe_selftest_wait_timeout(workspace: torch.Tensor, limit_cycles: int = 2_000_000) -> torch.Tensor:
+    """Runs the bounded-wait failure self-test on `workspace`; returns the device count of waits that gave up."""
+    gave_up = torch.zeros(1, dtype=torch.int32, device=workspace.device)
+    st = load().moe_selftest_wait_timeout(_ptr(workspace), limit_cycles, _ptr(gave_up), _stream(workspace))
+    _check(st, "moe_selftest_wait_timeout")
+    return gave_up
 
 
 def moe_profile_enable(max_calls: int) -> None:

@@ -179,3 +179,11 @@ def test_masked_host_checks(lib):
     a = gbmoe.moe_workspace_size_masked(32, 128, 7168, 2048, gbmoe.MOE_WEIGHT_FP8)
     assert a > 32 * 128 * (7168 + 2048) * 2
     assert gbmoe.moe_workspace_size_masked(32, 128, 7168, 2048, gbmoe.MOE_WEIGHT_INT8) == 0
+
+
+def test_selftest_host_checks(lib):
+    p = ctypes.c_void_p(256)
+    assert lib.moe_selftest_wait_timeout(None, 10000, p, None) == 1
+    assert lib.moe_selftest_wait_timeout(p, 10, p, None) == 1          # limit below 1000 cycles
+    assert lib.moe_selftest_wait_timeout(p, 1 << 40, p, None) == 1     # above 2^31
+    assert lib.moe_selftest_wait_timeout(ctypes.c_void_p(16), 10000, p, None) == 3  # misaligned workspace
