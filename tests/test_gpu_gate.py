@@ -79,6 +79,9 @@ def test_softmax_gate(M, E, k, shared, kind, unaligned):
     (300, 256, 8, 8, 8, "normal"),    # every group kept
     (300, 256, 8, 1, 1, "normal"),    # no grouping
     (100, 32, 4, 32, 4, "normal"),    # groups of one expert
+    (100, 512, 8, 16, 4, "normal"),   # 16 experts per lane, 2 lanes per group
+    (100, 1024, 8, 32, 4, "normal"),  # the largest router: 32 experts per lane, a lane per group
+    (100, 1024, 16, 8, 3, "normal"),  # 4 lanes per group of 128
 ])
 def test_grouped_sigmoid_gate(M, E, k, n_group, topk_group, kind):
     lg = _logits(M, E, seed=3 * M + E + n_group, kind=kind)
