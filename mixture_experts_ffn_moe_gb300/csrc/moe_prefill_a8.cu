@@ -26,7 +26,7 @@
 // overlap the promotion of the previous one.
 //
 // Warp roles (12 warps = 3 warpgroups, 1 CTA per SM, persistent):
-//   warp 0      TMA producer of weight tiles (2 x 16 KB per K block, ring of 4)
+//   warp 0      TMA producer of weight tiles (2 x 16 KB per K block, ring of 4 in GEMM1, 3 in GEMM2)
 //   warp 1      TMEM allocator + tcgen05.mma issuer
 //   warp 2      TMA producer of activation tiles (16 KB) and activation scale vectors (ring of 8)
 //   warp 3      scale warp: per K block, the factor vectors a_scale x w_scale of both accumulators
@@ -34,7 +34,8 @@
 //               promotion, then the epilogue of the tile:
 //                 GEMM1: h = SiLU(gate) * up, quantised to E4M3 per 1 x 128 group (the tile's
 //                        128 rows are one group of I) -> h codes [cap, I] and scales [I/128, cap]
-//                 GEMM2: y[slot] = acc * routing weight
+//                 GEMM2: y[slot] = acc * routing weight, staged through shared memory so that
+//                        every store instruction writes whole 128-byte row segments
 // Every wait is bounded; a time-out sets the status flag and every role drains.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -51,10 +52,8 @@ using namespace sm100;
 constexpr int BK = 128;                  // K per stage: one 128-deep scale block (bytes of E4M3)
 constexpr int BM = 128;                  // weight rows per accumulator (MMA N)
 constexpr int MAXN = kPrefillTileTokens; // tokens per tile (MMA M = 128)
-constexpr int W_STAGES = 4;
-constexpr int A_STAGES = 4;  // the weight and activation rings advance together (one K block per stage)
-static_assert(W_STAGES == A_STAGES, "one stage-empty barrier serves both rings");
-constexpr int S_STAGES = 8;              // deeper than A_STAGES + the 2 TMEM buffers the MMA may lead by
+constexpr int MAX_STAGES = 4;            // K-block stages of the weight and activation rings (they advance together)
+constexpr int S_STAGES = 8;              // deeper than the stages + the 2 TMEM buffers the MMA may lead by
 constexpr int W_TILE = BM * BK;          // 16 KB per accumulator
 constexpr int A_TILE = MAXN * BK;        // 16 KB
 constexpr int S_SLOT = 3 * MAXN * 4;     // activation scales, factors of accumulator 0, factors of accumulator 1
@@ -68,19 +67,31 @@ constexpr int REGS_ACC = 224;            // warpgroups 1 and 2
 static_assert(128 * REGS_SUPPORT + 256 * REGS_ACC <= NUM_THREADS * REGS_AT_LAUNCH, "register split exceeds the pool");
 constexpr uint32_t TMEM_COLS = 512;      // 2 buffers x 2 accumulators x 128 columns
 
-constexpr int OFF_W = 0;
-constexpr int OFF_A = OFF_W + W_STAGES * 2 * W_TILE;
-constexpr int OFF_S = OFF_A + A_STAGES * A_TILE;
-constexpr int OFF_RED = OFF_S + S_STAGES * S_SLOT;
 constexpr int RED_BYTES = 2 * 2 * MAXN * 4;  // [tile parity][column half][token] floats
-constexpr int OFF_BAR = OFF_RED + RED_BYTES;
-constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;  // + slack to align the base to 1024
+
+// Shared-memory layout per GEMM (measured): GEMM1 keeps 4 K-block stages; GEMM2, whose short
+// K loop (I = 2048) makes its y stores a large share of the tile, trades one stage for a
+// 4 KB y staging buffer per accumulator warp (32 columns, 128-byte row segments).
+template <bool GATED>
+struct Lay {
+  static constexpr int STAGES = GATED ? 4 : 3;
+  static constexpr int Y_COLS = 32;                            // GEMM2: columns of y a warp stages at a time
+  static constexpr int STG_BYTES = GATED ? 0 : 32 * Y_COLS * 4;  // per accumulator warp: 32 tokens x Y_COLS fp32
+  static constexpr int OFF_W = 0;
+  static constexpr int OFF_A = OFF_W + STAGES * 2 * W_TILE;
+  static constexpr int OFF_S = OFF_A + STAGES * A_TILE;
+  static constexpr int OFF_RED = OFF_S + S_STAGES * S_SLOT;
+  static constexpr int OFF_STG = OFF_RED + RED_BYTES;
+  static constexpr int OFF_BAR = OFF_STG + N_ACC_WARPS * STG_BYTES;
+  static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;  // + slack to align the base to 1024
+  static_assert(STAGES <= MAX_STAGES && SMEM_BYTES <= 232448, "shared memory per CTA");
+};
 constexpr long long kWaitLimit = 4000000000LL;    // ~2 s of SM clocks per wait
 
 struct Bars {
-  uint64_t w_full[W_STAGES];
-  uint64_t a_full[A_STAGES];
-  uint64_t st_empty[W_STAGES];  // the MMAs of a K block have read its weight and activation stages
+  uint64_t w_full[MAX_STAGES];
+  uint64_t a_full[MAX_STAGES];
+  uint64_t st_empty[MAX_STAGES];  // the MMAs of a K block have read its weight and activation stages
   uint64_t s_full[S_STAGES];   // activation scale vector landed (TMA)
   uint64_t f_full[S_STAGES];   // factor vectors written (scale warp)
   uint64_t s_empty[S_STAGES];  // factor vectors consumed (accumulator warps)
@@ -150,11 +161,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                       const __grid_constant__ CUtensorMap tmap_s, Args p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sW = smem + OFF_W;
-  uint8_t* sA = smem + OFF_A;
-  float* sS = reinterpret_cast<float*>(smem + OFF_S);
-  float* red = reinterpret_cast<float*>(smem + OFF_RED);
-  Bars* bars = reinterpret_cast<Bars*>(smem + OFF_BAR);
+  using L = Lay<GATED>;
+  constexpr int W_STAGES = L::STAGES, A_STAGES = L::STAGES;
+  uint8_t* sW = smem + L::OFF_W;
+  uint8_t* sA = smem + L::OFF_A;
+  float* sS = reinterpret_cast<float*>(smem + L::OFF_S);
+  float* red = reinterpret_cast<float*>(smem + L::OFF_RED);
+  Bars* bars = reinterpret_cast<Bars*>(smem + L::OFF_BAR);
   volatile int* abort = &bars->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -353,8 +366,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (live) slot = __ldg(p.sorted_ids + tl.pos0 + tok);
       }
       for (int kc = 0; kc < KC; ++kc) {
-        if (!(ok = mbar_wait(&bars->f_full[ss], fph, abort, p.status, kWaitLimit))) break;
-        if (!(ok = mbar_wait(&bars->p_full[buf], pph[buf], abort, p.status, kWaitLimit))) break;
+        // a lane that gives up takes its whole warp with it (the warp meets at __syncwarp below)
+        ok = mbar_wait(&bars->f_full[ss], fph, abort, p.status, kWaitLimit) &&
+             mbar_wait(&bars->p_full[buf], pph[buf], abort, p.status, kWaitLimit);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
         tc_fence_after();
         if (quarter_live) {
           const float* fs = sS + ss * (S_SLOT / 4);
@@ -409,9 +424,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int rb = ntile & 1;
         red[(rb * 2 + ch) * MAXN + tok] = m;
         mbar_arrive(&bars->red_full[rb][q]);
-        if (!(ok = mbar_wait(&bars->red_full[rb][q], static_cast<uint32_t>((ntile >> 1) & 1), abort, p.status,
-                             kWaitLimit)))
-          break;
+        ok = mbar_wait(&bars->red_full[rb][q], static_cast<uint32_t>((ntile >> 1) & 1), abort, p.status, kWaitLimit);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
         const float amax = fmaxf(m, red[(rb * 2 + (ch ^ 1)) * MAXN + tok]);
         if (live) {
           // s = amax / 448 and codes of h / s, by reciprocals (h codes are covered by the layer tolerance)
@@ -436,17 +450,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (ch == 0) p.hs[static_cast<size_t>(tl.n0 / kQBlock) * p.cap + pos] = s;
         }
       } else {
-        if (live) {
-          float4* yr = reinterpret_cast<float4*>(p.y + static_cast<size_t>(slot) * p.n_rows_out + tl.n0 + ch * 64);
+        // y[slot] = acc x routing weight.  A thread holds one token's row, so direct stores would
+        // put 32 rows in every warp instruction; instead the warp stages Y_COLS columns of its 32
+        // rows in shared memory and writes them back row by row: Y_COLS * 4 contiguous bytes per
+        // row, 32 / CPR rows per instruction.  The 16-byte chunk j of row r sits at chunk
+        // j ^ swz(r), which keeps both the row-wise writes and the column-wise reads free of bank
+        // conflicts (8 lanes, one 128-byte phase, always touch 8 different chunk columns).
+        constexpr int Y_COLS = L::Y_COLS;
+        constexpr int CPR = Y_COLS / 4;  // 16-byte chunks per staged row
+        static_assert(CPR == 4 || CPR == 8, "staging swizzle");
+        auto swz = [](int r) { return CPR == 8 ? (r & 7) : ((r >> 1) & 3); };
+        float4* stg = reinterpret_cast<float4*>(smem + L::OFF_STG + (warp - WARP_ACC0) * L::STG_BYTES);
+        const int rr = lane / CPR, cj = lane % CPR;  // read-back: rows rr + (32 / CPR) i, chunk cj
 #pragma unroll
-          for (int v = 0; v < 16; ++v)
-            yr[v] = make_float4(acc0[2 * v].x * wgt, acc0[2 * v].y * wgt, acc0[2 * v + 1].x * wgt,
-                                acc0[2 * v + 1].y * wgt);
-          if (tl.two) {
+        for (int b = 0; b < 2; ++b) {
+          if (!quarter_live || (b == 1 && !tl.two)) break;
+          const float2* a = b ? acc1 : acc0;
 #pragma unroll
-            for (int v = 0; v < 16; ++v)
-              yr[BM / 4 + v] = make_float4(acc1[2 * v].x * wgt, acc1[2 * v].y * wgt, acc1[2 * v + 1].x * wgt,
-                                           acc1[2 * v + 1].y * wgt);
+          for (int cc = 0; cc < 64 / Y_COLS; ++cc) {
+#pragma unroll
+            for (int j = 0; j < CPR; ++j) {
+              const float2 u = a[(cc * Y_COLS + 4 * j) / 2], v = a[(cc * Y_COLS + 4 * j) / 2 + 1];
+              stg[lane * CPR + (j ^ swz(lane))] = make_float4(u.x * wgt, u.y * wgt, v.x * wgt, v.y * wgt);
+            }
+            __syncwarp();
+            const int col = tl.n0 + b * BM + ch * 64 + cc * Y_COLS + cj * 4;
+#pragma unroll
+            for (int i = 0; i < CPR; ++i) {
+              const int r = rr + (32 / CPR) * i;
+              const int rslot = __shfl_sync(0xffffffffu, slot, r);
+              const float4 val = stg[r * CPR + (cj ^ swz(r))];
+              if (q * 32 + r < tl.cnt)
+                *reinterpret_cast<float4*>(p.y + static_cast<size_t>(rslot) * p.n_rows_out + col) = val;
+            }
+            __syncwarp();
           }
         }
       }
@@ -519,6 +556,7 @@ static cudaError_t launch_a8_gemm(const pfa8::Args& a, const void* w, uint64_t w
   if (!encode_tmap_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, bs, static_cast<uint64_t>(a.cap),
                       static_cast<uint64_t>(a.K / kQBlock), MAXN, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
+  constexpr int SMEM_BYTES = Lay<GATED>::SMEM_BYTES;
   err = set_smem_limit_once(reinterpret_cast<const void*>(kern), SMEM_BYTES);
   if (err != cudaSuccess) return err;
   return launch_kernel(kern, dim3(num_sms), dim3(NUM_THREADS), SMEM_BYTES, s, true, mw, mb, ms, a);
