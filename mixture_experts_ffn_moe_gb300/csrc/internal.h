@@ -166,6 +166,9 @@ cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cud
 cudaError_t launch_prefill_a8(const LayerPlan& P, int num_sms, cudaStream_t s, const StageHook& hook);
 cudaError_t launch_combine(const float* y, const int32_t* inv_pos, int M, int topk, int H, __nv_bfloat16* out,
                            int num_sms, cudaStream_t s);
+// y in bf16 (the FP8-activation path)
+cudaError_t launch_combine(const __nv_bfloat16* y, const int32_t* inv_pos, int M, int topk, int H,
+                           __nv_bfloat16* out, int num_sms, cudaStream_t s);
 // 2D row-major tensor [outer, inner] of `esize`-byte elements, TMA box [box_outer, box_inner].
 bool encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner,
                     uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);

@@ -657,6 +657,48 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   }
 }
 
+// The same sum over bf16 y rows (the FP8-activation path), eight columns per thread.
+__global__ void __launch_bounds__(256) combine_bf16_kernel(const __nv_bfloat16* __restrict__ y,
+                                                           const int32_t* __restrict__ inv_pos, int M, int topk, int H,
+                                                           __nv_bfloat16* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
+  const int q = H / 8;
+  const long long total = static_cast<long long>(M) * q;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(i / q), c = static_cast<int>(i - static_cast<long long>(t) * q);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int k0 = 0; k0 < topk; k0 += 8) {
+      uint4 v[8];  // all loads of a group in flight together, then summed in slot order
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int k = k0 + j, slot = t * topk + k;
+        v[j] = (k < topk && __ldg(inv_pos + slot) >= 0)
+                   ? __ldg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(slot) * H) + c)
+                   : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[u]));
+          acc[2 * u] += f.x;
+          acc[2 * u + 1] += f.y;
+        }
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * u], acc[2 * u + 1]);
+      o[u] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -781,6 +823,16 @@ cudaError_t launch_combine(const float* y, const int32_t* inv_pos, int M, int to
   if (grid < 1) grid = 1;
   return launch_kernel(combine_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, true, y, inv_pos, M, topk,
                        H, out);
+}
+
+cudaError_t launch_combine(const __nv_bfloat16* y, const int32_t* inv_pos, int M, int topk, int H,
+                           __nv_bfloat16* out, int num_sms, cudaStream_t s) {
+  const long long work = static_cast<long long>(M) * (H / 8);
+  long long grid = (work + 255) / 256;
+  if (grid > num_sms * 16) grid = num_sms * 16;
+  if (grid < 1) grid = 1;
+  return launch_kernel(combine_bf16_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, true, y, inv_pos, M,
+                       topk, H, out);
 }
 
 size_t prefill_smem_bytes() { return pf::SMEM_BYTES; }

@@ -34,8 +34,8 @@
 //               promotion, then the epilogue of the tile:
 //                 GEMM1: h = SiLU(gate) * up, quantised to E4M3 per 1 x 128 group (the tile's
 //                        128 rows are one group of I) -> h codes [cap, I] and scales [I/128, cap]
-//                 GEMM2: y[slot] = acc * routing weight, staged through shared memory so that
-//                        every store instruction writes whole 128-byte row segments
+//                 GEMM2: y[slot] = acc * routing weight in bf16, staged through shared memory so
+//                        that every store instruction writes whole 128-byte row segments
 // Every wait is bounded; a time-out sets the status flag and every role drains.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -71,12 +71,11 @@ constexpr int RED_BYTES = 2 * 2 * MAXN * 4;  // [tile parity][column half][token
 
 // Shared-memory layout per GEMM (measured): GEMM1 keeps 4 K-block stages; GEMM2, whose short
 // K loop (I = 2048) makes its y stores a large share of the tile, trades one stage for a
-// 4 KB y staging buffer per accumulator warp (32 columns, 128-byte row segments).
+// 4 KB y staging buffer per accumulator warp (64 bf16 columns, 128-byte row segments).
 template <bool GATED>
 struct Lay {
   static constexpr int STAGES = GATED ? 4 : 3;
-  static constexpr int Y_COLS = 32;                            // GEMM2: columns of y a warp stages at a time
-  static constexpr int STG_BYTES = GATED ? 0 : 32 * Y_COLS * 4;  // per accumulator warp: 32 tokens x Y_COLS fp32
+  static constexpr int STG_BYTES = GATED ? 0 : 32 * 64 * 2;  // per accumulator warp: 32 tokens x 64 bf16 of y
   static constexpr int OFF_W = 0;
   static constexpr int OFF_A = OFF_W + STAGES * 2 * W_TILE;
   static constexpr int OFF_S = OFF_A + STAGES * A_TILE;
@@ -118,7 +117,7 @@ struct Args {
   const float* topk_w;   // GEMM2
   uint8_t* hq;           // GEMM1 out: h codes [cap, I]
   float* hs;             // GEMM1 out: h scales [I/128, cap]
-  float* y;              // GEMM2 out: [M*topk, H]
+  __nv_bfloat16* y;      // GEMM2 out: [M*topk, H]
   DeviceStatus* status;
 };
 
@@ -450,41 +449,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (ch == 0) p.hs[static_cast<size_t>(tl.n0 / kQBlock) * p.cap + pos] = s;
         }
       } else {
-        // y[slot] = acc x routing weight.  A thread holds one token's row, so direct stores would
-        // put 32 rows in every warp instruction; instead the warp stages Y_COLS columns of its 32
-        // rows in shared memory and writes them back row by row: Y_COLS * 4 contiguous bytes per
-        // row, 32 / CPR rows per instruction.  The 16-byte chunk j of row r sits at chunk
-        // j ^ swz(r), which keeps both the row-wise writes and the column-wise reads free of bank
-        // conflicts (8 lanes, one 128-byte phase, always touch 8 different chunk columns).
-        constexpr int Y_COLS = L::Y_COLS;
-        constexpr int CPR = Y_COLS / 4;  // 16-byte chunks per staged row
-        static_assert(CPR == 4 || CPR == 8, "staging swizzle");
-        auto swz = [](int r) { return CPR == 8 ? (r & 7) : ((r >> 1) & 3); };
-        float4* stg = reinterpret_cast<float4*>(smem + L::OFF_STG + (warp - WARP_ACC0) * L::STG_BYTES);
-        const int rr = lane / CPR, cj = lane % CPR;  // read-back: rows rr + (32 / CPR) i, chunk cj
+        // y[slot] = acc x routing weight in bf16.  A thread holds one token's row, so direct stores
+        // would put 32 rows in every warp instruction; instead the warp stages the 64 columns of
+        // its 32 rows in shared memory and writes them back row by row: 128 contiguous bytes per
+        // row, 4 rows per instruction.  The 16-byte chunk j of row r sits at chunk j ^ (r & 7),
+        // which keeps both the row-wise writes and the column-wise reads free of bank conflicts
+        // (8 lanes, one 128-byte phase, always touch 8 different chunk columns).
+        uint4* stg = reinterpret_cast<uint4*>(smem + L::OFF_STG + (warp - WARP_ACC0) * L::STG_BYTES);
+        const int rr = lane >> 3, cj = lane & 7;  // read-back: rows rr + 4i, chunk cj
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
           if (!quarter_live || (b == 1 && !tl.two)) break;
           const float2* a = b ? acc1 : acc0;
 #pragma unroll
-          for (int cc = 0; cc < 64 / Y_COLS; ++cc) {
+          for (int j = 0; j < 8; ++j) {
+            uint32_t w[4];
 #pragma unroll
-            for (int j = 0; j < CPR; ++j) {
-              const float2 u = a[(cc * Y_COLS + 4 * j) / 2], v = a[(cc * Y_COLS + 4 * j) / 2 + 1];
-              stg[lane * CPR + (j ^ swz(lane))] = make_float4(u.x * wgt, u.y * wgt, v.x * wgt, v.y * wgt);
+            for (int u = 0; u < 4; ++u) {
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(a[4 * j + u].x * wgt, a[4 * j + u].y * wgt);
+              w[u] = *reinterpret_cast<const uint32_t*>(&h2);
             }
-            __syncwarp();
-            const int col = tl.n0 + b * BM + ch * 64 + cc * Y_COLS + cj * 4;
-#pragma unroll
-            for (int i = 0; i < CPR; ++i) {
-              const int r = rr + (32 / CPR) * i;
-              const int rslot = __shfl_sync(0xffffffffu, slot, r);
-              const float4 val = stg[r * CPR + (cj ^ swz(r))];
-              if (q * 32 + r < tl.cnt)
-                *reinterpret_cast<float4*>(p.y + static_cast<size_t>(rslot) * p.n_rows_out + col) = val;
-            }
-            __syncwarp();
+            stg[lane * 8 + (j ^ (lane & 7))] = make_uint4(w[0], w[1], w[2], w[3]);
           }
+          __syncwarp();
+          const int col = tl.n0 + b * BM + ch * 64 + cj * 8;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = rr + 4 * i;
+            const int rslot = __shfl_sync(0xffffffffu, slot, r);
+            const uint4 val = stg[r * 8 + (cj ^ (r & 7))];
+            if (q * 32 + r < tl.cnt)
+              *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(rslot) * p.n_rows_out + col) = val;
+          }
+          __syncwarp();
         }
       }
       ++ntile;
@@ -600,12 +597,12 @@ cudaError_t launch_prefill_a8(const LayerPlan& P, int num_sms, cudaStream_t s, c
   g2.wscale = P.s2;
   g2.sorted_ids = P.sorted_ids;
   g2.topk_w = P.topk_w;
-  g2.y = P.y;
+  g2.y = reinterpret_cast<__nv_bfloat16*>(P.y);  // bf16 rows in the fp32 buffer's space
   g2.status = P.status;
   err = launch_a8_gemm<false>(g2, P.w2, static_cast<uint64_t>(P.E) * P.H, P.h8, P.sh8, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("prefill_gemm2", s);
-  err = launch_combine(P.y, P.inv_pos, P.M, P.topk, P.H, P.out, num_sms, s);
+  err = launch_combine(reinterpret_cast<const __nv_bfloat16*>(P.y), P.inv_pos, P.M, P.topk, P.H, P.out, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("combine", s);
   return cudaSuccess;
