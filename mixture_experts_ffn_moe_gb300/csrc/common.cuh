@@ -168,7 +168,10 @@ __device__ __forceinline__ void mma_f16_16816(float d[4], const uint32_t a[4], u
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
+// SiLU with the fast exponential and division (a few ulp; the result is rounded to fp16 or
+// quantised right after).  __fdividef returns 0 once 1 + exp(-g) exceeds 2^126, i.e. for
+// g < -87, where SiLU(g) is below 1e-36 anyway.
+__device__ __forceinline__ float silu_f32(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // ---------------------------------------------------------------- programmatic dependent launch
 // A kernel launched with programmatic stream serialization may start while its

@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
           const float g = elem(acc0, j);
-          hv[j] = g * __frcp_rn(1.0f + __expf(-g)) * elem(acc1, j);
+          hv[j] = __fdividef(g, 1.0f + __expf(-g)) * elem(acc1, j);  // fast division: 0 once exp(-g) > 2^126
           m = fmaxf(m, fabsf(hv[j]));
         }
         const int rb = ntile & 1;
