@@ -116,79 +116,170 @@ __device__ void align_cta(const AlignArgs& a) {
   }
 }
 
-// FP8 E4M3 codes of one row in groups of 128 columns: s = amax / 448 (fp32,
-// 1 for an all-zero group), q = E4M3(x / s) rounded to nearest even with
-// saturation, the division in IEEE fp32.  One warp per group, 4 columns a lane.
-__device__ void prep_row_fp8_1x128(const __nv_bfloat16* xr, uint8_t* qr, float* sr, int H) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  for (int g = warp; g < H / kQBlock; g += nw) {
-    const uint2 raw = *reinterpret_cast<const uint2*>(xr + g * kQBlock + lane * 4);
-    const __nv_bfloat162 b0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-    const __nv_bfloat162 b1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-    const float2 f0 = __bfloat1622float2(b0), f1 = __bfloat1622float2(b1);
-    float m = fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
-    m = warp_max(m);
-    const float s = m > 0.f ? __fdiv_rn(m, 448.0f) : 1.0f;
-    const uint32_t c0 = e4m3_code(__fdiv_rn(f0.x, s)), c1 = e4m3_code(__fdiv_rn(f0.y, s));
-    const uint32_t c2 = e4m3_code(__fdiv_rn(f1.x, s)), c3 = e4m3_code(__fdiv_rn(f1.y, s));
-    *reinterpret_cast<uint32_t*>(qr + g * kQBlock + lane * 4) = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
-    if (lane == 0) sr[g] = s;
-  }
-}
-
-// Row preparation of the activations, one CTA per row at a time.
+// Activation preparation.  The element-wise kinds run as one flat pass over
+// the [M, H] matrix (H is a multiple of 128, so rows never split a vector or a
+// group); every thread keeps kPrepBatch 16-byte loads in flight.
 //   kind 1: x bf16 -> fp16 (RN)               (FP8 weight-only path)
-//   kind 2: x bf16 -> int8 codes + fp32 scale (DA8W8 path); codes stored as
-//           fp16 (exact) or int8
+//   kind 2: x bf16 -> int8 codes + fp32 scale per row (DA8W8 path), a CTA or a
+//           warp per row; codes stored as fp16 (exact) or int8
 //   kind 3: x bf16 -> E4M3 codes + one fp32 scale per 128 columns (FP8 A8 path)
 //   kind 4: x bf16 -> fp16 (RN), each group of 8 columns stored in the order
 //           0 4 1 5 2 6 3 7 (INT4 path: the order its weights expand in)
+constexpr int kPrepBatch = 4;
+
+__device__ __forceinline__ float2 bf2_lo_hi(uint32_t w) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+}
+
+// kinds 1 and 4: 8 columns per 16-byte chunk; `first` / `stride` count threads
+template <bool INT4_ORDER>
+__device__ void prep_f16_flat(const PrepArgs& p, long long first, long long stride) {
+  const long long n = static_cast<long long>(p.M) * (p.H / 8);
+  const uint4* src = reinterpret_cast<const uint4*>(p.x);
+  uint4* dst = static_cast<uint4*>(p.q);
+  for (long long i0 = first; i0 < n; i0 += kPrepBatch * stride) {
+    uint4 v[kPrepBatch];
+#pragma unroll
+    for (int u = 0; u < kPrepBatch; ++u) {
+      const long long i = i0 + u * stride;
+      if (i < n) v[u] = ld_v4(src + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kPrepBatch; ++u) {
+      const long long i = i0 + u * stride;
+      if (i >= n) break;
+      const float2 f01 = bf2_lo_hi(v[u].x), f23 = bf2_lo_hi(v[u].y);
+      const float2 f45 = bf2_lo_hi(v[u].z), f67 = bf2_lo_hi(v[u].w);
+      dst[i] = INT4_ORDER ? make_uint4(pack_half2(f01.x, f45.x), pack_half2(f01.y, f45.y), pack_half2(f23.x, f67.x),
+                                       pack_half2(f23.y, f67.y))
+                          : make_uint4(pack_half2(f01.x, f01.y), pack_half2(f23.x, f23.y), pack_half2(f45.x, f45.y),
+                                       pack_half2(f67.x, f67.y));
+    }
+  }
+}
+
+// kind 3: FP8 E4M3 codes in groups of 128 columns, s = amax / 448 (fp32, 1 for an
+// all-zero group), q = E4M3(x / s) rounded to nearest even with saturation, the
+// division in IEEE fp32.  One warp per group, 4 columns a lane; `first` / `stride`
+// count warps, and a group index is warp-uniform.
+__device__ void prep_fp8_flat(const PrepArgs& p, long long first, long long stride) {
+  const int lane = threadIdx.x & 31;
+  const long long ng = static_cast<long long>(p.M) * (p.H / kQBlock);
+  uint8_t* q = static_cast<uint8_t*>(p.q);
+  for (long long g0 = first; g0 < ng; g0 += kPrepBatch * stride) {
+    uint2 raw[kPrepBatch];
+#pragma unroll
+    for (int u = 0; u < kPrepBatch; ++u) {
+      const long long gi = g0 + u * stride;
+      if (gi < ng) raw[u] = *reinterpret_cast<const uint2*>(p.x + gi * kQBlock + lane * 4);
+    }
+#pragma unroll
+    for (int u = 0; u < kPrepBatch; ++u) {
+      const long long gi = g0 + u * stride;
+      if (gi >= ng) break;
+      const float2 f0 = bf2_lo_hi(raw[u].x), f1 = bf2_lo_hi(raw[u].y);
+      float m = fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y)));
+      m = warp_max(m);
+      const float sc = m > 0.f ? __fdiv_rn(m, 448.0f) : 1.0f;
+      const uint32_t c0 = e4m3_code(__fdiv_rn(f0.x, sc)), c1 = e4m3_code(__fdiv_rn(f0.y, sc));
+      const uint32_t c2 = e4m3_code(__fdiv_rn(f1.x, sc)), c3 = e4m3_code(__fdiv_rn(f1.y, sc));
+      *reinterpret_cast<uint32_t*>(q + gi * kQBlock + lane * 4) = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+      if (lane == 0) p.scale[gi] = sc;
+    }
+  }
+}
+
+// kind 2: s = max|x| / 127 over the row, codes RNE(x / s) clamped to +-127.
+__device__ __forceinline__ float absmax8(const uint4& v) {
+  const float2 f01 = bf2_lo_hi(v.x), f23 = bf2_lo_hi(v.y), f45 = bf2_lo_hi(v.z), f67 = bf2_lo_hi(v.w);
+  return fmaxf(fmaxf(fmaxf(fabsf(f01.x), fabsf(f01.y)), fmaxf(fabsf(f23.x), fabsf(f23.y))),
+               fmaxf(fmaxf(fabsf(f45.x), fabsf(f45.y)), fmaxf(fabsf(f67.x), fabsf(f67.y))));
+}
+
 template <typename QT>
-__device__ void prep_rows(const PrepArgs& p, int row0, int rstride) {
+__device__ __forceinline__ void store_codes8(QT* dst, const uint4& v, float sc) {
+  const float2 f01 = bf2_lo_hi(v.x), f23 = bf2_lo_hi(v.y), f45 = bf2_lo_hi(v.z), f67 = bf2_lo_hi(v.w);
+  const float e[8] = {f01.x, f01.y, f23.x, f23.y, f45.x, f45.y, f67.x, f67.y};
+  QT o[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) o[j] = static_cast<QT>(quant_s8_rne(e[j], sc));
+  if constexpr (sizeof(QT) == 2) {
+    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(o);
+  } else {
+    *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(o);
+  }
+}
+
+// Few rows per CTA: the whole CTA takes one row at a time (block-wide amax).
+// Many rows: one warp per row, each lane keeping kPrepBatch loads in flight.
+template <typename QT>
+__device__ void prep_int8_rows(const PrepArgs& p, int cta, int nctas) {
   __shared__ float red[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-  for (int r = row0; r < p.M; r += rstride) {
-    const __nv_bfloat16* xr = p.x + static_cast<size_t>(r) * p.H;
-    if (p.kind == 3) {
-      prep_row_fp8_1x128(xr, static_cast<uint8_t*>(p.q) + static_cast<size_t>(r) * p.H,
-                         p.scale + static_cast<size_t>(r) * (p.H / kQBlock), p.H);
-      continue;
-    }
-    if (p.kind == 4) {
-      uint4* qr4 = reinterpret_cast<uint4*>(static_cast<__half*>(p.q) + static_cast<size_t>(r) * p.H);
-      for (int c = tid; c < p.H / 8; c += blockDim.x) {
-        const uint4 raw = *reinterpret_cast<const uint4*>(xr + 8 * c);
-        const float2 f01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
-        const float2 f23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
-        const float2 f45 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.z));
-        const float2 f67 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.w));
-        qr4[c] = make_uint4(pack_half2(f01.x, f45.x), pack_half2(f01.y, f45.y), pack_half2(f23.x, f67.x),
-                            pack_half2(f23.y, f67.y));
+  const int chunks = p.H / 8;
+  if (p.M <= 4 * nctas) {
+    for (int r = cta; r < p.M; r += nctas) {
+      const uint4* xr = reinterpret_cast<const uint4*>(p.x + static_cast<size_t>(r) * p.H);
+      float m = 0.f;
+      for (int c = tid; c < chunks; c += blockDim.x) m = fmaxf(m, absmax8(ld_v4(xr + c)));
+      m = warp_max(m);
+      if (lane == 0) red[warp] = m;
+      __syncthreads();
+      if (warp == 0) {
+        float v = lane < nw ? red[lane] : 0.f;
+        v = warp_max(v);
+        if (lane == 0) red[0] = v;
       }
-      continue;
+      __syncthreads();
+      const float amax = red[0];
+      const float sc = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 1.0f;
+      if (tid == 0 && p.scale) p.scale[r] = sc;
+      QT* qr = static_cast<QT*>(p.q) + static_cast<size_t>(r) * p.H;
+      for (int c = tid; c < chunks; c += blockDim.x) store_codes8<QT>(qr + 8 * c, ld_v4(xr + c), sc);
+      __syncthreads();  // red is rewritten for the next row
     }
-    QT* qr = reinterpret_cast<QT*>(p.q) + static_cast<size_t>(r) * p.H;
-    if (p.kind == 1) {
-      for (int c = tid; c < p.H; c += blockDim.x) qr[c] = static_cast<QT>(__bfloat162float(xr[c]));
-      continue;
-    }
+    return;
+  }
+  const long long wstride = static_cast<long long>(nctas) * nw;
+  for (long long r = static_cast<long long>(cta) * nw + warp; r < p.M; r += wstride) {
+    const uint4* xr = reinterpret_cast<const uint4*>(p.x + r * p.H);
     float m = 0.f;
-    for (int c = tid; c < p.H; c += blockDim.x) m = fmaxf(m, fabsf(__bfloat162float(xr[c])));
-    m = warp_max(m);
-    if (lane == 0) red[warp] = m;
-    __syncthreads();
-    if (warp == 0) {
-      float v = lane < nw ? red[lane] : 0.f;
-      v = warp_max(v);
-      if (lane == 0) red[0] = v;
+    for (int c0 = lane; c0 < chunks; c0 += 32 * kPrepBatch) {
+      uint4 v[kPrepBatch];
+#pragma unroll
+      for (int u = 0; u < kPrepBatch; ++u)
+        if (c0 + 32 * u < chunks) v[u] = ld_v4(xr + c0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < kPrepBatch; ++u)
+        if (c0 + 32 * u < chunks) m = fmaxf(m, absmax8(v[u]));
     }
-    __syncthreads();
-    const float amax = red[0];
-    const float s = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 1.0f;
-    if (tid == 0 && p.scale) p.scale[r] = s;
-    for (int c = tid; c < p.H; c += blockDim.x)
-      qr[c] = static_cast<QT>(quant_s8_rne(__bfloat162float(xr[c]), s));
-    __syncthreads();
+    const float amax = warp_max(m);
+    const float sc = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 1.0f;
+    if (lane == 0 && p.scale) p.scale[r] = sc;
+    QT* qr = static_cast<QT*>(p.q) + r * p.H;
+    for (int c0 = lane; c0 < chunks; c0 += 32 * kPrepBatch) {
+      uint4 v[kPrepBatch];
+#pragma unroll
+      for (int u = 0; u < kPrepBatch; ++u)
+        if (c0 + 32 * u < chunks) v[u] = ld_v4(xr + c0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < kPrepBatch; ++u)
+        if (c0 + 32 * u < chunks) store_codes8<QT>(qr + 8 * (c0 + 32 * u), v[u], sc);
+    }
+  }
+}
+
+// The preparation pass spread over `nctas` CTAs, this being CTA `cta` of them.
+template <typename QT>
+__device__ void prep_rows(const PrepArgs& p, int cta, int nctas) {
+  const long long tfirst = static_cast<long long>(cta) * blockDim.x + threadIdx.x;
+  const long long tstride = static_cast<long long>(nctas) * blockDim.x;
+  switch (p.kind) {
+    case 1: prep_f16_flat<false>(p, tfirst, tstride); break;
+    case 4: prep_f16_flat<true>(p, tfirst, tstride); break;
+    case 3: prep_fp8_flat(p, tfirst >> 5, tstride >> 5); break;
+    case 2: prep_int8_rows<QT>(p, cta, nctas); break;
+    default: break;
   }
 }
 

@@ -276,7 +276,9 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
   p.q = at<void>(ws, L.xq);
   p.scale = at<float>(ws, L.sx);
   if (kind == MOE_WEIGHT_INT8) { p.zero_words = at<uint32_t>(ws, L.hmax); p.n_zero = static_cast<int>(L.cap); }
-  const int prep_ctas = M < 2 * sms ? (M > 0 ? M : 1) : 2 * sms;
+  // one 1024-thread prologue CTA per SM (its register count allows no second one): the
+  // alignment CTA and up to sms - 1 CTAs of the flat activation pass
+  const int prep_ctas = M < sms - 1 ? (M > 0 ? M : 1) : (sms > 1 ? sms - 1 : 1);
   const StageHook hook = prof_begin_call(stream);
   const bool gate_inline = gate && M <= MOE_GATE_INLINE_TOKENS && gate->E <= 256;
   cudaError_t err;
