@@ -298,7 +298,8 @@ moe_status_t fused_moe_int4(const void* x_bf16, const int32_t* topk_ids, const f
  *                                 combine of the dispatch applies it).
  *   workspace  moe_workspace_size_masked(E, cap, H, I, weight_kind) bytes,
  *              256-byte aligned
- * H and I multiples of 128, E <= MOE_MAX_EXPERTS, cap >= 1.  The products
+ * x, w13 and w2 16-byte aligned; out_bf16 2-byte aligned, 16-byte aligned
+ * with MOE_PATH_PREFILL (else MOE_ERR_INVALID_ARG).  H and I multiples of 128, E <= MOE_MAX_EXPERTS, cap >= 1.  The products
  * use the arithmetic of the weight kind's layer entry point.  Since the counts
  * are on the device the caller picks the kernels: MOE_PATH_AUTO or
  * MOE_PATH_DECODE runs the weight-streaming kernels (best for a few rows per
@@ -375,6 +376,27 @@ moe_status_t fused_moe_fp8_static_scratch(const void* x_bf16, const int32_t* top
  * Returns MOE_ERR_BAD_IDS / MOE_ERR_TIMEOUT when they are non-zero.
  */
 moe_status_t moe_read_status(const void* workspace, int32_t status_out[2], moe_stream_t stream);
+
+/*
+ * The routing alignment (step 1) that the last routed fused call on
+ * `workspace` computed -- fused_moe_fp8, fused_moe_int8, fused_moe_int4 or
+ * fused_moe_gated, called with these same M, H, I, E (all stored experts),
+ * topk (all columns) and flags.  Outputs are as moe_align_block_size defines
+ * them, for the block size the layer chose for its path (8 on the
+ * weight-streaming kernels, 16 on the tcgen05 ones):
+ *   block_size      HOST int out (may be NULL)
+ *   sorted_ids      device int32 [moe_align_max_padded(M, topk, E, *block_size)]
+ *   expert_ids      device int32 [that / *block_size]
+ *   num_tokens_post_padded  device int32 [1]
+ *   expert_offsets  device int32 [E + 1]
+ * Any output pointer may be NULL (block_size alone answers the sizing
+ * question).  The copies are stream-ordered device-to-device copies after
+ * the layer's kernels; nothing synchronises.  The masked layout has no
+ * alignment and is not covered.  Bad sizes give MOE_ERR_INVALID_ARG.
+ */
+moe_status_t moe_read_routing(const void* workspace, int M, int H, int I, int E, int topk, int weight_kind,
+                              unsigned flags, int* block_size, int32_t* sorted_ids, int32_t* expert_ids,
+                              int32_t* num_tokens_post_padded, int32_t* expert_offsets, moe_stream_t stream);
 
 /*
  * Self-test of the failure path of the bounded device waits.  Launches one

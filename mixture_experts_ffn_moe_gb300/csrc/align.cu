@@ -8,11 +8,16 @@
 // inside a group is fixed here (ascending slot index) so the result equals a
 // stable argsort and is deterministic.
 //
-// GB300 design: one CTA of 1024 threads does the whole alignment in three
-// passes over shared memory -- per-warp expert histograms, one block-wide
-// scan that turns them into write cursors, and a warp-ordered scatter in which
-// __match_any_sync ranks equal ids inside each 32-slot step.  The other CTAs of
-// the same launch prepare the activation rows for the expert GEMMs.
+// GB300 design: the alignment runs in three passes over shared memory --
+// per-warp expert histograms, one block-wide scan that turns them into write
+// cursors, and a warp-ordered scatter in which __match_any_sync ranks equal
+// ids inside each 32-slot step.  Up to kAlignChunkSlots slots one CTA of 1024
+// threads does all of it, and the other CTAs of the same launch prepare the
+// activation rows for the expert GEMMs.  Longer id lists are cut into
+// consecutive chunks, one CTA each: the prologue's first CTAs write every
+// chunk's expert histogram to the workspace, and a second launch gives each
+// chunk's CTA the sum over the chunks before it as its starting cursors, so
+// the scatter is the same stable order as the single CTA's.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -24,32 +29,49 @@ namespace gbmoe {
 constexpr int kAlignThreads = 1024;
 constexpr int kAlignWarps = kAlignThreads / 32;
 
-// One CTA: the full alignment.  Shared memory: kAlignWarps * E ints (per-warp
-// histograms, later per-warp write cursors) + 64 ints.
-__device__ void align_cta(const AlignArgs& a) {
-  extern __shared__ int smem[];
-  int* cur = smem;                              // [kAlignWarps][E]
-  int* scan_tmp = smem + kAlignWarps * a.E;     // [33]
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = a.M * a.topk;
-  const int sentinel = n;
-  const int B = a.block;
-
-  for (int i = tid; i < kAlignWarps * a.E; i += kAlignThreads) cur[i] = 0;
-  for (int i = tid; i < a.cap; i += kAlignThreads) a.sorted_ids[i] = sentinel;
-  for (int i = tid; i < a.cap / B; i += kAlignThreads) a.expert_ids[i] = -1;
-  __syncthreads();
-
-  // pass 1: per-warp histogram over a contiguous segment of slots
-  const int seg = (n + kAlignWarps - 1) / kAlignWarps;
-  const int beg = min(n, warp * seg), end = min(n, beg + seg);
+// Per-warp histograms of slots [lo, hi): warp w takes a contiguous segment
+// [beg, end).  Returns the ids outside [0, E) the warp saw.
+__device__ __forceinline__ int align_histogram(const AlignArgs& a, int* cur, int lo, int hi, int& beg, int& end) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int seg = (hi - lo + kAlignWarps - 1) / kAlignWarps;
+  beg = min(hi, lo + warp * seg);
+  end = min(hi, beg + seg);
   int bad = 0;
   for (int i = beg + lane; i < end; i += 32) {
     const int e = a.topk_ids[i];
     if (e >= 0 && e < a.E) atomicAdd(&cur[warp * a.E + e], 1);
     else ++bad;
   }
-  bad = warp_sum_i(bad);
+  return warp_sum_i(bad);
+}
+
+// The alignment of slots [lo, hi) by one CTA.  Shared memory: kAlignWarps * E
+// ints (per-warp histograms, later per-warp write cursors) + 64 ints.
+//   !SPLIT: [lo, hi) is every slot; this CTA fills the padding, counts, plans
+//     and scatters (chunk_counts unused).
+//   SPLIT: chunk_counts[c * E + e] holds every chunk's histogram; this CTA
+//     is chunk `chunk` and scatters its slots after those of chunks
+//     0..chunk-1 (the first launch filled the padding); chunk 0 writes the plan.
+template <bool SPLIT>
+__device__ void align_core(const AlignArgs& a, int lo, int hi, const int* chunk_counts, int chunk, int nchunks) {
+  extern __shared__ int smem[];
+  int* cur = smem;                              // [kAlignWarps][E]
+  int* scan_tmp = smem + kAlignWarps * a.E;     // [33]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = a.block;
+  const bool plan = !SPLIT || chunk == 0;  // CTA-uniform
+
+  for (int i = tid; i < kAlignWarps * a.E; i += kAlignThreads) cur[i] = 0;
+  if constexpr (!SPLIT) {
+    const int sentinel = a.M * a.topk;
+    for (int i = tid; i < a.cap; i += kAlignThreads) a.sorted_ids[i] = sentinel;
+    for (int i = tid; i < a.cap / B; i += kAlignThreads) a.expert_ids[i] = -1;
+  }
+  __syncthreads();
+
+  // pass 1: per-warp histogram over a contiguous segment of slots
+  int beg, end;
+  const int bad = align_histogram(a, cur, lo, hi, beg, end);
   if (lane == 0 && bad && a.status) atomicAdd(&a.status->bad_ids, bad);
   __syncthreads();
 
@@ -57,36 +79,47 @@ __device__ void align_cta(const AlignArgs& a) {
   for (int e0 = 0; e0 < a.E; e0 += kAlignThreads) {
     // E <= MOE_MAX_EXPERTS == kAlignThreads, so this loop runs once
     const int e = e0 + tid;
-    int cnt = 0;
+    int cnt = 0, before = 0;  // slots of expert e in every chunk / in the chunks before this one
     if (e < a.E) {
+      if constexpr (SPLIT) {
+        for (int c = 0; c < nchunks; ++c) {
+          const int v = chunk_counts[c * a.E + e];
+          cnt += v;
+          if (c < chunk) before += v;
+        }
+      } else {
 #pragma unroll 4
-      for (int w = 0; w < kAlignWarps; ++w) cnt += cur[w * a.E + e];
+        for (int w = 0; w < kAlignWarps; ++w) cnt += cur[w * a.E + e];
+      }
     }
     const int padded = (cnt + B - 1) / B * B;
     int total;
     const int off = block_exclusive_scan(padded, scan_tmp, total);
-    int nact;
-    const int act_idx = block_exclusive_scan(cnt > 0 ? 1 : 0, scan_tmp, nact);
     const int ntt = a.ttiles ? (cnt + a.tile_tokens - 1) / a.tile_tokens : 0;
-    int n_tt;
-    const int tt0 = block_exclusive_scan(ntt, scan_tmp, n_tt);
+    int nact = 0, n_tt = 0, act_idx = 0, tt0 = 0;
+    if (plan) {
+      act_idx = block_exclusive_scan(cnt > 0 ? 1 : 0, scan_tmp, nact);
+      tt0 = block_exclusive_scan(ntt, scan_tmp, n_tt);
+    }
     if (e < a.E) {
-      int c = off;
+      int c = off + before;
       for (int w = 0; w < kAlignWarps; ++w) {
         const int t = cur[w * a.E + e];
         cur[w * a.E + e] = c;
         c += t;
       }
-      if (a.expert_offsets) a.expert_offsets[e] = off;
-      if (a.counts) a.counts[e] = cnt;
-      if (a.active && cnt > 0) a.active[act_idx] = e;
-      for (int b = off / B; b < (off + padded) / B; ++b) a.expert_ids[b] = e;
-      for (int i = 0; i < ntt; ++i) {
-        const int start = i * a.tile_tokens;
-        a.ttiles[tt0 + i] = make_int4(e, off + start, min(a.tile_tokens, cnt - start), 0);
+      if (plan) {
+        if (a.expert_offsets) a.expert_offsets[e] = off;
+        if (a.counts) a.counts[e] = cnt;
+        if (a.active && cnt > 0) a.active[act_idx] = e;
+        for (int b = off / B; b < (off + padded) / B; ++b) a.expert_ids[b] = e;
+        for (int i = 0; i < ntt; ++i) {
+          const int start = i * a.tile_tokens;
+          a.ttiles[tt0 + i] = make_int4(e, off + start, min(a.tile_tokens, cnt - start), 0);
+        }
       }
     }
-    if (tid == 0) {
+    if (plan && tid == 0) {
       if (a.expert_offsets) a.expert_offsets[a.E] = total;
       if (a.num_post) *a.num_post = total;
       if (a.num_active) *a.num_active = nact;
@@ -114,6 +147,48 @@ __device__ void align_cta(const AlignArgs& a) {
     if (ok && rank == 0) cur[warp * a.E + e] += __popc(peers);
     __syncwarp();
   }
+}
+
+__device__ void align_cta(const AlignArgs& a) { align_core<false>(a, 0, a.M * a.topk, nullptr, 0, 1); }
+
+// First launch of the split alignment, CTA `chunk` of `nchunks`: its share of
+// the padding fill and the expert histogram of its chunk.
+__device__ void align_count_chunk(const AlignArgs& a, int* chunk_counts, int chunk, int nchunks) {
+  extern __shared__ int smem[];
+  int* cur = smem;
+  const int tid = threadIdx.x;
+  const int n = a.M * a.topk, sentinel = n;
+  const int stride = nchunks * kAlignThreads;
+  for (int i = chunk * kAlignThreads + tid; i < a.cap; i += stride) a.sorted_ids[i] = sentinel;
+  for (int i = chunk * kAlignThreads + tid; i < a.cap / a.block; i += stride) a.expert_ids[i] = -1;
+  for (int i = tid; i < kAlignWarps * a.E; i += kAlignThreads) cur[i] = 0;
+  __syncthreads();
+  const int S = align_chunk_slots(n, nchunks);
+  int beg, end;
+  align_histogram(a, cur, chunk * S, min(n, (chunk + 1) * S), beg, end);  // bad ids: counted by the scatter
+  __syncthreads();
+  for (int e = tid; e < a.E; e += kAlignThreads) {
+    int cnt = 0;
+#pragma unroll 4
+    for (int w = 0; w < kAlignWarps; ++w) cnt += cur[w * a.E + e];
+    chunk_counts[chunk * a.E + e] = cnt;
+  }
+}
+
+// Second launch of the split alignment: CTA c < nchunks plans (c == 0) and
+// scatters chunk c; the CTAs after them prepare the activations.
+__device__ void prep_part(const PrepArgs& p, int cta, int nctas);
+
+__global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(AlignArgs a, PrepArgs p,
+                                                                      const int* chunk_counts, int nchunks) {
+  pdl_trigger();
+  pdl_wait();  // histograms, padding fill and status reset come from the previous launch
+  if (blockIdx.x >= nchunks) {
+    prep_part(p, blockIdx.x - nchunks, gridDim.x - nchunks);
+    return;
+  }
+  const int n = a.M * a.topk, S = align_chunk_slots(n, nchunks);
+  align_core<true>(a, blockIdx.x * S, min(n, (blockIdx.x + 1) * S), chunk_counts, blockIdx.x, nchunks);
 }
 
 // Activation preparation.  The element-wise kinds run as one flat pass over
@@ -283,14 +358,32 @@ __device__ void prep_rows(const PrepArgs& p, int cta, int nctas) {
   }
 }
 
+// The preparation pass and the clearing of the INT8 intermediate's amax words,
+// on `nctas` CTAs of which this is CTA `cta`.
+__device__ void prep_part(const PrepArgs& p, int cta, int nctas) {
+  if (p.zero_words) {
+    const int stride = nctas * blockDim.x;
+    for (int i = cta * blockDim.x + threadIdx.x; i < p.n_zero; i += stride) p.zero_words[i] = 0u;
+  }
+  if (p.kind != 0) prep_rows<__half>(p, cta, nctas);
+}
+
 // GV > 0: the alignment CTA first ranks every token's experts (router gating,
 // GV experts per lane) and writes topk_ids / topk_weights, then aligns them.
+// chunk_counts != nullptr: the first launch of the split alignment, whose CTAs
+// each histogram one chunk (the activations are prepared by the second launch,
+// align_scatter_kernel); otherwise CTA 0 aligns and the others prepare.
 template <int GV>
-__global__ void __launch_bounds__(kAlignThreads) prologue_kernel(AlignArgs a, PrepArgs p, GateArgs g) {
+__global__ void __launch_bounds__(kAlignThreads) prologue_kernel(AlignArgs a, PrepArgs p, GateArgs g,
+                                                                 int* chunk_counts, int nchunks) {
   pdl_trigger();  // the next kernel may set itself up; it waits for this grid before reading
   pdl_wait();     // inputs (and this workspace's previous readers) belong to earlier kernels
+  if (blockIdx.x == 0 && a.status && threadIdx.x == 0) { a.status->bad_ids = 0; a.status->flags = 0; }
+  if (chunk_counts) {
+    align_count_chunk(a, chunk_counts, blockIdx.x, nchunks);
+    return;
+  }
   if (blockIdx.x == 0) {
-    if (a.status && threadIdx.x == 0) { a.status->bad_ids = 0; a.status->flags = 0; }
     if constexpr (GV > 0) {
       for (int t = threadIdx.x >> 5; t < g.M; t += kAlignWarps) gate_token<GV>(g, t, threadIdx.x & 31);
     }
@@ -298,12 +391,7 @@ __global__ void __launch_bounds__(kAlignThreads) prologue_kernel(AlignArgs a, Pr
     align_cta(a);
     return;
   }
-  // zero the per-row amax words of the INT8 intermediate
-  if (p.zero_words) {
-    const int stride = (gridDim.x - 1) * blockDim.x;
-    for (int i = (blockIdx.x - 1) * blockDim.x + threadIdx.x; i < p.n_zero; i += stride) p.zero_words[i] = 0u;
-  }
-  if (p.kind != 0) prep_rows<__half>(p, blockIdx.x - 1, gridDim.x - 1);
+  prep_part(p, blockIdx.x - 1, gridDim.x - 1);
 }
 
 __global__ void __launch_bounds__(256) quant_rows_kernel(PrepArgs p) {
@@ -314,22 +402,32 @@ size_t align_smem_bytes(int E) { return static_cast<size_t>(kAlignWarps * E + 64
 
 template <int GV>
 static cudaError_t launch_prologue_t(const AlignArgs& a, const PrepArgs& p, const GateArgs& g, int prep_ctas,
-                                     cudaStream_t s) {
+                                     int* chunk_counts, int nchunks, cudaStream_t s) {
   const size_t smem = align_smem_bytes(a.E);
-  cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(prologue_kernel<GV>),
-                                        static_cast<int>(align_smem_bytes(MOE_MAX_EXPERTS)));
+  const int max_smem = static_cast<int>(align_smem_bytes(MOE_MAX_EXPERTS));
+  cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(prologue_kernel<GV>), max_smem);
   if (err != cudaSuccess) return err;
-  return launch_kernel(prologue_kernel<GV>, dim3(1 + prep_ctas), dim3(kAlignThreads), smem, s, true, a, p, g);
+  const bool prep = p.kind != 0 || p.zero_words;
+  const int first_ctas = chunk_counts ? nchunks : 1 + (prep ? prep_ctas : 0);
+  err = launch_kernel(prologue_kernel<GV>, dim3(first_ctas), dim3(kAlignThreads), smem, s, true, a, p, g,
+                      chunk_counts, nchunks);
+  if (err != cudaSuccess || !chunk_counts) return err;
+  err = set_smem_limit_once(reinterpret_cast<const void*>(align_scatter_kernel), max_smem);
+  if (err != cudaSuccess) return err;
+  return launch_kernel(align_scatter_kernel, dim3(nchunks + (prep ? prep_ctas : 0)), dim3(kAlignThreads), smem, s,
+                       true, a, p, static_cast<const int*>(chunk_counts), nchunks);
 }
 
 cudaError_t launch_prologue(const AlignArgs& a, const PrepArgs& p, int prep_ctas, cudaStream_t s,
-                            const GateArgs* inline_gate) {
-  if (!inline_gate) return launch_prologue_t<0>(a, p, GateArgs{}, prep_ctas, s);
+                            const GateArgs* inline_gate, int* chunk_counts) {
+  const int nchunks = align_num_chunks(static_cast<long long>(a.M) * a.topk);
+  if (nchunks < 2 || inline_gate) chunk_counts = nullptr;  // one CTA aligns (and ranks) everything
+  if (!inline_gate) return launch_prologue_t<0>(a, p, GateArgs{}, prep_ctas, chunk_counts, nchunks, s);
   switch (gate_vpl(inline_gate->E)) {
-    case 1: return launch_prologue_t<1>(a, p, *inline_gate, prep_ctas, s);
-    case 2: return launch_prologue_t<2>(a, p, *inline_gate, prep_ctas, s);
-    case 4: return launch_prologue_t<4>(a, p, *inline_gate, prep_ctas, s);
-    case 8: return launch_prologue_t<8>(a, p, *inline_gate, prep_ctas, s);
+    case 1: return launch_prologue_t<1>(a, p, *inline_gate, prep_ctas, nullptr, 1, s);
+    case 2: return launch_prologue_t<2>(a, p, *inline_gate, prep_ctas, nullptr, 1, s);
+    case 4: return launch_prologue_t<4>(a, p, *inline_gate, prep_ctas, nullptr, 1, s);
+    case 8: return launch_prologue_t<8>(a, p, *inline_gate, prep_ctas, nullptr, 1, s);
   }
   return cudaErrorInvalidValue;  // the caller ranks more than 256 experts in its own launch
 }

@@ -69,7 +69,7 @@ struct PrefillArgs {
   const float* sx;       // INT8 GEMM1: per-token activation scale
   const float* sh;       // INT8 GEMM2: per-position scale of the requantised h
   const float* topk_w;   // GEMM2: routing weights per slot
-  void* out;             // GEMM1: h by position (fp16 FP8 / fp32 INT8); GEMM2: y fp32 by slot (weighted)
+  void* out;             // GEMM1: h by position (fp16 FP8 / fp32 INT8); GEMM2: y bf16 by slot (weighted)
   int out_ld;
   uint32_t* hmax;        // INT8 GEMM1: per-position max |h| (bits)
   DeviceStatus* status;
@@ -136,10 +136,26 @@ struct SkinnyArgs {
 };
 
 size_t align_smem_bytes(int E);
+
+// Alignment of more than kAlignChunkSlots slots runs split over consecutive
+// chunks of slots, one CTA each (at most kAlignMaxChunks), which needs a
+// workspace of kAlignMaxChunks * E ints for the chunks' histograms.
+constexpr int kAlignChunkSlots = 4096;
+constexpr int kAlignMaxChunks = 64;
+__host__ __device__ inline int align_num_chunks(long long n) {
+  if (n <= kAlignChunkSlots) return 1;
+  const long long c = (n + kAlignChunkSlots - 1) / kAlignChunkSlots;
+  return c < kAlignMaxChunks ? static_cast<int>(c) : kAlignMaxChunks;
+}
+__host__ __device__ inline int align_chunk_slots(int n, int nchunks) { return (n + nchunks - 1) / nchunks; }
+
 // inline_gate (may be null; at most 256 experts): rank the tokens' experts in
 // the alignment CTA before aligning; a.topk_ids must then be inline_gate->ids.
+// chunk_counts (may be null: one CTA aligns): kAlignMaxChunks * E ints of
+// scratch, used when the slots need more than one chunk.  A split alignment is
+// two launches (the second one a single-purpose scatter kernel).
 cudaError_t launch_prologue(const AlignArgs& a, const PrepArgs& p, int prep_ctas, cudaStream_t s,
-                            const GateArgs* inline_gate = nullptr);
+                            const GateArgs* inline_gate = nullptr, int* chunk_counts = nullptr);
 cudaError_t launch_gate(const GateArgs& g, int num_sms, cudaStream_t s);
 
 // Masked layout: from masked_m [E] (clamped to [0, cap]) builds the token tiles of

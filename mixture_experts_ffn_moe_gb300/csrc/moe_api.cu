@@ -98,7 +98,8 @@ struct Layout {
   size_t cap = 0;
   size_t status = 0, sorted = 0, expert_ids = 0, offsets = 0, counts = 0, active = 0, scalars = 0,
          inv_pos = 0, xq = 0, sx = 0, h = 0, hmax = 0, hq = 0, sh = 0, ttiles = 0, act = 0, sa = 0, y = 0,
-         total = 0;
+         chunk_counts = 0, total = 0;
+  int align_chunks = 1;  // CTAs of the alignment (more than one: split over chunks of slots)
   bool a8 = false;
   size_t max_ttiles = 0;
   int tile_tokens = 0;
@@ -126,6 +127,8 @@ static Layout plan(int M, int H, int I, int E, int topk, int kind, unsigned flag
   L.active = take(static_cast<size_t>(E) * 4);
   L.scalars = take(16);
   L.inv_pos = take(static_cast<size_t>(M) * topk * 4);
+  L.align_chunks = align_num_chunks(static_cast<long long>(M) * topk);
+  if (L.align_chunks > 1) L.chunk_counts = take(static_cast<size_t>(kAlignMaxChunks) * E * 4);
   L.a8 = kind == MOE_WEIGHT_FP8 && (flags & MOE_ACT_FP8_1X128);
   L.tile_tokens = L.path == MOE_PATH_PREFILL ? kPrefillTileTokens : kDecodeBlock;
   L.max_ttiles = static_cast<size_t>(E) + static_cast<size_t>(M) * topk / L.tile_tokens + 1;
@@ -138,7 +141,7 @@ static Layout plan(int M, int H, int I, int E, int topk, int kind, unsigned flag
     L.ttiles = take(L.max_ttiles * 16);
     L.act = take(L.cap * H);
     L.sa = take(L.cap * (H / kQBlock) * 4);
-    L.y = take(static_cast<size_t>(M) * topk * H * 4);
+    L.y = take(static_cast<size_t>(M) * topk * H * 2);  // bf16 y
     L.total = o;
     return L;
   }
@@ -154,7 +157,7 @@ static Layout plan(int M, int H, int I, int E, int topk, int kind, unsigned flag
   }
   L.ttiles = take(L.max_ttiles * 16);
   if (L.path == MOE_PATH_PREFILL) L.act = take(L.cap * H * 2);
-  L.y = take(static_cast<size_t>(M) * topk * H * 4);
+  L.y = take(static_cast<size_t>(M) * topk * H * (L.path == MOE_PATH_PREFILL ? 2 : 4));  // bf16 / fp32 y
   L.total = o;
   return L;
 }
@@ -276,18 +279,21 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
   p.q = at<void>(ws, L.xq);
   p.scale = at<float>(ws, L.sx);
   if (kind == MOE_WEIGHT_INT8) { p.zero_words = at<uint32_t>(ws, L.hmax); p.n_zero = static_cast<int>(L.cap); }
-  // one 1024-thread prologue CTA per SM (its register count allows no second one): the
-  // alignment CTA and up to sms - 1 CTAs of the flat activation pass
-  const int prep_ctas = M < sms - 1 ? (M > 0 ? M : 1) : (sms > 1 ? sms - 1 : 1);
-  const StageHook hook = prof_begin_call(stream);
   const bool gate_inline = gate && M <= MOE_GATE_INLINE_TOKENS && gate->E <= 256;
+  // one 1024-thread prologue CTA per SM (its register count allows no second one): the
+  // alignment CTA(s) -- one when it also ranks the experts -- and the flat activation pass
+  const int align_ctas = gate_inline ? 1 : L.align_chunks;
+  const int free_sms = sms - align_ctas > 1 ? sms - align_ctas : 1;
+  const int prep_ctas = M < free_sms ? (M > 0 ? M : 1) : free_sms;
+  const StageHook hook = prof_begin_call(stream);
   cudaError_t err;
   if (gate && !gate_inline) {
     err = launch_gate(*gate, sms, stream);
     if (err != cudaSuccess) return cuda_fail(err, "gate launch");
     hook("gate", stream);
   }
-  err = launch_prologue(a, p, prep_ctas, stream, gate_inline ? gate : nullptr);
+  err = launch_prologue(a, p, prep_ctas, stream, gate_inline ? gate : nullptr,
+                        L.align_chunks > 1 ? at<int>(ws, L.chunk_counts) : nullptr);
   if (err != cudaSuccess) return cuda_fail(err, "prologue launch");
   hook(gate_inline ? "prologue_gate_align_prep" : "prologue_align_prep", stream);
 
@@ -379,6 +385,8 @@ static moe_status_t masked_impl(int kind, const void* x, const int32_t* masked_m
   if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(w13) % 16 ||
       reinterpret_cast<uintptr_t>(w2) % 16 || reinterpret_cast<uintptr_t>(out) % 2)
     return fail(MOE_ERR_INVALID_ARG, "x, w13 and w2 must be 16-byte aligned, out 2-byte aligned");
+  if (tc && reinterpret_cast<uintptr_t>(out) % 16)  // the tcgen05 epilogue writes 16-byte row pieces
+    return fail(MOE_ERR_INVALID_ARG, "out must be 16-byte aligned with MOE_PATH_PREFILL");
   const MaskedLayout L = plan_masked(E, cap, H, I);
   if (!ws) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
   if (reinterpret_cast<uintptr_t>(ws) % 256) return fail(MOE_ERR_WORKSPACE, "workspace must be 256-byte aligned");
@@ -597,6 +605,34 @@ moe_status_t moe_read_status(const void* workspace, int32_t status_out[2], moe_s
   status_out[1] = host.flags;
   if (host.flags & 1) return fail(MOE_ERR_TIMEOUT, "a bounded device wait gave up");
   if (host.bad_ids) return fail(MOE_ERR_BAD_IDS, "topk_ids outside [0, E)");
+  return MOE_OK;
+}
+
+moe_status_t moe_read_routing(const void* workspace, int M, int H, int I, int E, int topk, int weight_kind,
+                              unsigned flags, int* block_size, int32_t* sorted_ids, int32_t* expert_ids,
+                              int32_t* num_tokens_post_padded, int32_t* expert_offsets, moe_stream_t stream) {
+  g_last_error.clear();
+  if (M <= 0 || H <= 0 || I <= 0 || E <= 0 || topk <= 0 || E > MOE_MAX_EXPERTS || topk > 32 ||
+      !known_kind(weight_kind) || !known_flags(weight_kind, flags) ||
+      static_cast<long long>(M) * topk > (1LL << 30) || static_cast<long long>(M) * H > (1LL << 40))
+    return fail(MOE_ERR_INVALID_ARG, "sizes, weight kind or flags do not describe a routed layer call");
+  const Layout L = plan(M, H, I, E, topk, weight_kind, flags);
+  if (block_size) *block_size = L.B;
+  if (!sorted_ids && !expert_ids && !num_tokens_post_padded && !expert_offsets) return MOE_OK;
+  if (!workspace) return fail(MOE_ERR_INVALID_ARG, "NULL workspace");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const char* ws = static_cast<const char*>(workspace);
+  struct { void* dst; size_t off, bytes; } copies[] = {
+      {sorted_ids, L.sorted, L.cap * 4},
+      {expert_ids, L.expert_ids, L.cap / L.B * 4},
+      {num_tokens_post_padded, L.scalars, 4},
+      {expert_offsets, L.offsets, (static_cast<size_t>(E) + 1) * 4},
+  };
+  for (const auto& c : copies) {
+    if (!c.dst) continue;
+    cudaError_t err = cudaMemcpyAsync(c.dst, ws + c.off, c.bytes, cudaMemcpyDeviceToDevice, s);
+    if (err != cudaSuccess) return cuda_fail(err, "moe_read_routing");
+  }
   return MOE_OK;
 }
 

@@ -13,7 +13,9 @@
 //    [C1, C2], and the epilogue computes SiLU(C1) * C2 (Xeon 6 / SGLang blog,
 //    section "MoE");
 //  * GEMM2: two consecutive 128-row blocks of W2, so every activation byte
-//    fetched feeds 256 output rows.
+//    fetched feeds 256 output rows; it writes each slot's row times its
+//    routing weight in bf16, and a separate pass sums every token's rows in
+//    slot order.
 // Orientation (measured per GEMM).  GEMM1, and GEMM2 with INT8 or INT4 weights, put
 // the tokens on the MMA's M = 128 side and both converted weight blocks,
 // adjacent in shared memory, on its N = 256 side: one MMA per K step instead
@@ -517,23 +519,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_ld32(lane_addr + c0, g);
           tmem_ld_wait();
           const int n = tl.n0 + c0;
-          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + static_cast<size_t>(slot) * p.out_ld + n);
-          uint2* dstb = reinterpret_cast<uint2*>(p.out_bf16 + static_cast<size_t>(slot) * p.out_ld + n);
+          __nv_bfloat16* yb = p.out_bf16 ? p.out_bf16 : static_cast<__nv_bfloat16*>(p.out);
+          uint4* dstb = reinterpret_cast<uint4*>(yb + static_cast<size_t>(slot) * p.out_ld + n);
 #pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            float4 sc = make_float4(wgt, wgt, wgt, wgt);
-            if constexpr (WK == MOE_WEIGHT_INT8) {
-              const float4 cs = __ldg(reinterpret_cast<const float4*>(chs + n) + v);
-              sc = make_float4(wgt * cs.x, wgt * cs.y, wgt * cs.z, wgt * cs.w);
+          for (int v = 0; v < 4; ++v) {  // 8 columns, one 16-byte store
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int q = 2 * v + h;
+              float4 sc = make_float4(wgt, wgt, wgt, wgt);
+              if constexpr (WK == MOE_WEIGHT_INT8) {
+                const float4 cs = __ldg(reinterpret_cast<const float4*>(chs + n) + q);
+                sc = make_float4(wgt * cs.x, wgt * cs.y, wgt * cs.z, wgt * cs.w);
+              }
+              const __nv_bfloat162 lo = __floats2bfloat162_rn(__uint_as_float(g[4 * q]) * sc.x,
+                                                              __uint_as_float(g[4 * q + 1]) * sc.y);
+              const __nv_bfloat162 hi = __floats2bfloat162_rn(__uint_as_float(g[4 * q + 2]) * sc.z,
+                                                              __uint_as_float(g[4 * q + 3]) * sc.w);
+              w[2 * h] = *reinterpret_cast<const uint32_t*>(&lo);
+              w[2 * h + 1] = *reinterpret_cast<const uint32_t*>(&hi);
             }
-            const float4 r = make_float4(__uint_as_float(g[4 * v]) * sc.x, __uint_as_float(g[4 * v + 1]) * sc.y,
-                                         __uint_as_float(g[4 * v + 2]) * sc.z, __uint_as_float(g[4 * v + 3]) * sc.w);
-            if (live && p.out_bf16) {
-              const __nv_bfloat162 lo = __floats2bfloat162_rn(r.x, r.y), hi = __floats2bfloat162_rn(r.z, r.w);
-              dstb[v] = make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
-            } else if (live) {
-              dst[v] = r;
-            }
+            if (live) dstb[v] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
       } else {
@@ -579,7 +585,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int slot = __ldg(p.sorted_ids + pos);
                 float s = __ldg(p.topk_w + slot);
                 if constexpr (WK == MOE_WEIGHT_INT8) s *= __ldg(p.sh + pos) * sw;
-                reinterpret_cast<float*>(p.out)[static_cast<size_t>(slot) * p.out_ld + n] = __uint_as_float(g[j]) * s;
+                static_cast<__nv_bfloat16*>(p.out)[static_cast<size_t>(slot) * p.out_ld + n] =
+                    __float2bfloat16_rn(__uint_as_float(g[j]) * s);
               }
             }
           }
@@ -809,7 +816,7 @@ cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cud
   if (err != cudaSuccess) return err;
   hook("prefill_gemm2", s);
   if (P.out_direct) return cudaSuccess;  // masked layout: GEMM2 wrote the output rows
-  err = launch_combine(P.y, P.inv_pos, P.M, P.topk, P.H, P.out, num_sms, s);
+  err = launch_combine(reinterpret_cast<const __nv_bfloat16*>(P.y), P.inv_pos, P.M, P.topk, P.H, P.out, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("combine", s);
   return cudaSuccess;

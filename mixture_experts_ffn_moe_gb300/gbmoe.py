@@ -63,6 +63,7 @@ _SIGS = {
     "fused_moe_masked": (_i, [_i] + [_vp] * 6 + [_i] * 4 + [_u, _vp, _vp, _sz, _vp]),
     "fused_moe_fp8_static_scratch": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp]),
     "moe_read_status": (_i, [_vp, _vp, _vp]),
+    "moe_read_routing": (_i, [_vp] + [_i] * 6 + [_u] + [_vp] * 6),
     "moe_selftest_wait_timeout": (_i, [_vp, ctypes.c_longlong, _vp, _vp]),
     "moe_profile_enable": (_i, [_i]),
     "moe_profile_read": (_i, [_vp, _vp, _i, _vp, _vp]),
@@ -367,6 +368,28 @@ def moe_read_status(workspace: torch.Tensor):
     buf = (ctypes.c_int32 * 2)()
     st = load().moe_read_status(_ptr(workspace), ctypes.cast(buf, ctypes.c_void_p), _stream(workspace))
     return int(buf[0]), int(buf[1]), int(st)
+
+
+def moe_read_routing(workspace: torch.Tensor, M, H, I, E, topk, weight_kind, flags=MOE_PATH_AUTO):
+    """The alignment a routed fused call on `workspace` used, with the same sizes and flags.
+
+    Returns (block_size, sorted_ids, expert_ids, num_tokens_post_padded, expert_offsets) as
+    moe_align_block_size would give them for that block size (see include/gbmoe.h).
+    """
+    L = load()
+    bs = ctypes.c_int(0)
+    _check(L.moe_read_routing(None, M, H, I, E, topk, weight_kind, flags, ctypes.byref(bs), None, None, None, None,
+                              None), "moe_read_routing")
+    B = bs.value
+    cap = moe_align_max_padded(M, topk, E, B)
+    dev = workspace.device
+    sorted_ids = torch.empty(cap, dtype=torch.int32, device=dev)
+    expert_ids = torch.empty(cap // B, dtype=torch.int32, device=dev)
+    npp = torch.empty(1, dtype=torch.int32, device=dev)
+    offs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    _check(L.moe_read_routing(_ptr(workspace), M, H, I, E, topk, weight_kind, flags, None, _ptr(sorted_ids),
+                              _ptr(expert_ids), _ptr(npp), _ptr(offs), _stream(workspace)), "moe_read_routing")
+    return B, sorted_ids, expert_ids, npp, offs
 
 
 def moe_selftest_wait_timeout(workspace: torch.Tensor, limit_cycles: int = 2_000_000) -> torch.Tensor:

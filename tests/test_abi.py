@@ -176,6 +176,10 @@ def test_masked_host_checks(lib):
     assert call(null=True) == 1
     assert call() == 3                            # valid: fails on the workspace
     assert call(kind=2) == 3
+    odd = ctypes.c_void_p(18)  # an output 2-byte aligned only: fine for the weight-streaming kernels
+    assert lib.fused_moe_masked(0, p, p, p, p, p, p, 8, 16, 256, 128, 0, odd, p, 0, None) == 3
+    assert lib.fused_moe_masked(0, p, p, p, p, p, p, 8, 16, 256, 128, gbmoe.MOE_PATH_PREFILL, odd, p, 0,
+                                None) == 1  # the tcgen05 epilogue stores 16-byte row pieces
     a = gbmoe.moe_workspace_size_masked(32, 128, 7168, 2048, gbmoe.MOE_WEIGHT_FP8)
     assert a > 32 * 128 * (7168 + 2048) * 2
     assert gbmoe.moe_workspace_size_masked(32, 128, 7168, 2048, gbmoe.MOE_WEIGHT_INT8) == 0
@@ -187,3 +191,20 @@ def test_selftest_host_checks(lib):
     assert lib.moe_selftest_wait_timeout(p, 10, p, None) == 1          # limit below 1000 cycles
     assert lib.moe_selftest_wait_timeout(p, 1 << 40, p, None) == 1     # above 2^31
     assert lib.moe_selftest_wait_timeout(ctypes.c_void_p(16), 10000, p, None) == 3  # misaligned workspace
+
+
+def test_read_routing_reports_the_block_size_without_a_device(lib):
+    bs = ctypes.c_int(0)
+    st = lib.moe_read_routing(None, 4, 7168, 2048, 257, 9, gbmoe.MOE_WEIGHT_FP8, gbmoe.MOE_PATH_AUTO,
+                              ctypes.byref(bs), None, None, None, None, None)
+    assert st == gbmoe.MOE_OK and bs.value == 8
+    st = lib.moe_read_routing(None, 4, 7168, 2048, 257, 9, gbmoe.MOE_WEIGHT_FP8, gbmoe.MOE_PATH_PREFILL,
+                              ctypes.byref(bs), None, None, None, None, None)
+    assert st == gbmoe.MOE_OK and bs.value == 16
+    assert lib.moe_read_routing(None, 0, 7168, 2048, 257, 9, gbmoe.MOE_WEIGHT_FP8, 0, ctypes.byref(bs),
+                                None, None, None, None, None) == 1
+    assert lib.moe_read_routing(None, 4, 7168, 2048, 257, 9, gbmoe.MOE_WEIGHT_INT8, gbmoe.MOE_ACT_FP8_1X128,
+                                ctypes.byref(bs), None, None, None, None, None) == 1
+    out = (ctypes.c_int32 * 1)()
+    assert lib.moe_read_routing(None, 4, 7168, 2048, 257, 9, gbmoe.MOE_WEIGHT_FP8, 0, None, out, None, None,
+                                None, None) == 1  # MOE_ERR_INVALID_ARG: an output but no workspace
