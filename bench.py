@@ -178,7 +178,7 @@ def stage_work(shape, ids: torch.Tensor):
         "decode_gemm1": (int(active * (2 * I * H * wb + s13)) + M * H * 2 + valid * I * 2, f1),
         "decode_gemm2": (int(active * (H * I * wb + s2)) + valid * I * 2 + valid * H * 4, f2),
         "prefill_gemm1": (active * (2 * I * H + s13) + valid * H * ab + valid * I * ab, f1),
-        "prefill_gemm2": (active * (H * I + s2) + valid * I * ab + valid * H * 4, f2),
+        "prefill_gemm2": (active * (H * I + s2) + valid * I * ab + valid * H * 2, f2),  # y in bf16
     }
 
 

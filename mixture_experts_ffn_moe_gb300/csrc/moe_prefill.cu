@@ -182,10 +182,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = bars->tmem_base;
-  // The weight stream (raw producer, converters, MMA) needs only the tile list,
-  // written two kernels back; the activation producer and the epilogue read the
-  // predecessor's output (activations, h, h scales) and wait for it.
-  if (warp == WARP_ATMA || warp >= WARP_EPI0) pdl_wait();
+  // GEMM2's weight stream (raw producer, converters, MMA) needs only the tile list, written
+  // two kernels back; its activation producer and epilogue read GEMM1's output (h, h scales)
+  // and wait for it.  GEMM1 waits in every role: with the masked layout it directly follows
+  // the kernel that writes the tile list (and its trigger then comes after that wait).
+  if (GATED || warp == WARP_ATMA || warp >= WARP_EPI0) pdl_wait();
   pdl_trigger();
 
   if (warp == WARP_WTMA) {
