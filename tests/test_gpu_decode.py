@@ -188,3 +188,13 @@ def test_deepseek_r1_decode_sweep_batch64_uniform():
 
 def test_qwen3_int8_full_size_batch16():
     _full_size_check(synth.qwen3_235b(16), seed=14, rows=[0, 15], kind="int8")
+
+
+def test_qwen3_int8_full_size_batch1():
+    _full_size_check(synth.qwen3_235b(1), seed=15, rows=[0], kind="int8")
+
+
+@pytest.mark.parametrize("M", [2, 8, 16, 32])
+def test_deepseek_r1_decode_sweep_uniform(M):
+    # the decode batch sweep of DeepSeek-R1 shapes with uniform routing; first and last token checked
+    _full_size_check(synth.deepseek_r1(M, routing="uniform"), seed=20 + M, rows=[0, M - 1], kind="fp8")
