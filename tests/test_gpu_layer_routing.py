@@ -87,13 +87,20 @@ def test_split_alignment_counts_every_bad_id_once():
     assert_layer_close(out.float().cpu().numpy(), oracle.fused_moe_fp8(**d), "split alignment with bad ids")
 
 
-@pytest.mark.parametrize("kind,M", [("int8", 4096), ("int4", 700), ("int8", 16)])
-def test_layer_alignment_other_weight_kinds(kind, M):
+@pytest.mark.parametrize("kind,M,flags", [
+    ("int8", 4096, gbmoe.MOE_PATH_AUTO), ("int4", 700, gbmoe.MOE_PATH_AUTO), ("int8", 16, gbmoe.MOE_PATH_AUTO),
+    ("int4", 700, gbmoe.MOE_PATH_DECODE),  # the weight-streaming kernels behind a split alignment
+])
+def test_layer_alignment_other_weight_kinds(kind, M, flags):
     E, topk, H, I = 128, 8, 256, 128
     shape = synth.LayerShape("k", M, H, I, E, topk, kind, "softmax")
-    d = to_device(synth.make_layer(shape, seed=M))
+    dh = synth.make_layer(shape, seed=M)
+    d = to_device(dh)
     k = {"int8": gbmoe.MOE_WEIGHT_INT8, "int4": gbmoe.MOE_WEIGHT_INT4}[kind]
     fn = {"int8": gbmoe.fused_moe_int8, "int4": gbmoe.fused_moe_int4}[kind]
-    ws = gbmoe.alloc_workspace(M, H, I, E, topk, k)
-    fn(d["x"], d["topk_ids"], d["topk_weights"], d["w13"], d["w13_scale"], d["w2"], d["w2_scale"], workspace=ws)
-    _routing_matches_oracle(ws, d["topk_ids"].cpu().numpy(), M, H, I, E, topk, k, gbmoe.MOE_PATH_AUTO)
+    ws = gbmoe.alloc_workspace(M, H, I, E, topk, k, flags)
+    out = fn(d["x"], d["topk_ids"], d["topk_weights"], d["w13"], d["w13_scale"], d["w2"], d["w2_scale"],
+             flags=flags, workspace=ws)
+    _routing_matches_oracle(ws, d["topk_ids"].cpu().numpy(), M, H, I, E, topk, k, flags)
+    ref = (oracle.fused_moe_int8 if kind == "int8" else oracle.fused_moe_int4)(**dh)
+    assert_layer_close(out.float().cpu().numpy(), ref, f"{kind} M={M} flags {flags:#x}")
