@@ -490,8 +490,12 @@ static cudaError_t launch_skinny(const SkinnyArgs& a, const void* w, uint64_t w_
     (void)max_items;
     return launch_skinny_occ<WK, GATED, 2>(a, w, w_rows, num_sms, s);
   } else {
-    return max_items >= 3LL * num_sms ? launch_skinny_occ<WK, GATED, 3>(a, w, w_rows, num_sms, s)
-                                      : launch_skinny_occ<WK, GATED, 2>(a, w, w_rows, num_sms, s);
+    // GEMM2 keeps two CTAs per SM (the deeper rings) below 6 items per SM (measured: DeepSeek-R1 at
+    // one token 0.0959 -> 0.0918 ms, its 504 items no longer leaving 48 of 456 CTAs a second item;
+    // two tokens are faster at three CTAs per SM)
+    const long long occ3_min = GATED ? 3LL * num_sms : 6LL * num_sms;
+    return max_items >= occ3_min ? launch_skinny_occ<WK, GATED, 3>(a, w, w_rows, num_sms, s)
+                                 : launch_skinny_occ<WK, GATED, 2>(a, w, w_rows, num_sms, s);
   }
 }
 
