@@ -490,10 +490,11 @@ static cudaError_t launch_skinny(const SkinnyArgs& a, const void* w, uint64_t w_
     (void)max_items;
     return launch_skinny_occ<WK, GATED, 2>(a, w, w_rows, num_sms, s);
   } else {
-    // GEMM2 keeps two CTAs per SM (the deeper rings) below 6 items per SM (measured: DeepSeek-R1 at
-    // one token 0.0959 -> 0.0918 ms, its 504 items no longer leaving 48 of 456 CTAs a second item;
-    // two tokens are faster at three CTAs per SM)
-    const long long occ3_min = GATED ? 3LL * num_sms : 6LL * num_sms;
+    // Two CTAs per SM (the deeper rings) below 9 (GEMM1) or 6 (GEMM2) items per SM, measured: at
+    // DeepSeek-R1 shapes GEMM1 of two tokens 0.102 -> 0.092 ms and of four 0.172 -> 0.166 ms, GEMM2
+    // of one token 0.037 -> 0.031 ms (its 504 items no longer leave 48 of 456 CTAs a second
+    // item); GEMM2 of two tokens is faster at three CTAs per SM.
+    const long long occ3_min = GATED ? 9LL * num_sms : 6LL * num_sms;
     return max_items >= occ3_min ? launch_skinny_occ<WK, GATED, 3>(a, w, w_rows, num_sms, s)
                                  : launch_skinny_occ<WK, GATED, 2>(a, w, w_rows, num_sms, s);
   }
