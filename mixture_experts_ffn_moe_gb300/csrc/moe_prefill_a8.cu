@@ -88,8 +88,7 @@ struct Lay {
 constexpr long long kWaitLimit = 4000000000LL;    // ~2 s of SM clocks per wait
 
 struct Bars {
-  uint64_t w_full[MAX_STAGES];
-  uint64_t a_full[MAX_STAGES];
+  uint64_t op_full[MAX_STAGES];   // weight and activation stages of a K block landed (TMA, two producers)
   uint64_t st_empty[MAX_STAGES];  // the MMAs of a K block have read its weight and activation stages
   uint64_t s_full[S_STAGES];   // activation scale vector landed (TMA)
   uint64_t f_full[S_STAGES];   // factor vectors written (scale warp)
@@ -174,8 +173,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < W_STAGES; ++i) {
-      mbar_init(&bars->w_full[i], 1);
-      mbar_init(&bars->a_full[i], 1);
+      mbar_init(&bars->op_full[i], 2);  // both producers arrive: weights and activations of a K block
       mbar_init(&bars->st_empty[i], 1);
     }
     for (int i = 0; i < S_STAGES; ++i) {
@@ -226,15 +224,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int row0 = tl.e * p.rows_per_expert + tl.n0;
           for (int kc = 0; kc < KC; ++kc) {
             if (!(ok = mbar_wait(&bars->st_empty[ws], wph ^ 1, abort, p.status, kWaitLimit))) break;
-            mbar_arrive_expect_tx(&bars->w_full[ws], (tl.two ? 2 : 1) * W_TILE);
+            mbar_arrive_expect_tx(&bars->op_full[ws], (tl.two ? 2 : 1) * W_TILE);
             uint8_t* dst = sW + ws * 2 * W_TILE;
-            tma_load_2d(dst, &tmap_w, &bars->w_full[ws], kc * BK, row0);
-            if (tl.two) tma_load_2d(dst + W_TILE, &tmap_w, &bars->w_full[ws], kc * BK, row0 + p.second_rows);
+            tma_load_2d(dst, &tmap_w, &bars->op_full[ws], kc * BK, row0);
+            if (tl.two) tma_load_2d(dst + W_TILE, &tmap_w, &bars->op_full[ws], kc * BK, row0 + p.second_rows);
             ++seq;
             if (++ws == W_STAGES) { ws = 0; wph ^= 1; }
           }
         }
-        drain_ring(bars->w_full, W_STAGES, seq);  // never leave with copies in flight into shared memory
+        drain_ring(bars->op_full, W_STAGES, seq);  // never leave with copies in flight into shared memory
       }
     } else if (warp == WARP_ATMA) {
       // ---------------------------------------------------------------- activation + scale producer
@@ -247,10 +245,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const Tile tl = get_tile<GATED>(p, t);
           for (int kc = 0; kc < KC; ++kc) {
             if (!(ok = mbar_wait(&bars->st_empty[as], aph ^ 1, abort, p.status, kWaitLimit))) break;
-            mbar_arrive_expect_tx(&bars->a_full[as], tl.nmma * BK);
+            mbar_arrive_expect_tx(&bars->op_full[as], tl.nmma * BK);
             uint8_t* dst = sA + as * A_TILE;
             for (int r = 0; r < tl.nmma; r += 16)
-              tma_load_2d(dst + r * BK, &tmap_b, &bars->a_full[as], kc * BK, tl.pos0 + r);
+              tma_load_2d(dst + r * BK, &tmap_b, &bars->op_full[as], kc * BK, tl.pos0 + r);
             ++aseq;
             if (++as == A_STAGES) { as = 0; aph ^= 1; }
 
@@ -261,14 +259,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (++ss == S_STAGES) { ss = 0; sph ^= 1; }
           }
         }
-        drain_ring(bars->a_full, A_STAGES, aseq);
+        drain_ring(bars->op_full, A_STAGES, aseq);
         drain_ring(bars->s_full, S_STAGES, sseq);
       }
     } else if (warp == WARP_MMA) {
       // ---------------------------------------------------------------- MMA issuer
       if (lane == 0) {
         int ws = 0, as = 0, buf = 0;
-        uint32_t wph = 0, aph = 0;
+        uint32_t wph = 0;
         uint32_t eph[2] = {0, 0};
         bool ok = true;
         for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
@@ -276,8 +274,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t idesc = idesc_e4m3_f32(MAXN, BM);  // M = 128 tokens, N = 128 weight rows
           for (int kc = 0; kc < KC; ++kc) {
             if (!(ok = mbar_wait(&bars->p_empty[buf], eph[buf] ^ 1, abort, p.status, kWaitLimit))) break;
-            if (!(ok = mbar_wait(&bars->w_full[ws], wph, abort, p.status, kWaitLimit))) break;
-            if (!(ok = mbar_wait(&bars->a_full[as], aph, abort, p.status, kWaitLimit))) break;
+            if (!(ok = mbar_wait(&bars->op_full[ws], wph, abort, p.status, kWaitLimit))) break;
             tc_fence_after();
             const uint32_t d0 = tbase + static_cast<uint32_t>(buf * 2 * BM);
             const uint64_t ad = sw128_kmajor_desc(smem_addr(sA + as * A_TILE));           // tokens
@@ -293,7 +290,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             eph[buf] ^= 1;
             buf ^= 1;
             if (++ws == W_STAGES) { ws = 0; wph ^= 1; }
-            if (++as == A_STAGES) { as = 0; aph ^= 1; }
+            if (++as == A_STAGES) as = 0;
           }
         }
         // every issued MMA must finish before TMEM is released
