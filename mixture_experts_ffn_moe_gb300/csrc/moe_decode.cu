@@ -56,11 +56,13 @@ constexpr long long kWaitLimit = 4000000000LL;  // ~2 s of SM clocks per wait
 // OCC resident CTAs per SM (measured): 2 CTAs with an 80 KB ring each and B
 // fragments two K blocks ahead when there are few work items, 3 CTAs with
 // 48 KB rings and one block ahead otherwise -- more warps hide more latency.
-template <bool GATED, int OCC> struct Cfg {
+// INT4 (always 2 CTAs per SM) is bound by its nibble expansion, not by bytes in
+// flight, and runs fastest with 48 KB rings (measured against 64 and 80 KB).
+template <bool GATED, int OCC, bool I4 = false> struct Cfg {
   // One stage = 128 bytes of 128 weight rows (GATED: 64 gate rows and the matching
   // 64 up rows): one 128-wide K block of 8-bit codes or 256 K values of INT4.
   // Consumer warp w owns 16-row m-tile w of every stage.
-  static constexpr int RING_BYTES = OCC == 2 ? 80 * 1024 : 48 * 1024;
+  static constexpr int RING_BYTES = OCC == 2 && !I4 ? 80 * 1024 : 48 * 1024;
   static constexpr int BPF = OCC == 2 ? 2 : 1;             // stages of B fragments loaded ahead
   static constexpr int STAGE = NCW * 16 * KBLK;            // 16 KB of weight codes
   static constexpr int NS = RING_BYTES / STAGE;            // ring stages
@@ -159,7 +161,7 @@ __device__ __forceinline__ Item get_item(const SkinnyArgs& a, int it) {
 template <int WK, bool GATED, int OCC>
 __global__ void __launch_bounds__(NUM_THREADS, OCC)
     skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, SkinnyArgs a) {
-  using C = Cfg<GATED, OCC>;
+  using C = Cfg<GATED, OCC, WK == MOE_WEIGHT_INT4>;
   constexpr bool I4 = WK == MOE_WEIGHT_INT4;
   constexpr int KST = I4 ? 2 * KBLK : KBLK;  // K values per stage
   constexpr int XB = I4 ? 8 : 4;             // 16-byte B fragments per stage and lane
@@ -468,7 +470,7 @@ cudaError_t launch_requant_rows(const void* h, const uint32_t* hmax, const int32
 template <int WK, bool GATED, int OCC>
 static cudaError_t launch_skinny_occ(const SkinnyArgs& a, const void* w, uint64_t w_rows, int num_sms,
                                      cudaStream_t s) {
-  using C = dec::Cfg<GATED, OCC>;
+  using C = dec::Cfg<GATED, OCC, WK == MOE_WEIGHT_INT4>;
   CUtensorMap mw;
   // a row holds K bytes of 8-bit codes or K/2 bytes of INT4; a stage takes 128 of them
   const uint64_t row_bytes = WK == MOE_WEIGHT_INT4 ? a.K / 2 : a.K;
