@@ -17,7 +17,8 @@
 // consecutive chunks, one CTA each: the prologue's first CTAs write every
 // chunk's expert histogram to the workspace, and a second launch gives each
 // chunk's CTA the sum over the chunks before it as its starting cursors, so
-// the scatter is the same stable order as the single CTA's.
+// the scatter is the same stable order as the single CTA's; that launch's
+// other CTAs prepare the activations.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
