@@ -53,9 +53,10 @@ constexpr int KBLK = 128;                     // K per stage (one FP8 scale bloc
 
 constexpr long long kWaitLimit = 4000000000LL;  // ~2 s of SM clocks per wait
 
-// OCC resident CTAs per SM (measured): 2 CTAs with an 80 KB ring each and B
-// fragments two K blocks ahead when there are few work items, 3 CTAs with
-// 48 KB rings and one block ahead otherwise -- more warps hide more latency.
+// OCC resident CTAs per SM (measured): 2 CTAs with an 80 KB ring each when
+// there are few work items, 3 CTAs with 48 KB rings otherwise -- more warps
+// hide more latency.  B fragments are loaded one K block ahead (two ahead at
+// 2 CTAs per SM measured no faster, three slower).
 // INT4 (always 2 CTAs per SM) is bound by its nibble expansion, not by bytes in
 // flight, and runs fastest with 48 KB rings (measured against 64 and 80 KB).
 template <bool GATED, int OCC, bool I4 = false> struct Cfg {
@@ -63,7 +64,7 @@ template <bool GATED, int OCC, bool I4 = false> struct Cfg {
   // 64 up rows): one 128-wide K block of 8-bit codes or 256 K values of INT4.
   // Consumer warp w owns 16-row m-tile w of every stage.
   static constexpr int RING_BYTES = OCC == 2 && !I4 ? 80 * 1024 : 48 * 1024;
-  static constexpr int BPF = OCC == 2 ? 2 : 1;             // stages of B fragments loaded ahead
+  static constexpr int BPF = 1;                            // stages of B fragments loaded ahead
   static constexpr int STAGE = NCW * 16 * KBLK;            // 16 KB of weight codes
   static constexpr int NS = RING_BYTES / STAGE;            // ring stages
   static constexpr int OFF_RED = RING_BYTES;
