@@ -217,10 +217,17 @@ size_t moe_workspace_size(int M, int H, int I, int E, int topk, int weight_kind,
  *                 bytes of device memory, 256-byte aligned
  * H and I must be multiples of 128; 1 <= topk <= 32; M >= 0 (M == 0 is a
  * no-op).  A shared expert is passed as one more expert with a top-k column
- * of weight 1.0.  The products run on tensor cores with fp16 operands (the
- * E4M3 to fp16 expansion is exact; bf16 activations are rounded to fp16,
- * exact for magnitudes in [2^-14, 65504]) and fp32 accumulation; each
- * 128x128 block scale is applied once per 128-deep partial sum.
+ * of weight 1.0.  The products run on tensor cores with fp16 operands and
+ * fp32 accumulation; each 128x128 block scale is applied once per 128-deep
+ * partial sum.  Operands keep the range of their source type: the E4M3 to
+ * fp16 expansion is exact; each x row is stored as fp16 in a power-of-two
+ * frame of its own (its max |x| scaled into [2^14, 2^15), so every bf16 value
+ * within 2^-28 of the row's largest is exact); the intermediate h is stored
+ * as fp16 in a power-of-two frame per row (values within 2^-21 of the row's
+ * largest keep full fp16 precision); on the tcgen05 path the block scales
+ * are folded into the fp16 weights relative to a power of two per 128-row
+ * block.  The frames are taken back in fp32, so no finite input overflows an
+ * fp16 operand.
  * With MOE_ACT_FP8_1X128 in flags, x is quantised as moe_quant_act_fp8 does,
  * and so is each intermediate row h (fp32, per 128 columns of I) of a
  * (token, expert) pair before the down projection; the products are E4M3 x
@@ -262,8 +269,9 @@ moe_status_t fused_moe_int8(const void* x_bf16, const int32_t* topk_ids, const f
  *   w13_scale  fp32 [E, 2I, H/128]  W13[e,n,k] = q * w13_scale[e, n, k/128]
  *   w2         uint8 [E, H, I/2],   w2_scale fp32 [E, H, I/128]
  * other arguments as for fused_moe_fp8.  Activations enter the products at
- * their bf16 values (rounded to fp16, as on the FP8 weight-only path) and
- * each 128-deep partial sum is scaled by its row's group scale in fp32.
+ * their bf16 values (in fp16 power-of-two frames, as on the FP8 weight-only
+ * path) and each 128-deep partial sum is scaled by its row's group scale in
+ * fp32.
  * H and I must be multiples of 128.  Paths as for fused_moe_fp8 (the
  * weight-streaming kernels up to MOE_MAX_DECODE_TOKENS tokens, the tcgen05
  * grouped GEMMs above; MOE_PATH_DECODE is accepted at any M for INT4);

@@ -192,46 +192,23 @@ __global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(AlignArgs 
   align_core<true>(a, blockIdx.x * S, min(n, (blockIdx.x + 1) * S), chunk_counts, blockIdx.x, nchunks);
 }
 
-// Activation preparation.  The element-wise kinds run as one flat pass over
-// the [M, H] matrix (H is a multiple of 128, so rows never split a vector or a
+// Activation preparation.  The row-wise kinds take one row at a time (its max
+// |x| decides the row's scale); the FP8 kind runs as one flat pass over the
+// [M, H] matrix (H is a multiple of 128, so rows never split a vector or a
 // group); every thread keeps kPrepBatch 16-byte loads in flight.
-//   kind 1: x bf16 -> fp16 (RN)               (FP8 weight-only path)
-//   kind 2: x bf16 -> int8 codes + fp32 scale per row (DA8W8 path), a CTA or a
-//           warp per row; codes stored as fp16 (exact) or int8
+//   kind 1: x bf16 -> fp16 x * 2^-e with the row's max |x| * 2^-e in [2^14, 2^15),
+//           scale[r] = 2^e (FP8 weight-only path)
+//   kind 2: x bf16 -> int8 codes + fp32 scale per row (DA8W8 path); codes stored
+//           as fp16 (exact) or int8
 //   kind 3: x bf16 -> E4M3 codes + one fp32 scale per 128 columns (FP8 A8 path)
-//   kind 4: x bf16 -> fp16 (RN), each group of 8 columns stored in the order
-//           0 4 1 5 2 6 3 7 (INT4 path: the order its weights expand in)
+//   kind 4: as kind 1, each group of 8 columns stored in the order 0 4 1 5 2 6 3 7
+//           (INT4 path: the order its weights expand in)
+// Kinds 1, 2 and 4 take a CTA per row when there are few rows and a warp per row
+// otherwise.
 constexpr int kPrepBatch = 4;
 
 __device__ __forceinline__ float2 bf2_lo_hi(uint32_t w) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
-}
-
-// kinds 1 and 4: 8 columns per 16-byte chunk; `first` / `stride` count threads
-template <bool INT4_ORDER>
-__device__ void prep_f16_flat(const PrepArgs& p, long long first, long long stride) {
-  const long long n = static_cast<long long>(p.M) * (p.H / 8);
-  const uint4* src = reinterpret_cast<const uint4*>(p.x);
-  uint4* dst = static_cast<uint4*>(p.q);
-  for (long long i0 = first; i0 < n; i0 += kPrepBatch * stride) {
-    uint4 v[kPrepBatch];
-#pragma unroll
-    for (int u = 0; u < kPrepBatch; ++u) {
-      const long long i = i0 + u * stride;
-      if (i < n) v[u] = ld_v4(src + i);
-    }
-#pragma unroll
-    for (int u = 0; u < kPrepBatch; ++u) {
-      const long long i = i0 + u * stride;
-      if (i >= n) break;
-      const float2 f01 = bf2_lo_hi(v[u].x), f23 = bf2_lo_hi(v[u].y);
-      const float2 f45 = bf2_lo_hi(v[u].z), f67 = bf2_lo_hi(v[u].w);
-      dst[i] = INT4_ORDER ? make_uint4(pack_half2(f01.x, f45.x), pack_half2(f01.y, f45.y), pack_half2(f23.x, f67.x),
-                                       pack_half2(f23.y, f67.y))
-                          : make_uint4(pack_half2(f01.x, f01.y), pack_half2(f23.x, f23.y), pack_half2(f45.x, f45.y),
-                                       pack_half2(f67.x, f67.y));
-    }
-  }
 }
 
 // kind 3: FP8 E4M3 codes in groups of 128 columns, s = amax / 448 (fp32, 1 for an
@@ -265,31 +242,58 @@ __device__ void prep_fp8_flat(const PrepArgs& p, long long first, long long stri
   }
 }
 
-// kind 2: s = max|x| / 127 over the row, codes RNE(x / s) clamped to +-127.
 __device__ __forceinline__ float absmax8(const uint4& v) {
   const float2 f01 = bf2_lo_hi(v.x), f23 = bf2_lo_hi(v.y), f45 = bf2_lo_hi(v.z), f67 = bf2_lo_hi(v.w);
   return fmaxf(fmaxf(fmaxf(fabsf(f01.x), fabsf(f01.y)), fmaxf(fabsf(f23.x), fabsf(f23.y))),
                fmaxf(fmaxf(fabsf(f45.x), fabsf(f45.y)), fmaxf(fabsf(f67.x), fabsf(f67.y))));
 }
 
-template <typename QT>
-__device__ __forceinline__ void store_codes8(QT* dst, const uint4& v, float sc) {
+// Row-wise kinds: the factor a row's values are stored with, from its max |x|, and
+// the scale recorded for the row (kind 2: s = amax / 127, codes RNE(x / s) clamped
+// to +-127; kinds 1 and 4: the row's power-of-two frame).
+template <int KIND>
+struct RowQuant {
+  float store;   // kind 2: the divisor s; kinds 1, 4: the multiplier 2^-e
+  float record;  // scale[r]
+  __device__ __forceinline__ explicit RowQuant(float amax) {
+    if constexpr (KIND == 2) {
+      store = record = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 1.0f;
+    } else {
+      const int e = x_frame_exp(amax);
+      store = exp2i(-e);
+      record = exp2i(e);
+    }
+  }
+};
+
+// Stores the 8 values of one 16-byte chunk of a row.
+template <int KIND, typename QT>
+__device__ __forceinline__ void store_row8(QT* dst, const uint4& v, const RowQuant<KIND>& rq) {
   const float2 f01 = bf2_lo_hi(v.x), f23 = bf2_lo_hi(v.y), f45 = bf2_lo_hi(v.z), f67 = bf2_lo_hi(v.w);
-  const float e[8] = {f01.x, f01.y, f23.x, f23.y, f45.x, f45.y, f67.x, f67.y};
-  QT o[8];
+  if constexpr (KIND == 2) {
+    const float e[8] = {f01.x, f01.y, f23.x, f23.y, f45.x, f45.y, f67.x, f67.y};
+    QT o[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) o[j] = static_cast<QT>(quant_s8_rne(e[j], sc));
-  if constexpr (sizeof(QT) == 2) {
-    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(o);
+    for (int j = 0; j < 8; ++j) o[j] = static_cast<QT>(quant_s8_rne(e[j], rq.store));
+    if constexpr (sizeof(QT) == 2) {
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(o);
+    } else {
+      *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(o);
+    }
   } else {
-    *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(o);
+    const float m = rq.store;
+    *reinterpret_cast<uint4*>(dst) =
+        KIND == 4 ? make_uint4(pack_half2(f01.x * m, f45.x * m), pack_half2(f01.y * m, f45.y * m),
+                               pack_half2(f23.x * m, f67.x * m), pack_half2(f23.y * m, f67.y * m))
+                  : make_uint4(pack_half2(f01.x * m, f01.y * m), pack_half2(f23.x * m, f23.y * m),
+                               pack_half2(f45.x * m, f45.y * m), pack_half2(f67.x * m, f67.y * m));
   }
 }
 
 // Few rows per CTA: the whole CTA takes one row at a time (block-wide amax).
 // Many rows: one warp per row, each lane keeping kPrepBatch loads in flight.
-template <typename QT>
-__device__ void prep_int8_rows(const PrepArgs& p, int cta, int nctas) {
+template <int KIND, typename QT>
+__device__ void prep_rows_amax(const PrepArgs& p, int cta, int nctas) {
   __shared__ float red[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
   const int chunks = p.H / 8;
@@ -307,11 +311,10 @@ __device__ void prep_int8_rows(const PrepArgs& p, int cta, int nctas) {
         if (lane == 0) red[0] = v;
       }
       __syncthreads();
-      const float amax = red[0];
-      const float sc = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 1.0f;
-      if (tid == 0 && p.scale) p.scale[r] = sc;
+      const RowQuant<KIND> rq(red[0]);
+      if (tid == 0 && p.scale) p.scale[r] = rq.record;
       QT* qr = static_cast<QT*>(p.q) + static_cast<size_t>(r) * p.H;
-      for (int c = tid; c < chunks; c += blockDim.x) store_codes8<QT>(qr + 8 * c, ld_v4(xr + c), sc);
+      for (int c = tid; c < chunks; c += blockDim.x) store_row8<KIND, QT>(qr + 8 * c, ld_v4(xr + c), rq);
       __syncthreads();  // red is rewritten for the next row
     }
     return;
@@ -329,9 +332,8 @@ __device__ void prep_int8_rows(const PrepArgs& p, int cta, int nctas) {
       for (int u = 0; u < kPrepBatch; ++u)
         if (c0 + 32 * u < chunks) m = fmaxf(m, absmax8(v[u]));
     }
-    const float amax = warp_max(m);
-    const float sc = amax > 0.f ? __fdiv_rn(amax, 127.0f) : 1.0f;
-    if (lane == 0 && p.scale) p.scale[r] = sc;
+    const RowQuant<KIND> rq(warp_max(m));
+    if (lane == 0 && p.scale) p.scale[r] = rq.record;
     QT* qr = static_cast<QT*>(p.q) + r * p.H;
     for (int c0 = lane; c0 < chunks; c0 += 32 * kPrepBatch) {
       uint4 v[kPrepBatch];
@@ -340,7 +342,7 @@ __device__ void prep_int8_rows(const PrepArgs& p, int cta, int nctas) {
         if (c0 + 32 * u < chunks) v[u] = ld_v4(xr + c0 + 32 * u);
 #pragma unroll
       for (int u = 0; u < kPrepBatch; ++u)
-        if (c0 + 32 * u < chunks) store_codes8<QT>(qr + 8 * (c0 + 32 * u), v[u], sc);
+        if (c0 + 32 * u < chunks) store_row8<KIND, QT>(qr + 8 * (c0 + 32 * u), v[u], rq);
     }
   }
 }
@@ -351,15 +353,15 @@ __device__ void prep_rows(const PrepArgs& p, int cta, int nctas) {
   const long long tfirst = static_cast<long long>(cta) * blockDim.x + threadIdx.x;
   const long long tstride = static_cast<long long>(nctas) * blockDim.x;
   switch (p.kind) {
-    case 1: prep_f16_flat<false>(p, tfirst, tstride); break;
-    case 4: prep_f16_flat<true>(p, tfirst, tstride); break;
+    case 1: prep_rows_amax<1, __half>(p, cta, nctas); break;
+    case 4: prep_rows_amax<4, __half>(p, cta, nctas); break;
     case 3: prep_fp8_flat(p, tfirst >> 5, tstride >> 5); break;
-    case 2: prep_int8_rows<QT>(p, cta, nctas); break;
+    case 2: prep_rows_amax<2, QT>(p, cta, nctas); break;
     default: break;
   }
 }
 
-// The preparation pass and the clearing of the INT8 intermediate's amax words,
+// The preparation pass and the clearing of the intermediate's amax / frame words,
 // on `nctas` CTAs of which this is CTA `cta`.
 __device__ void prep_part(const PrepArgs& p, int cta, int nctas) {
   if (p.zero_words) {

@@ -137,6 +137,65 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// ---------------------------------------------------------------- power-of-two frames of fp16 operands
+// The weight-only paths multiply fp16 operands on the tensor cores, while x arrives as bf16 (the range of
+// fp32) and the intermediate h is an fp32 result.  Both are therefore stored as fp16 values v * 2^-e in a
+// frame 2^e chosen from their magnitude; the fp32 accumulators take the factor 2^e back.  Scaling by a power
+// of two is exact, so a value keeps the full fp16 precision whenever it lies within 2^-14 of the frame's
+// top binade, and the sums are the same as with unscaled operands wherever those were in range.
+//
+// x: one frame per row, with the row's max |x| in [2^14, 2^15).
+// h: one frame per (row, 32 columns) block, with the block's max |h| in [2^7, 2^15) and the exponent a
+// multiple of 8, so the blocks of a row mostly share one frame.  The row frame is the largest block
+// exponent; blocks stored lower are scaled down to it before they enter the down projection.
+// Exponents are kept biased by kExpBias (1..255); 0 marks an all-zero block.
+constexpr int kExpBias = 128;
+constexpr int kHBlock = 32;  // columns of h per frame block
+
+// floor(log2(a)) for finite a > 0, with fp32 subnormals counted as 2^-127.
+__device__ __forceinline__ int ilog2f(float a) { return ((__float_as_int(a) >> 23) & 0xff) - 127; }
+
+// Frame exponent of an x row with max |x| = amax: amax * 2^-e in [2^14, 2^15); 0 for a zero row.
+__device__ __forceinline__ int x_frame_exp(float amax) {
+  if (!(amax > 0.f)) return 0;
+  const int e = ilog2f(amax) - 14;
+  return e < -126 ? -126 : e;
+}
+
+// Biased frame exponent of an h block with max |h| = amax (0 for a zero block): the smallest multiple
+// of 8 with amax * 2^-e < 2^15, so amax * 2^-e lies in [2^7, 2^15).  (A coarser grid would let more
+// blocks share a frame but would also let the row frame -- the largest block exponent -- sit higher above
+// the row's values: with multiples of 8 every element within 2^-21 of its row's largest stays a normal
+// fp16 number.)
+__device__ __forceinline__ int h_frame_exp_biased(float amax) {
+  if (!(amax > 0.f)) return 0;
+  int e = ilog2f(amax) - 14;
+  e = e < -120 ? -120 : (e > 120 ? 120 : e);
+  e = (e + 127) / 8 * 8 - 120;  // round up to a multiple of 8 (e + 127 >= 7 keeps the division exact)
+  return e + kExpBias;
+}
+
+// 2^e as fp32 for -126 <= e <= 127 (0 below).
+__device__ __forceinline__ float exp2i(int e) { return e < -126 ? 0.f : __int_as_float((e + 127) << 23); }
+
+// fp16 pair (2^d, 2^d) for d <= 0; zero below 2^-24 (fp16 subnormals cover 2^-24 .. 2^-15).
+__device__ __forceinline__ __half2 exp2i_h2(int d) {
+  const uint16_t b = d >= -14 ? static_cast<uint16_t>((d + 15) << 10)
+                              : (d >= -24 ? static_cast<uint16_t>(1u << (d + 24)) : static_cast<uint16_t>(0));
+  const __half h = __ushort_as_half(b);
+  return __halves2half2(h, h);
+}
+
+// Multiplies the 8 fp16 values of v by the power of two f (exact unless they become subnormal).
+__device__ __forceinline__ void scale_h8(uint4& v, __half2 f) {
+  uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&w[i]), f);
+    w[i] = *reinterpret_cast<const uint32_t*>(&r);
+  }
+}
+
 // ---------------------------------------------------------------- memory
 
 // Streaming 16-byte load that does not allocate in L1 (weights are read once).

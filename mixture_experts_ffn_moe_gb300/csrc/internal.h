@@ -74,6 +74,11 @@ struct PrefillArgs {
   uint32_t* hmax;        // INT8 GEMM1: per-position max |h| (bits)
   DeviceStatus* status;
   __nv_bfloat16* out_bf16;  // GEMM2 (FP8): if set, bf16 output rows out_bf16[slot] (unweighted), not y
+  // power-of-two frames of the fp16 operands (FP8 and INT4 weights)
+  int x_by_pos;          // GEMM1: sx is indexed by position (masked layout), else by token
+  uint32_t* hexp;        // GEMM1: per position, the largest biased frame exponent of its h blocks (atomicMax)
+  uint8_t* hblk;         // GEMM1: [cap, I/32] biased frame exponent each 32-column block of h was stored with
+  const float* hsc;      // GEMM2: per position, 2^e of the row frame h was brought to
 };
 
 // Everything the path launchers need (host view of one call).
@@ -110,6 +115,13 @@ struct LayerPlan {
   // order) and GEMM2 writes bf16 rows straight to out_direct[sorted_ids[pos]], unweighted;
   // there is no combine
   __nv_bfloat16* out_direct;
+  // power-of-two frames of the fp16 operands (FP8 and INT4 weights): sx holds 2^e of every x row
+  // (by token, or by position on the masked layout); GEMM1 stores h blocks in their own frames
+  uint32_t* hexp;        // [2 cap] largest biased block exponent of each position, then 256 - the smallest
+                         // nonzero one (decode path); zeroed by the prologue
+  uint8_t* hblk;         // [cap, I/32] biased exponent of each 32-column block of h
+  float* hsc;            // [cap] tcgen05 path: 2^e of the row frame after the frame pass
+  bool x_by_pos;         // masked layout: sx by position
 };
 
 // One skinny grouped GEMM of the decode path (device view).
@@ -133,6 +145,11 @@ struct SkinnyArgs {
   DeviceStatus* status;
   int b_by_pos;          // GEMM1: activation rows by position (masked layout), not by token
   __nv_bfloat16* out_bf16;  // GEMM2: if set, bf16 output rows out_bf16[slot] (unweighted), not y
+  // power-of-two frames of the fp16 operands (FP8 and INT4 weights): GEMM1 takes x's row frames from sx
+  // and writes h's block frames; GEMM2 reads them
+  uint32_t* hexp;        // per position, the largest biased frame exponent of its h blocks
+  uint32_t* hexp_lo;     // per position, 256 - the smallest nonzero one (0: none)
+  uint8_t* hblk;         // [cap, I/32] biased frame exponent of each 32-column block of h
 };
 
 size_t align_smem_bytes(int E);
@@ -167,7 +184,10 @@ struct MaskedArgs {
   const __nv_bfloat16* x;   // [E * cap, H]
   const int32_t* masked_m;  // [E]
   int E, cap, H, kind, block, tile;
-  __half* xq;               // [E * round16(cap), H]
+  __half* xq;               // [E * round16(cap), H]  x * 2^-e per row (frame of the row's max |x|)
+  float* xs;                // [E * round16(cap)]     2^e of each position's row
+  uint32_t* zero_words;     // words to clear (the intermediate's frame words)
+  int n_zero;
   int32_t* sorted_ids;      // [E * round16(cap)]
   int4* ttiles;             // [E * ceil(cap / tile)]
   int32_t* num_ttiles;
@@ -190,6 +210,10 @@ bool encode_tmap_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const voi
                     uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
 cudaError_t launch_requant_rows(const void* h, const uint32_t* hmax, const int32_t* num_post, int cap, int I,
                                 __half* hq, float* sh, int num_sms, cudaStream_t s);
+// tcgen05 path, FP8 and INT4 weights: brings every position's h blocks to the row frame (the largest
+// block exponent) in place and writes hsc[pos] = 2^e of that frame.
+cudaError_t launch_h_frame(__half* h, const uint32_t* hexp, const uint8_t* hblk, const int32_t* num_post, int cap,
+                           int I, float* hsc, int num_sms, cudaStream_t s);
 size_t prefill_smem_bytes();
 
 // Records `msg` as the calling thread's last error (moe_last_error) and returns `st`.

@@ -12,8 +12,9 @@
 // for the decode kernels, 16 for the tcgen05 ones), so a token tile never reads
 // past the buffers and starts where the tcgen05 path's 16-row loads need it.
 // Every CTA computes the prefix sum itself (E <= 1024 counts, one scan); CTA 0
-// writes the tile list and sorted_ids[pos] = e * cap + i (the output row), the others copy
-// the real rows of x into position order, converted to fp16.
+// writes the tile list and sorted_ids[pos] = e * cap + i (the output row), the others clear
+// the intermediate's frame words and copy the real rows of x into position order, converted
+// to fp16 in a power-of-two frame per row.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -59,7 +60,11 @@ __global__ void __launch_bounds__(kMaskedThreads) masked_prologue_kernel(MaskedA
     return;
   }
   __syncthreads();
-  // activation rows, one warp per row; H is a multiple of 128, so a lane moves whole 8-column groups
+  // the intermediate's frame words of every position start at zero
+  for (int i = (blockIdx.x - 1) * kMaskedThreads + tid; i < m.n_zero; i += (gridDim.x - 1) * kMaskedThreads)
+    m.zero_words[i] = 0u;
+  // activation rows, one warp per row; H is a multiple of 128, so a lane moves whole 8-column groups.
+  // Each row is stored as fp16 x * 2^-e with its max |x| * 2^-e in [2^14, 2^15); xs[pos] = 2^e.
   const int warp = tid >> 5, lane = tid & 31;
   const int nw = kMaskedThreads / 32;
   const long long rows = static_cast<long long>(m.E) * m.cap;
@@ -68,17 +73,31 @@ __global__ void __launch_bounds__(kMaskedThreads) masked_prologue_kernel(MaskedA
     const int e = static_cast<int>(r / m.cap), i = static_cast<int>(r - static_cast<long long>(e) * m.cap);
     if (i >= cnt[e]) continue;
     const uint4* src = reinterpret_cast<const uint4*>(m.x + r * m.H);
-    uint4* dst = reinterpret_cast<uint4*>(m.xq + static_cast<size_t>(off[e] + i) * m.H);
+    const int pos = off[e] + i;
+    uint4* dst = reinterpret_cast<uint4*>(m.xq + static_cast<size_t>(pos) * m.H);
+    float amax = 0.f;
+    for (int g = lane; g < m.H / 8; g += 32) {
+      const uint4 raw = __ldg(src + g);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+    const int ex = x_frame_exp(warp_max(amax));
+    const float mul = exp2i(-ex);
+    if (lane == 0) m.xs[pos] = exp2i(ex);
     for (int g = lane; g < m.H / 8; g += 32) {
       const uint4 raw = __ldg(src + g);
       const float2 f01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.x));
       const float2 f23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.y));
       const float2 f45 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.z));
       const float2 f67 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw.w));
-      dst[g] = m.kind == 4 ? make_uint4(pack_half2(f01.x, f45.x), pack_half2(f01.y, f45.y),
-                                        pack_half2(f23.x, f67.x), pack_half2(f23.y, f67.y))
-                           : make_uint4(pack_half2(f01.x, f01.y), pack_half2(f23.x, f23.y),
-                                        pack_half2(f45.x, f45.y), pack_half2(f67.x, f67.y));
+      dst[g] = m.kind == 4 ? make_uint4(pack_half2(f01.x * mul, f45.x * mul), pack_half2(f01.y * mul, f45.y * mul),
+                                        pack_half2(f23.x * mul, f67.x * mul), pack_half2(f23.y * mul, f67.y * mul))
+                           : make_uint4(pack_half2(f01.x * mul, f01.y * mul), pack_half2(f23.x * mul, f23.y * mul),
+                                        pack_half2(f45.x * mul, f45.y * mul), pack_half2(f67.x * mul, f67.y * mul));
     }
   }
 }

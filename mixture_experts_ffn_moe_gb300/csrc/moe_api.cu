@@ -98,7 +98,7 @@ struct Layout {
   size_t cap = 0;
   size_t status = 0, sorted = 0, expert_ids = 0, offsets = 0, counts = 0, active = 0, scalars = 0,
          inv_pos = 0, xq = 0, sx = 0, h = 0, hmax = 0, hq = 0, sh = 0, ttiles = 0, act = 0, sa = 0, y = 0,
-         chunk_counts = 0, total = 0;
+         chunk_counts = 0, hexp = 0, hblk = 0, hsc = 0, total = 0;
   int align_chunks = 1;  // CTAs of the alignment (more than one: split over chunks of slots)
   bool a8 = false;
   size_t max_ttiles = 0;
@@ -148,7 +148,10 @@ static Layout plan(int M, int H, int I, int E, int topk, int kind, unsigned flag
   L.xq = take(static_cast<size_t>(M) * H * 2);
   L.sx = take(static_cast<size_t>(M) * 4);
   if (kind != MOE_WEIGHT_INT8) {
-    L.h = take(L.cap * I * 2);  // fp16 h (FP8, INT4)
+    L.h = take(L.cap * I * 2);  // fp16 h (FP8, INT4), each 32-column block in its power-of-two frame
+    L.hexp = take(L.cap * 8);   // largest and smallest block exponent per position (cleared by the prologue)
+    L.hblk = take(L.cap * (I / kHBlock));
+    if (L.path == MOE_PATH_PREFILL) L.hsc = take(L.cap * 4);
   } else {
     L.h = take(L.cap * I * 4);
     L.hmax = take(L.cap * 4);
@@ -278,7 +281,10 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
   p.kind = L.a8 ? 3 : kind == MOE_WEIGHT_FP8 ? 1 : kind == MOE_WEIGHT_INT4 ? 4 : 2;
   p.q = at<void>(ws, L.xq);
   p.scale = at<float>(ws, L.sx);
-  if (kind == MOE_WEIGHT_INT8) { p.zero_words = at<uint32_t>(ws, L.hmax); p.n_zero = static_cast<int>(L.cap); }
+  if (!L.a8) {  // the intermediate's amax (INT8) or frame exponent (FP8, INT4) per position starts at zero
+    p.zero_words = at<uint32_t>(ws, kind == MOE_WEIGHT_INT8 ? L.hmax : L.hexp);
+    p.n_zero = static_cast<int>(kind == MOE_WEIGHT_INT8 ? L.cap : 2 * L.cap);
+  }
   const bool gate_inline = gate && M <= MOE_GATE_INLINE_TOKENS && gate->E <= 256;
   // one 1024-thread prologue CTA per SM (its register count allows no second one): the
   // alignment CTA(s) -- one when it also ranks the experts -- and the flat activation pass
@@ -317,6 +323,10 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
     P.hmax = at<uint32_t>(ws, L.hmax);
     P.hq = at<__half>(ws, L.hq);
     P.sh = at<float>(ws, L.sh);
+  } else if (!L.a8) {
+    P.hexp = at<uint32_t>(ws, L.hexp);
+    P.hblk = at<uint8_t>(ws, L.hblk);
+    if (L.path == MOE_PATH_PREFILL) P.hsc = at<float>(ws, L.hsc);
   }
   P.y = at<float>(ws, L.y);
   P.out = static_cast<__nv_bfloat16*>(out);
@@ -346,7 +356,8 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
 
 // ------------------------------------------------------------------ masked layout
 struct MaskedLayout {
-  size_t status = 0, sorted = 0, ttiles = 0, scalars = 0, xq = 0, h = 0, total = 0;
+  size_t status = 0, sorted = 0, ttiles = 0, scalars = 0, xq = 0, xs = 0, h = 0, hexp = 0, hblk = 0, hsc = 0,
+         total = 0;
 };
 
 static MaskedLayout plan_masked(int E, int cap, int H, int I) {
@@ -360,7 +371,11 @@ static MaskedLayout plan_masked(int E, int cap, int H, int I) {
   L.ttiles = take(static_cast<size_t>(E) * ((cap + 7) / 8) * 16);  // decode tiles (8 rows) outnumber tcgen05 ones
   L.scalars = take(16);
   L.xq = take(positions * H * 2);
+  L.xs = take(positions * 4);
   L.h = take(positions * I * 2);
+  L.hexp = take(positions * 8);
+  L.hblk = take(positions * (I / kHBlock));
+  L.hsc = take(positions * 4);
   L.total = o;
   return L;
 }
@@ -402,6 +417,9 @@ static moe_status_t masked_impl(int kind, const void* x, const int32_t* masked_m
   m.block = tc ? kPrefillBlock : kDecodeBlock;
   m.tile = tc ? kPrefillTileTokens : kDecodeBlock;
   m.xq = at<__half>(ws, L.xq);
+  m.xs = at<float>(ws, L.xs);
+  m.zero_words = at<uint32_t>(ws, L.hexp);
+  m.n_zero = static_cast<int>(2 * static_cast<size_t>(E) * ((static_cast<size_t>(cap) + 15) / 16 * 16));
   m.sorted_ids = at<int32_t>(ws, L.sorted);
   m.ttiles = at<int4>(ws, L.ttiles);
   m.num_ttiles = at<int32_t>(ws, L.scalars);
@@ -416,6 +434,8 @@ static moe_status_t masked_impl(int kind, const void* x, const int32_t* masked_m
   P.M = E * cap; P.H = H; P.I = I; P.E = E; P.topk = 1;
   P.cap = static_cast<int>(static_cast<size_t>(E) * ((cap + 15) / 16 * 16));
   P.xq = m.xq;
+  P.sx = m.xs;
+  P.x_by_pos = true;
   P.act = m.xq;  // tcgen05 path: the activation rows, already in position order
   P.w13 = static_cast<const uint8_t*>(w13);
   P.s13 = s13;
@@ -426,6 +446,9 @@ static moe_status_t masked_impl(int kind, const void* x, const int32_t* masked_m
   P.ttiles = m.ttiles;
   P.num_ttiles = m.num_ttiles;
   P.h = at<void>(ws, L.h);
+  P.hexp = at<uint32_t>(ws, L.hexp);
+  P.hblk = at<uint8_t>(ws, L.hblk);
+  P.hsc = at<float>(ws, L.hsc);
   P.status = m.status;
   P.out_direct = static_cast<__nv_bfloat16*>(out);
   err = tc ? launch_prefill(P, kind, sms, stream, hook) : launch_decode(P, kind, sms, stream, hook);

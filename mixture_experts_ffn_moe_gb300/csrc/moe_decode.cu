@@ -23,6 +23,11 @@
 //  * GEMM2 (down projection) writes each (token, slot) row already times its
 //    routing weight, indexed by slot; a separate pass sums the top-k rows of
 //    every token in slot order (deterministic, no atomics).
+//  * FP8 and INT4: x rows arrive as fp16 in a power-of-two frame per row, and
+//    GEMM1 stores h as fp16 in a frame per (row, 32 columns); GEMM1 takes x's
+//    frames back in its epilogue, GEMM2 scales the rare blocks below their
+//    row's frame down to it and takes the row frame back in its epilogue, so
+//    no operand leaves fp16's range whatever the magnitudes.
 //
 // GB300 mapping.  A work item is (token tile of <= 8 slots of one expert) x
 // (a block of weight rows).  One producer warp streams the item's weight rows
@@ -37,6 +42,8 @@
 // directly.
 #include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -68,7 +75,8 @@ template <bool GATED, int OCC, bool I4 = false> struct Cfg {
   static constexpr int STAGE = NCW * 16 * KBLK;            // 16 KB of weight codes
   static constexpr int NS = RING_BYTES / STAGE;            // ring stages
   static constexpr int OFF_RED = RING_BYTES;
-  static constexpr int RED_BYTES = 4 * 4 * 32 * 4;         // up accumulators handed to the gate warps
+  static constexpr int RED_BYTES = 4 * 4 * 32 * 4 + 256;   // up accumulators handed to the gate warps, then the
+                                                           // h block maxima (4 x 8) and frame exponents (8)
   static constexpr int OFF_BAR = OFF_RED + RED_BYTES;
   static constexpr int SMEM = OFF_BAR + 2 * NS * 8 + 64 + 1024;
   static constexpr int ROWS = GATED ? 64 : 128;            // output rows per item
@@ -148,6 +156,8 @@ __device__ __forceinline__ void load_b32(uint4* xb, const __half* row, bool vali
 
 // Consumer-warps-only barrier (named barrier 1).
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory"); }
+// Gate-warps-only barrier of GEMM1's epilogue (named barrier 2, warps 0-3).
+__device__ __forceinline__ void gate_warps_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 struct Item {
   int e, pos0, cnt, rt;
@@ -268,6 +278,33 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
     if constexpr (I4) load_b32(xb + 4, brow + static_cast<size_t>(kb) * KST + KBLK + t * 32,
                                valid && kb * KST + KBLK < a.K);
   };
+  // GEMM2 on h (FP8, INT4): the lane's B values of a stage are one 32-column block of h per 128 K
+  // (FP8: block 4kb + t; INT4: blocks 8kb + t and 8kb + 4 + t), stored in that block's frame.
+  // The epilogue applies the row frame (the largest block exponent).  A row whose blocks do not all
+  // share it ("mixed": its smallest block exponent is lower) has those blocks scaled down here, after
+  // the stage's fragments have arrived; items whose rows each have one frame, the usual case, run a
+  // K loop without this step.
+  constexpr bool HF = !GATED && WK != MOE_WEIGHT_INT8;
+  const int hld = a.K / kHBlock;
+  // bits 0-7: biased row frame of this lane's B column (0: none, nothing to scale); bit 8: the row has
+  // blocks below its frame; bit 9: some lane of the warp has such a row
+  uint32_t fst = 0;
+  auto frame_fix = [&](uint4* xb, const Item& x, int kb) {
+    if constexpr (HF) {
+      const uint32_t eg = fst & 0xffu;
+      const int b0 = (I4 ? 8 * kb : 4 * kb) + t;
+      const uint8_t* hp = a.hblk + static_cast<size_t>(x.pos0 + g) * hld + b0;
+#pragma unroll
+      for (int grp = 0; grp < (I4 ? 2 : 1); ++grp) {  // INT4: the stage's two 128-wide groups in turn
+        const uint32_t b = (fst & 0x100u) && b0 + 4 * grp < hld ? __ldg(hp + 4 * grp) : 0u;
+        if (b != 0u && b != eg) {
+          const __half2 f = exp2i_h2(static_cast<int>(b) - static_cast<int>(eg));
+#pragma unroll
+          for (int i = 0; i < 4; ++i) scale_h8(xb[4 * grp + i], f);
+        }
+      }
+    }
+  };
   for (int it = it_begin; it < it_end; it += it_step) {
     const Item im = get_item(a, it);
     const int r0 = im.rt * C::ROWS;  // first output row of the item inside the expert
@@ -278,6 +315,28 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
     const float* sg_row = a.wscale + (static_cast<size_t>(im.e) * a.rows_per_expert + mrow + g) * kblocks;
     bool bvalid;
     const __half* brow = b_row(im, bvalid);
+    // GEMM2 on h: the B column's row frame and lowest block frame (consumed after the fragment prefetch
+    // below is in flight, so the two loads' latencies overlap)
+    uint32_t eg_ld = 0u, lo_ld = 0u;
+    if constexpr (HF) {
+      if (bvalid) {
+        eg_ld = __ldg(a.hexp + im.pos0 + g);
+        lo_ld = __ldg(a.hexp_lo + im.pos0 + g);
+      }
+    }
+    // GEMM1 (FP8, INT4): the x frames of this thread's two epilogue columns 2t, 2t+1 -- loaded here
+    // for FP8, in the epilogue for INT4 (whose registers are all taken by the K loop)
+    float sxc[2] = {0.f, 0.f};
+    auto load_sxc = [&]() {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int col = 2 * t + c, pos = im.pos0 + col;
+        if (col < im.cnt) sxc[c] = __ldg(a.sx + (a.b_by_pos ? pos : __ldg(a.sorted_ids + pos) / a.topk));
+      }
+    };
+    if constexpr (GATED && WK == MOE_WEIGHT_FP8) {
+      if (warp < 4) load_sxc();
+    }
     float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
     float scr[BPF];     // FP8 block scales of the prefetched stages
     float sgs[BPF][4];  // INT4: group scales of rows g, g+8 (group 0) and g, g+8 (group 1)
@@ -298,64 +357,80 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
         load_scales(d, d);
       }
     }
-    for (int kb0 = 0; kb0 < KB; kb0 += BPF) {
-#pragma unroll
-    for (int d = 0; d < BPF; ++d) {
-      const int kb = kb0 + d;
-      if (kb >= KB) break;
-      const uint4* xb = xr[d];
-      if (ok) ok = mbar_wait(&full[slot], phase, abort, a.status, kWaitLimit);
-      if (!ok) {
-      } else if constexpr (I4) {
-        // rows warp*16 + g and + 8 of the stage; 16-byte chunk c of row r sits at c ^ (r % 8);
-        // chunks 0-3 are group 0, chunks 4-7 group 1, and lane t takes chunk t of each
-        const uint8_t* rg = smem + slot * C::STAGE + (warp * 16 + g) * KBLK;
-        const uint8_t* rh = rg + 8 * KBLK;
-        const uint4 ra0 = lds_v4_once(rg + ((t ^ g) << 4));
-        const uint4 ra1 = lds_v4_once(rg + (((t + 4) ^ g) << 4));
-        const uint4 rb0 = lds_v4_once(rh + ((t ^ g) << 4));
-        const uint4 rb1 = lds_v4_once(rh + (((t + 4) ^ g) << 4));
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
-        float q0[4] = {0.f, 0.f, 0.f, 0.f}, q1[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_mma_int4(p0, p1, ra0, rb0, xb);
-        tile_mma_int4(q0, q1, ra1, rb1, xb + 4);  // zero codes and activations past K
-        const float* sc = sgs[d];
-        acc[0] = fmaf(sc[0], p0[0] + p1[0], fmaf(sc[2], q0[0] + q1[0], acc[0]));
-        acc[1] = fmaf(sc[0], p0[1] + p1[1], fmaf(sc[2], q0[1] + q1[1], acc[1]));
-        acc[2] = fmaf(sc[1], p0[2] + p1[2], fmaf(sc[3], q0[2] + q1[2], acc[2]));
-        acc[3] = fmaf(sc[1], p0[3] + p1[3], fmaf(sc[3], q0[3] + q1[3], acc[3]));
-      } else {
-        // rows warp*16 + g and + 8 of the stage; 16-byte chunk c of row r sits at c ^ (r % 8)
-        const uint8_t* rg = smem + slot * C::STAGE + (warp * 16 + g) * KBLK;
-        const uint8_t* rh = rg + 8 * KBLK;
-        const uint4 ra0 = lds_v4_once(rg + (((2 * t) ^ g) << 4));
-        const uint4 ra1 = lds_v4_once(rg + (((2 * t + 1) ^ g) << 4));
-        const uint4 rb0 = lds_v4_once(rh + (((2 * t) ^ g) << 4));
-        const uint4 rb1 = lds_v4_once(rh + (((2 * t + 1) ^ g) << 4));
-        // the fragments are in registers; order these generic-proxy reads before the
-        // TMA (async proxy) that will overwrite the slot once every warp has released it
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
-        if constexpr (WK == MOE_WEIGHT_FP8) {
-          float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
-          tile_mma_128<WK>(p0, p1, ra0, ra1, rb0, rb1, xb);
-          const float sc = scr[d];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) acc[i] = fmaf(sc, p0[i] + p1[i], acc[i]);
-        } else {
-          tile_mma_128<WK>(acc, acc1, ra0, ra1, rb0, rb1, xb);
-        }
-      }
-      if (kb + BPF < KB) {
-        load_stage(xr[d], brow, kb + BPF, bvalid);
-        load_scales(d, kb + BPF);
-      }
-      if (++slot == C::NS) { slot = 0; phase ^= 1; }
+    if constexpr (HF) {
+      fst = eg_ld | (lo_ld != 0u && 256u - lo_ld != eg_ld ? 0x100u : 0u);
+      if (__any_sync(0xffffffffu, fst & 0x100u)) fst |= 0x200u;
     }
+    // The K loop, compiled twice: with the frame fix for items where some lane's row of h has blocks
+    // below its frame, and without it (the usual case, which then pays nothing per stage).
+    auto k_loop = [&](auto fix_tag) {
+      constexpr bool FIX = decltype(fix_tag)::value;
+      for (int kb0 = 0; kb0 < KB; kb0 += BPF) {
+#pragma unroll
+      for (int d = 0; d < BPF; ++d) {
+        const int kb = kb0 + d;
+        if (kb >= KB) break;
+        uint4* xb = xr[d];
+        if (ok) ok = mbar_wait(&full[slot], phase, abort, a.status, kWaitLimit);
+        if constexpr (FIX) frame_fix(xb, im, kb);
+        if (!ok) {
+        } else if constexpr (I4) {
+          // rows warp*16 + g and + 8 of the stage; 16-byte chunk c of row r sits at c ^ (r % 8);
+          // chunks 0-3 are group 0, chunks 4-7 group 1, and lane t takes chunk t of each
+          const uint8_t* rg = smem + slot * C::STAGE + (warp * 16 + g) * KBLK;
+          const uint8_t* rh = rg + 8 * KBLK;
+          const uint4 ra0 = lds_v4_once(rg + ((t ^ g) << 4));
+          const uint4 ra1 = lds_v4_once(rg + (((t + 4) ^ g) << 4));
+          const uint4 rb0 = lds_v4_once(rh + ((t ^ g) << 4));
+          const uint4 rb1 = lds_v4_once(rh + (((t + 4) ^ g) << 4));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[slot]);
+          float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
+          float q0[4] = {0.f, 0.f, 0.f, 0.f}, q1[4] = {0.f, 0.f, 0.f, 0.f};
+          tile_mma_int4(p0, p1, ra0, rb0, xb);
+          tile_mma_int4(q0, q1, ra1, rb1, xb + 4);  // zero codes and activations past K
+          const float* sc = sgs[d];
+          acc[0] = fmaf(sc[0], p0[0] + p1[0], fmaf(sc[2], q0[0] + q1[0], acc[0]));
+          acc[1] = fmaf(sc[0], p0[1] + p1[1], fmaf(sc[2], q0[1] + q1[1], acc[1]));
+          acc[2] = fmaf(sc[1], p0[2] + p1[2], fmaf(sc[3], q0[2] + q1[2], acc[2]));
+          acc[3] = fmaf(sc[1], p0[3] + p1[3], fmaf(sc[3], q0[3] + q1[3], acc[3]));
+        } else {
+          // rows warp*16 + g and + 8 of the stage; 16-byte chunk c of row r sits at c ^ (r % 8)
+          const uint8_t* rg = smem + slot * C::STAGE + (warp * 16 + g) * KBLK;
+          const uint8_t* rh = rg + 8 * KBLK;
+          const uint4 ra0 = lds_v4_once(rg + (((2 * t) ^ g) << 4));
+          const uint4 ra1 = lds_v4_once(rg + (((2 * t + 1) ^ g) << 4));
+          const uint4 rb0 = lds_v4_once(rh + (((2 * t) ^ g) << 4));
+          const uint4 rb1 = lds_v4_once(rh + (((2 * t + 1) ^ g) << 4));
+          // the fragments are in registers; order these generic-proxy reads before the
+          // TMA (async proxy) that will overwrite the slot once every warp has released it
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[slot]);
+          if constexpr (WK == MOE_WEIGHT_FP8) {
+            float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
+            tile_mma_128<WK>(p0, p1, ra0, ra1, rb0, rb1, xb);
+            const float sc = scr[d];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] = fmaf(sc, p0[i] + p1[i], acc[i]);
+          } else {
+            tile_mma_128<WK>(acc, acc1, ra0, ra1, rb0, rb1, xb);
+          }
+        }
+        if (kb + BPF < KB) {
+          load_stage(xr[d], brow, kb + BPF, bvalid);
+          load_scales(d, kb + BPF);
+        }
+        if (++slot == C::NS) { slot = 0; phase ^= 1; }
+      }
+      }
+    };
+    if constexpr (HF) {
+      if (fst & 0x200u) k_loop(std::true_type{});
+      else k_loop(std::false_type{});
+    } else {
+      k_loop(std::false_type{});
     }
 
     if constexpr (WK == MOE_WEIGHT_INT8) {
@@ -370,25 +445,17 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
       }
       consumers_sync();
       if (warp < 4) {
-        float cmax[2] = {0.f, 0.f};
+        if constexpr (WK == MOE_WEIGHT_INT8) {
+          float cmax[2] = {0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float G = acc[i], U = red[(warp * 4 + i) * 32 + lane];
-          const int row = g + ((i & 2) ? 8 : 0);
-          const int col = 2 * t + (i & 1);
-          const bool valid = col < im.cnt;
-          const int pos = im.pos0 + col;
-          const int n = r0 + warp * 16 + row;
-          if constexpr (WK == MOE_WEIGHT_FP8) {
-            if (valid) reinterpret_cast<__half*>(a.out)[static_cast<size_t>(pos) * a.out_ld + n] =
-                __float2half_rn(silu_f32(G) * U);
-          } else if constexpr (WK == MOE_WEIGHT_INT4) {
-            // h feeds GEMM2's activations: stored in the INT4 K order
-            if (valid) reinterpret_cast<__half*>(a.out)[static_cast<size_t>(pos) * a.out_ld + int4_kperm(n)] =
-                __float2half_rn(silu_f32(G) * U);
-          } else {
+          for (int i = 0; i < 4; ++i) {
+            const float G = acc[i], U = red[(warp * 4 + i) * 32 + lane];
+            const int row = g + ((i & 2) ? 8 : 0);
+            const int col = 2 * t + (i & 1);
+            const int pos = im.pos0 + col;
+            const int n = r0 + warp * 16 + row;
             float h = 0.f;
-            if (valid) {
+            if (col < im.cnt) {
               const float sx = __ldg(a.sx + __ldg(a.sorted_ids + pos) / a.topk);
               const float gv = G * sx * __ldg(a.wscale + static_cast<size_t>(im.e) * a.rows_per_expert + n);
               const float uv =
@@ -398,8 +465,6 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
             }
             cmax[i & 1] = fmaxf(cmax[i & 1], fabsf(h));
           }
-        }
-        if constexpr (WK == MOE_WEIGHT_INT8) {
 #pragma unroll
           for (int c = 0; c < 2; ++c) {  // max over the 16 rows of each column (lanes with equal t)
             float v = cmax[c];
@@ -409,10 +474,68 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
             const int col = 2 * t + c;
             if (g == 0 && col < im.cnt) atomicMax(a.hmax + im.pos0 + col, __float_as_uint(v));
           }
+        } else {
+          // FP8 / INT4: h = SiLU(g) * u in fp32 from the x frames of the thread's two token columns, then
+          // stored in fp16 in the frame of its (position, 32-column block): gate warps 0-1 hold the item's
+          // first block, warps 2-3 its second, and the max over a pair's 32 rows decides the frame
+          float* hred = red + 4 * 4 * 32;                               // [4 warps][8 columns]
+          uint32_t* hexp_s = reinterpret_cast<uint32_t*>(hred + 32);    // [2 blocks][8 columns]
+          float hv[4], cmax[2] = {0.f, 0.f};
+          if constexpr (WK == MOE_WEIGHT_INT4) load_sxc();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float G = acc[i] * sxc[i & 1], U = red[(warp * 4 + i) * 32 + lane] * sxc[i & 1];
+            hv[i] = silu_f32(G) * U;
+            cmax[i & 1] = fmaxf(cmax[i & 1], fabsf(hv[i]));
+          }
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {  // max over the warp's 16 rows of each column (lanes with equal t)
+            float v = cmax[c];
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+            v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+            if (g == 0) hred[warp * 8 + 2 * t + c] = v;
+          }
+          gate_warps_sync();
+          if (warp == 0 && lane < 16) {  // one lane per (token column, block) decides the block's frame
+            const int col = lane & 7, blk = lane >> 3;
+            uint32_t eb = 0;
+            if (col < im.cnt) {
+              eb = static_cast<uint32_t>(h_frame_exp_biased(fmaxf(hred[16 * blk + col], hred[16 * blk + 8 + col])));
+              const int pos = im.pos0 + col;
+              a.hblk[static_cast<size_t>(pos) * (a.out_ld / kHBlock) + 2 * im.rt + blk] = static_cast<uint8_t>(eb);
+              if (eb) {
+                atomicMax(a.hexp + pos, eb);
+                atomicMax(a.hexp_lo + pos, 256u - eb);  // 256 - the smallest nonzero block exponent
+              }
+            }
+            hexp_s[lane] = eb;
+          }
+          gate_warps_sync();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int row = g + ((i & 2) ? 8 : 0);
+            const int col = 2 * t + (i & 1);
+            if (col >= im.cnt) continue;
+            const uint32_t eb = hexp_s[8 * (warp >> 1) + col];
+            const float mul = eb ? exp2i(kExpBias - static_cast<int>(eb)) : 1.f;
+            const int pos = im.pos0 + col;
+            const int n = r0 + warp * 16 + row;
+            // (INT4: h feeds GEMM2's activations, stored in the INT4 K order)
+            reinterpret_cast<__half*>(a.out)[static_cast<size_t>(pos) * a.out_ld +
+                                             (WK == MOE_WEIGHT_INT4 ? int4_kperm(n) : n)] = __float2half_rn(hv[i] * mul);
+          }
         }
       }
       consumers_sync();  // red is reused by the next item
     } else {
+      // h's row frames of the thread's columns 2t, 2t+1, from the lanes that hold them as B columns
+      float hf[2] = {1.f, 1.f};
+      if constexpr (HF) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          hf[c] = exp2i(static_cast<int>(__shfl_sync(0xffffffffu, fst & 0xffu, 4 * (2 * t + c))) - kExpBias);
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int row = g + ((i & 2) ? 8 : 0);
@@ -421,14 +544,15 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
           const int pos = im.pos0 + col;
           const int n = r0 + warp * 16 + row;
           const int slot = __ldg(a.sorted_ids + pos);
+          const float v = acc[i] * hf[i & 1];
           if (a.out_bf16) {  // masked layout: the output row itself, unweighted
-            a.out_bf16[static_cast<size_t>(slot) * a.out_ld + n] = __float2bfloat16_rn(acc[i]);
+            a.out_bf16[static_cast<size_t>(slot) * a.out_ld + n] = __float2bfloat16_rn(v);
             continue;
           }
           float wgt = __ldg(a.topk_w + slot);
           if constexpr (WK == MOE_WEIGHT_INT8)
             wgt *= __ldg(a.sh + pos) * __ldg(a.wscale + static_cast<size_t>(im.e) * a.rows_per_expert + n);
-          reinterpret_cast<float*>(a.out)[static_cast<size_t>(slot) * a.out_ld + n] = acc[i] * wgt;
+          reinterpret_cast<float*>(a.out)[static_cast<size_t>(slot) * a.out_ld + n] = v * wgt;
         }
       }
     }
@@ -524,6 +648,9 @@ cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cuda
   g1.hmax = P.hmax;
   g1.status = P.status;
   g1.b_by_pos = P.out_direct ? 1 : 0;
+  g1.hexp = P.hexp;
+  g1.hexp_lo = P.hexp + P.cap;
+  g1.hblk = P.hblk;
   const uint64_t rows1 = static_cast<uint64_t>(P.E) * 2 * P.I;
   cudaError_t err =
       weight_kind == MOE_WEIGHT_FP8
@@ -557,6 +684,9 @@ cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cuda
   g2.out_ld = P.H;
   g2.status = P.status;
   g2.out_bf16 = P.out_direct;
+  g2.hexp = P.hexp;
+  g2.hexp_lo = P.hexp + P.cap;
+  g2.hblk = P.hblk;
   const uint64_t rows2 = static_cast<uint64_t>(P.E) * P.H;
   err = weight_kind == MOE_WEIGHT_FP8
             ? launch_skinny<MOE_WEIGHT_FP8, false>(g2, P.w2, rows2, max_tiles * g2.n_rt, num_sms, s)

@@ -28,10 +28,16 @@
 // Weights stay FP8 E4M3 (or INT8) in HBM.  TMA brings raw 128x64-byte weight
 // tiles into shared memory; converter warps expand them to fp16 in registers
 // and write the tcgen05 operand (K-major, 128-byte swizzle).  For FP8 the
-// 128x128 block scale is folded into that conversion (the scale rounded to
-// fp16, one fp16 multiply per weight; an exact fp32 product when the scale
-// lies outside the fp16 normal range), because a tensor-core accumulator
-// cannot be rescaled per K block without a second TMEM pass.  INT8 weights convert
+// 128x128 block scale is folded into that conversion, because a tensor-core
+// accumulator cannot be rescaled per K block without a second TMEM pass: each
+// 128-row block has a power-of-two frame 2^P (its largest scale times 2^-P in
+// [2^6, 2^7)), the producer warp hands the converters every stage's scales
+// times 2^-P, a converter multiplies by that scale rounded to fp16 (an exact
+// fp32 product, rounded once, for scales far below the frame), and the
+// epilogue multiplies by 2^P.  So no scale overflows an fp16 weight.
+// Activations arrive as fp16 in power-of-two frames (x per row; h per row and
+// 32 columns, brought to one frame per row by h_frame_kernel between the
+// GEMMs); the epilogues take the frames back in fp32.  INT8 weights convert
 // exactly and the per-row x per-channel scales are applied in the epilogue.
 // INT4 weights (two per byte, one scale per row and 128 columns) arrive as
 // 32-byte rows per stage, expand to fp16 in the INT4 K order (pairs k0,k4 /
@@ -101,6 +107,7 @@ struct Bars {
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
+  float wsc[RAW_STAGES][2];  // FP8: each raw stage's two block scales, folded into the weight frames
 };
 static_assert(sizeof(Bars) <= 512, "barrier block too large");
 
@@ -124,6 +131,20 @@ __device__ __forceinline__ Tile get_tile(const PrefillArgs& p, int t) {
   r.nmma = (d.z + 15) & ~15;
   r.two = GATED || (r.n0 + BM < p.rows_per_expert);
   return r;
+}
+
+// FP8 weight frame of one 128-row block of an expert: the power of two P with the block's largest
+// scale * 2^-P in [2^6, 2^7), so that every scale folded into the fp16 weights as scale * 2^-P keeps
+// code * scale * 2^-P <= 448 * 2^7 < 65504.  The epilogue multiplies the accumulator by 2^P.
+// Warp-cooperative (every lane returns P); srow holds the block's kblocks scales.
+__device__ __forceinline__ int wblock_frame(const float* srow, int kblocks) {
+  const int lane = threadIdx.x & 31;
+  float m = 0.f;
+  for (int i = lane; i < kblocks; i += 32) m = fmaxf(m, fabsf(__ldg(srow + i)));
+  m = warp_max(m);
+  if (!(m > 0.f)) return 0;
+  const int P = ilog2f(m) - 6;
+  return P < -120 ? -120 : (P > 120 ? 120 : P);
 }
 
 template <int WK, bool GATED>
@@ -191,30 +212,67 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == WARP_WTMA) {
     // ---------------------------------------------------------------- raw weight producer
-    if (lane == 0) {
-      int rs = 0;
-      uint32_t rph = 0;
-      int last_par[RAW_STAGES];
+    // The whole warp walks the tiles; lane 0 waits for ring slots and issues the copies.  For FP8 the
+    // warp also finds each tile's two weight frames and hands the converters every stage's block
+    // scales already folded into them (through the stage's slot in wsc), so the converters, the
+    // bottleneck of this kernel, wait on no global load.
+    int rs = 0;
+    uint32_t rph = 0;
+    int last_par[RAW_STAGES];
 #pragma unroll
-      for (int i = 0; i < RAW_STAGES; ++i) last_par[i] = -1;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-        const Tile tl = get_tile<GATED>(p, t);
-        const int row0 = tl.e * p.rows_per_expert + tl.n0;
-        for (int kc = 0; kc < KC; ++kc) {
-          if (!(ok = mbar_wait(&bars->raw_empty[rs], rph ^ 1, abort, p.status, kWaitLimit))) break;
-          mbar_arrive_expect_tx(&bars->raw_full[rs], (tl.two ? 2 : 1) * RAWB);
-          uint8_t* dst = sRaw + rs * 2 * RAW_TILE;
-          const int kx = I4 ? kc * (BK / 2) : kc * BK;  // K offset in bytes of the stored rows
-          tma_load_2d(dst, &tmap_w, &bars->raw_full[rs], kx, row0);
-          if (tl.two) tma_load_2d(dst + RAW_TILE, &tmap_w, &bars->raw_full[rs], kx, row0 + second_rows);
+    for (int i = 0; i < RAW_STAGES; ++i) last_par[i] = -1;
+    bool ok = true;
+    const int kblocks = p.K / kQBlock, rblocks = p.rows_per_expert / kQBlock;
+    for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+      const Tile tl = get_tile<GATED>(p, t);
+      const int row0 = tl.e * p.rows_per_expert + tl.n0;
+      const float* srow[2] = {nullptr, nullptr};
+      float sv[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // K blocks lane and lane + 32 of each row block
+      float fr[2] = {1.f, 1.f};                    // 2^-P of each row block
+      if constexpr (WK == MOE_WEIGHT_FP8) {
+        const float* s0 = p.wscale + static_cast<size_t>(tl.e) * rblocks * kblocks;
+        srow[0] = s0 + static_cast<size_t>(tl.n0 / kQBlock) * kblocks;
+        srow[1] = s0 + static_cast<size_t>((tl.n0 + second_rows) / kQBlock) * kblocks;
 #pragma unroll
-          for (int i = 0; i < RAW_STAGES; ++i)
-            if (i == rs) last_par[i] = static_cast<int>(rph);
-          if (++rs == RAW_STAGES) { rs = 0; rph ^= 1; }
+        for (int a = 0; a < 2; ++a) {
+          if (a == 1 && !tl.two) break;
+          if (lane < kblocks) sv[a][0] = __ldg(srow[a] + lane);
+          if (lane + 32 < kblocks) sv[a][1] = __ldg(srow[a] + lane + 32);
+          fr[a] = exp2i(-wblock_frame(srow[a], kblocks));
         }
       }
-      // never leave with copies in flight into this CTA's shared memory
+      for (int kc = 0; kc < KC; ++kc) {
+        float f[2] = {0.f, 0.f};
+        if constexpr (WK == MOE_WEIGHT_FP8) {
+          const int kb = (kc * BK) / kQBlock;  // warp-uniform
+#pragma unroll
+          for (int a = 0; a < 2; ++a) {
+            const float v = __shfl_sync(0xffffffffu, kb < 32 ? sv[a][0] : sv[a][1], kb & 31);
+            f[a] = (kb < 64 ? v : (tl.two || a == 0 ? __ldg(srow[a] + kb) : 0.f)) * fr[a];
+          }
+        }
+        if (lane == 0) {
+          ok = mbar_wait(&bars->raw_empty[rs], rph ^ 1, abort, p.status, kWaitLimit);
+          if (ok) {
+            bars->wsc[rs][0] = f[0];
+            bars->wsc[rs][1] = f[1];
+            mbar_arrive_expect_tx(&bars->raw_full[rs], (tl.two ? 2 : 1) * RAWB);
+            uint8_t* dst = sRaw + rs * 2 * RAW_TILE;
+            const int kx = I4 ? kc * (BK / 2) : kc * BK;  // K offset in bytes of the stored rows
+            tma_load_2d(dst, &tmap_w, &bars->raw_full[rs], kx, row0);
+            if (tl.two) tma_load_2d(dst + RAW_TILE, &tmap_w, &bars->raw_full[rs], kx, row0 + second_rows);
+#pragma unroll
+            for (int i = 0; i < RAW_STAGES; ++i)
+              if (i == rs) last_par[i] = static_cast<int>(rph);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (++rs == RAW_STAGES) { rs = 0; rph ^= 1; }
+      }
+    }
+    // never leave with copies in flight into this CTA's shared memory
+    if (lane == 0) {
 #pragma unroll
       for (int i = 0; i < RAW_STAGES; ++i)
         if (last_par[i] >= 0) {
@@ -308,7 +366,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t rph = 0, cph = 0;
     bool ok = true;
     const int kblocks = p.K / kQBlock;
-    const int rblocks = p.rows_per_expert / kQBlock;
     for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
       const Tile tl = get_tile<GATED>(p, t);
       const int nchunks = (tl.two ? 2 : 1) * (I4 ? CHUNKS_PER_ACC_I4 : CHUNKS_PER_ACC);
@@ -339,9 +396,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float sc[2] = {1.f, 1.f};
         bool sc16[2] = {true, true};  // the scale is a normal fp16 number and q*s cannot overflow fp16
         if constexpr (WK == MOE_WEIGHT_FP8) {
-          const float* s = p.wscale + static_cast<size_t>(tl.e) * rblocks * kblocks + (kc * BK) / kQBlock;
-          sc[0] = __ldg(s + static_cast<size_t>(tl.n0 / kQBlock) * kblocks);
-          if (tl.two) sc[1] = __ldg(s + static_cast<size_t>((tl.n0 + second_rows) / kQBlock) * kblocks);
+          // the stage's block scales in the tile's weight frames, from the producer
+          sc[0] = bars->wsc[rs][0];
+          sc[1] = bars->wsc[rs][1];
 #pragma unroll
           for (int a = 0; a < 2; ++a) {
             const float m = fabsf(sc[a]);
@@ -413,7 +470,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   o[i] = *reinterpret_cast<uint32_t*>(&v2);
                 }
               } else {
-                // scales outside the fp16 normal range: exact fp32 product, rounded once
+                // scales below the fp16 normal range (blocks far below the frame): exact fp32 product,
+                // rounded once
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                   const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&o[i]));
@@ -455,57 +513,79 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const uint32_t lane_addr = tbase + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(buf * 2 * BM);
       const float* chs = p.wscale + static_cast<size_t>(tl.e) * p.rows_per_expert;  // INT8 channel scales
-      if constexpr (GATED) {
-        float sx = 1.f, hmax = 0.f;
-        if constexpr (WK == MOE_WEIGHT_INT8) sx = live ? __ldg(p.sx + __ldg(p.sorted_ids + pos) / p.topk) : 0.f;
+      if constexpr (GATED && WK == MOE_WEIGHT_INT8) {
+        float hmax = 0.f;
+        const float sx = live ? __ldg(p.sx + __ldg(p.sorted_ids + pos) / p.topk) : 0.f;
         for (int c0 = 0; c0 < BM; c0 += 32) {  // gate columns c0.., up columns BM + c0..
           uint32_t g[32], u[32];
           tmem_ld32(lane_addr + c0, g);
           tmem_ld32(lane_addr + BM + c0, u);
           tmem_ld_wait();
           const int n = tl.n0 + c0;
-          if constexpr (WK == MOE_WEIGHT_FP8 || I4) {
-            uint32_t hw[16];
-            if constexpr (I4) {  // h feeds GEMM2's activations: INT4 K order within each 8 columns
+          float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + static_cast<size_t>(pos) * p.out_ld + n);
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const int a = 8 * (j >> 2) + (j & 3), b = a + 4;
-                hw[j] = pack_half2(silu_f32(__uint_as_float(g[a])) * __uint_as_float(u[a]),
-                                   silu_f32(__uint_as_float(g[b])) * __uint_as_float(u[b]));
-              }
-            } else {
+          for (int v = 0; v < 8; ++v) {
+            const float4 sg = __ldg(reinterpret_cast<const float4*>(chs + n) + v);
+            const float4 su = __ldg(reinterpret_cast<const float4*>(chs + p.up_offset + n) + v);
+            float h[4];
+            const float sgv[4] = {sg.x, sg.y, sg.z, sg.w}, suv[4] = {su.x, su.y, su.z, su.w};
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float g0 = __uint_as_float(g[2 * j]), g1 = __uint_as_float(g[2 * j + 1]);
-              hw[j] = pack_half2(silu_f32(g0) * __uint_as_float(u[2 * j]), silu_f32(g1) * __uint_as_float(u[2 * j + 1]));
+            for (int i = 0; i < 4; ++i) {
+              const int j = 4 * v + i;
+              h[i] = silu_f32(__uint_as_float(g[j]) * sx * sgv[i]) * (__uint_as_float(u[j]) * sx * suv[i]);
+              hmax = fmaxf(hmax, fabsf(h[i]));
             }
-            }
-            if (live) {
-              uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(p.out) + static_cast<size_t>(pos) * p.out_ld + n);
-#pragma unroll
-              for (int v = 0; v < 4; ++v) dst[v] = make_uint4(hw[4 * v], hw[4 * v + 1], hw[4 * v + 2], hw[4 * v + 3]);
-            }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + static_cast<size_t>(pos) * p.out_ld + n);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const float4 sg = __ldg(reinterpret_cast<const float4*>(chs + n) + v);
-              const float4 su = __ldg(reinterpret_cast<const float4*>(chs + p.up_offset + n) + v);
-              float h[4];
-              const float sgv[4] = {sg.x, sg.y, sg.z, sg.w}, suv[4] = {su.x, su.y, su.z, su.w};
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int j = 4 * v + i;
-                h[i] = silu_f32(__uint_as_float(g[j]) * sx * sgv[i]) * (__uint_as_float(u[j]) * sx * suv[i]);
-                hmax = fmaxf(hmax, fabsf(h[i]));
-              }
-              if (live) dst[v] = make_float4(h[0], h[1], h[2], h[3]);
-            }
+            if (live) dst[v] = make_float4(h[0], h[1], h[2], h[3]);
           }
         }
-        if constexpr (WK == MOE_WEIGHT_INT8) {
-          if (live) atomicMax(p.hmax + pos, __float_as_uint(hmax));
+        if (live) atomicMax(p.hmax + pos, __float_as_uint(hmax));
+      } else if constexpr (GATED) {
+        // FP8 / INT4: h = SiLU(g) * u in fp32, with the token's x frame and (FP8) the gate and up blocks'
+        // weight frames taken back; each 32 columns (one frame block) stored in fp16 in their own frame.
+        float gm = 0.f, um = 0.f;
+        if (live) gm = um = __ldg(p.sx + (p.x_by_pos ? pos : __ldg(p.sorted_ids + pos) / p.topk));
+        if constexpr (WK == MOE_WEIGHT_FP8) {
+          const float* s0 = p.wscale + static_cast<size_t>(tl.e) * (p.rows_per_expert / kQBlock) * (p.K / kQBlock);
+          gm *= exp2i(wblock_frame(s0 + static_cast<size_t>(tl.n0 / kQBlock) * (p.K / kQBlock), p.K / kQBlock));
+          um *= exp2i(wblock_frame(s0 + static_cast<size_t>((tl.n0 + p.up_offset) / kQBlock) * (p.K / kQBlock),
+                                   p.K / kQBlock));
         }
+        uint32_t emax = 0;
+        for (int c0 = 0; c0 < BM; c0 += kHBlock) {  // gate columns c0.., up columns BM + c0..
+          uint32_t g[32], u[32];
+          tmem_ld32(lane_addr + c0, g);
+          tmem_ld32(lane_addr + BM + c0, u);
+          tmem_ld_wait();
+          float m = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {  // h in place of the gate values
+            const float h = silu_f32(__uint_as_float(g[j]) * gm) * (__uint_as_float(u[j]) * um);
+            g[j] = __float_as_uint(h);
+            m = fmaxf(m, fabsf(h));
+          }
+          const uint32_t eb = static_cast<uint32_t>(h_frame_exp_biased(m));
+          const float mb = eb ? exp2i(kExpBias - static_cast<int>(eb)) : 1.f;
+          emax = eb > emax ? eb : emax;
+          const int n = tl.n0 + c0;
+          uint32_t hw[16];
+          if constexpr (I4) {  // h feeds GEMM2's activations: INT4 K order within each 8 columns
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int a = 8 * (j >> 2) + (j & 3), b = a + 4;
+              hw[j] = pack_half2(__uint_as_float(g[a]) * mb, __uint_as_float(g[b]) * mb);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) hw[j] = pack_half2(__uint_as_float(g[2 * j]) * mb, __uint_as_float(g[2 * j + 1]) * mb);
+          }
+          if (live) {
+            p.hblk[static_cast<size_t>(pos) * (p.out_ld / kHBlock) + n / kHBlock] = static_cast<uint8_t>(eb);
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(p.out) + static_cast<size_t>(pos) * p.out_ld + n);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(hw[4 * v], hw[4 * v + 1], hw[4 * v + 2], hw[4 * v + 3]);
+          }
+        }
+        if (live && emax) atomicMax(p.hexp + pos, emax);
       } else if constexpr (TOKM) {
         int slot = 0;
         float wgt = 0.f;
@@ -513,6 +593,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           slot = __ldg(p.sorted_ids + pos);
           wgt = p.out_bf16 ? 1.f : __ldg(p.topk_w + slot);  // masked layout: unweighted bf16 rows
           if constexpr (WK == MOE_WEIGHT_INT8) wgt *= __ldg(p.sh + pos);
+          else wgt *= __ldg(p.hsc + pos);  // h's row frame
         }
 #pragma unroll 1
         for (int c0 = 0; c0 < (tl.two ? 2 * BM : BM); c0 += 32) {  // output rows n0 + c0..
@@ -544,51 +625,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       } else {
-        // weights on the M side: TMEM lane = output row, columns = tokens
+        // weights on the M side (FP8 only): TMEM lane = output row, columns = tokens
         const int row = tok;
-        if (p.out_bf16) {
-          // masked layout: the output rows themselves, unweighted
-#pragma unroll 1
-          for (int a = 0; a < 2; ++a) {
-            if (a == 1 && !tl.two) break;
-            const int n = tl.n0 + a * BM + row;
-            for (int c0 = 0; c0 < tl.nmma; c0 += 32) {
-              uint32_t g[32];
-              __syncwarp();
-              tmem_ld32(lane_addr + a * BM + c0, g);
-              tmem_ld_wait();
+        // the weight frames of the tile's two row blocks, taken back here with h's row frame
+        float wfm[2] = {1.f, 1.f};
+        {
+          const int kblocks = p.K / kQBlock;
+          const float* s0 = p.wscale + static_cast<size_t>(tl.e) * (p.rows_per_expert / kQBlock) * kblocks;
+          wfm[0] = exp2i(wblock_frame(s0 + static_cast<size_t>(tl.n0 / kQBlock) * kblocks, kblocks));
+          if (tl.two) wfm[1] = exp2i(wblock_frame(s0 + static_cast<size_t>(tl.n0 / kQBlock + 1) * kblocks, kblocks));
+        }
+        // each lane loads the output slot and factor (routing weight -- 1 on the masked layout, whose
+        // bf16 rows are unweighted -- times h's row frame) of columns lane, lane + 32, lane + 64,
+        // lane + 96 once per tile; the column loop takes them by shuffle
+        int cs[4];
+        float cf[4];
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int col = c0 + j;
-                if (col >= tl.cnt) continue;  // warp-uniform
-                const int slot = __ldg(p.sorted_ids + tl.pos0 + col);
-                p.out_bf16[static_cast<size_t>(slot) * p.out_ld + n] = __float2bfloat16_rn(__uint_as_float(g[j]));
-              }
-            }
+        for (int q = 0; q < 4; ++q) {
+          const int col = 32 * q + lane;
+          cs[q] = 0;
+          cf[q] = 0.f;
+          if (col < tl.cnt) {
+            const int pos = tl.pos0 + col;
+            cs[q] = __ldg(p.sorted_ids + pos);
+            cf[q] = (p.out_bf16 ? 1.f : __ldg(p.topk_w + cs[q])) * __ldg(p.hsc + pos);
           }
-        } else {
+        }
+        __nv_bfloat16* ob = p.out_bf16 ? p.out_bf16 : static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll 1
-          for (int a = 0; a < 2; ++a) {
-            if (a == 1 && !tl.two) break;
-            const int n = tl.n0 + a * BM + row;
-            float sw = 1.f;
-            if constexpr (WK == MOE_WEIGHT_INT8) sw = __ldg(p.wscale + static_cast<size_t>(tl.e) * p.rows_per_expert + n);
-            for (int c0 = 0; c0 < tl.nmma; c0 += 32) {
-              uint32_t g[32];
-              __syncwarp();
-              tmem_ld32(lane_addr + a * BM + c0, g);
-              tmem_ld_wait();
+        for (int a = 0; a < 2; ++a) {
+          if (a == 1 && !tl.two) break;
+          const int n = tl.n0 + a * BM + row;
+          for (int c0 = 0; c0 < tl.nmma; c0 += 32) {
+            uint32_t g[32];
+            __syncwarp();
+            tmem_ld32(lane_addr + a * BM + c0, g);
+            tmem_ld_wait();
+            const int q = c0 >> 5;
+            const int sl = q == 0 ? cs[0] : q == 1 ? cs[1] : q == 2 ? cs[2] : cs[3];
+            const float fl = (q == 0 ? cf[0] : q == 1 ? cf[1] : q == 2 ? cf[2] : cf[3]) * wfm[a];
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const int col = c0 + j;
-                if (col >= tl.cnt) continue;  // warp-uniform
-                const int pos = tl.pos0 + col;
-                const int slot = __ldg(p.sorted_ids + pos);
-                float s = __ldg(p.topk_w + slot);
-                if constexpr (WK == MOE_WEIGHT_INT8) s *= __ldg(p.sh + pos) * sw;
-                static_cast<__nv_bfloat16*>(p.out)[static_cast<size_t>(slot) * p.out_ld + n] =
-                    __float2bfloat16_rn(__uint_as_float(g[j]) * s);
-              }
+            for (int j = 0; j < 32; ++j) {
+              if (c0 + j >= tl.cnt) continue;  // warp-uniform
+              const int slot = __shfl_sync(0xffffffffu, sl, j);
+              const float f = __shfl_sync(0xffffffffu, fl, j);
+              ob[static_cast<size_t>(slot) * p.out_ld + n] = __float2bfloat16_rn(__uint_as_float(g[j]) * f);
             }
           }
         }
@@ -631,6 +712,46 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __half* __restri
     if (slot < n_slots) v = ld_v4(xq + static_cast<size_t>(slot / topk) * H + c * 8);
     *reinterpret_cast<uint4*>(act + static_cast<size_t>(pos) * H + c * 8) = v;
   }
+}
+
+// The intermediate's row frames (FP8 and INT4 weights on this path): GEMM1 stored every 32-column
+// block of h in its own power-of-two frame; the down projection needs one frame per row, the
+// largest.  Blocks stored lower are scaled down to it in place (rare: a block's frame exponent is
+// a multiple of 8, so the blocks of a row mostly share it), and hsc[pos] = 2^e of the row frame.
+// One warp per position, lanes over its blocks.
+__global__ void __launch_bounds__(256) h_frame_kernel(__half* __restrict__ h, const uint32_t* __restrict__ hexp,
+                                                      const uint8_t* __restrict__ hblk,
+                                                      const int32_t* __restrict__ num_post, int I,
+                                                      float* __restrict__ hsc) {
+  pdl_wait();
+  pdl_trigger();
+  const int rows = *num_post, nb = I / kHBlock, lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
+    const uint32_t ef = hexp[r];  // 0: no nonzero block (a padding row or an all-zero h)
+    if (lane == 0) hsc[r] = ef ? exp2i(static_cast<int>(ef) - kExpBias) : 1.f;
+    if (!ef) continue;
+    for (int b = lane; b < nb; b += 32) {
+      const uint32_t eb = hblk[static_cast<size_t>(r) * nb + b];
+      if (eb == 0u || eb == ef) continue;
+      const __half2 f = exp2i_h2(static_cast<int>(eb) - static_cast<int>(ef));
+      uint4* q = reinterpret_cast<uint4*>(h + static_cast<size_t>(r) * I + b * kHBlock);
+#pragma unroll
+      for (int i = 0; i < kHBlock / 8; ++i) {
+        uint4 v = q[i];
+        scale_h8(v, f);
+        q[i] = v;
+      }
+    }
+  }
+}
+
+cudaError_t launch_h_frame(__half* h, const uint32_t* hexp, const uint8_t* hblk, const int32_t* num_post, int cap,
+                           int I, float* hsc, int num_sms, cudaStream_t s) {
+  int grid = (cap + 7) / 8;
+  if (grid > num_sms * 4) grid = num_sms * 4;
+  if (grid < 1) grid = 1;
+  return launch_kernel(h_frame_kernel, dim3(grid), dim3(256), 0, s, true, h, hexp, hblk, num_post, I, hsc);
 }
 
 // out[t, n] = sum over k (in slot order) of y[t*topk + k, n] for the slots that were routed
@@ -779,6 +900,9 @@ cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cud
   g1.out_ld = P.I;
   g1.hmax = P.hmax;
   g1.status = P.status;
+  g1.x_by_pos = P.x_by_pos ? 1 : 0;
+  g1.hexp = P.hexp;
+  g1.hblk = P.hblk;
   const uint64_t rows1 = static_cast<uint64_t>(P.E) * 2 * P.I;
   err = weight_kind == MOE_WEIGHT_FP8 ? launch_gemm<MOE_WEIGHT_FP8, true>(g1, P.w13, rows1, P.act, P.cap, num_sms, s)
         : weight_kind == MOE_WEIGHT_INT4
@@ -792,6 +916,10 @@ cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cud
     if (err != cudaSuccess) return err;
     hook("requant_h", s);
     b2 = P.hq;
+  } else {
+    err = launch_h_frame(static_cast<__half*>(P.h), P.hexp, P.hblk, P.num_post, P.cap, P.I, P.hsc, num_sms, s);
+    if (err != cudaSuccess) return err;
+    hook("h_frame", s);
   }
   PrefillArgs g2{};
   g2.K = P.I;
@@ -804,6 +932,7 @@ cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cud
   g2.sorted_ids = P.sorted_ids;
   g2.topk = P.topk;
   g2.sh = P.sh;
+  g2.hsc = P.hsc;
   g2.topk_w = P.topk_w;
   g2.out = P.y;
   g2.out_ld = P.H;
