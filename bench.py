@@ -2,7 +2,12 @@
 
 A step is one call of the whole layer (routing alignment, activation
 preparation, gate/up GEMM with SiLU*mul, down projection and weighted
-combine) on one batch of synthetic, seeded input.  The default workload is a
+combine) on one batch of synthetic, seeded input.  After the default line's
+own measurements, the line's "also" object times every other configuration
+of the layer the same way (DeepSeek-R1 decode at 1 token and the 1..64-token
+sweep, the 2048- and 16,384-token prefill with bf16 and FP8 activations,
+Qwen3 INT8 at 1/16/256/4096 tokens), each with its clocks, routing histogram
+and a parity check of one token against the oracle (--no-also skips it).  The default workload is a
 DeepSeek-R1-shaped MoE decode layer: 4 tokens, hidden 7168, expert
 intermediate 2048, 256 routed experts top-8 (sigmoid scores, 8 groups / top-4
 groups) plus 1 shared expert, FP8 E4M3 weights with 128x128 block scales,
@@ -19,6 +24,7 @@ from __future__ import annotations
 
 import argparse
 import dataclasses
+import datetime
 import hashlib
 import json
 import os
@@ -152,6 +158,107 @@ def ncu_traffic(workload: str, kernel: str, a8: bool = False):
     return rec.get("dram_bytes_per_launch")
 
 
+def roofline_of(shape, ids, stages, n_calls, workload, peaks):
+    """Roofline of the dominant kernel of a call: its algorithmic bytes (or flops, above the ridge) over its
+    average per-kernel event time, against the measured peak."""
+    work = stage_work(shape, ids)
+    stage_avg = {name: ms / max(n_calls, 1) for name, ms in stages}
+    dominant = max((n for n in stage_avg if n in work), key=lambda n: stage_avg[n])
+    dbytes, dflops = work[dominant]
+    secs = stage_avg[dominant] * 1e-3
+    # Tensor peak of the kernel's operand type, burst figure: fp16 MMA runs at the measured dense
+    # bf16 rate; E4M3 x E4M3 at twice it (the nominal FP8:BF16 ratio, 4.5 : 2.25 PFLOP/s).
+    if shape.act == "fp8_1x128":
+        tpeak, tsrc = 2.0 * peaks["bf16_tflops"], peaks["source"] + " bf16 dense x 2 (nominal FP8:BF16 ratio)"
+    else:
+        tpeak, tsrc = peaks["bf16_tflops"], peaks["source"] + " bf16 dense (fp16 same rate)"
+    ridge = tpeak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    a8 = shape.act == "fp8_1x128"
+    if dflops / dbytes > ridge:
+        achieved = dflops / secs / 1e12
+        return {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
+                "frac": achieved / tpeak, "traffic": ncu_traffic(workload, dominant, a8),
+                "algorithmic_flops": dflops, "algorithmic_bytes": dbytes, "peak_source": tsrc}
+    achieved = dbytes / secs / 1e9
+    return {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": ncu_traffic(workload, dominant, a8),
+            "algorithmic_bytes": dbytes, "algorithmic_flops": dflops, "peak_source": peaks["source"]}
+
+
+def routing_summary(shape, ids):
+    """The realised expert histogram of a call: active experts, tokens per active expert and the balance
+    (mean / max, 1.0 = even), over all experts and over the routed ones alone (a shared expert takes
+    every token)."""
+    hist = synth.expert_histogram(shape, ids)
+
+    def stats(h):
+        act = h[h > 0].double()
+        if not act.numel():
+            return None
+        q = torch.quantile(act, torch.tensor([0.0, 0.5, 0.9, 1.0], dtype=torch.float64)).tolist()
+        return {"active_experts": int(act.numel()), "min": q[0], "median": q[1], "p90": q[2], "max": q[3],
+                "mean": float(act.mean()), "balance_mean_over_max": float(act.mean() / act.max())}
+
+    return {"experts": shape.E_total, "all": stats(hist),
+            "routed": stats(hist[:shape.E]) if shape.shared_expert else None}
+
+
+def parity_rows(shape, x, ids, w, weights, out, tokens):
+    """rel-L2 and max-abs / max|ref| of the layer's output rows `tokens` against the oracle."""
+    import oracle
+    ref = oracle.fused_moe_rows(x, ids, w, *weights, kind=shape.weight_kind, tokens=tokens, act=shape.act)
+    got = out[torch.as_tensor(tokens, dtype=torch.long, device=out.device)].float().cpu().numpy().astype(np.float64)
+    rel = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+    mabs = float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-300))
+    experts = int(np.unique(ids[tokens].numpy()).size)
+    return {"rel_l2": rel, "max_abs_over_max_ref": mabs, "tokens": len(tokens), "experts_covered": experts,
+            "within_tolerance": rel <= 5e-3 and mabs <= 1e-2, "tolerance": "rel-L2 <= 5e-3, max-abs <= 1e-2 max|ref|"}
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+ONE_CORE_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1",
+                "BLIS_NUM_THREADS": "1", "NUMEXPR_NUM_THREADS": "1"}
+
+
+def oracle_one_core(shape, x, ids, w, weights, tokens):
+    """Seconds the oracle takes for `tokens` in a child process limited to one thread (its BLAS and
+    OpenMP pools set to 1 before numpy loads).  Only the involved experts' weights are handed over."""
+    import tempfile
+    used = sorted({int(e) for e in ids[tokens].reshape(-1).tolist() if 0 <= e < shape.E_total})
+    remap = {e: i for i, e in enumerate(used)}
+    sub_ids = ids[tokens].clone().apply_(lambda e: remap.get(int(e), -1))
+    payload = {"x": x[tokens], "ids": sub_ids, "w": w[tokens], "kind": shape.weight_kind, "act": shape.act,
+               "weights": [t[used].cpu() for t in weights]}
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "sample.pt")
+        torch.save(payload, path)
+        code = ("import sys, time, torch; sys.path.insert(0, %r); import oracle; p = torch.load(%r); "
+                "t0 = time.perf_counter(); oracle.fused_moe_rows(p['x'], p['ids'], p['w'], *p['weights'], "
+                "kind=p['kind'], tokens=list(range(p['x'].shape[0])), act=p['act']); "
+                "print(time.perf_counter() - t0)") % (ROOT, path)
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600,
+                           env={**os.environ, **ONE_CORE_ENV})
+    if r.returncode != 0:
+        return None
+    return float(r.stdout.strip().splitlines()[-1])
+
+
 def stage_work(shape, ids: torch.Tensor):
     """Algorithmic (bytes, flops) per kernel of one call.
 
@@ -185,7 +292,7 @@ def stage_work(shape, ids: torch.Tensor):
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -193,6 +300,14 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.path = os.path.join("/tmp", f"gbmoe_clocks_{os.getpid()}.csv")
+        self.samples = None
+
+    def _lines(self):
+        try:
+            with open(self.path) as f:
+                return sum(1 for _ in f)
+        except OSError:
+            return 0
 
     def __enter__(self):
         try:
@@ -201,37 +316,50 @@ class ClockSampler:
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (FileNotFoundError, OSError):
             self.proc = None
-        time.sleep(0.3)
+        # the sampler's start-up takes a moment: time nothing before its first sample is written
+        t0 = time.time()
+        while self.proc is not None and self._lines() < 1 and time.time() - t0 < 5.0:
+            time.sleep(0.05)
         return self
 
     def __exit__(self, *a):
         if self.proc is not None:
-            time.sleep(0.25)
+            n, t0 = self._lines(), time.time()
+            while self._lines() < n + 2 and time.time() - t0 < 2.0:  # samples that follow the timed work
+                time.sleep(0.05)
             self.proc.terminate()
             self.proc.wait()
 
-    def summary(self):
+    def _read(self):
+        """[(unix time, sm MHz, max sm MHz, set of active reasons)], read once after the sampler stops."""
+        if self.samples is not None:
+            return self.samples
+        self.samples = []
         if self.proc is None or not os.path.exists(self.path):
-            return None
-        sm, smax, reasons = [], 0.0, set()
+            return self.samples
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax = max(smax, float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                sm, smax = float(f[2]), float(f[3])
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
+            self.samples.append((ts, sm, smax, {n for n, v in zip(names, f[6:10]) if v.lower() == "active"}))
         os.unlink(self.path)
-        if not sm:
+        return self.samples
+
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, max clock and throttle reasons of the samples taken in [t0, t1] widened by one
+        sampling period (unix time; all samples when not given)."""
+        sel = [x for x in self._read() if (t0 is None or x[0] >= t0 - 0.2) and (t1 is None or x[0] <= t1 + 0.2)]
+        if not sel:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = set().union(*(x[3] for x in sel))
+        return {"sm_mhz": statistics.median(x[1] for x in sel), "sm_max_mhz": max(x[2] for x in sel),
+                "reasons": sorted(reasons), "samples": len(sel)}
 
 
 def dist_setup():
@@ -437,30 +565,8 @@ def run_ours(args, shape):
     # ---- roofline of the dominant kernel
     peaks = measured_peaks()
     # (masked: the activation terms count the real rows only)
-    work = stage_work(dataclasses.replace(shape, M=units) if masked else shape, ids)
-    stage_avg = {name: ms / max(n_calls, 1) for name, ms in stages}
-    dominant = max((n for n in stage_avg if n in work), key=lambda n: stage_avg[n])
-    dbytes, dflops = work[dominant]
-    secs = stage_avg[dominant] * 1e-3
-    # Tensor peak of the kernel's operand type, burst figure: fp16 MMA runs at the measured dense
-    # bf16 rate; E4M3 x E4M3 at twice it (the nominal FP8:BF16 ratio, 4.5 : 2.25 PFLOP/s).
-    if shape.act == "fp8_1x128":
-        tpeak, tsrc = 2.0 * peaks["bf16_tflops"], peaks["source"] + " bf16 dense x 2 (nominal FP8:BF16 ratio)"
-    else:
-        tpeak, tsrc = peaks["bf16_tflops"], peaks["source"] + " bf16 dense (fp16 same rate)"
-    ridge = tpeak * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if dflops / dbytes > ridge:
-        achieved = dflops / secs / 1e12
-        roofline = {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": tpeak,
-                    "unit": "TFLOP/s", "frac": achieved / tpeak,
-                    "traffic": ncu_traffic(args.workload, dominant, shape.act == "fp8_1x128"), "algorithmic_flops": dflops,
-                    "algorithmic_bytes": dbytes, "peak_source": tsrc}
-    else:
-        achieved = dbytes / secs / 1e9
-        roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": peaks["hbm_gbs"],
-                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                    "traffic": ncu_traffic(args.workload, dominant, shape.act == "fp8_1x128"), "algorithmic_bytes": dbytes,
-                    "algorithmic_flops": dflops, "peak_source": peaks["source"]}
+    roofline = roofline_of(dataclasses.replace(shape, M=units) if masked else shape, ids, stages, n_calls,
+                           args.workload, peaks)
     layer_bytes = synth.distinct_weight_bytes(shape, ids)
     flops = synth.algorithmic_flops(shape, ids)
 
@@ -495,23 +601,39 @@ def run_ours(args, shape):
 
     if rank != 0:
         return
-    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
+    stage_avg = {name: ms / max(n_calls, 1) for name, ms in stages}
+    # ---- parity of the timed output against the oracle (rank 0): every token up to 16 tokens, else a
+    # bounded sample; the routing the call realised
+    real = [int(t) for t in ((ids >= 0) & (ids < shape.E_total)).any(dim=1).nonzero().flatten()]
+    ptoks = real if len(real) <= 16 else real[:: max(1, len(real) // 8)][:8]
+    parity = parity_rows(shape, x, ids, w, (w13, s13, w2, s2), out, ptoks) if ptoks and not masked else None
+    routing = routing_summary(shape, ids)
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only), on every host core and on
+    # one, with the host's CPU model
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        v, dt, text = oracle_sample(shape, x, ids, w, (w13, s13, w2, s2), token=int((ids[:, 0] >= 0).nonzero()[0]))
+        tok = int((ids[:, 0] >= 0).nonzero()[0])
+        v, dt, text = oracle_sample(shape, x, ids, w, (w13, s13, w2, s2), token=tok)
+        one = oracle_one_core(shape, x, ids, w, (w13, s13, w2, s2), [tok])
         cpu = {"value": v, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle", "sample": text,
-               "seconds": dt}
+               "seconds": dt, "cpu_model": cpu_model(),
+               "one_core": {"value": 1.0 / one, "unit": "tokens/s", "cores": 1, "seconds": one} if one else None,
+               "tiny_layer": tiny_cpu_baseline()}
+    # ---- the other configurations of the layer, each timed the same way (N = 1 only)
+    also = None
+    if world == 1 and not args.no_also and args.workload == DEFAULT_WORKLOAD:
+        also = run_also(dev, flush, peaks, (w13, s13, w2, s2), shape)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": ("fp8 x fp8 mma, f32 acc" if shape.act == "fp8_1x128" else
-                                       "fp8->f16 mma, f32 acc") if kind == 0 else
-                                      ("int8->f16 mma, f32 acc" if kind == 1 else "int4->f16 mma, f32 acc"),
+        "vs_baseline": None, "dtype": dtype_of(shape, kind),
         "data": "synthetic", "config": config_of(shape, args),
         "roofline": roofline, "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": sum(1 for _ in stages) * n_calls,
         "clocks": clocks.summary(),
+        "parity": parity,
+        "routing": routing,
         "layer": {"weight_gbs": layer_bytes / (ms_per_step * 1e-3) / 1e9,
                   "weight_bytes": layer_bytes, "hbm_frac": layer_bytes / (ms_per_step * 1e-3) / 1e9 / peaks["hbm_gbs"],
                   "tflops": flops / (ms_per_step * 1e-3) / 1e12,
@@ -522,9 +644,126 @@ def run_ours(args, shape):
                   int((synth.expert_histogram(shape, ids) > 0).sum()),
                   "stages_ms": {n: round(v, 5) for n, v in stage_avg.items()},
                   "ms_per_step_with_kernel_events": prof_ms / args.steps},
+        "also": also,
         "wall_s": wall,
     }
     print(json.dumps(line), flush=True)
+
+
+def dtype_of(shape, kind):
+    if kind == gbmoe.MOE_WEIGHT_FP8:
+        return "fp8 x fp8 mma, f32 acc" if shape.act == "fp8_1x128" else "fp8->f16 mma, f32 acc"
+    return "int8->f16 mma, f32 acc" if kind == gbmoe.MOE_WEIGHT_INT8 else "int4->f16 mma, f32 acc"
+
+
+def tiny_cpu_baseline():
+    """The oracle on the whole tiny layer (16 tokens), on every host core and on one."""
+    import oracle
+    shape = synth.tiny()
+    d = synth.make_layer(shape, 1234)
+    args = [d[k] for k in ("x", "topk_ids", "topk_weights", "w13", "w13_scale", "w2", "w2_scale")]
+    t0 = time.perf_counter()
+    reps = 5
+    for _ in range(reps):
+        oracle.fused_moe_fp8(*args)
+    dt = (time.perf_counter() - t0) / reps
+    one = oracle_one_core(shape, d["x"], d["topk_ids"], d["topk_weights"], args[3:], list(range(shape.M)))
+    return {"workload": "tiny_M16", "tokens_per_s": shape.M / dt, "cores": cpu_cores(),
+            "tokens_per_s_one_core": shape.M / one if one else None}
+
+
+# The other workloads of the layer's configurations, timed after the default line: DeepSeek-R1 single-token
+# decode, the uniform-routing decode sweep, the 2048-token Zipf prefill and the 16,384-token prefill
+# (weight-only and FP8 activations), and the Qwen3 INT8 layer at 1, 16, 256 and 4096 tokens.
+ALSO_WORKLOADS = (["dsr1_decode_M1"] + [f"dsr1_sweep_M{m}" for m in (1, 2, 4, 8, 16, 32, 64)] +
+                  ["dsr1_prefill_M2048", "dsr1_prefill_M2048_a8", "dsr1_prefill_M16384", "dsr1_prefill_M16384_a8",
+                   "qwen3_M1", "qwen3_M16", "qwen3_M256", "qwen3_M4096"])
+ALSO_MIN_SECONDS = 0.3   # timed work per entry (so the clock sampler sees it)
+
+
+def run_also(dev, flush, peaks, main_weights, main_shape):
+    """Times every ALSO_WORKLOADS entry as the default line is timed (L2 flushed between steps, CUDA events
+    on the launch stream, a per-kernel pass for the roofline) and checks one token against the oracle."""
+    stream = torch.cuda.current_stream(dev)
+    cache = {(main_shape.E_total, main_shape.H, main_shape.I, main_shape.weight_kind): main_weights}
+    results, windows = {}, {}
+    with ClockSampler(dev.index) as clocks:
+        for name in ALSO_WORKLOADS:
+            shape = workloads()[name]
+            key = (shape.E_total, shape.H, shape.I, shape.weight_kind)
+            if key not in cache:
+                cache = {key: synth.make_weights(shape, 1234, device="cuda")}
+                torch.cuda.empty_cache()
+            weights = cache[key]
+            ids, tw = synth.make_routing(shape, 1234)
+            x = synth.make_x(shape, 1234)
+            xd, idsd, twd = x.to(dev), ids.to(dev), tw.to(dev)
+            kind = {"fp8": gbmoe.MOE_WEIGHT_FP8, "int8": gbmoe.MOE_WEIGHT_INT8,
+                    "int4": gbmoe.MOE_WEIGHT_INT4}[shape.weight_kind]
+            fn = {gbmoe.MOE_WEIGHT_FP8: gbmoe.fused_moe_fp8, gbmoe.MOE_WEIGHT_INT8: gbmoe.fused_moe_int8,
+                  gbmoe.MOE_WEIGHT_INT4: gbmoe.fused_moe_int4}[kind]
+            flags = gbmoe.MOE_ACT_FP8_1X128 if shape.act == "fp8_1x128" else gbmoe.MOE_PATH_AUTO
+            ws = gbmoe.alloc_workspace(shape.M, shape.H, shape.I, shape.E_total, shape.topk_total, kind, flags, dev)
+            o = torch.empty(shape.M, shape.H, dtype=torch.bfloat16, device=dev)
+
+            def step():
+                fn(xd, idsd, twd, *weights, flags=flags, out=o, workspace=ws)
+
+            for _ in range(3):
+                flush.zero_()
+                step()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(3):
+                flush.zero_()
+                step()
+            e1.record(stream)
+            e1.synchronize()
+            steps = int(min(4000, max(5, ALSO_MIN_SECONDS * 1e3 / (e0.elapsed_time(e1) / 3))))
+            starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+            ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+            torch.cuda.synchronize()
+            t0 = time.time()
+            for i in range(steps):
+                flush.zero_()
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+            torch.cuda.synchronize()
+            windows[name] = (t0, time.time())
+            ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / steps
+            bad, dev_flags, st = gbmoe.moe_read_status(ws)
+            if st != 0:
+                raise SystemExit(f"{name}: device status bad ids {bad}, flags {dev_flags}")
+            npass = min(steps, 10)
+            gbmoe.moe_profile_enable(npass)
+            for _ in range(npass):
+                flush.zero_()
+                step()
+            n_calls, stages = gbmoe.moe_profile_read()
+            gbmoe.moe_profile_enable(0)
+            roof = roofline_of(shape, ids, stages, n_calls, name, peaks)
+            layer_bytes = synth.distinct_weight_bytes(shape, ids)
+            flops = synth.algorithmic_flops(shape, ids)
+            tok = int((ids[:, 0] >= 0).nonzero()[0])
+            results[name] = {
+                "M": shape.M, "ms": ms, "tokens_per_s": shape.M / (ms * 1e-3), "steps": steps,
+                "dtype": dtype_of(shape, kind),
+                "roofline": {k: roof[k] for k in ("kernel", "bound", "achieved", "unit", "peak", "frac")},
+                "layer": {"weight_gbs": layer_bytes / (ms * 1e-3) / 1e9,
+                          "hbm_frac": layer_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                          "tflops": flops / (ms * 1e-3) / 1e12,
+                          "tflops_frac_bf16": flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                          "tflops_frac_fp8": flops / (ms * 1e-3) / 1e12 / (2.0 * peaks["bf16_tflops"])},
+                "stages_ms": {n: round(v / max(n_calls, 1), 5) for n, v in stages},
+                "routing": routing_summary(shape, ids),
+                "parity": parity_rows(shape, x, ids, tw, weights, o, [tok]),
+            }
+            del ws, o, xd, idsd, twd
+    for name, (t0, t1) in windows.items():
+        results[name]["clocks"] = clocks.summary(t0, t1)
+    return results
 
 
 def main():
@@ -535,6 +774,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(all_workloads()))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-also", action="store_true", help="time the default workload only")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -358,16 +358,20 @@ moe_status_t fused_moe_gated(int weight_kind, const void* x_bf16, const float* r
  * workspace: the scratch is a static device buffer of
  * MOE_STATIC_SCRATCH_BYTES inside the library.  Each device on which it runs
  * holds that buffer from its first call until the process exits.
- *  - The first call on a device looks the buffer's address up once
+ *  - The first call on a device looks the buffer's address up
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
- *  - Sizes whose moe_workspace_size(..., MOE_WEIGHT_FP8, flags) exceeds
+ *    before any stream capture.  After a device reset the next call on that
+ *    device looks it up again (a new CUDA context), so it too must come
+ *    before any capture.
+ *  - Invalid arguments return what fused_moe_fp8 returns for them.  Valid
+ *    sizes whose moe_workspace_size(..., MOE_WEIGHT_FP8, flags) exceeds
  *    MOE_STATIC_SCRATCH_BYTES return MOE_ERR_UNSUPPORTED with a message that
  *    names the limit; nothing is launched.
  *  - Nothing is allocated or freed.  All calls share the buffer, which keeps
  *    the last call's contents; the kernels clear what must start at zero.
  *    Calls that overlap on the GPU race on it: serialise them.
- *  - Its device status words are not readable through moe_read_status.
+ *  - Its device status words (ids out of range, a bounded wait that gave up)
+ *    are read with moe_read_static_scratch_status.
  */
 #define MOE_STATIC_SCRATCH_BYTES (16u << 20)
 moe_status_t fused_moe_fp8_static_scratch(const void* x_bf16, const int32_t* topk_ids,
@@ -375,6 +379,14 @@ moe_status_t fused_moe_fp8_static_scratch(const void* x_bf16, const int32_t* top
                                           const float* w13_scale, const void* w2_e4m3,
                                           const float* w2_scale, int M, int H, int I, int E, int topk,
                                           unsigned flags, void* out_bf16, moe_stream_t stream);
+
+/*
+ * moe_read_status for the static buffer of fused_moe_fp8_static_scratch on
+ * the current device: waits for `stream`, then copies the status words of
+ * the last call that ran there (see moe_read_status).  The pages have no
+ * counterpart of this function either.
+ */
+moe_status_t moe_read_static_scratch_status(int32_t status_out[2], moe_stream_t stream);
 
 /*
  * Waits for `stream`, then copies the workspace's status words to the host:

@@ -216,6 +216,12 @@ cudaError_t launch_h_frame(__half* h, const uint32_t* hexp, const uint8_t* hblk,
                            int I, float* hsc, int num_sms, cudaStream_t s);
 size_t prefill_smem_bytes();
 
+// The host-side argument checks of fused_moe_fp8 (sizes, flags, NULL pointers), without the workspace:
+// MOE_OK or the status fused_moe_fp8 would return, with its message.
+moe_status_t check_fp8_layer_args(const void* x, const int32_t* ids, const float* tw, const void* w13,
+                                  const float* s13, const void* w2, const float* s2, int M, int H, int I, int E,
+                                  int topk, unsigned flags, const void* out);
+
 // Records `msg` as the calling thread's last error (moe_last_error) and returns `st`.
 moe_status_t report_error(moe_status_t st, const std::string& msg);
 

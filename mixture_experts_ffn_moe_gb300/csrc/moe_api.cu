@@ -196,6 +196,13 @@ static moe_status_t check_layer_args(int kind, const void* x, const void* ids, c
   return MOE_OK;
 }
 
+moe_status_t check_fp8_layer_args(const void* x, const int32_t* ids, const float* tw, const void* w13,
+                                  const float* s13, const void* w2, const float* s2, int M, int H, int I, int E,
+                                  int topk, unsigned flags, const void* out) {
+  g_last_error.clear();
+  return check_layer_args(MOE_WEIGHT_FP8, x, ids, tw, w13, s13, w2, s2, M, H, I, E, topk, flags, out);
+}
+
 template <typename T>
 static T* at(void* base, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(base) + off);

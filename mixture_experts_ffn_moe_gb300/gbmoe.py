@@ -63,6 +63,7 @@ _SIGS = {
     "fused_moe_masked": (_i, [_i] + [_vp] * 6 + [_i] * 4 + [_u, _vp, _vp, _sz, _vp]),
     "fused_moe_fp8_static_scratch": (_i, [_vp] * 7 + [_i] * 5 + [_u, _vp, _vp]),
     "moe_read_status": (_i, [_vp, _vp, _vp]),
+    "moe_read_static_scratch_status": (_i, [_vp, _vp]),
     "moe_read_routing": (_i, [_vp] + [_i] * 6 + [_u] + [_vp] * 6),
     "moe_selftest_wait_timeout": (_i, [_vp, ctypes.c_longlong, _vp, _vp]),
     "moe_profile_enable": (_i, [_i]),
@@ -361,6 +362,14 @@ def fused_moe_fp8_static_scratch(x, topk_ids, topk_weights, w13, w13_scale, w2, 
                                              topk_ids.shape[1], flags, _ptr(out), _stream(x))
     _check(st, "fused_moe_fp8_static_scratch")
     return out
+
+
+def moe_read_static_scratch_status(device=None):
+    """(bad_id_count, flags, status) of the last fused_moe_fp8_static_scratch call on the current device."""
+    buf = (ctypes.c_int32 * 2)()
+    stream = torch.cuda.current_stream(device).cuda_stream
+    st = load().moe_read_static_scratch_status(ctypes.cast(buf, ctypes.c_void_p), ctypes.c_void_p(stream))
+    return int(buf[0]), int(buf[1]), int(st)
 
 
 def moe_read_status(workspace: torch.Tensor):

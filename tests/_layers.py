@@ -56,3 +56,30 @@ def assert_layer_close(out, ref, what=""):
 
 def to_device(d, device="cuda"):
     return {k: (v.to(device) if hasattr(v, "to") else v) for k, v in d.items()}
+
+
+def covering_rows(ids, E_total, limit=None):
+    """Token rows whose experts cover every active expert, plus the last token routed to the heaviest
+    experts (so the last token tile of the most loaded expert is checked) and the first and last token.
+
+    Each active expert contributes the first token that visits it, unless an earlier pick already does.
+    The oracle dequantises each expert once per call, so checking every expert costs about as much as
+    checking one token per expert.
+    """
+    ids = np.asarray(ids)
+    M = ids.shape[0]
+    valid = (ids >= 0) & (ids < E_total)
+    picked, covered = [], set()
+    for e in np.unique(ids[valid]):
+        if int(e) in covered:
+            continue
+        t = int(np.nonzero((ids == e).any(axis=1))[0][0])
+        picked.append(t)
+        covered.update(int(v) for v in ids[t][valid[t]])
+    counts = np.bincount(ids[valid].ravel(), minlength=E_total)
+    for e in np.argsort(-counts, kind="stable")[:2]:  # the two heaviest experts (the shared one first, if any)
+        if counts[e]:
+            picked.append(int(np.nonzero((ids == e).any(axis=1))[0][-1]))
+    picked += [0, M - 1]
+    rows = sorted(set(picked))
+    return rows if limit is None else rows[:limit]

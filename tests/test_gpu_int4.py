@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from _layers import assert_layer_close, to_device
+from _layers import assert_layer_close, covering_rows, to_device
 from mixture_experts_ffn_moe_gb300 import build, gbmoe, synth
 
 pytestmark = pytest.mark.gpu
@@ -58,7 +58,7 @@ def test_int4_tcgen05_path(M, H, I, E, k):
 
 
 def test_int4_qwen3_shape_prefill_4096():
-    _full_size(synth.qwen3_235b(4096, weight_kind="int4"), seed=23, rows=[0, 2047, 4095])
+    _full_size(synth.qwen3_235b(4096, weight_kind="int4"), seed=23)
 
 
 def test_int4_every_code_and_extreme_group_scales():
@@ -117,8 +117,10 @@ def test_int4_deterministic():
     assert np.array_equal(_run(d), _run(d))
 
 
-def _full_size(shape, seed, rows):
+def _full_size(shape, seed, rows=None):
     ids, w = synth.make_routing(shape, seed)
+    if rows is None:  # rows covering every active expert, and the last token of the most loaded experts
+        rows = covering_rows(ids.numpy(), shape.E_total)
     x = synth.make_x(shape, seed)
     w13, s13, w2, s2 = synth.make_weights(shape, seed, device="cuda")
     out = gbmoe.fused_moe_int4(x.cuda(), ids.cuda(), w.cuda(), w13, s13, w2, s2).float().cpu().numpy()
@@ -127,11 +129,11 @@ def _full_size(shape, seed, rows):
 
 
 def test_int4_deepseek_r1_shape_decode_batch4():
-    _full_size(synth.deepseek_r1(4, weight_kind="int4"), seed=21, rows=[0, 3])
+    _full_size(synth.deepseek_r1(4, weight_kind="int4"), seed=21, rows=[0, 1, 2, 3])
 
 
 def test_int4_qwen3_shape_batch16():
-    _full_size(synth.qwen3_235b(16, weight_kind="int4"), seed=22, rows=[1, 15])
+    _full_size(synth.qwen3_235b(16, weight_kind="int4"), seed=22, rows=list(range(16)))
 
 
 def test_int4_gated_layer():

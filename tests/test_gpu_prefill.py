@@ -7,7 +7,7 @@ import pytest
 import torch
 
 import oracle
-from _layers import assert_layer_close, expert_id_expected, expert_id_layer, to_device
+from _layers import assert_layer_close, covering_rows, expert_id_expected, expert_id_layer, to_device
 from mixture_experts_ffn_moe_gb300 import build, gbmoe, synth
 
 pytestmark = pytest.mark.gpu
@@ -99,8 +99,11 @@ def test_prefill_deterministic():
     assert np.array_equal(_run(d, "fp8"), _run(d, "fp8"))
 
 
-def _full_size_check(shape, seed, rows, kind, flags=gbmoe.MOE_PATH_AUTO):
+def _full_size_check(shape, seed, kind, flags=gbmoe.MOE_PATH_AUTO):
+    """Rows covering every active expert, and the last token of the most loaded experts (the last token
+    tile of the heaviest Zipf expert)."""
     ids, w = synth.make_routing(shape, seed)
+    rows = covering_rows(ids.numpy(), shape.E_total)
     x = synth.make_x(shape, seed)
     w13, s13, w2, s2 = synth.make_weights(shape, seed, device="cuda")
     fn = gbmoe.fused_moe_fp8 if kind == "fp8" else gbmoe.fused_moe_int8
@@ -111,12 +114,17 @@ def _full_size_check(shape, seed, rows, kind, flags=gbmoe.MOE_PATH_AUTO):
 
 
 def test_deepseek_r1_prefill_2048_zipf_full_size():
-    _full_size_check(synth.deepseek_r1(2048, routing="deepseek_zipf"), seed=51, rows=[0, 1000, 2047], kind="fp8")
+    _full_size_check(synth.deepseek_r1(2048, routing="deepseek_zipf"), seed=51, kind="fp8")
+
+
+def test_deepseek_r1_prefill_16384_zipf_full_size():
+    # the compute-bound weight-only point: 16,384 tokens, the alignment split over 36 chunks
+    _full_size_check(synth.deepseek_r1(16384, routing="deepseek_zipf"), seed=54, kind="fp8")
 
 
 def test_qwen3_int8_prefill_256_full_size():
-    _full_size_check(synth.qwen3_235b(256), seed=52, rows=[3, 255], kind="int8", flags=PREFILL)
+    _full_size_check(synth.qwen3_235b(256), seed=52, kind="int8", flags=PREFILL)
 
 
 def test_qwen3_int8_prefill_4096_full_size():
-    _full_size_check(synth.qwen3_235b(4096), seed=53, rows=[0, 4095], kind="int8")
+    _full_size_check(synth.qwen3_235b(4096), seed=53, kind="int8")
