@@ -203,6 +203,10 @@ __global__ void __launch_bounds__(kAlignThreads) align_scatter_kernel(AlignArgs 
 //   kind 3: x bf16 -> E4M3 codes + one fp32 scale per 128 columns (FP8 A8 path)
 //   kind 4: as kind 1, each group of 8 columns stored in the order 0 4 1 5 2 6 3 7
 //           (INT4 path: the order its weights expand in)
+//   kind 5: x bf16 -> two E4M3 codes per value in a power-of-two frame per 128 columns
+//           (FP8 weight-only path on the FP8 tensor cores): hi = E4M3(x * 2^-e), lo = E4M3 of
+//           the remainder, with the group's max |x| * 2^-e in [2^7, 2^8); hi codes in rows
+//           0..M-1 of q, lo codes in rows M..2M-1, scale[r, g] = 2^e
 // Kinds 1, 2 and 4 take a CTA per row when there are few rows and a warp per row
 // otherwise.
 constexpr int kPrepBatch = 4;
@@ -238,6 +242,37 @@ __device__ void prep_fp8_flat(const PrepArgs& p, long long first, long long stri
       const uint32_t c2 = e4m3_code(__fdiv_rn(f1.x, sc)), c3 = e4m3_code(__fdiv_rn(f1.y, sc));
       *reinterpret_cast<uint32_t*>(q + gi * kQBlock + lane * 4) = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
       if (lane == 0) p.scale[gi] = sc;
+    }
+  }
+}
+
+// kind 5: x = 2^e (hi + lo) per 1 x 128 group, hi and lo E4M3 codes (round to nearest even; no
+// saturation is reached: |x| * 2^-e < 2^8 < 448).  One warp per group, 4 columns a lane; `first` /
+// `stride` count warps.
+__device__ void prep_split_flat(const PrepArgs& p, long long first, long long stride) {
+  const int lane = threadIdx.x & 31;
+  const long long ng = static_cast<long long>(p.M) * (p.H / kQBlock);
+  uint8_t* q = static_cast<uint8_t*>(p.q);
+  const size_t lo_off = static_cast<size_t>(p.M) * p.H;
+  for (long long g0 = first; g0 < ng; g0 += kPrepBatch * stride) {
+    uint2 raw[kPrepBatch];
+#pragma unroll
+    for (int u = 0; u < kPrepBatch; ++u) {
+      const long long gi = g0 + u * stride;
+      if (gi < ng) raw[u] = *reinterpret_cast<const uint2*>(p.x + gi * kQBlock + lane * 4);
+    }
+#pragma unroll
+    for (int u = 0; u < kPrepBatch; ++u) {
+      const long long gi = g0 + u * stride;
+      if (gi >= ng) break;
+      const float2 f0 = bf2_lo_hi(raw[u].x), f1 = bf2_lo_hi(raw[u].y);
+      const float m = warp_max(fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y))));
+      const int e = m > 0.f ? e4m3_split_exp(m) : 0;
+      uint32_t hi, lo;
+      e4m3_split4(make_float4(f0.x, f0.y, f1.x, f1.y), exp2i(-e), hi, lo);
+      *reinterpret_cast<uint32_t*>(q + gi * kQBlock + lane * 4) = hi;
+      *reinterpret_cast<uint32_t*>(q + lo_off + gi * kQBlock + lane * 4) = lo;
+      if (lane == 0) p.scale[gi] = exp2i(e);
     }
   }
 }
@@ -356,6 +391,7 @@ __device__ void prep_rows(const PrepArgs& p, int cta, int nctas) {
     case 1: prep_rows_amax<1, __half>(p, cta, nctas); break;
     case 4: prep_rows_amax<4, __half>(p, cta, nctas); break;
     case 3: prep_fp8_flat(p, tfirst >> 5, tstride >> 5); break;
+    case 5: prep_split_flat(p, tfirst >> 5, tstride >> 5); break;
     case 2: prep_rows_amax<2, QT>(p, cta, nctas); break;
     default: break;
   }

@@ -186,6 +186,36 @@ __device__ __forceinline__ __half2 exp2i_h2(int d) {
   return __halves2half2(h, h);
 }
 
+// Two-term E4M3 form of values carried on the FP8 tensor cores in place of bf16 or fp32 operands: in a
+// power-of-two frame 2^e per group of 128 with the group's max |v| * 2^-e in [2^7, 2^8), a value is
+// hi + lo with hi = E4M3(v * 2^-e) and lo = E4M3(v * 2^-e - hi) (round to nearest even; |v| * 2^-e < 256,
+// so nothing saturates).  A bf16 value is exact in this form when v * 2^-e >= 2^-2 (its 8 significant bits
+// split into two 4-bit halves that are both E4M3 normals or exact subnormals); smaller values keep an
+// absolute error below 2^-10 in the frame, i.e. below 2^-17 of the group's max.
+__device__ __forceinline__ int e4m3_split_exp(float amax) {
+  const int e = ilog2f(amax) - 7;
+  return e < -126 ? -126 : (e > 120 ? 120 : e);
+}
+
+// E4M3 code pair (the low two bytes of w16) -> float2, exact.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t w16) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 l;\n\tcvt.u16.u32 l, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t}" : "=r"(h) : "r"(w16));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// The two-term form of four values, mul = 2^-e: hi and lo codes, byte i from value i.
+__device__ __forceinline__ void e4m3_split4(float4 v, float mul, uint32_t& hi, uint32_t& lo) {
+  const float a0 = v.x * mul, a1 = v.y * mul, a2 = v.z * mul, a3 = v.w * mul;
+  const uint32_t h01 = __nv_cvt_float2_to_fp8x2(make_float2(a0, a1), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t h23 = __nv_cvt_float2_to_fp8x2(make_float2(a2, a3), __NV_SATFINITE, __NV_E4M3);
+  const float2 b01 = e4m3x2_to_float2(h01), b23 = e4m3x2_to_float2(h23);
+  const uint32_t l01 = __nv_cvt_float2_to_fp8x2(make_float2(a0 - b01.x, a1 - b01.y), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t l23 = __nv_cvt_float2_to_fp8x2(make_float2(a2 - b23.x, a3 - b23.y), __NV_SATFINITE, __NV_E4M3);
+  hi = (h01 & 0xffffu) | (h23 << 16);
+  lo = (l01 & 0xffffu) | (l23 << 16);
+}
+
 // Multiplies the 8 fp16 values of v by the power of two f (exact unless they become subnormal).
 __device__ __forceinline__ void scale_h8(uint4& v, __half2 f) {
   uint32_t* w = reinterpret_cast<uint32_t*>(&v);

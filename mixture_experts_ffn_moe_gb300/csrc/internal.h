@@ -39,7 +39,7 @@ struct PrepArgs {
   const __nv_bfloat16* x;  // [M, H]
   int M, H;
   int kind;                // 0 none, 1 bf16 -> fp16, 2 per-row int8, 3 FP8 E4M3 per 1x128 group,
-                           // 4 bf16 -> fp16 in the INT4 K order
+                           // 4 bf16 -> fp16 in the INT4 K order, 5 two-term E4M3 per 1x128 group
   void* q;                 // [M, H] fp16 (kinds 1, 2 in the prologue), int8 (quant entry) or E4M3 codes (kind 3)
   float* scale;            // [M] (kind 2) or [M, H/128] (kind 3)
   uint32_t* zero_words;    // words to clear (may be null)
@@ -104,12 +104,13 @@ struct LayerPlan {
   float* y;              // [M*topk, H] weighted expert outputs by slot
   __nv_bfloat16* out;
   DeviceStatus* status;
-  // FP8-activation (A8) prefill only
-  const uint8_t* xq8;    // [M, H] E4M3 codes of x
+  // FP8-operand prefill (MOE_ACT_FP8_1X128, and the FP8 weight-only layer's two-term form)
+  int e4m3_terms;        // 1: E4M3 activations; 2: x and h as two E4M3 terms (hi rows, then lo rows)
+  const uint8_t* xq8;    // [terms * M, H] E4M3 codes of x
   const float* sx8;      // [M, H/128] their scales
-  uint8_t* act8;         // [cap, H] gathered codes by position
+  uint8_t* act8;         // [terms * cap, H] gathered codes by position
   float* sa8;            // [H/128, cap] gathered scales, transposed
-  uint8_t* h8;           // [cap, I] E4M3 codes of h by position
+  uint8_t* h8;           // [terms * cap, I] E4M3 codes of h by position
   float* sh8;            // [I/128, cap] their scales, transposed
   // masked layout: GEMM1 reads its activations by position (xq holds them in position
   // order) and GEMM2 writes bf16 rows straight to out_direct[sorted_ids[pos]], unweighted;

@@ -101,6 +101,7 @@ struct Layout {
          chunk_counts = 0, hexp = 0, hblk = 0, hsc = 0, total = 0;
   int align_chunks = 1;  // CTAs of the alignment (more than one: split over chunks of slots)
   bool a8 = false;
+  int terms = 0;  // FP8-operand tcgen05 kernels: 1 (E4M3 activations), 2 (two-term form of bf16 x / fp32 h)
   size_t max_ttiles = 0;
   int tile_tokens = 0;
 };
@@ -130,16 +131,19 @@ static Layout plan(int M, int H, int I, int E, int topk, int kind, unsigned flag
   L.align_chunks = align_num_chunks(static_cast<long long>(M) * topk);
   if (L.align_chunks > 1) L.chunk_counts = take(static_cast<size_t>(kAlignMaxChunks) * E * 4);
   L.a8 = kind == MOE_WEIGHT_FP8 && (flags & MOE_ACT_FP8_1X128);
+  // FP8 weights on the tcgen05 path run on the FP8 tensor cores: E4M3 activations (A8), or for the
+  // weight-only layer x and h in their two-term E4M3 form
+  L.terms = L.a8 ? 1 : (kind == MOE_WEIGHT_FP8 && L.path == MOE_PATH_PREFILL) ? 2 : 0;
   L.tile_tokens = L.path == MOE_PATH_PREFILL ? kPrefillTileTokens : kDecodeBlock;
   L.max_ttiles = static_cast<size_t>(E) + static_cast<size_t>(M) * topk / L.tile_tokens + 1;
-  if (L.a8) {
-    // E4M3 codes with 1 x 128 scales; scales of gathered rows are stored transposed [K/128, cap]
-    L.xq = take(static_cast<size_t>(M) * H);
+  if (L.terms) {
+    // E4M3 codes (per term) with 1 x 128 scales; scales of gathered rows are stored transposed [K/128, cap]
+    L.xq = take(static_cast<size_t>(L.terms) * M * H);
     L.sx = take(static_cast<size_t>(M) * (H / kQBlock) * 4);
-    L.h = take(L.cap * I);
+    L.h = take(L.terms * L.cap * I);
     L.sh = take(L.cap * (I / kQBlock) * 4);
     L.ttiles = take(L.max_ttiles * 16);
-    L.act = take(L.cap * H);
+    L.act = take(L.terms * L.cap * H);
     L.sa = take(L.cap * (H / kQBlock) * 4);
     L.y = take(static_cast<size_t>(M) * topk * H * 2);  // bf16 y
     L.total = o;
@@ -285,10 +289,10 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
   PrepArgs p{};
   p.x = static_cast<const __nv_bfloat16*>(x);
   p.M = M; p.H = H;
-  p.kind = L.a8 ? 3 : kind == MOE_WEIGHT_FP8 ? 1 : kind == MOE_WEIGHT_INT4 ? 4 : 2;
+  p.kind = L.terms == 1 ? 3 : L.terms == 2 ? 5 : kind == MOE_WEIGHT_FP8 ? 1 : kind == MOE_WEIGHT_INT4 ? 4 : 2;
   p.q = at<void>(ws, L.xq);
   p.scale = at<float>(ws, L.sx);
-  if (!L.a8) {  // the intermediate's amax (INT8) or frame exponent (FP8, INT4) per position starts at zero
+  if (!L.terms) {  // the intermediate's amax (INT8) or frame exponent (FP8, INT4) per position starts at zero
     p.zero_words = at<uint32_t>(ws, kind == MOE_WEIGHT_INT8 ? L.hmax : L.hexp);
     p.n_zero = static_cast<int>(kind == MOE_WEIGHT_INT8 ? L.cap : 2 * L.cap);
   }
@@ -330,7 +334,7 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
     P.hmax = at<uint32_t>(ws, L.hmax);
     P.hq = at<__half>(ws, L.hq);
     P.sh = at<float>(ws, L.sh);
-  } else if (!L.a8) {
+  } else if (!L.terms) {
     P.hexp = at<uint32_t>(ws, L.hexp);
     P.hblk = at<uint8_t>(ws, L.hblk);
     if (L.path == MOE_PATH_PREFILL) P.hsc = at<float>(ws, L.hsc);
@@ -338,7 +342,8 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
   P.y = at<float>(ws, L.y);
   P.out = static_cast<__nv_bfloat16*>(out);
   P.status = a.status;
-  if (L.a8) {
+  if (L.terms) {
+    P.e4m3_terms = L.terms;
     P.xq8 = at<uint8_t>(ws, L.xq);
     P.sx8 = at<float>(ws, L.sx);
     P.act8 = at<uint8_t>(ws, L.act);
@@ -348,7 +353,7 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
     err = launch_prefill_a8(P, sms, stream, hook);
     if (err == cudaErrorInvalidConfiguration)
       return fail(MOE_ERR_CUDA, "FP8 x FP8 kernel was not built with its designed register count");
-    if (err != cudaSuccess) return cuda_fail(err, "prefill (FP8 activations) launch");
+    if (err != cudaSuccess) return cuda_fail(err, "prefill (FP8 tensor cores) launch");
     return MOE_OK;
   }
   if (L.path == MOE_PATH_PREFILL) {

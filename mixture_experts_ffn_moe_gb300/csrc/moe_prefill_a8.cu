@@ -72,13 +72,16 @@ constexpr int RED_BYTES = 2 * 2 * MAXN * 4;  // [tile parity][column half][token
 // Shared-memory layout per GEMM (measured): GEMM1 keeps 4 K-block stages; GEMM2, whose short
 // K loop (I = 2048) makes its y stores a large share of the tile, trades one stage for a
 // 4 KB y staging buffer per accumulator warp (64 bf16 columns, 128-byte row segments).
-template <bool GATED>
+// NT = 2 (two activation terms per value) doubles the activation tiles of a stage: both GEMMs then
+// keep 3 stages, and GEMM2 stages 32 columns of y at a time (2 KB per accumulator warp).
+template <bool GATED, int NT>
 struct Lay {
-  static constexpr int STAGES = GATED ? 4 : 3;
-  static constexpr int STG_BYTES = GATED ? 0 : 32 * 64 * 2;  // per accumulator warp: 32 tokens x 64 bf16 of y
+  static constexpr int STAGES = NT == 1 ? (GATED ? 4 : 3) : 3;
+  static constexpr int STG_COLS = NT == 1 ? 64 : 32;                // y columns staged per pass
+  static constexpr int STG_BYTES = GATED ? 0 : 32 * STG_COLS * 2;    // per accumulator warp: 32 tokens
   static constexpr int OFF_W = 0;
   static constexpr int OFF_A = OFF_W + STAGES * 2 * W_TILE;
-  static constexpr int OFF_S = OFF_A + STAGES * A_TILE;
+  static constexpr int OFF_S = OFF_A + STAGES * NT * A_TILE;
   static constexpr int OFF_RED = OFF_S + S_STAGES * S_SLOT;
   static constexpr int OFF_STG = OFF_RED + RED_BYTES;
   static constexpr int OFF_BAR = OFF_STG + N_ACC_WARPS * STG_BYTES;
@@ -153,13 +156,16 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int stages, long long
   }
 }
 
-template <bool GATED>
+// NT: activation terms per value -- 1: E4M3 activations (MOE_ACT_FP8_1X128); 2: the two-term E4M3 form
+// of the weight-only layer's bf16 x and fp32 h (hi codes in rows 0..cap-1 of the activation tensor, lo
+// codes in rows cap..2cap-1), whose two products accumulate into one partial sum.
+template <bool GATED, int NT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefill_a8_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
                       const __grid_constant__ CUtensorMap tmap_s, Args p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  using L = Lay<GATED>;
+  using L = Lay<GATED, NT>;
   constexpr int W_STAGES = L::STAGES, A_STAGES = L::STAGES;
   uint8_t* sW = smem + L::OFF_W;
   uint8_t* sA = smem + L::OFF_A;
@@ -245,10 +251,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const Tile tl = get_tile<GATED>(p, t);
           for (int kc = 0; kc < KC; ++kc) {
             if (!(ok = mbar_wait(&bars->st_empty[as], aph ^ 1, abort, p.status, kWaitLimit))) break;
-            mbar_arrive_expect_tx(&bars->op_full[as], tl.nmma * BK);
-            uint8_t* dst = sA + as * A_TILE;
-            for (int r = 0; r < tl.nmma; r += 16)
-              tma_load_2d(dst + r * BK, &tmap_b, &bars->op_full[as], kc * BK, tl.pos0 + r);
+            mbar_arrive_expect_tx(&bars->op_full[as], NT * tl.nmma * BK);
+            uint8_t* dst = sA + as * NT * A_TILE;
+#pragma unroll
+            for (int term = 0; term < NT; ++term)  // the lo codes of a position sit cap rows below its hi codes
+              for (int r = 0; r < tl.nmma; r += 16)
+                tma_load_2d(dst + term * A_TILE + r * BK, &tmap_b, &bars->op_full[as], kc * BK,
+                            term * p.cap + tl.pos0 + r);
             ++aseq;
             if (++as == A_STAGES) { as = 0; aph ^= 1; }
 
@@ -277,13 +286,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!(ok = mbar_wait(&bars->op_full[ws], wph, abort, p.status, kWaitLimit))) break;
             tc_fence_after();
             const uint32_t d0 = tbase + static_cast<uint32_t>(buf * 2 * BM);
-            const uint64_t ad = sw128_kmajor_desc(smem_addr(sA + as * A_TILE));           // tokens
+            uint64_t ad[NT];  // tokens: one tile per activation term
+#pragma unroll
+            for (int term = 0; term < NT; ++term)
+              ad[term] = sw128_kmajor_desc(smem_addr(sA + (as * NT + term) * A_TILE));
             const uint64_t b0 = sw128_kmajor_desc(smem_addr(sW + ws * 2 * W_TILE));        // weight block 0
             const uint64_t b1 = sw128_kmajor_desc(smem_addr(sW + ws * 2 * W_TILE + W_TILE));  // block 1
-  #pragma unroll
+#pragma unroll
             for (int k = 0; k < BK / 32; ++k) {  // 32 bytes (K = 32) per instruction: +2 in the encoded address
-              umma_e4m3(d0, ad + 2 * k, b0 + 2 * k, idesc, k != 0);
-              if (tl.two) umma_e4m3(d0 + BM, ad + 2 * k, b1 + 2 * k, idesc, k != 0);
+#pragma unroll
+              for (int term = 0; term < NT; ++term) {  // every term of the tokens into the same partial sum
+                umma_e4m3(d0, ad[term] + 2 * k, b0 + 2 * k, idesc, (k | term) != 0);
+                if (tl.two) umma_e4m3(d0 + BM, ad[term] + 2 * k, b1 + 2 * k, idesc, (k | term) != 0);
+              }
             }
             umma_commit(&bars->st_empty[ws]);  // == as: both rings advance one stage per K block
             umma_commit(&bars->p_full[buf]);
@@ -423,7 +438,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ok = mbar_wait(&bars->red_full[rb][q], static_cast<uint32_t>((ntile >> 1) & 1), abort, p.status, kWaitLimit);
         if (!(ok = __all_sync(0xffffffffu, ok))) break;
         const float amax = fmaxf(m, red[(rb * 2 + (ch ^ 1)) * MAXN + tok]);
-        if (live) {
+        if (live && NT == 2) {
+          // the two-term form of h in the frame of its 1 x 128 group: hi codes in row pos, lo codes in
+          // row cap + pos, the group's scale 2^e
+          const int e = amax > 0.f ? e4m3_split_exp(amax) : 0;
+          const float mul = exp2i(-e);
+          const int pos = tl.pos0 + tok;
+          uint4* dhi = reinterpret_cast<uint4*>(p.hq + static_cast<size_t>(pos) * p.n_rows_out + tl.n0 + ch * 64);
+          uint4* dlo = reinterpret_cast<uint4*>(p.hq + static_cast<size_t>(p.cap + pos) * p.n_rows_out + tl.n0 + ch * 64);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t whi[4], wlo[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int j = v * 16 + u * 4;
+              e4m3_split4(make_float4(hv[j], hv[j + 1], hv[j + 2], hv[j + 3]), mul, whi[u], wlo[u]);
+            }
+            dhi[v] = make_uint4(whi[0], whi[1], whi[2], whi[3]);
+            dlo[v] = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
+          }
+          if (ch == 0) p.hs[static_cast<size_t>(tl.n0 / kQBlock) * p.cap + pos] = exp2i(e);
+        } else if (live) {
           // s = amax / 448 and codes of h / s, by reciprocals (h codes are covered by the layer tolerance)
           const float s = amax > 0.f ? amax * (1.0f / 448.0f) : 1.0f;
           const float inv = amax > 0.f ? 448.0f * __frcp_rn(amax) : 1.0f;
@@ -447,38 +482,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       } else {
         // y[slot] = acc x routing weight in bf16.  A thread holds one token's row, so direct stores
-        // would put 32 rows in every warp instruction; instead the warp stages the 64 columns of
-        // its 32 rows in shared memory and writes them back row by row: 128 contiguous bytes per
-        // row, 4 rows per instruction.  The 16-byte chunk j of row r sits at chunk j ^ (r & 7),
-        // which keeps both the row-wise writes and the column-wise reads free of bank conflicts
-        // (8 lanes, one 128-byte phase, always touch 8 different chunk columns).
+        // would put 32 rows in every warp instruction; instead the warp stages STG_COLS columns of its
+        // 32 rows in shared memory at a time and writes them back row by row (2 * STG_COLS contiguous
+        // bytes per row).  The 16-byte chunk j of row r sits at chunk j ^ (r & 7) with 8 chunks a row,
+        // j ^ ((r >> 1) & 3) with 4, which keeps both the row-wise writes and the column-wise reads
+        // free of bank conflicts (8 lanes, one 128-byte phase, always touch 8 different chunk columns).
+        constexpr int CH = L::STG_COLS / 8;  // 16-byte chunks per staged row
+        constexpr int RPI = 32 / CH;         // rows per read-back instruction
+        auto swz = [](int r, int j) { return CH == 8 ? (j ^ (r & 7)) : (j ^ ((r >> 1) & 3)); };
         uint4* stg = reinterpret_cast<uint4*>(smem + L::OFF_STG + (warp - WARP_ACC0) * L::STG_BYTES);
-        const int rr = lane >> 3, cj = lane & 7;  // read-back: rows rr + 4i, chunk cj
+        const int rr = lane / CH, cj = lane % CH;  // read-back: rows rr + RPI i, chunk cj
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
           if (!quarter_live || (b == 1 && !tl.two)) break;
           const float2* a = b ? acc1 : acc0;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint32_t w[4];
+          for (int part = 0; part < 64 / L::STG_COLS; ++part) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(a[4 * j + u].x * wgt, a[4 * j + u].y * wgt);
-              w[u] = *reinterpret_cast<const uint32_t*>(&h2);
+            for (int j = 0; j < CH; ++j) {
+              uint32_t w[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float2 v2 = a[4 * (part * CH + j) + u];
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(v2.x * wgt, v2.y * wgt);
+                w[u] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+              stg[lane * CH + swz(lane, j)] = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            stg[lane * 8 + (j ^ (lane & 7))] = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-          __syncwarp();
-          const int col = tl.n0 + b * BM + ch * 64 + cj * 8;
+            __syncwarp();
+            const int col = tl.n0 + b * BM + ch * 64 + part * L::STG_COLS + cj * 8;
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int r = rr + 4 * i;
-            const int rslot = __shfl_sync(0xffffffffu, slot, r);
-            const uint4 val = stg[r * 8 + (cj ^ (r & 7))];
-            if (q * 32 + r < tl.cnt)
-              *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(rslot) * p.n_rows_out + col) = val;
+            for (int i = 0; i < CH; ++i) {
+              const int r = rr + RPI * i;
+              const int rslot = __shfl_sync(0xffffffffu, slot, r);
+              const uint4 val = stg[r * CH + swz(r, cj)];
+              if (q * 32 + r < tl.cnt)
+                *reinterpret_cast<uint4*>(p.y + static_cast<size_t>(rslot) * p.n_rows_out + col) = val;
+            }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
       ++ntile;
@@ -500,11 +542,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // E4M3 activation rows and their 1 x 128 scales in sorted (expert-contiguous)
 // order; padding rows get zero codes and zero scales.  Scales are stored
 // transposed, [H/128, cap], so a token tile's scales of one K block are
-// contiguous for the TMA.
+// contiguous for the TMA.  With nt = 2 the codes come in two terms: rows
+// M..2M-1 of xq (the lo codes) go to rows cap..2cap-1 of act.
 __global__ void __launch_bounds__(256) gather_a8_kernel(const uint8_t* __restrict__ xq, const float* __restrict__ sx,
                                                         const int32_t* __restrict__ sorted_ids,
                                                         const int32_t* __restrict__ num_post, int n_slots, int topk,
-                                                        int H, int cap, uint8_t* __restrict__ act,
+                                                        int H, int cap, int M, int nt, uint8_t* __restrict__ act,
                                                         float* __restrict__ sa) {
   pdl_wait();
   pdl_trigger();
@@ -513,12 +556,16 @@ __global__ void __launch_bounds__(256) gather_a8_kernel(const uint8_t* __restric
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   const long long first = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
   const long long total = static_cast<long long>(rows) * chunks;
-  for (long long i = first; i < total; i += stride) {
-    const int pos = static_cast<int>(i / chunks), c = static_cast<int>(i - static_cast<long long>(pos) * chunks);
-    const int slot = __ldg(sorted_ids + pos);
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (slot < n_slots) v = ld_v4(xq + static_cast<size_t>(slot / topk) * H + c * 16);
-    *reinterpret_cast<uint4*>(act + static_cast<size_t>(pos) * H + c * 16) = v;
+  for (int term = 0; term < nt; ++term) {
+    const uint8_t* src = xq + static_cast<size_t>(term) * M * H;
+    uint8_t* dst = act + static_cast<size_t>(term) * cap * H;
+    for (long long i = first; i < total; i += stride) {
+      const int pos = static_cast<int>(i / chunks), c = static_cast<int>(i - static_cast<long long>(pos) * chunks);
+      const int slot = __ldg(sorted_ids + pos);
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (slot < n_slots) v = ld_v4(src + static_cast<size_t>(slot / topk) * H + c * 16);
+      *reinterpret_cast<uint4*>(dst + static_cast<size_t>(pos) * H + c * 16) = v;
+    }
   }
   const long long total_s = static_cast<long long>(G) * rows;
   for (long long i = first; i < total_s; i += stride) {
@@ -529,11 +576,11 @@ __global__ void __launch_bounds__(256) gather_a8_kernel(const uint8_t* __restric
 }
 
 // ------------------------------------------------------------------ host side
-template <bool GATED>
+template <bool GATED, int NT>
 static cudaError_t launch_a8_gemm(const pfa8::Args& a, const void* w, uint64_t w_rows, const void* b,
                                   const float* bs, int num_sms, cudaStream_t s) {
   using namespace pfa8;
-  auto kern = prefill_a8_kernel<GATED>;
+  auto kern = prefill_a8_kernel<GATED, NT>;
   // The register split (setmaxnreg) is only safe when the kernel was built with
   // the launch-bounds register count it was designed for.
   cudaFuncAttributes fa;
@@ -545,23 +592,24 @@ static cudaError_t launch_a8_gemm(const pfa8::Args& a, const void* w, uint64_t w
                       CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, static_cast<uint64_t>(a.K),
-                      static_cast<uint64_t>(a.cap), BK, 16, CU_TENSOR_MAP_SWIZZLE_128B))
+                      static_cast<uint64_t>(NT) * a.cap, BK, 16, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, bs, static_cast<uint64_t>(a.cap),
                       static_cast<uint64_t>(a.K / kQBlock), MAXN, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  constexpr int SMEM_BYTES = Lay<GATED>::SMEM_BYTES;
+  constexpr int SMEM_BYTES = Lay<GATED, NT>::SMEM_BYTES;
   err = set_smem_limit_once(reinterpret_cast<const void*>(kern), SMEM_BYTES);
   if (err != cudaSuccess) return err;
   return launch_kernel(kern, dim3(num_sms), dim3(NUM_THREADS), SMEM_BYTES, s, true, mw, mb, ms, a);
 }
 
-cudaError_t launch_prefill_a8(const LayerPlan& P, int num_sms, cudaStream_t s, const StageHook& hook) {
+template <int NT>
+static cudaError_t launch_prefill_e4m3(const LayerPlan& P, int num_sms, cudaStream_t s, const StageHook& hook) {
   cudaError_t err;
   {
     const int grid = num_sms * 8;
     err = launch_kernel(gather_a8_kernel, dim3(grid), dim3(256), 0, s, true, P.xq8, P.sx8, P.sorted_ids,
-                        P.num_post, P.M * P.topk, P.topk, P.H, P.cap, P.act8, P.sa8);
+                        P.num_post, P.M * P.topk, P.topk, P.H, P.cap, P.M, NT, P.act8, P.sa8);
     if (err != cudaSuccess) return err;
     hook("prefill_gather", s);
   }
@@ -579,7 +627,7 @@ cudaError_t launch_prefill_a8(const LayerPlan& P, int num_sms, cudaStream_t s, c
   g1.hq = P.h8;
   g1.hs = P.sh8;
   g1.status = P.status;
-  err = launch_a8_gemm<true>(g1, P.w13, static_cast<uint64_t>(P.E) * 2 * P.I, P.act8, P.sa8, num_sms, s);
+  err = launch_a8_gemm<true, NT>(g1, P.w13, static_cast<uint64_t>(P.E) * 2 * P.I, P.act8, P.sa8, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("prefill_gemm1", s);
   pfa8::Args g2{};
@@ -596,13 +644,17 @@ cudaError_t launch_prefill_a8(const LayerPlan& P, int num_sms, cudaStream_t s, c
   g2.topk_w = P.topk_w;
   g2.y = reinterpret_cast<__nv_bfloat16*>(P.y);  // bf16 rows in the fp32 buffer's space
   g2.status = P.status;
-  err = launch_a8_gemm<false>(g2, P.w2, static_cast<uint64_t>(P.E) * P.H, P.h8, P.sh8, num_sms, s);
+  err = launch_a8_gemm<false, NT>(g2, P.w2, static_cast<uint64_t>(P.E) * P.H, P.h8, P.sh8, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("prefill_gemm2", s);
   err = launch_combine(reinterpret_cast<const __nv_bfloat16*>(P.y), P.inv_pos, P.M, P.topk, P.H, P.out, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("combine", s);
   return cudaSuccess;
+}
+
+cudaError_t launch_prefill_a8(const LayerPlan& P, int num_sms, cudaStream_t s, const StageHook& hook) {
+  return P.e4m3_terms == 2 ? launch_prefill_e4m3<2>(P, num_sms, s, hook) : launch_prefill_e4m3<1>(P, num_sms, s, hook);
 }
 
 }  // namespace gbmoe
