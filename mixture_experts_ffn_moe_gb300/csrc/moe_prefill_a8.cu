@@ -251,13 +251,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const Tile tl = get_tile<GATED>(p, t);
           for (int kc = 0; kc < KC; ++kc) {
             if (!(ok = mbar_wait(&bars->st_empty[as], aph ^ 1, abort, p.status, kWaitLimit))) break;
-            mbar_arrive_expect_tx(&bars->op_full[as], NT * tl.nmma * BK);
+            // one 128-row box per term: the MMA always reads 128 token rows, and the rows past the tile's
+            // count (the next positions, or zero fill past the tensor) only feed TMEM lanes nobody reads
+            mbar_arrive_expect_tx(&bars->op_full[as], NT * A_TILE);
             uint8_t* dst = sA + as * NT * A_TILE;
 #pragma unroll
             for (int term = 0; term < NT; ++term)  // the lo codes of a position sit cap rows below its hi codes
-              for (int r = 0; r < tl.nmma; r += 16)
-                tma_load_2d(dst + term * A_TILE + r * BK, &tmap_b, &bars->op_full[as], kc * BK,
-                            term * p.cap + tl.pos0 + r);
+              tma_load_2d(dst + term * A_TILE, &tmap_b, &bars->op_full[as], kc * BK, term * p.cap + tl.pos0);
             ++aseq;
             if (++as == A_STAGES) { as = 0; aph ^= 1; }
 
@@ -592,7 +592,7 @@ static cudaError_t launch_a8_gemm(const pfa8::Args& a, const void* w, uint64_t w
                       CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, static_cast<uint64_t>(a.K),
-                      static_cast<uint64_t>(NT) * a.cap, BK, 16, CU_TENSOR_MAP_SWIZZLE_128B))
+                      static_cast<uint64_t>(NT) * a.cap, BK, MAXN, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, bs, static_cast<uint64_t>(a.cap),
                       static_cast<uint64_t>(a.K / kQBlock), MAXN, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
