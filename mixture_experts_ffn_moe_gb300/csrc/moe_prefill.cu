@@ -293,10 +293,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const Tile tl = get_tile<GATED>(p, t);
         for (int kc = 0; kc < KC; ++kc) {
           if (!(ok = mbar_wait(&bars->act_empty[as], aph ^ 1, abort, p.status, kWaitLimit))) break;
-          mbar_arrive_expect_tx(&bars->act_full[as], tl.nmma * BK * 2);
-          uint8_t* dst = sB + as * B_TILE;
-          for (int r = 0; r < tl.nmma; r += 16)
-            tma_load_2d(dst + r * (BK * 2), &tmap_b, &bars->act_full[as], kc * BK, tl.pos0 + r);
+          // one 128-row box: rows past the tile's count (the next positions, or zero fill past the
+          // tensor) only feed accumulator lanes or columns that no epilogue reads
+          mbar_arrive_expect_tx(&bars->act_full[as], B_TILE);
+          tma_load_2d(sB + as * B_TILE, &tmap_b, &bars->act_full[as], kc * BK, tl.pos0);
 #pragma unroll
           for (int i = 0; i < ACT_STAGES; ++i)
             if (i == as) last_par[i] = static_cast<int>(aph);
@@ -867,7 +867,7 @@ static cudaError_t launch_gemm(const PrefillArgs& a, const void* w, uint64_t w_r
   if (!encode_tmap_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, static_cast<uint64_t>(I4 ? a.K / 2 : a.K), w_rows,
                       I4 ? pf::BK / 2 : pf::BK, pf::BM, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  if (!encode_tmap_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, b, static_cast<uint64_t>(a.K), b_rows, pf::BK, 16,
+  if (!encode_tmap_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, b, static_cast<uint64_t>(a.K), b_rows, pf::BK, pf::MAXN,
                 CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   auto kern = pf::prefill_gemm_kernel<WK, GATED>;
