@@ -126,7 +126,8 @@ KERNEL_SOURCES = {  # kernel -> the source files that define it
 
 
 def source_hash(kernel: str, a8: bool = False) -> str:
-    """Hash of the kernel's own source file and the headers it includes."""
+    """Hash of the kernel's own source file and the headers it includes (a8: the FP8-operand prefill kernels,
+    which run every FP8-weight layer on the tcgen05 path)."""
     csrc = os.path.join(ROOT, "mixture_experts_ffn_moe_gb300", "csrc")
     h = hashlib.sha256()
     src = "moe_prefill_a8.cu" if a8 and kernel.startswith("prefill") else KERNEL_SOURCES.get(kernel, "")
@@ -170,10 +171,14 @@ def roofline_of(shape, ids, stages, n_calls, workload, peaks):
     # bf16 rate; E4M3 x E4M3 at twice it (the nominal FP8:BF16 ratio, 4.5 : 2.25 PFLOP/s).
     if shape.act == "fp8_1x128":
         tpeak, tsrc = 2.0 * peaks["bf16_tflops"], peaks["source"] + " bf16 dense x 2 (nominal FP8:BF16 ratio)"
+    elif shape.weight_kind == "fp8" and shape.M > gbmoe.MOE_MAX_DECODE_TOKENS and dominant.startswith("prefill"):
+        # two E4M3 products per product at the FP8 rate (twice bf16): the same bound as one bf16 product
+        tpeak, tsrc = peaks["bf16_tflops"], peaks["source"] + (" bf16 dense (two-term E4M3 activations: two FP8 "
+                                                                "products per product at twice the bf16 rate)")
     else:
         tpeak, tsrc = peaks["bf16_tflops"], peaks["source"] + " bf16 dense (fp16 same rate)"
     ridge = tpeak * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    a8 = shape.act == "fp8_1x128"
+    a8 = shape.weight_kind == "fp8" and dominant.startswith("prefill")  # FP8 weights: the FP8-operand kernels
     if dflops / dbytes > ridge:
         achieved = dflops / secs / 1e12
         return {"bound": "tensor", "kernel": dominant, "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
@@ -296,10 +301,13 @@ class ClockSampler:
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
+    _count = 0
+
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join("/tmp", f"gbmoe_clocks_{os.getpid()}.csv")
+        ClockSampler._count += 1  # one file per sampler: several may run in one process
+        self.path = os.path.join("/tmp", f"gbmoe_clocks_{os.getpid()}_{ClockSampler._count}.csv")
         self.samples = None
 
     def _lines(self):
@@ -619,6 +627,7 @@ def run_ours(args, shape):
                "seconds": dt, "cpu_model": cpu_model(),
                "one_core": {"value": 1.0 / one, "unit": "tokens/s", "cores": 1, "seconds": one} if one else None,
                "tiny_layer": tiny_cpu_baseline()}
+    main_clocks = clocks.summary()
     # ---- the other configurations of the layer, each timed the same way (N = 1 only)
     also = None
     if world == 1 and not args.no_also and args.workload == DEFAULT_WORKLOAD:
@@ -631,7 +640,7 @@ def run_ours(args, shape):
         "roofline": roofline, "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": sum(1 for _ in stages) * n_calls,
-        "clocks": clocks.summary(),
+        "clocks": main_clocks,
         "parity": parity,
         "routing": routing,
         "layer": {"weight_gbs": layer_bytes / (ms_per_step * 1e-3) / 1e9,
@@ -651,8 +660,14 @@ def run_ours(args, shape):
 
 
 def dtype_of(shape, kind):
+    """The arithmetic the call's path computes in (MOE_PATH_AUTO: the weight-streaming kernels up to
+    MOE_MAX_DECODE_TOKENS tokens, the tcgen05 kernels above; FP8 activations always on tcgen05)."""
     if kind == gbmoe.MOE_WEIGHT_FP8:
-        return "fp8 x fp8 mma, f32 acc" if shape.act == "fp8_1x128" else "fp8->f16 mma, f32 acc"
+        if shape.act == "fp8_1x128":
+            return "fp8 x fp8 mma, f32 acc"
+        if shape.M > gbmoe.MOE_MAX_DECODE_TOKENS:
+            return "fp8 x fp8 mma (bf16 x and fp32 h as two e4m3 terms), f32 acc"
+        return "fp8->f16 mma, f32 acc"
     return "int8->f16 mma, f32 acc" if kind == gbmoe.MOE_WEIGHT_INT8 else "int4->f16 mma, f32 acc"
 
 
