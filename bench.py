@@ -56,6 +56,8 @@ def workloads():
         "dsr1_prefill_M16384_a8": synth.deepseek_r1(16384, routing="deepseek_zipf", act="fp8_1x128"),
         **{f"dsr1_sweep_M{m}": synth.deepseek_r1(m, routing="uniform") for m in (1, 2, 4, 8, 16, 32, 64)},
         **{f"qwen3_M{m}": synth.qwen3_235b(m) for m in (1, 16, 256, 4096)},
+        **{f"qwen3_M{m}": synth.qwen3_235b(m) for m in (64, 96, 128)},
+        **{f"dsr1_decode_M{m}": synth.deepseek_r1(m) for m in (64, 96, 128)},
         "tiny_M16": synth.tiny(),
         # same per-expert work with 32+1 experts: small enough for full ncu captures
         "dsr1_decode_M4_E32": synth.deepseek_r1(4, E=32),
@@ -171,7 +173,7 @@ def roofline_of(shape, ids, stages, n_calls, workload, peaks):
     # bf16 rate; E4M3 x E4M3 at twice it (the nominal FP8:BF16 ratio, 4.5 : 2.25 PFLOP/s).
     if shape.act == "fp8_1x128":
         tpeak, tsrc = 2.0 * peaks["bf16_tflops"], peaks["source"] + " bf16 dense x 2 (nominal FP8:BF16 ratio)"
-    elif shape.weight_kind == "fp8" and shape.M > gbmoe.MOE_MAX_DECODE_TOKENS and dominant.startswith("prefill"):
+    elif shape.weight_kind == "fp8" and shape.M >= gbmoe.MOE_AUTO_PREFILL_TOKENS and dominant.startswith("prefill"):
         # two E4M3 products per product at the FP8 rate (twice bf16): the same bound as one bf16 product
         tpeak, tsrc = peaks["bf16_tflops"], peaks["source"] + (" bf16 dense (two-term E4M3 activations: two FP8 "
                                                                 "products per product at twice the bf16 rate)")
@@ -661,11 +663,11 @@ def run_ours(args, shape):
 
 def dtype_of(shape, kind):
     """The arithmetic the call's path computes in (MOE_PATH_AUTO: the weight-streaming kernels up to
-    MOE_MAX_DECODE_TOKENS tokens, the tcgen05 kernels above; FP8 activations always on tcgen05)."""
+    MOE_AUTO_PREFILL_TOKENS tokens, the tcgen05 kernels from there; FP8 activations always on tcgen05)."""
     if kind == gbmoe.MOE_WEIGHT_FP8:
         if shape.act == "fp8_1x128":
             return "fp8 x fp8 mma, f32 acc"
-        if shape.M > gbmoe.MOE_MAX_DECODE_TOKENS:
+        if shape.M >= gbmoe.MOE_AUTO_PREFILL_TOKENS:
             return "fp8 x fp8 mma (bf16 x and fp32 h as two e4m3 terms), f32 acc"
         return "fp8->f16 mma, f32 acc"
     return "int8->f16 mma, f32 acc" if kind == gbmoe.MOE_WEIGHT_INT8 else "int4->f16 mma, f32 acc"

@@ -57,7 +57,8 @@ typedef enum {
 } moe_status_t;
 
 /* flags of fused_moe_fp8 / fused_moe_int8 / fused_moe_int4 / fused_moe_gated */
-#define MOE_PATH_AUTO 0x0u    /* pick by tokens per expert                          */
+#define MOE_PATH_AUTO 0x0u    /* decode below MOE_AUTO_PREFILL_TOKENS tokens (INT4: up to
+                                 MOE_MAX_DECODE_TOKENS), else prefill                 */
 #define MOE_PATH_DECODE 0x1u  /* weight-streaming GEMV path (small token counts)    */
 #define MOE_PATH_PREFILL 0x2u /* tcgen05 grouped-GEMM path (large token counts)     */
 #define MOE_PATH_MASK 0x3u
@@ -75,6 +76,7 @@ typedef enum {
 /* Limits of this implementation (larger sizes return MOE_ERR_UNSUPPORTED). */
 #define MOE_MAX_EXPERTS 1024
 #define MOE_MAX_DECODE_TOKENS 128 /* MOE_PATH_DECODE handles M <= this */
+#define MOE_AUTO_PREFILL_TOKENS 128 /* MOE_PATH_AUTO takes the tcgen05 path from this many tokens */
 
 /*
  * Capacity (entries) of sorted_ids for the given routing problem:

@@ -110,7 +110,10 @@ static int choose_path(int M, int kind, unsigned flags) {
   const unsigned p = flags & MOE_PATH_MASK;
   if (p == MOE_PATH_DECODE || p == MOE_PATH_PREFILL) return static_cast<int>(p);
   if (flags & MOE_ACT_FP8_1X128) return MOE_PATH_PREFILL;  // the FP8 x FP8 products run on tcgen05 only
-  return M <= MOE_MAX_DECODE_TOKENS ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
+  // measured crossover (A/B on GB300): the weight-streaming kernels win at 96 tokens (DeepSeek-R1 FP8 3%, Qwen3
+  // INT8 14%), the tcgen05 kernels at 128 (3% and 7%); INT4 keeps the weight-streaming kernels up to 128
+  if (kind == MOE_WEIGHT_INT4) return M <= MOE_MAX_DECODE_TOKENS ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
+  return M < MOE_AUTO_PREFILL_TOKENS ? MOE_PATH_DECODE : MOE_PATH_PREFILL;
 }
 
 static Layout plan(int M, int H, int I, int E, int topk, int kind, unsigned flags) {

@@ -586,6 +586,7 @@ __global__ void __launch_bounds__(128) requant_h_kernel(const float* __restrict_
 
 cudaError_t launch_requant_rows(const void* h, const uint32_t* hmax, const int32_t* num_post, int cap, int I,
                                 __half* hq, float* sh, int num_sms, cudaStream_t s) {
+  // cap: an upper bound of the padded positions (a CTA per row up to 8 per SM); the device count decides
   int grid = cap < num_sms * 8 ? cap : num_sms * 8;
   if (grid < 1) grid = 1;
   return launch_kernel(requant_h_kernel, dim3(grid), dim3(128), 0, s, true, static_cast<const float*>(h), hmax,
@@ -662,7 +663,10 @@ cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cuda
   hook("decode_gemm1", s);
   const __half* b2 = static_cast<const __half*>(P.h);
   if (weight_kind == MOE_WEIGHT_INT8) {
-    err = launch_requant_rows(P.h, P.hmax, P.num_post, P.cap, P.I, P.hq, P.sh, num_sms, s);
+    // padded positions: the slots plus at most B - 1 padding rows for each of at most min(E, slots) experts
+    const long long rows = slots + (slots < P.E ? slots : P.E) * (kDecodeBlock - 1);
+    err = launch_requant_rows(P.h, P.hmax, P.num_post, rows < P.cap ? static_cast<int>(rows) : P.cap, P.I, P.hq,
+                              P.sh, num_sms, s);
     if (err != cudaSuccess) return err;
     hook("requant_h", s);
     b2 = P.hq;

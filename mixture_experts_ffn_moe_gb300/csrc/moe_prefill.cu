@@ -912,7 +912,11 @@ cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cud
   hook("prefill_gemm1", s);
   const __half* b2 = reinterpret_cast<const __half*>(P.h);
   if (weight_kind == MOE_WEIGHT_INT8) {
-    err = launch_requant_rows(P.h, P.hmax, P.num_post, P.cap, P.I, P.hq, P.sh, num_sms, s);
+    // padded positions: the slots plus at most B - 1 padding rows for each of at most min(E, slots) experts
+    const long long slots = static_cast<long long>(P.M) * P.topk;
+    const long long rows = slots + (slots < P.E ? slots : P.E) * (kPrefillBlock - 1);
+    err = launch_requant_rows(P.h, P.hmax, P.num_post, rows < P.cap ? static_cast<int>(rows) : P.cap, P.I, P.hq,
+                              P.sh, num_sms, s);
     if (err != cudaSuccess) return err;
     hook("requant_h", s);
     b2 = P.hq;

@@ -24,6 +24,7 @@ MOE_WEIGHT_INT8 = 1
 MOE_WEIGHT_INT4 = 2
 MOE_MAX_EXPERTS = 1024
 MOE_MAX_DECODE_TOKENS = 128
+MOE_AUTO_PREFILL_TOKENS = 128
 MOE_STATIC_SCRATCH_BYTES = 16 << 20
 MOE_GATE_SOFTMAX = 0
 MOE_GATE_SIGMOID_GROUPED = 1
