@@ -2,7 +2,7 @@
 
 The FP8 and INT4 weight-only layers multiply fp16 operands on the tensor cores while
 x arrives as bf16 (the exponent range of fp32) and the intermediate h is an fp32
-result.  Both are carried in power-of-two frames (one per x row, one per 64-column
+result.  Both are carried in power-of-two frames (one per x row, one per 32-column
 block of h, brought to one frame per row before the down projection), and on the
 tcgen05 path the FP8 block scales are folded into the weights relative to a frame per
 128-row block.  These tests push each of those past fp16's range on both kernel
@@ -11,7 +11,7 @@ paths:
 * x rows whose magnitudes run from 1e-12 to 1e15 (fp16 holds neither end), each row
   also checked against its own norm;
 * an intermediate h far past fp16's largest value (65504);
-* rows of h whose 64-column blocks lie up to 18 binades apart, with the down projection
+* rows of h whose 32-column blocks lie up to 18 binades apart, with the down projection
   weighting the small blocks up so that they carry half of every output;
 * FP8 block scales drawn log-uniformly from 2^-20 to 2^8.
 """
@@ -109,7 +109,7 @@ def test_h_past_fp16_max(kind, path):
 
 @pytest.mark.parametrize("path", sorted(PATHS))
 def test_h_blocks_in_distant_frames(path):
-    """Gate row block rb of every expert scaled by 2^(6 rb): h's 64-column blocks 2 rb, 2 rb + 1
+    """Gate row block rb of every expert scaled by 2^(6 rb): h's 32-column blocks 4 rb .. 4 rb + 3
     then lie 6 binades apart per row block, 18 across the row (several frames, so rows have
     blocks below their frame), and W2's K blocks are scaled by 2^(-6 kb) so each carries as
     much of y."""
