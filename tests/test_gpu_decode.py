@@ -121,7 +121,9 @@ def test_fp8_expert_id_structured_layer():
     assert np.all(out == out[:, :1])
 
 
-@pytest.mark.parametrize("M,H,I,E,k", [(16, 256, 128, 8, 2), (50, 512, 384, 12, 4), (128, 256, 256, 5, 2)])
+# from under one slot per expert (6 x 2 over 16 experts) to about 51 (128 x 2 over 5: seven 8-slot tiles each)
+@pytest.mark.parametrize("M,H,I,E,k", [(16, 256, 128, 8, 2), (50, 512, 384, 12, 4), (128, 256, 256, 5, 2),
+                                       (6, 256, 128, 16, 2)])
 def test_int8_layer(M, H, I, E, k):
     shape = synth.LayerShape("q", M, H, I, E, k, "int8", "softmax")
     d = synth.make_layer(shape, seed=M * 3 + E)
@@ -196,6 +198,12 @@ def test_qwen3_int8_full_size_batch16():
 
 def test_qwen3_int8_full_size_batch1():
     _full_size_check(synth.qwen3_235b(1), seed=15, rows=[0], kind="int8")
+
+
+def test_qwen3_int8_full_size_batch96():
+    # the largest batch MOE_PATH_AUTO gives the weight-streaming kernels: 768 slots over 128 experts, 21 of
+    # them with more than one 8-slot tile; rows covering every active expert
+    _full_size_check(synth.qwen3_235b(96), seed=16, rows=None, kind="int8")
 
 
 @pytest.mark.parametrize("M", [2, 8, 16, 32])
