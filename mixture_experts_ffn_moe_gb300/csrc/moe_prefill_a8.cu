@@ -382,6 +382,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
              mbar_wait(&bars->p_full[buf], pph[buf], abort, p.status, kWaitLimit);
         if (!(ok = __all_sync(0xffffffffu, ok))) break;
         tc_fence_after();
+        // the TMEM buffer and the factor slot go back as soon as the last partials are in registers,
+        // before their FMAs
+        auto release = [&]() {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&bars->p_empty[buf]);
+            mbar_arrive(&bars->s_empty[ss]);
+          }
+        };
         if (quarter_live) {
           const float* fs = sS + ss * (S_SLOT / 4);
           const float2 fa = make_float2(fs[MAXN + tok], fs[MAXN + tok]);          // a_scale x w_scale, block 0
@@ -393,6 +403,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_ld32(base + c * 32, r0);
             if (tl.two) tmem_ld32(base + BM + c * 32, r1);
             tmem_ld_wait();
+            if (c == 1) release();
 #pragma unroll
             for (int j = 0; j < 32; j += 2)
               acc0[(c * 32 + j) / 2] =
@@ -404,12 +415,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                     fb, acc1[(c * 32 + j) / 2]);
             }
           }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&bars->p_empty[buf]);
-          mbar_arrive(&bars->s_empty[ss]);
+        } else {
+          release();
         }
         if constexpr (!GATED) {
           if (kc == 0 && live) wgt = __ldg(p.topk_w + slot);  // the slot has arrived by now
