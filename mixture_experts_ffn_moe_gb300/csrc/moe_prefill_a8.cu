@@ -87,17 +87,17 @@ struct Lay {
   static constexpr int OFF_BAR = OFF_STG + N_ACC_WARPS * STG_BYTES;
   static constexpr int SMEM_BYTES = OFF_BAR + 512 + 1024;  // + slack to align the base to 1024
   static_assert(STAGES <= MAX_STAGES && SMEM_BYTES <= 232448, "shared memory per CTA");
+  static_assert(STAGES >= 3, "the accumulator warps wait on the stage barriers: more stages than TMEM buffers");
 };
 constexpr long long kWaitLimit = 4000000000LL;    // ~2 s of SM clocks per wait
 
 struct Bars {
   uint64_t op_full[MAX_STAGES];   // weight and activation stages of a K block landed (TMA, two producers)
-  uint64_t st_empty[MAX_STAGES];  // the MMAs of a K block have read its weight and activation stages
+  uint64_t st_empty[MAX_STAGES];  // the MMAs of a K block are done: its stages are free, its partials in TMEM
   uint64_t s_full[S_STAGES];   // activation scale vector landed (TMA)
   uint64_t f_full[S_STAGES];   // factor vectors written (scale warp)
   uint64_t s_empty[S_STAGES];  // factor vectors consumed (accumulator warps)
-  uint64_t p_full[2];          // partial sums of a K block in TMEM buffer
-  uint64_t p_empty[2];
+  uint64_t p_empty[2];         // the accumulator warps have read a TMEM buffer
   uint64_t red_full[2][4];     // [tile parity][lane quarter]: both column halves wrote their token maxima
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -188,7 +188,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&bars->s_empty[i], N_ACC_WARPS);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->p_full[i], 1);
       mbar_init(&bars->p_empty[i], N_ACC_WARPS);
       for (int j = 0; j < 4; ++j) mbar_init(&bars->red_full[i][j], 64);
     }
@@ -300,8 +299,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (tl.two) umma_e4m3(d0 + BM, ad[term] + 2 * k, b1 + 2 * k, idesc, (k | term) != 0);
               }
             }
-            umma_commit(&bars->st_empty[ws]);  // == as: both rings advance one stage per K block
-            umma_commit(&bars->p_full[buf]);
+            // one commit per K block (== as: both rings advance one stage per K block): it frees the stage and
+            // tells the accumulator warps that the partial sums are in TMEM buffer `buf`
+            umma_commit(&bars->st_empty[ws]);
             eph[buf] ^= 1;
             buf ^= 1;
             if (++ws == W_STAGES) { ws = 0; wph ^= 1; }
@@ -359,9 +359,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int tok = q * 32 + lane;              // token (TMEM lane) inside the tile
     const uint32_t lane_addr = tbase + (static_cast<uint32_t>(q * 32) << 16);
     int ntile = 0;  // tiles this CTA has finished (selects the exchange buffer and its phase)
-    int ss = 0, buf = 0;
-    uint32_t fph = 0;
-    uint32_t pph[2] = {0, 0};
+    // The partial sums of K block j are ready when its stage barrier st_empty[j % STAGES] completes phase
+    // j / STAGES.  That barrier cannot run a phase ahead of these warps: its next phase needs the MMAs of
+    // K block j + STAGES, which wait for the TMEM buffer these warps free after K block j + STAGES - 2 > j.
+    int ss = 0, buf = 0, ks = 0;
+    uint32_t fph = 0, kph = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
       const Tile tl = get_tile<GATED>(p, t);
@@ -379,7 +381,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int kc = 0; kc < KC; ++kc) {
         // a lane that gives up takes its whole warp with it (the warp meets at __syncwarp below)
         ok = mbar_wait(&bars->f_full[ss], fph, abort, p.status, kWaitLimit) &&
-             mbar_wait(&bars->p_full[buf], pph[buf], abort, p.status, kWaitLimit);
+             mbar_wait(&bars->st_empty[ks], kph, abort, p.status, kWaitLimit);
         if (!(ok = __all_sync(0xffffffffu, ok))) break;
         tc_fence_after();
         // the TMEM buffer and the factor slot go back as soon as the last partials are in registers,
@@ -421,8 +423,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if constexpr (!GATED) {
           if (kc == 0 && live) wgt = __ldg(p.topk_w + slot);  // the slot has arrived by now
         }
-        pph[buf] ^= 1;
         buf ^= 1;
+        if (++ks == W_STAGES) { ks = 0; kph ^= 1; }
         if (++ss == S_STAGES) { ss = 0; fph ^= 1; }
       }
       if (!ok) break;
