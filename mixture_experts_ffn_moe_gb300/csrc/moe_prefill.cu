@@ -701,16 +701,17 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __half* __restri
                                                           int topk, int H, __half* __restrict__ act) {
   pdl_wait();
   pdl_trigger();
+  // one warp per position, its lanes over the row's 16-byte chunks
   const int rows = *num_post;
-  const int chunks = H / 8;
-  const long long total = static_cast<long long>(rows) * chunks;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int pos = static_cast<int>(i / chunks), c = static_cast<int>(i - static_cast<long long>(pos) * chunks);
+  const int chunks = H / 8, lane = threadIdx.x & 31;
+  const int nw = gridDim.x * (blockDim.x >> 5);
+  for (int pos = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); pos < rows; pos += nw) {
     const int slot = __ldg(sorted_ids + pos);
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (slot < n_slots) v = ld_v4(xq + static_cast<size_t>(slot / topk) * H + c * 8);
-    *reinterpret_cast<uint4*>(act + static_cast<size_t>(pos) * H + c * 8) = v;
+    const bool valid = slot < n_slots;
+    const uint4* src = reinterpret_cast<const uint4*>(xq + static_cast<size_t>(valid ? slot / topk : 0) * H);
+    uint4* dst = reinterpret_cast<uint4*>(act + static_cast<size_t>(pos) * H);
+#pragma unroll 4
+    for (int c = lane; c < chunks; c += 32) dst[c] = valid ? ld_v4(src + c) : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -786,45 +787,49 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   }
 }
 
-// The same sum over bf16 y rows (the FP8-activation path), eight columns per thread.
+// The same sum over bf16 y rows (the tcgen05 path), eight columns per lane: a warp per (token, 32 chunks),
+// so that the token's routed slots are read once, as a ballot (topk <= 32), and no thread divides per chunk.
 __global__ void __launch_bounds__(256) combine_bf16_kernel(const __nv_bfloat16* __restrict__ y,
                                                            const int32_t* __restrict__ inv_pos, int M, int topk, int H,
                                                            __nv_bfloat16* __restrict__ out) {
   pdl_wait();
   pdl_trigger();
-  const int q = H / 8;
-  const long long total = static_cast<long long>(M) * q;
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int t = static_cast<int>(i / q), c = static_cast<int>(i - static_cast<long long>(t) * q);
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int k0 = 0; k0 < topk; k0 += 8) {
-      uint4 v[8];  // all loads of a group in flight together, then summed in slot order
+  const int q = H / 8, lane = threadIdx.x & 31, nseg = (q + 31) / 32;
+  const long long nw = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long it = blockIdx.x * static_cast<long long>(blockDim.x >> 5) + (threadIdx.x >> 5);
+       it < static_cast<long long>(M) * nseg; it += nw) {
+    const int t = static_cast<int>(it / nseg), c = static_cast<int>(it - static_cast<long long>(t) * nseg) * 32 + lane;
+    const unsigned routed = __ballot_sync(0xffffffffu, lane < topk && __ldg(inv_pos + t * topk + lane) >= 0);
+    const uint4* yt = reinterpret_cast<const uint4*>(y + static_cast<size_t>(t) * topk * H);
+    if (c < q) {
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int k0 = 0; k0 < topk; k0 += 8) {
+        uint4 v[8];  // all loads of a group in flight together, then summed in slot order
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int k = k0 + j, slot = t * topk + k;
-        v[j] = (k < topk && __ldg(inv_pos + slot) >= 0)
-                   ? __ldg(reinterpret_cast<const uint4*>(y + static_cast<size_t>(slot) * H) + c)
-                   : make_uint4(0u, 0u, 0u, 0u);
-      }
+        for (int j = 0; j < 8; ++j) {
+          const int k = k0 + j;
+          v[j] = (k < topk && ((routed >> k) & 1u)) ? __ldg(yt + static_cast<size_t>(k) * q + c)
+                                                    : make_uint4(0u, 0u, 0u, 0u);
+        }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[u]));
-          acc[2 * u] += f.x;
-          acc[2 * u + 1] += f.y;
+          for (int u = 0; u < 4; ++u) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[u]));
+            acc[2 * u] += f.x;
+            acc[2 * u + 1] += f.y;
+          }
         }
       }
-    }
-    uint32_t o[4];
+      uint32_t o[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * u], acc[2 * u + 1]);
-      o[u] = *reinterpret_cast<const uint32_t*>(&b);
+      for (int u = 0; u < 4; ++u) {
+        const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * u], acc[2 * u + 1]);
+        o[u] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      *reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    *reinterpret_cast<uint4*>(out + static_cast<size_t>(t) * H + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -968,8 +973,8 @@ cudaError_t launch_combine(const float* y, const int32_t* inv_pos, int M, int to
 
 cudaError_t launch_combine(const __nv_bfloat16* y, const int32_t* inv_pos, int M, int topk, int H,
                            __nv_bfloat16* out, int num_sms, cudaStream_t s) {
-  const long long work = static_cast<long long>(M) * (H / 8);
-  long long grid = (work + 255) / 256;
+  const long long warps = static_cast<long long>(M) * ((H / 8 + 31) / 32);
+  long long grid = (warps + 7) / 8;
   if (grid > num_sms * 16) grid = num_sms * 16;
   if (grid < 1) grid = 1;
   return launch_kernel(combine_bf16_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, true, y, inv_pos, M,

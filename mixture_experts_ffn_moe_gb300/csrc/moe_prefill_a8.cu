@@ -553,6 +553,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // transposed, [H/128, cap], so a token tile's scales of one K block are
 // contiguous for the TMA.  With nt = 2 the codes come in two terms: rows
 // M..2M-1 of xq (the lo codes) go to rows cap..2cap-1 of act.
+// One warp per (term, position) row, its lanes over the row's 16-byte chunks; then one thread
+// per position writes its scales, so that every group's row of sa is written coalesced.
 __global__ void __launch_bounds__(256) gather_a8_kernel(const uint8_t* __restrict__ xq, const float* __restrict__ sx,
                                                         const int32_t* __restrict__ sorted_ids,
                                                         const int32_t* __restrict__ num_post, int n_slots, int topk,
@@ -561,26 +563,24 @@ __global__ void __launch_bounds__(256) gather_a8_kernel(const uint8_t* __restric
   pdl_wait();
   pdl_trigger();
   const int rows = *num_post;
-  const int chunks = H / 16, G = H / kQBlock;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  const long long first = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-  const long long total = static_cast<long long>(rows) * chunks;
-  for (int term = 0; term < nt; ++term) {
-    const uint8_t* src = xq + static_cast<size_t>(term) * M * H;
-    uint8_t* dst = act + static_cast<size_t>(term) * cap * H;
-    for (long long i = first; i < total; i += stride) {
-      const int pos = static_cast<int>(i / chunks), c = static_cast<int>(i - static_cast<long long>(pos) * chunks);
-      const int slot = __ldg(sorted_ids + pos);
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (slot < n_slots) v = ld_v4(src + static_cast<size_t>(slot / topk) * H + c * 16);
-      *reinterpret_cast<uint4*>(dst + static_cast<size_t>(pos) * H + c * 16) = v;
-    }
-  }
-  const long long total_s = static_cast<long long>(G) * rows;
-  for (long long i = first; i < total_s; i += stride) {
-    const int g = static_cast<int>(i / rows), pos = static_cast<int>(i - static_cast<long long>(g) * rows);
+  const int chunks = H / 16, G = H / kQBlock, lane = threadIdx.x & 31;
+  const int nw = gridDim.x * (blockDim.x >> 5);
+  for (int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < nt * rows; r += nw) {
+    const int term = r >= rows ? 1 : 0;  // nt <= 2
+    const int pos = r - term * rows;
     const int slot = __ldg(sorted_ids + pos);
-    sa[static_cast<size_t>(g) * cap + pos] = slot < n_slots ? __ldg(sx + static_cast<size_t>(slot / topk) * G + g) : 0.f;
+    const bool valid = slot < n_slots;
+    const uint4* src = reinterpret_cast<const uint4*>(xq + (static_cast<size_t>(term) * M + (valid ? slot / topk : 0)) * H);
+    uint4* dst = reinterpret_cast<uint4*>(act + (static_cast<size_t>(term) * cap + pos) * H);
+#pragma unroll 4
+    for (int c = lane; c < chunks; c += 32) dst[c] = valid ? ld_v4(src + c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  const int nthr = gridDim.x * blockDim.x;
+  for (int pos = blockIdx.x * blockDim.x + threadIdx.x; pos < rows; pos += nthr) {
+    const int slot = __ldg(sorted_ids + pos);
+    const bool valid = slot < n_slots;
+    const float* s = sx + static_cast<size_t>(valid ? slot / topk : 0) * G;
+    for (int g = 0; g < G; ++g) sa[static_cast<size_t>(g) * cap + pos] = valid ? __ldg(s + g) : 0.f;
   }
 }
 
