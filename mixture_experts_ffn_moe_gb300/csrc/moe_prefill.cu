@@ -82,7 +82,6 @@ constexpr int WARP_EPI0 = WARP_CONV0 + N_CONV_WARPS;
 constexpr int NUM_WARPS = WARP_EPI0 + N_EPI_WARPS;
 constexpr int NUM_THREADS = NUM_WARPS * 32;
 constexpr int CONV_THREADS = N_CONV_WARPS * 32;
-constexpr int EPI_THREADS = N_EPI_WARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;    // 2 buffers x 2 accumulators x 128 columns
 constexpr int CHUNKS_PER_ACC = BM * BK / 16;  // 16-byte raw chunks per accumulator and stage
 constexpr int RAW_TILE_I4 = BM * BK / 2;      // INT4: 4 KB of codes per accumulator and stage
