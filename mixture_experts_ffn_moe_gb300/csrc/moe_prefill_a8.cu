@@ -162,6 +162,7 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, int stages, long long
 template <bool GATED, int NT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     prefill_a8_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b,
+                      const __grid_constant__ CUtensorMap tmap_b32, const __grid_constant__ CUtensorMap tmap_b64,
                       const __grid_constant__ CUtensorMap tmap_s, Args p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -202,6 +203,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == WARP_WTMA && lane == 0) {
     prefetch_tmap(&tmap_w);
     prefetch_tmap(&tmap_b);
+    prefetch_tmap(&tmap_b32);
+    prefetch_tmap(&tmap_b64);
     prefetch_tmap(&tmap_s);
   }
   tc_fence_before();
@@ -250,13 +253,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const Tile tl = get_tile<GATED>(p, t);
           for (int kc = 0; kc < KC; ++kc) {
             if (!(ok = mbar_wait(&bars->st_empty[as], aph ^ 1, abort, p.status, kWaitLimit))) break;
-            // one 128-row box per term: the MMA always reads 128 token rows, and the rows past the tile's
-            // count (the next positions, or zero fill past the tensor) only feed TMEM lanes nobody reads
-            mbar_arrive_expect_tx(&bars->op_full[as], NT * A_TILE);
+            // one box per term of the first 32, 64 or 128 rows, whichever holds the tile's tokens: the MMA
+            // always reads 128 token rows, and the rows past the tile's count (the next positions, zero fill
+            // past the tensor, or rows a smaller box left as they were) only feed TMEM lanes nobody reads
+            const int arows = tl.cnt <= 32 ? 32 : tl.cnt <= 64 ? 64 : MAXN;
+            const CUtensorMap* amap = arows == 32 ? &tmap_b32 : arows == 64 ? &tmap_b64 : &tmap_b;
+            mbar_arrive_expect_tx(&bars->op_full[as], NT * arows * BK);
             uint8_t* dst = sA + as * NT * A_TILE;
 #pragma unroll
             for (int term = 0; term < NT; ++term)  // the lo codes of a position sit cap rows below its hi codes
-              tma_load_2d(dst + term * A_TILE, &tmap_b, &bars->op_full[as], kc * BK, term * p.cap + tl.pos0);
+              tma_load_2d(dst + term * A_TILE, amap, &bars->op_full[as], kc * BK, term * p.cap + tl.pos0);
             ++aseq;
             if (++as == A_STAGES) { as = 0; aph ^= 1; }
 
@@ -600,8 +606,13 @@ static cudaError_t launch_a8_gemm(const pfa8::Args& a, const void* w, uint64_t w
   if (!encode_tmap_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, static_cast<uint64_t>(a.K), w_rows, BK, BM,
                       CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  CUtensorMap mb32, mb64;  // the same activations in boxes of 128, 32 and 64 rows
   if (!encode_tmap_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, static_cast<uint64_t>(a.K),
-                      static_cast<uint64_t>(NT) * a.cap, BK, MAXN, CU_TENSOR_MAP_SWIZZLE_128B))
+                      static_cast<uint64_t>(NT) * a.cap, BK, MAXN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_2d(&mb32, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, static_cast<uint64_t>(a.K),
+                      static_cast<uint64_t>(NT) * a.cap, BK, 32, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_2d(&mb64, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, b, static_cast<uint64_t>(a.K),
+                      static_cast<uint64_t>(NT) * a.cap, BK, 64, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, bs, static_cast<uint64_t>(a.cap),
                       static_cast<uint64_t>(a.K / kQBlock), MAXN, 1, CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -609,7 +620,7 @@ static cudaError_t launch_a8_gemm(const pfa8::Args& a, const void* w, uint64_t w
   constexpr int SMEM_BYTES = Lay<GATED, NT>::SMEM_BYTES;
   err = set_smem_limit_once(reinterpret_cast<const void*>(kern), SMEM_BYTES);
   if (err != cudaSuccess) return err;
-  return launch_kernel(kern, dim3(num_sms), dim3(NUM_THREADS), SMEM_BYTES, s, true, mw, mb, ms, a);
+  return launch_kernel(kern, dim3(num_sms), dim3(NUM_THREADS), SMEM_BYTES, s, true, mw, mb, mb32, mb64, ms, a);
 }
 
 template <int NT>
