@@ -169,9 +169,12 @@ __device__ __forceinline__ Item get_item(const SkinnyArgs& a, int it) {
   return Item{d.x, d.y, d.z, it - tt * a.n_rt};
 }
 
-template <int WK, bool GATED, int OCC>
+// RQ: INT8 GEMM2 that quantises h itself: its B fragments are read from GEMM1's fp32 h and coded per
+// position (s = max|h| / 127) in registers, so no requant launch sits between the GEMMs.
+template <int WK, bool GATED, int OCC, bool RQ = false>
 __global__ void __launch_bounds__(NUM_THREADS, OCC)
     skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, SkinnyArgs a) {
+  static_assert(!RQ || (WK == MOE_WEIGHT_INT8 && !GATED), "h is quantised in the INT8 down projection only");
   using C = Cfg<GATED, OCC, WK == MOE_WEIGHT_INT4>;
   constexpr bool I4 = WK == MOE_WEIGHT_INT4;
   constexpr int KST = I4 ? 2 * KBLK : KBLK;  // K values per stage
@@ -273,6 +276,23 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
   // B fragments of the next BPF stages are loaded ahead (a ring in registers).  INT4:
   // the two groups of a stage, the second absent past K.
   uint4 xr[BPF][XB];
+  // RQ: the lane's 32 fp32 values of h of the next BPF stages, and 127 / max|h| of its B column
+  uint4 hr[RQ ? BPF : 1][RQ ? 8 : 1];
+  float rq_r = 1.f;
+  auto load_stage_rq = [&](uint4* raw, const float* hrow, int kb, bool valid) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      raw[i] = valid ? ld_v4(hrow + static_cast<size_t>(kb) * KBLK + t * 32 + 4 * i) : make_uint4(0u, 0u, 0u, 0u);
+  };
+  auto quant_stage = [&](uint4* xb, const uint4* raw) {  // codes RNE(h * 127 / max|h|), as fp16
+    auto q = [&](uint32_t v) { return fminf(fmaxf(rintf(__uint_as_float(v) * rq_r), -127.0f), 127.0f); };
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 a0 = raw[2 * i], a1 = raw[2 * i + 1];
+      xb[i] = make_uint4(pack_half2(q(a0.x), q(a0.y)), pack_half2(q(a0.z), q(a0.w)), pack_half2(q(a1.x), q(a1.y)),
+                         pack_half2(q(a1.z), q(a1.w)));
+    }
+  };
   auto load_stage = [&](uint4* xb, const __half* brow, int kb, bool valid) {
     load_b32(xb, brow + static_cast<size_t>(kb) * KST + t * 32, valid);
     if constexpr (I4) load_b32(xb + 4, brow + static_cast<size_t>(kb) * KST + KBLK + t * 32,
@@ -315,6 +335,12 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
     const float* sg_row = a.wscale + (static_cast<size_t>(im.e) * a.rows_per_expert + mrow + g) * kblocks;
     bool bvalid;
     const __half* brow = b_row(im, bvalid);
+    const float* hrow = nullptr;  // RQ: the fp32 h row of the lane's B column
+    if constexpr (RQ) {
+      hrow = a.bh + static_cast<size_t>(im.pos0 + (bvalid ? g : 0)) * a.K;
+      const float amax = bvalid ? __uint_as_float(__ldg(a.hmax + im.pos0 + g)) : 0.f;
+      rq_r = amax > 0.f ? 127.0f / amax : 1.0f;
+    }
     // GEMM2 on h: the B column's row frame and lowest block frame (consumed after the fragment prefetch
     // below is in flight, so the two loads' latencies overlap)
     uint32_t eg_ld = 0u, lo_ld = 0u;
@@ -353,7 +379,8 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
 #pragma unroll
     for (int d = 0; d < BPF; ++d) {
       if (d < KB) {
-        load_stage(xr[d], brow, d, bvalid);
+        if constexpr (RQ) load_stage_rq(hr[d], hrow, d, bvalid);
+        else load_stage(xr[d], brow, d, bvalid);
         load_scales(d, d);
       }
     }
@@ -408,6 +435,7 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[slot]);
+          if constexpr (RQ) quant_stage(xb, hr[d]);  // after the release (its loads were issued a stage ago)
           if constexpr (WK == MOE_WEIGHT_FP8) {
             float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
             tile_mma_128<WK>(p0, p1, ra0, ra1, rb0, rb1, xb);
@@ -419,7 +447,8 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
           }
         }
         if (kb + BPF < KB) {
-          load_stage(xr[d], brow, kb + BPF, bvalid);
+          if constexpr (RQ) load_stage_rq(hr[d], hrow, kb + BPF, bvalid);
+          else load_stage(xr[d], brow, kb + BPF, bvalid);
           load_scales(d, kb + BPF);
         }
         if (++slot == C::NS) { slot = 0; phase ^= 1; }
@@ -550,8 +579,13 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
             continue;
           }
           float wgt = __ldg(a.topk_w + slot);
-          if constexpr (WK == MOE_WEIGHT_INT8)
+          if constexpr (RQ) {  // the scale of the codes this kernel made
+            const float amax = __uint_as_float(__ldg(a.hmax + pos));
+            wgt *= (amax > 0.f ? amax * (1.0f / 127.0f) : 1.0f) *
+                   __ldg(a.wscale + static_cast<size_t>(im.e) * a.rows_per_expert + n);
+          } else if constexpr (WK == MOE_WEIGHT_INT8) {
             wgt *= __ldg(a.sh + pos) * __ldg(a.wscale + static_cast<size_t>(im.e) * a.rows_per_expert + n);
+          }
           reinterpret_cast<float*>(a.out)[static_cast<size_t>(slot) * a.out_ld + n] = v * wgt;
         }
       }
@@ -593,7 +627,7 @@ cudaError_t launch_requant_rows(const void* h, const uint32_t* hmax, const int32
                        num_post, I, hq, sh);
 }
 
-template <int WK, bool GATED, int OCC>
+template <int WK, bool GATED, int OCC, bool RQ = false>
 static cudaError_t launch_skinny_occ(const SkinnyArgs& a, const void* w, uint64_t w_rows, int num_sms,
                                      cudaStream_t s) {
   using C = dec::Cfg<GATED, OCC, WK == MOE_WEIGHT_INT4>;
@@ -603,7 +637,7 @@ static cudaError_t launch_skinny_occ(const SkinnyArgs& a, const void* w, uint64_
   if (!encode_tmap_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, row_bytes, w_rows, dec::KBLK, C::ROWS,
                       CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  auto kern = dec::skinny_gemm_kernel<WK, GATED, OCC>;
+  auto kern = dec::skinny_gemm_kernel<WK, GATED, OCC, RQ>;
   cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM);
   if (err != cudaSuccess) return err;
   return launch_kernel(kern, dim3(OCC * num_sms), dim3(dec::NUM_THREADS), C::SMEM, s, true, mw, a);
@@ -613,6 +647,9 @@ static cudaError_t launch_skinny_occ(const SkinnyArgs& a, const void* w, uint64_
 template <int WK, bool GATED>
 static cudaError_t launch_skinny(const SkinnyArgs& a, const void* w, uint64_t w_rows, long long max_items,
                                  int num_sms, cudaStream_t s) {
+  if constexpr (WK == MOE_WEIGHT_INT8 && !GATED) {
+    if (a.bh) return launch_skinny_occ<WK, GATED, 2, true>(a, w, w_rows, num_sms, s);  // (two CTAs per SM only)
+  }
   // INT4 keeps two CTAs per SM: at three, its B fragments of two groups do not fit the registers
   if constexpr (WK == MOE_WEIGHT_INT4) {
     (void)max_items;
@@ -662,7 +699,11 @@ cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cuda
   if (err != cudaSuccess) return err;
   hook("decode_gemm1", s);
   const __half* b2 = static_cast<const __half*>(P.h);
-  if (weight_kind == MOE_WEIGHT_INT8) {
+  const int n_rt2 = (P.H + dec::Cfg<false, 2>::ROWS - 1) / dec::Cfg<false, 2>::ROWS;
+  // INT8 with a GEMM2 of two CTAs per SM (few items, under 6 per SM): GEMM2 quantises h itself from GEMM1's
+  // fp32 h and row maxima, and the requant launch goes (measured at one Qwen3 token: 6 us of a 60 us layer)
+  const bool rq = weight_kind == MOE_WEIGHT_INT8 && !P.out_direct && max_tiles * n_rt2 < 6LL * num_sms;
+  if (weight_kind == MOE_WEIGHT_INT8 && !rq) {
     // padded positions: the slots plus at most B - 1 padding rows for each of at most min(E, slots) experts
     const long long rows = slots + (slots < P.E ? slots : P.E) * (kDecodeBlock - 1);
     err = launch_requant_rows(P.h, P.hmax, P.num_post, rows < P.cap ? static_cast<int>(rows) : P.cap, P.I, P.hq,
@@ -675,7 +716,7 @@ cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cuda
   g2.K = P.I;
   g2.rows_per_expert = P.H;
   g2.up_offset = 0;
-  g2.n_rt = (P.H + dec::Cfg<false, 2>::ROWS - 1) / dec::Cfg<false, 2>::ROWS;
+  g2.n_rt = n_rt2;
   g2.ttiles = P.ttiles;
   g2.num_ttiles = P.num_ttiles;
   g2.wscale = P.s2;
@@ -691,6 +732,10 @@ cudaError_t launch_decode(const LayerPlan& P, int weight_kind, int num_sms, cuda
   g2.hexp = P.hexp;
   g2.hexp_lo = P.hexp + P.cap;
   g2.hblk = P.hblk;
+  if (rq) {
+    g2.bh = static_cast<const float*>(P.h);
+    g2.hmax = P.hmax;
+  }
   const uint64_t rows2 = static_cast<uint64_t>(P.E) * P.H;
   err = weight_kind == MOE_WEIGHT_FP8
             ? launch_skinny<MOE_WEIGHT_FP8, false>(g2, P.w2, rows2, max_tiles * g2.n_rt, num_sms, s)
