@@ -23,12 +23,19 @@
 // Within a tile the factor is one scalar per (token, weight block), so a thread
 // needs two factors per K block.  TMEM holds the partials of two K blocks
 // (2 buffers x 2 accumulators x 128 columns), so the MMAs of one K block
-// overlap the promotion of the previous one.
+// overlap the promotion of the previous one.  One commit per K block frees the
+// operand stage and hands the partials over; the accumulator warps give the
+// TMEM buffer back as soon as its last partials are in registers.
+//
+// The weight-only layer runs on the same kernels with NT = 2: its bf16 x and fp32
+// h enter as two E4M3 terms (hi and lo codes in a power-of-two frame per 128
+// columns), whose two products accumulate into the same partial sums.
 //
 // Warp roles (12 warps = 3 warpgroups, 1 CTA per SM, persistent):
-//   warp 0      TMA producer of weight tiles (2 x 16 KB per K block, ring of 4 in GEMM1, 3 in GEMM2)
+//   warp 0      TMA producer of weight tiles (2 x 16 KB per K block, ring of 4 in GEMM1, 3 in GEMM2 and with NT = 2)
 //   warp 1      TMEM allocator + tcgen05.mma issuer
-//   warp 2      TMA producer of activation tiles (16 KB) and activation scale vectors (ring of 8)
+//   warp 2      TMA producer of activation tiles (per term one box of 32, 64 or 128 rows of 128 bytes) and
+//               activation scale vectors (ring of 8)
 //   warp 3      scale warp: per K block, the factor vectors a_scale x w_scale of both accumulators
 //   warps 4-11  accumulators (setmaxnreg: 224 registers, the first warpgroup gives up its share)
 //               promotion, then the epilogue of the tile:
