@@ -196,6 +196,10 @@ struct MaskedArgs {
   int32_t* num_ttiles;
   int32_t* num_post;
   DeviceStatus* status;
+  // kind 5 (FP8 weights on the tcgen05 path): x in its two-term E4M3 form by position instead of xq/xs
+  uint8_t* act8;            // [2 * pcap, H] hi codes in row pos, lo codes in row pcap + pos
+  float* sa8;               // [H / 128, pcap] 2^e of each (position, 128-column group)
+  int pcap;                 // positions: E * round16(cap)
 };
 cudaError_t launch_masked_prologue(const MaskedArgs& m, int num_sms, cudaStream_t s);
 cudaError_t launch_wait_timeout(DeviceStatus* status, long long limit, int32_t* gave_up, cudaStream_t s);

@@ -14,7 +14,8 @@
 // Every CTA computes the prefix sum itself (E <= 1024 counts, one scan); CTA 0
 // writes the tile list and sorted_ids[pos] = e * cap + i (the output row), the others clear
 // the intermediate's frame words and copy the real rows of x into position order, converted
-// to fp16 in a power-of-two frame per row.
+// to fp16 in a power-of-two frame per row -- or, for FP8 weights on the tcgen05 path (kind 5),
+// to the two-term E4M3 form that the FP8-operand kernels read.
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -72,8 +73,37 @@ __global__ void __launch_bounds__(kMaskedThreads) masked_prologue_kernel(MaskedA
        r += static_cast<long long>(gridDim.x - 1) * nw) {
     const int e = static_cast<int>(r / m.cap), i = static_cast<int>(r - static_cast<long long>(e) * m.cap);
     if (i >= cnt[e]) continue;
-    const uint4* src = reinterpret_cast<const uint4*>(m.x + r * m.H);
     const int pos = off[e] + i;
+    if (m.kind == 5) {
+      // the two-term E4M3 form, a frame 2^e per 128 columns (group max |x| * 2^-e in [2^7, 2^8)):
+      // hi codes in row pos of act8, lo codes in row pcap + pos, sa8[group * pcap + pos] = 2^e
+      const uint2* src2 = reinterpret_cast<const uint2*>(m.x + r * m.H);
+      constexpr int kBatch = 8;  // groups whose loads are in flight together (the byte stores could alias them)
+      const int G = m.H / kQBlock;
+      for (int g0 = 0; g0 < G; g0 += kBatch) {
+        uint2 raw[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+          raw[u] = g0 + u < G ? __ldg(src2 + (g0 + u) * 32 + lane) : make_uint2(0u, 0u);  // columns 128 gi + 4 lane..
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int gi = g0 + u;
+          if (gi >= G) break;
+          const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[u].x));
+          const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[u].y));
+          const float mx = warp_max(fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)), fmaxf(fabsf(f1.x), fabsf(f1.y))));
+          const int ex = mx > 0.f ? e4m3_split_exp(mx) : 0;
+          uint32_t hi, lo;
+          e4m3_split4(make_float4(f0.x, f0.y, f1.x, f1.y), exp2i(-ex), hi, lo);
+          const size_t col = static_cast<size_t>(gi) * kQBlock + lane * 4;
+          *reinterpret_cast<uint32_t*>(m.act8 + static_cast<size_t>(pos) * m.H + col) = hi;
+          *reinterpret_cast<uint32_t*>(m.act8 + (static_cast<size_t>(m.pcap) + pos) * m.H + col) = lo;
+          if (lane == 0) m.sa8[static_cast<size_t>(gi) * m.pcap + pos] = exp2i(ex);
+        }
+      }
+      continue;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(m.x + r * m.H);
     uint4* dst = reinterpret_cast<uint4*>(m.xq + static_cast<size_t>(pos) * m.H);
     float amax = 0.f;
     for (int g = lane; g < m.H / 8; g += 32) {

@@ -370,9 +370,13 @@ static moe_status_t fused_impl(int kind, const void* x, const int32_t* ids, cons
 }
 
 // ------------------------------------------------------------------ masked layout
+// FP8 weights on the tcgen05 path use the FP8-operand kernels: x's two-term codes (2 x positions x H bytes) take
+// xq's space, h's codes (2 x positions x I) h's, h's group frames (positions x I/128 floats) hblk's, and x's
+// group frames have sa8.
 struct MaskedLayout {
   size_t status = 0, sorted = 0, ttiles = 0, scalars = 0, xq = 0, xs = 0, h = 0, hexp = 0, hblk = 0, hsc = 0,
-         total = 0;
+         sa8 = 0, total = 0;
+  size_t positions = 0;
 };
 
 static MaskedLayout plan_masked(int E, int cap, int H, int I) {
@@ -391,6 +395,8 @@ static MaskedLayout plan_masked(int E, int cap, int H, int I) {
   L.hexp = take(positions * 8);
   L.hblk = take(positions * (I / kHBlock));
   L.hsc = take(positions * 4);
+  L.sa8 = take(positions * (H / kQBlock) * 4);
+  L.positions = positions;
   L.total = o;
   return L;
 }
@@ -428,13 +434,18 @@ static moe_status_t masked_impl(int kind, const void* x, const int32_t* masked_m
   m.x = static_cast<const __nv_bfloat16*>(x);
   m.masked_m = masked_m;
   m.E = E; m.cap = cap; m.H = H;
-  m.kind = kind == MOE_WEIGHT_INT4 ? 4 : 1;
+  // FP8 weights on the tcgen05 path: the FP8-operand kernels with x and h in their two-term E4M3 form
+  const bool e4m3 = tc && kind == MOE_WEIGHT_FP8;
+  m.kind = e4m3 ? 5 : kind == MOE_WEIGHT_INT4 ? 4 : 1;
   m.block = tc ? kPrefillBlock : kDecodeBlock;
   m.tile = tc ? kPrefillTileTokens : kDecodeBlock;
   m.xq = at<__half>(ws, L.xq);
   m.xs = at<float>(ws, L.xs);
   m.zero_words = at<uint32_t>(ws, L.hexp);
-  m.n_zero = static_cast<int>(2 * static_cast<size_t>(E) * ((static_cast<size_t>(cap) + 15) / 16 * 16));
+  m.n_zero = e4m3 ? 0 : static_cast<int>(2 * L.positions);  // (the two-term form keeps no frame words)
+  m.act8 = at<uint8_t>(ws, L.xq);
+  m.sa8 = at<float>(ws, L.sa8);
+  m.pcap = static_cast<int>(L.positions);
   m.sorted_ids = at<int32_t>(ws, L.sorted);
   m.ttiles = at<int4>(ws, L.ttiles);
   m.num_ttiles = at<int32_t>(ws, L.scalars);
@@ -466,7 +477,16 @@ static moe_status_t masked_impl(int kind, const void* x, const int32_t* masked_m
   P.hsc = at<float>(ws, L.hsc);
   P.status = m.status;
   P.out_direct = static_cast<__nv_bfloat16*>(out);
-  err = tc ? launch_prefill(P, kind, sms, stream, hook) : launch_decode(P, kind, sms, stream, hook);
+  if (e4m3) {
+    P.e4m3_terms = 2;
+    P.act8 = m.act8;
+    P.sa8 = m.sa8;
+    P.h8 = at<uint8_t>(ws, L.h);
+    P.sh8 = at<float>(ws, L.hblk);
+    err = launch_prefill_a8(P, sms, stream, hook);
+  } else {
+    err = tc ? launch_prefill(P, kind, sms, stream, hook) : launch_decode(P, kind, sms, stream, hook);
+  }
   if (err != cudaSuccess) return cuda_fail(err, "masked layout launch");
   return MOE_OK;
 }

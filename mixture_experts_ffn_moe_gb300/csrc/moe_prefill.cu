@@ -16,29 +16,20 @@
 //    fetched feeds 256 output rows; it writes each slot's row times its
 //    routing weight in bf16, and a separate pass sums every token's rows in
 //    slot order.
-// Orientation (measured per GEMM).  GEMM1, and GEMM2 with INT8 or INT4 weights, put
-// the tokens on the MMA's M = 128 side and both converted weight blocks,
-// adjacent in shared memory, on its N = 256 side: one MMA per K step instead
-// of two, and an epilogue in which each thread finishes one token.  The FP8
-// GEMM2 keeps weights on the M side and tokens as N (16..128, a multiple of
-// 16, swap-AB), where short token tiles read less activation data.
-// TMEM holds two accumulators of 256 columns, so the epilogue of one tile
-// overlaps the MMAs of the next.
+// Orientation (measured).  Both GEMMs put the tokens on the MMA's M = 128 side
+// and both converted weight blocks, adjacent in shared memory, on its N = 256
+// side: one MMA per K step instead of two, and an epilogue in which each thread
+// finishes one token.  TMEM holds two accumulators of 256 columns, so the
+// epilogue of one tile overlaps the MMAs of the next.
 //
-// Weights stay FP8 E4M3 (or INT8) in HBM.  TMA brings raw 128x64-byte weight
-// tiles into shared memory; converter warps expand them to fp16 in registers
-// and write the tcgen05 operand (K-major, 128-byte swizzle).  For FP8 the
-// 128x128 block scale is folded into that conversion, because a tensor-core
-// accumulator cannot be rescaled per K block without a second TMEM pass: each
-// 128-row block has a power-of-two frame 2^P (its largest scale times 2^-P in
-// [2^6, 2^7)), the producer warp hands the converters every stage's scales
-// times 2^-P, a converter multiplies by that scale rounded to fp16 (an exact
-// fp32 product, rounded once, for scales far below the frame), and the
-// epilogue multiplies by 2^P.  So no scale overflows an fp16 weight.
-// Activations arrive as fp16 in power-of-two frames (x per row; h per row and
-// 32 columns, brought to one frame per row by h_frame_kernel between the
-// GEMMs); the epilogues take the frames back in fp32.  INT8 weights convert
-// exactly and the per-row x per-channel scales are applied in the epilogue.
+// This kernel runs INT8 and INT4 weights (FP8 weights run on the FP8 tensor
+// cores, moe_prefill_a8.cu).  Weights stay INT8 / INT4 in HBM.  TMA brings raw
+// weight tiles into shared memory; converter warps expand them to fp16 in
+// registers and write the tcgen05 operand (K-major, 128-byte swizzle).  INT8
+// weights convert exactly and the per-row x per-channel scales are applied in
+// the epilogue; INT4 activations arrive as fp16 in power-of-two frames (x per
+// row; h per row and 32 columns, brought to one frame per row by h_frame_kernel
+// between the GEMMs), and the epilogues take the frames back in fp32.
 // INT4 weights (two per byte, one scale per row and 128 columns) arrive as
 // 32-byte rows per stage, expand to fp16 in the INT4 K order (pairs k0,k4 /
 // k1,k5 / ...; the activations and h are stored in that order too) and take
@@ -49,7 +40,7 @@
 //   warp 0      TMA producer of raw weight tiles        (ring of 4 stages)
 //   warp 1      TMEM allocator + tcgen05.mma issuer
 //   warp 2      TMA producer of activation tiles        (ring of 4 stages)
-//   warps 3-10  converters: raw FP8/INT8 -> fp16 swizzled operand (3 stages)
+//   warps 3-10  converters: raw INT8 / INT4 -> fp16 swizzled operand (3 stages)
 //   warps 11-14 epilogue: TMEM -> registers -> SiLU*mul / routing weight -> HBM
 // Every wait is bounded; a time-out sets the status flag and all roles drain.
 #include <cuda.h>
@@ -72,7 +63,7 @@ constexpr int MAXN = kPrefillTileTokens;  // tokens per tile (MMA N <= 128)
 constexpr int RAW_STAGES = 4;          // raw weight codes (HBM -> smem by TMA)
 constexpr int ACT_STAGES = 4;          // activation tiles (TMA)
 constexpr int CONV_STAGES = 3;         // converted fp16 weight operands
-constexpr int RAW_TILE = BM * BK;      // 8 KB of fp8/int8 codes per accumulator
+constexpr int RAW_TILE = BM * BK;      // 8 KB of int8 codes per accumulator
 constexpr int A_TILE = BM * BK * 2;    // 16 KB fp16 operand per accumulator
 constexpr int B_TILE = MAXN * BK * 2;  // 16 KB fp16 activations
 constexpr int N_CONV_WARPS = 8;
@@ -106,12 +97,11 @@ struct Bars {
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
-  float wsc[RAW_STAGES][2];  // FP8: each raw stage's two block scales, folded into the weight frames
 };
 static_assert(sizeof(Bars) <= 512, "barrier block too large");
 
 struct Tile {
-  int e, pos0, cnt, n0, nmma;
+  int e, pos0, cnt, n0;
   bool two;  // second accumulator in use
 };
 
@@ -127,23 +117,8 @@ __device__ __forceinline__ Tile get_tile(const PrefillArgs& p, int t) {
   r.cnt = d.z;
   const int nt = t - tt * p.n_tiles;
   r.n0 = nt * (GATED ? BM : 2 * BM);
-  r.nmma = (d.z + 15) & ~15;
   r.two = GATED || (r.n0 + BM < p.rows_per_expert);
   return r;
-}
-
-// FP8 weight frame of one 128-row block of an expert: the power of two P with the block's largest
-// scale * 2^-P in [2^6, 2^7), so that every scale folded into the fp16 weights as scale * 2^-P keeps
-// code * scale * 2^-P <= 448 * 2^7 < 65504.  The epilogue multiplies the accumulator by 2^P.
-// Warp-cooperative (every lane returns P); srow holds the block's kblocks scales.
-__device__ __forceinline__ int wblock_frame(const float* srow, int kblocks) {
-  const int lane = threadIdx.x & 31;
-  float m = 0.f;
-  for (int i = lane; i < kblocks; i += 32) m = fmaxf(m, fabsf(__ldg(srow + i)));
-  m = warp_max(m);
-  if (!(m > 0.f)) return 0;
-  const int P = ilog2f(m) - 6;
-  return P < -120 ? -120 : (P > 120 ? 120 : P);
 }
 
 template <int WK, bool GATED>
@@ -160,10 +135,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total_tiles = *p.num_ttiles * p.n_tiles;
-  // Orientation (measured per GEMM): tokens on the MMA's M side and both weight blocks as one N = 256
-  // operand for GEMM1 and for INT8 / INT4; weights on the M side (two MMAs of N = tokens) for the FP8 down
-  // projection, whose 128-token padding of the M side cost more shared-memory bandwidth than it saved.
-  constexpr bool TOKM = GATED || WK != MOE_WEIGHT_FP8;
+  static_assert(WK == MOE_WEIGHT_INT8 || WK == MOE_WEIGHT_INT4, "FP8 weights run on the FP8-operand kernels");
   constexpr bool I4 = WK == MOE_WEIGHT_INT4;
   constexpr int RAWB = I4 ? RAW_TILE_I4 : RAW_TILE;  // raw bytes per accumulator and stage
   const int KC = p.K / BK;
@@ -211,50 +183,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (warp == WARP_WTMA) {
     // ---------------------------------------------------------------- raw weight producer
-    // The whole warp walks the tiles; lane 0 waits for ring slots and issues the copies.  For FP8 the
-    // warp also finds each tile's two weight frames and hands the converters every stage's block
-    // scales already folded into them (through the stage's slot in wsc), so the converters, the
-    // bottleneck of this kernel, wait on no global load.
+    // The whole warp walks the tiles; lane 0 waits for ring slots and issues the copies.
     int rs = 0;
     uint32_t rph = 0;
     int last_par[RAW_STAGES];
 #pragma unroll
     for (int i = 0; i < RAW_STAGES; ++i) last_par[i] = -1;
     bool ok = true;
-    const int kblocks = p.K / kQBlock, rblocks = p.rows_per_expert / kQBlock;
     for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
       const Tile tl = get_tile<GATED>(p, t);
       const int row0 = tl.e * p.rows_per_expert + tl.n0;
-      const float* srow[2] = {nullptr, nullptr};
-      float sv[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // K blocks lane and lane + 32 of each row block
-      float fr[2] = {1.f, 1.f};                    // 2^-P of each row block
-      if constexpr (WK == MOE_WEIGHT_FP8) {
-        const float* s0 = p.wscale + static_cast<size_t>(tl.e) * rblocks * kblocks;
-        srow[0] = s0 + static_cast<size_t>(tl.n0 / kQBlock) * kblocks;
-        srow[1] = s0 + static_cast<size_t>((tl.n0 + second_rows) / kQBlock) * kblocks;
-#pragma unroll
-        for (int a = 0; a < 2; ++a) {
-          if (a == 1 && !tl.two) break;
-          if (lane < kblocks) sv[a][0] = __ldg(srow[a] + lane);
-          if (lane + 32 < kblocks) sv[a][1] = __ldg(srow[a] + lane + 32);
-          fr[a] = exp2i(-wblock_frame(srow[a], kblocks));
-        }
-      }
       for (int kc = 0; kc < KC; ++kc) {
-        float f[2] = {0.f, 0.f};
-        if constexpr (WK == MOE_WEIGHT_FP8) {
-          const int kb = (kc * BK) / kQBlock;  // warp-uniform
-#pragma unroll
-          for (int a = 0; a < 2; ++a) {
-            const float v = __shfl_sync(0xffffffffu, kb < 32 ? sv[a][0] : sv[a][1], kb & 31);
-            f[a] = (kb < 64 ? v : (tl.two || a == 0 ? __ldg(srow[a] + kb) : 0.f)) * fr[a];
-          }
-        }
         if (lane == 0) {
           ok = mbar_wait(&bars->raw_empty[rs], rph ^ 1, abort, p.status, kWaitLimit);
           if (ok) {
-            bars->wsc[rs][0] = f[0];
-            bars->wsc[rs][1] = f[1];
             mbar_arrive_expect_tx(&bars->raw_full[rs], (tl.two ? 2 : 1) * RAWB);
             uint8_t* dst = sRaw + rs * 2 * RAW_TILE;
             const int kx = I4 ? kc * (BK / 2) : kc * BK;  // K offset in bytes of the stored rows
@@ -319,9 +261,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
         const Tile tl = get_tile<GATED>(p, t);
-        // TOKM: M = 128 tokens, N = both weight blocks at once (256 rows; 128 when the second is absent);
-        // else M = 128 weight rows per block, N = the tile's tokens
-        const uint32_t idesc = TOKM ? idesc_f16_f32(MAXN, tl.two ? 2 * BM : BM) : idesc_f16_f32(BM, tl.nmma);
+        // M = 128 tokens, N = both weight blocks at once (256 rows; 128 when the second is absent)
+        const uint32_t idesc = idesc_f16_f32(MAXN, tl.two ? 2 * BM : BM);
         const uint32_t d0 = tbase + static_cast<uint32_t>(buf * 2 * BM);
         if (!(ok = mbar_wait(&bars->acc_empty[buf], eph[buf] ^ 1, abort, p.status, kWaitLimit))) break;
         tc_fence_after();
@@ -331,18 +272,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           const uint64_t xd = sw128_kmajor_desc(smem_addr(sB + as * B_TILE));       // tokens
           const uint64_t wd = sw128_kmajor_desc(smem_addr(sA + cs * 2 * A_TILE));  // converted weight blocks
-          const uint64_t wd1 = sw128_kmajor_desc(smem_addr(sA + cs * 2 * A_TILE + A_TILE));  // second block alone
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {  // +32 bytes along K per step
-            const uint32_t acc = (kc | k) != 0;
-            if constexpr (TOKM) {
-              // tokens (A, M side) x the two weight blocks, adjacent in shared memory (B, N side)
-              umma_f16(d0, xd + 2 * k, wd + 2 * k, idesc, acc);
-            } else {
-              umma_f16(d0, wd + 2 * k, xd + 2 * k, idesc, acc);
-              if (tl.two) umma_f16(d0 + BM, wd1 + 2 * k, xd + 2 * k, idesc, acc);
-            }
-          }
+          for (int k = 0; k < BK / 16; ++k)  // +32 bytes along K per step; tokens (A, M side) x the two weight
+            umma_f16(d0, xd + 2 * k, wd + 2 * k, idesc, (kc | k) != 0);  // blocks, adjacent (B, N side)
           umma_commit(&bars->conv_empty[cs]);
           umma_commit(&bars->act_empty[as]);
           if (++cs == CONV_STAGES) { cs = 0; cph ^= 1; }
@@ -392,18 +324,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (!(ok = mbar_wait(&bars->raw_full[rs], rph, abort, p.status, kWaitLimit))) break;
         if (!(ok = mbar_wait(&bars->conv_empty[cs], cph ^ 1, abort, p.status, kWaitLimit))) break;
-        float sc[2] = {1.f, 1.f};
-        bool sc16[2] = {true, true};  // the scale is a normal fp16 number and q*s cannot overflow fp16
-        if constexpr (WK == MOE_WEIGHT_FP8) {
-          // the stage's block scales in the tile's weight frames, from the producer
-          sc[0] = bars->wsc[rs][0];
-          sc[1] = bars->wsc[rs][1];
-#pragma unroll
-          for (int a = 0; a < 2; ++a) {
-            const float m = fabsf(sc[a]);
-            sc16[a] = m >= 6.103515625e-05f && m * 448.f <= 65504.f;
-          }
-        }
         const uint8_t* raw = sRaw + rs * 2 * RAW_TILE;
         uint8_t* dstA = sA + cs * 2 * A_TILE;
         if constexpr (I4) {
@@ -457,27 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
             uint32_t o[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) w8x4_to_f16x4<WK>(w[i], o[2 * i], o[2 * i + 1]);
-            if constexpr (WK == MOE_WEIGHT_FP8) {
-              const float s2 = acc ? sc[1] : sc[0];
-              if (acc ? sc16[1] : sc16[0]) {
-                // block scale rounded to fp16 once, product rounded once (fp16 FMA pipe)
-                const __half2 sh2 = __half2half2(__float2half_rn(s2));
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  __half2 v2 = __hmul2(*reinterpret_cast<const __half2*>(&o[i]), sh2);
-                  o[i] = *reinterpret_cast<uint32_t*>(&v2);
-                }
-              } else {
-                // scales below the fp16 normal range (blocks far below the frame): exact fp32 product,
-                // rounded once
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&o[i]));
-                  o[i] = pack_half2(f.x * s2, f.y * s2);
-                }
-              }
-            }
+            for (int i = 0; i < 4; ++i) w8x4_to_f16x4<WK>(w[i], o[2 * i], o[2 * i + 1]);  // INT8: exact
             // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
             uint8_t* rowp = dstA + acc * A_TILE + row * 128;
             const int r8 = row & 7;
@@ -539,16 +439,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (live) atomicMax(p.hmax + pos, __float_as_uint(hmax));
       } else if constexpr (GATED) {
-        // FP8 / INT4: h = SiLU(g) * u in fp32, with the token's x frame and (FP8) the gate and up blocks'
-        // weight frames taken back; each 32 columns (one frame block) stored in fp16 in their own frame.
+        // INT4: h = SiLU(g) * u in fp32, with the token's x frame taken back; each 32 columns (one frame
+        // block) stored in fp16 in their own frame.
         float gm = 0.f, um = 0.f;
         if (live) gm = um = __ldg(p.sx + (p.x_by_pos ? pos : __ldg(p.sorted_ids + pos) / p.topk));
-        if constexpr (WK == MOE_WEIGHT_FP8) {
-          const float* s0 = p.wscale + static_cast<size_t>(tl.e) * (p.rows_per_expert / kQBlock) * (p.K / kQBlock);
-          gm *= exp2i(wblock_frame(s0 + static_cast<size_t>(tl.n0 / kQBlock) * (p.K / kQBlock), p.K / kQBlock));
-          um *= exp2i(wblock_frame(s0 + static_cast<size_t>((tl.n0 + p.up_offset) / kQBlock) * (p.K / kQBlock),
-                                   p.K / kQBlock));
-        }
         uint32_t emax = 0;
         for (int c0 = 0; c0 < BM; c0 += kHBlock) {  // gate columns c0.., up columns BM + c0..
           uint32_t g[32], u[32];
@@ -585,7 +479,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         if (live && emax) atomicMax(p.hexp + pos, emax);
-      } else if constexpr (TOKM) {
+      } else {
         int slot = 0;
         float wgt = 0.f;
         if (live) {
@@ -621,55 +515,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               w[2 * h + 1] = *reinterpret_cast<const uint32_t*>(&hi);
             }
             if (live) dstb[v] = make_uint4(w[0], w[1], w[2], w[3]);
-          }
-        }
-      } else {
-        // weights on the M side (FP8 only): TMEM lane = output row, columns = tokens
-        const int row = tok;
-        // the weight frames of the tile's two row blocks, taken back here with h's row frame
-        float wfm[2] = {1.f, 1.f};
-        {
-          const int kblocks = p.K / kQBlock;
-          const float* s0 = p.wscale + static_cast<size_t>(tl.e) * (p.rows_per_expert / kQBlock) * kblocks;
-          wfm[0] = exp2i(wblock_frame(s0 + static_cast<size_t>(tl.n0 / kQBlock) * kblocks, kblocks));
-          if (tl.two) wfm[1] = exp2i(wblock_frame(s0 + static_cast<size_t>(tl.n0 / kQBlock + 1) * kblocks, kblocks));
-        }
-        // each lane loads the output slot and factor (routing weight -- 1 on the masked layout, whose
-        // bf16 rows are unweighted -- times h's row frame) of columns lane, lane + 32, lane + 64,
-        // lane + 96 once per tile; the column loop takes them by shuffle
-        int cs[4];
-        float cf[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int col = 32 * q + lane;
-          cs[q] = 0;
-          cf[q] = 0.f;
-          if (col < tl.cnt) {
-            const int pos = tl.pos0 + col;
-            cs[q] = __ldg(p.sorted_ids + pos);
-            cf[q] = (p.out_bf16 ? 1.f : __ldg(p.topk_w + cs[q])) * __ldg(p.hsc + pos);
-          }
-        }
-        __nv_bfloat16* ob = p.out_bf16 ? p.out_bf16 : static_cast<__nv_bfloat16*>(p.out);
-#pragma unroll 1
-        for (int a = 0; a < 2; ++a) {
-          if (a == 1 && !tl.two) break;
-          const int n = tl.n0 + a * BM + row;
-          for (int c0 = 0; c0 < tl.nmma; c0 += 32) {
-            uint32_t g[32];
-            __syncwarp();
-            tmem_ld32(lane_addr + a * BM + c0, g);
-            tmem_ld_wait();
-            const int q = c0 >> 5;
-            const int sl = q == 0 ? cs[0] : q == 1 ? cs[1] : q == 2 ? cs[2] : cs[3];
-            const float fl = (q == 0 ? cf[0] : q == 1 ? cf[1] : q == 2 ? cf[2] : cf[3]) * wfm[a];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (c0 + j >= tl.cnt) continue;  // warp-uniform
-              const int slot = __shfl_sync(0xffffffffu, sl, j);
-              const float f = __shfl_sync(0xffffffffu, fl, j);
-              ob[static_cast<size_t>(slot) * p.out_ld + n] = __float2bfloat16_rn(__uint_as_float(g[j]) * f);
-            }
           }
         }
       }
@@ -714,7 +559,7 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const __half* __restri
   }
 }
 
-// The intermediate's row frames (FP8 and INT4 weights on this path): GEMM1 stored every 32-column
+// The intermediate's row frames (INT4 weights on this path): GEMM1 stored every 32-column
 // block of h in its own power-of-two frame; the down projection needs one frame per row, the
 // largest.  Blocks stored lower are scaled down to it in place (rare: a block's frame exponent is
 // a multiple of 8, so the blocks of a row mostly share it), and hsc[pos] = 2^e of the row frame.
@@ -881,6 +726,7 @@ static cudaError_t launch_gemm(const PrefillArgs& a, const void* w, uint64_t w_r
 }
 
 cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cudaStream_t s, const StageHook& hook) {
+  if (weight_kind != MOE_WEIGHT_INT8 && weight_kind != MOE_WEIGHT_INT4) return cudaErrorInvalidValue;  // (FP8: a8)
   cudaError_t err;
   if (!P.out_direct) {  // (the masked layout's prologue already wrote the rows in position order)
     int grid = num_sms * 8;
@@ -908,10 +754,8 @@ cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cud
   g1.hexp = P.hexp;
   g1.hblk = P.hblk;
   const uint64_t rows1 = static_cast<uint64_t>(P.E) * 2 * P.I;
-  err = weight_kind == MOE_WEIGHT_FP8 ? launch_gemm<MOE_WEIGHT_FP8, true>(g1, P.w13, rows1, P.act, P.cap, num_sms, s)
-        : weight_kind == MOE_WEIGHT_INT4
-            ? launch_gemm<MOE_WEIGHT_INT4, true>(g1, P.w13, rows1, P.act, P.cap, num_sms, s)
-            : launch_gemm<MOE_WEIGHT_INT8, true>(g1, P.w13, rows1, P.act, P.cap, num_sms, s);
+  err = weight_kind == MOE_WEIGHT_INT4 ? launch_gemm<MOE_WEIGHT_INT4, true>(g1, P.w13, rows1, P.act, P.cap, num_sms, s)
+                                       : launch_gemm<MOE_WEIGHT_INT8, true>(g1, P.w13, rows1, P.act, P.cap, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("prefill_gemm1", s);
   const __half* b2 = reinterpret_cast<const __half*>(P.h);
@@ -947,10 +791,8 @@ cudaError_t launch_prefill(const LayerPlan& P, int weight_kind, int num_sms, cud
   g2.status = P.status;
   g2.out_bf16 = P.out_direct;
   const uint64_t rows2 = static_cast<uint64_t>(P.E) * P.H;
-  err = weight_kind == MOE_WEIGHT_FP8 ? launch_gemm<MOE_WEIGHT_FP8, false>(g2, P.w2, rows2, b2, P.cap, num_sms, s)
-        : weight_kind == MOE_WEIGHT_INT4
-            ? launch_gemm<MOE_WEIGHT_INT4, false>(g2, P.w2, rows2, b2, P.cap, num_sms, s)
-            : launch_gemm<MOE_WEIGHT_INT8, false>(g2, P.w2, rows2, b2, P.cap, num_sms, s);
+  err = weight_kind == MOE_WEIGHT_INT4 ? launch_gemm<MOE_WEIGHT_INT4, false>(g2, P.w2, rows2, b2, P.cap, num_sms, s)
+                                       : launch_gemm<MOE_WEIGHT_INT8, false>(g2, P.w2, rows2, b2, P.cap, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("prefill_gemm2", s);
   if (P.out_direct) return cudaSuccess;  // masked layout: GEMM2 wrote the output rows

@@ -131,7 +131,7 @@ struct Args {
 };
 
 struct Tile {
-  int e, pos0, cnt, n0, nmma;
+  int e, pos0, cnt, n0;
   bool two;
 };
 
@@ -145,7 +145,6 @@ __device__ __forceinline__ Tile get_tile(const Args& p, int t) {
   r.cnt = d.z;
   const int nt = t - tt * p.n_tiles;
   r.n0 = nt * (GATED ? BM : 2 * BM);
-  r.nmma = (d.z + 15) & ~15;
   r.two = GATED || (r.n0 + BM < p.rows_per_expert);
   return r;
 }
@@ -434,7 +433,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           release();
         }
         if constexpr (!GATED) {
-          if (kc == 0 && live) wgt = __ldg(p.topk_w + slot);  // the slot has arrived by now
+          // the slot has arrived by now (no routing weights: the masked layout's unweighted rows)
+          if (kc == 0 && live) wgt = p.topk_w ? __ldg(p.topk_w + slot) : 1.f;
         }
         buf ^= 1;
         if (++ks == W_STAGES) { ks = 0; kph ^= 1; }
@@ -633,7 +633,7 @@ static cudaError_t launch_a8_gemm(const pfa8::Args& a, const void* w, uint64_t w
 template <int NT>
 static cudaError_t launch_prefill_e4m3(const LayerPlan& P, int num_sms, cudaStream_t s, const StageHook& hook) {
   cudaError_t err;
-  {
+  if (!P.out_direct) {  // (the masked layout's prologue already wrote the codes in position order)
     const int grid = num_sms * 8;
     err = launch_kernel(gather_a8_kernel, dim3(grid), dim3(256), 0, s, true, P.xq8, P.sx8, P.sorted_ids,
                         P.num_post, P.M * P.topk, P.topk, P.H, P.cap, P.M, NT, P.act8, P.sa8);
@@ -669,11 +669,13 @@ static cudaError_t launch_prefill_e4m3(const LayerPlan& P, int num_sms, cudaStre
   g2.wscale = P.s2;
   g2.sorted_ids = P.sorted_ids;
   g2.topk_w = P.topk_w;
-  g2.y = reinterpret_cast<__nv_bfloat16*>(P.y);  // bf16 rows in the fp32 buffer's space
+  // bf16 rows by slot in the fp32 buffer's space; the masked layout's output rows, unweighted
+  g2.y = P.out_direct ? P.out_direct : reinterpret_cast<__nv_bfloat16*>(P.y);
   g2.status = P.status;
   err = launch_a8_gemm<false, NT>(g2, P.w2, static_cast<uint64_t>(P.E) * P.H, P.h8, P.sh8, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("prefill_gemm2", s);
+  if (P.out_direct) return cudaSuccess;  // the masked layout has no combine
   err = launch_combine(reinterpret_cast<const __nv_bfloat16*>(P.y), P.inv_pos, P.M, P.topk, P.H, P.out, num_sms, s);
   if (err != cudaSuccess) return err;
   hook("combine", s);
