@@ -128,6 +128,7 @@ struct Args {
   float* hs;             // GEMM1 out: h scales [I/128, cap]
   __nv_bfloat16* y;      // GEMM2 out: [M*topk, H]
   DeviceStatus* status;
+  int tiles_from_prev;   // the tile list comes from the kernel right before this one
 };
 
 struct Tile {
@@ -217,10 +218,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = bars->tmem_base;
-  // The weight stream and the MMA issuer need only the tile list (written two
-  // kernels back); the activation producer, the scale warp and the accumulators
-  // read the predecessor's output and wait for it.
-  if (warp == WARP_ATMA || warp >= WARP_SCALE) pdl_wait();
+  // The weight stream and the MMA issuer need only the tile list, written two
+  // kernels back on the routed layer, so they start at once; the activation
+  // producer, the scale warp and the accumulators read the predecessor's output
+  // and wait for it.  When the predecessor itself wrote the tile list (GEMM1
+  // of the masked layout, right after its prologue), every role waits.
+  if (p.tiles_from_prev || warp == WARP_ATMA || warp >= WARP_SCALE) pdl_wait();
   pdl_trigger();
   const int total_tiles = *p.num_ttiles * p.n_tiles;
   if (warp < WARP_ACC0) {
@@ -653,6 +656,7 @@ static cudaError_t launch_prefill_e4m3(const LayerPlan& P, int num_sms, cudaStre
   g1.sorted_ids = P.sorted_ids;
   g1.hq = P.h8;
   g1.hs = P.sh8;
+  g1.tiles_from_prev = P.out_direct ? 1 : 0;  // the masked layout: its prologue wrote the tile list
   g1.status = P.status;
   err = launch_a8_gemm<true, NT>(g1, P.w13, static_cast<uint64_t>(P.E) * 2 * P.I, P.act8, P.sa8, num_sms, s);
   if (err != cudaSuccess) return err;

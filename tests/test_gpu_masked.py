@@ -113,20 +113,23 @@ def test_masked_deepseek_local_experts_full_size():
     assert_layer_close(got, ref, "masked DeepSeek-R1 local experts")
 
 
-def test_masked_layout_in_a_cuda_graph_replays_with_new_counts():
-    E, cap, H, I = 8, 24, 256, 128
-    x, m, weights = _masked_inputs(E, cap, H, I, "fp8", seed=11, counts=[24, 3, 0, 9, 16, 1, 8, 24])
+# both paths: the weight-streaming kernels, and the tcgen05 ones (FP8: the two-term form written by the prologue)
+@pytest.mark.parametrize("flags,cap", [(gbmoe.MOE_PATH_AUTO, 24), (gbmoe.MOE_PATH_PREFILL, 150)])
+def test_masked_layout_in_a_cuda_graph_replays_with_new_counts(flags, cap):
+    E, H, I = 8, 256, 128
+    first = [min(c, cap) for c in (cap, 3, 0, 9, 16, 1, 8, cap)]
+    x, m, weights = _masked_inputs(E, cap, H, I, "fp8", seed=11, counts=first)
     xd, md = x.cuda(), m.cuda()
     w = [t.cuda() for t in weights]
     out = torch.full(x.shape, SENTINEL, dtype=torch.bfloat16, device="cuda")
     ws = torch.empty(gbmoe.moe_workspace_size_masked(E, cap, H, I, gbmoe.MOE_WEIGHT_FP8), dtype=torch.uint8,
                      device="cuda")
-    gbmoe.fused_moe_masked(gbmoe.MOE_WEIGHT_FP8, xd, md, *w, out=out, workspace=ws)  # eager first
+    gbmoe.fused_moe_masked(gbmoe.MOE_WEIGHT_FP8, xd, md, *w, out=out, workspace=ws, flags=flags)  # eager first
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        gbmoe.fused_moe_masked(gbmoe.MOE_WEIGHT_FP8, xd, md, *w, out=out, workspace=ws)
-    for counts in ([24, 3, 0, 9, 16, 1, 8, 24], [0, 24, 5, 0, 2, 23, 12, 7]):
+        gbmoe.fused_moe_masked(gbmoe.MOE_WEIGHT_FP8, xd, md, *w, out=out, workspace=ws, flags=flags)
+    for counts in (first, [0, cap, 5, 0, 2, cap - 1, 12, 7]):
         md.copy_(torch.tensor(counts, dtype=torch.int32))
         out.fill_(SENTINEL)
         g.replay()
