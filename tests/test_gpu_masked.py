@@ -138,11 +138,13 @@ def test_masked_layout_in_a_cuda_graph_replays_with_new_counts(flags, cap):
         _check(out.float().cpu().numpy(), ref, mc, f"graph replay {counts}")
 
 
-def test_routed_layer_in_a_cuda_graph_replays_with_new_routing():
-    shape = synth.LayerShape("g", 4, 512, 256, 16, 3, "fp8", "softmax")
+# 4 tokens take the weight-streaming kernels, 160 the tcgen05 ones (MOE_PATH_AUTO)
+@pytest.mark.parametrize("M", [4, 160])
+def test_routed_layer_in_a_cuda_graph_replays_with_new_routing(M):
+    shape = synth.LayerShape("g", M, 512, 256, 16, 3, "fp8", "softmax")
     d = to_device(synth.make_layer(shape, seed=12))
-    ws = gbmoe.alloc_workspace(4, 512, 256, 16, 3, gbmoe.MOE_WEIGHT_FP8)
-    out = torch.empty(4, 512, dtype=torch.bfloat16, device="cuda")
+    ws = gbmoe.alloc_workspace(M, 512, 256, 16, 3, gbmoe.MOE_WEIGHT_FP8)
+    out = torch.empty(M, 512, dtype=torch.bfloat16, device="cuda")
     args = (d["x"], d["topk_ids"], d["topk_weights"], d["w13"], d["w13_scale"], d["w2"], d["w2_scale"])
     gbmoe.fused_moe_fp8(*args, out=out, workspace=ws)
     torch.cuda.synchronize()
@@ -150,7 +152,7 @@ def test_routed_layer_in_a_cuda_graph_replays_with_new_routing():
     with torch.cuda.graph(g):
         gbmoe.fused_moe_fp8(*args, out=out, workspace=ws)
     for seed in (13, 14):
-        r = synth.make_layer(synth.LayerShape("g", 4, 512, 256, 16, 3, "fp8", "softmax"), seed=seed)
+        r = synth.make_layer(synth.LayerShape("g", M, 512, 256, 16, 3, "fp8", "softmax"), seed=seed)
         d["topk_ids"].copy_(r["topk_ids"])
         d["topk_weights"].copy_(r["topk_weights"])
         g.replay()
