@@ -171,7 +171,9 @@ __device__ __forceinline__ Item get_item(const SkinnyArgs& a, int it) {
 
 // RQ: INT8 GEMM2 that quantises h itself: its B fragments are read from GEMM1's fp32 h and coded per
 // position (s = max|h| / 127) in registers, so no requant launch sits between the GEMMs.
-template <int WK, bool GATED, int OCC, bool RQ = false>
+// EQ: only as many CTAs take items as give every one of them the same count (a separate build: the
+// item bounds it keeps in registers slowed the kernel where it does not help).
+template <int WK, bool GATED, int OCC, bool RQ = false, bool EQ = false>
 __global__ void __launch_bounds__(NUM_THREADS, OCC)
     skinny_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, SkinnyArgs a) {
   static_assert(!RQ || (WK == MOE_WEIGHT_INT8 && !GATED), "h is quantised in the INT8 down projection only");
@@ -211,12 +213,24 @@ __global__ void __launch_bounds__(NUM_THREADS, OCC)
   if (!GATED || n_items <= 2 * static_cast<int>(gridDim.x)) pdl_trigger();
 
   // Item order (measured): GEMM1 items go round-robin over the CTAs; GEMM2 items
-  // go in contiguous runs per CTA, so a CTA streams adjacent weight rows.
+  // go in contiguous runs per CTA, so a CTA streams adjacent weight rows.  EQ: k =
+  // ceil(items / grid) items for each of ceil(items / k) CTAs, the others leave at
+  // once -- a last round that leaves part of the CTAs idle streams too few bytes at
+  // once to keep HBM busy.
+  int ctas = static_cast<int>(gridDim.x);
+  if constexpr (EQ) {
+    const int k = (n_items + ctas - 1) / ctas;
+    if (k > 1) ctas = (n_items + k - 1) / k;
+  }
+  const bool has_items = !EQ || static_cast<int>(blockIdx.x) < ctas;
   const int it_begin =
-      GATED ? static_cast<int>(blockIdx.x) : static_cast<int>(static_cast<long long>(n_items) * blockIdx.x / gridDim.x);
-  const int it_end =
-      GATED ? n_items : static_cast<int>(static_cast<long long>(n_items) * (blockIdx.x + 1) / gridDim.x);
-  const int it_step = GATED ? static_cast<int>(gridDim.x) : 1;
+      !has_items ? 0
+      : GATED    ? static_cast<int>(blockIdx.x)
+                 : static_cast<int>(static_cast<long long>(n_items) * blockIdx.x / ctas);
+  const int it_end = !has_items ? 0
+                     : GATED    ? n_items
+                                : static_cast<int>(static_cast<long long>(n_items) * (blockIdx.x + 1) / ctas);
+  const int it_step = GATED ? ctas : 1;
 
   if (warp == NCW) {
     // ---------------------------------------------------------------- TMA producer
@@ -627,7 +641,7 @@ cudaError_t launch_requant_rows(const void* h, const uint32_t* hmax, const int32
                        num_post, I, hq, sh);
 }
 
-template <int WK, bool GATED, int OCC, bool RQ = false>
+template <int WK, bool GATED, int OCC, bool RQ = false, bool EQ = false>
 static cudaError_t launch_skinny_occ(const SkinnyArgs& a, const void* w, uint64_t w_rows, int num_sms,
                                      cudaStream_t s) {
   using C = dec::Cfg<GATED, OCC, WK == MOE_WEIGHT_INT4>;
@@ -637,10 +651,21 @@ static cudaError_t launch_skinny_occ(const SkinnyArgs& a, const void* w, uint64_
   if (!encode_tmap_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, row_bytes, w_rows, dec::KBLK, C::ROWS,
                       CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  auto kern = dec::skinny_gemm_kernel<WK, GATED, OCC, RQ>;
+  auto kern = dec::skinny_gemm_kernel<WK, GATED, OCC, RQ, EQ>;
   cudaError_t err = set_smem_limit_once(reinterpret_cast<const void*>(kern), C::SMEM);
   if (err != cudaSuccess) return err;
   return launch_kernel(kern, dim3(OCC * num_sms), dim3(dec::NUM_THREADS), C::SMEM, s, true, mw, a);
+}
+
+// The EQ build where the host's bound puts 2.5 to 10 items on a CTA (measured: DeepSeek-R1 at 4 and 8
+// tokens 2-3% faster; at 1 and 2 tokens, 64 tokens and with INT4 weights the plain build is faster).
+template <int WK, bool GATED, int OCC>
+static cudaError_t launch_skinny_eq(const SkinnyArgs& a, const void* w, uint64_t w_rows, long long max_items,
+                                    int num_sms, cudaStream_t s) {
+  const long long grid = static_cast<long long>(OCC) * num_sms;
+  return 2 * max_items >= 5 * grid && max_items <= 10 * grid
+             ? launch_skinny_occ<WK, GATED, OCC, false, true>(a, w, w_rows, num_sms, s)
+             : launch_skinny_occ<WK, GATED, OCC>(a, w, w_rows, num_sms, s);
 }
 
 // max_items: an upper bound of the work items the launch can see.
@@ -660,8 +685,8 @@ static cudaError_t launch_skinny(const SkinnyArgs& a, const void* w, uint64_t w_
     // of one token 0.037 -> 0.031 ms (its 504 items no longer leave 48 of 456 CTAs a second
     // item); GEMM2 of two tokens is faster at three CTAs per SM.
     const long long occ3_min = GATED ? 9LL * num_sms : 6LL * num_sms;
-    return max_items >= occ3_min ? launch_skinny_occ<WK, GATED, 3>(a, w, w_rows, num_sms, s)
-                                 : launch_skinny_occ<WK, GATED, 2>(a, w, w_rows, num_sms, s);
+    return max_items >= occ3_min ? launch_skinny_eq<WK, GATED, 3>(a, w, w_rows, max_items, num_sms, s)
+                                 : launch_skinny_eq<WK, GATED, 2>(a, w, w_rows, max_items, num_sms, s);
   }
 }
 
