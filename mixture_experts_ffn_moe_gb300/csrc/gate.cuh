@@ -153,7 +153,7 @@ __device__ __forceinline__ void gate_token(const GateArgs& g, int t, int lane) {
     }
   }
   // ids stay in [0, E) whatever the scores: keys of existing experts are >= 1
-  // and topk <= E, so every round's maximum lies on an existing expert.
+  // and topk <= E, so every selection step.s maximum lies on an existing expert.
   if (my_id >= g.E) my_id = g.E - 1;
 
   // ---- weights
@@ -161,7 +161,7 @@ __device__ __forceinline__ void gate_token(const GateArgs& g, int t, int lane) {
   if (sigm) {
     ex = lane < g.topk ? my_v : 0.f;
   } else {
-    const float vmax = __shfl_sync(0xffffffffu, my_v, 0);  // round 0 took the largest logit
+    const float vmax = __shfl_sync(0xffffffffu, my_v, 0);  // the first selection took the largest logit
     ex = lane < g.topk ? expf(my_v - vmax) : 0.f;
   }
   float sum = ex;
