@@ -153,7 +153,7 @@ __device__ __forceinline__ void gate_token(const GateArgs& g, int t, int lane) {
     }
   }
   // ids stay in [0, E) whatever the scores: keys of existing experts are >= 1
-  // and topk <= E, so every selection step.s maximum lies on an existing expert.
+  // and topk <= E, so every selection step's maximum lies on an existing expert.
   if (my_id >= g.E) my_id = g.E - 1;
 
   // ---- weights
