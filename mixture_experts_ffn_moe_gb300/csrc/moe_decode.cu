@@ -658,7 +658,7 @@ static cudaError_t launch_skinny_occ(const SkinnyArgs& a, const void* w, uint64_
 }
 
 // The EQ build where the host's bound puts 2.5 to 10 items on a CTA (measured: DeepSeek-R1 at 4 and 8
-// tokens 2-3% faster; at 1 and 2 tokens, 64 tokens and with INT4 weights the plain build is faster).
+// tokens 2-3% faster; at 1, 2 and 64 tokens and with INT4 weights it gained nothing).
 template <int WK, bool GATED, int OCC>
 static cudaError_t launch_skinny_eq(const SkinnyArgs& a, const void* w, uint64_t w_rows, long long max_items,
                                     int num_sms, cudaStream_t s) {
