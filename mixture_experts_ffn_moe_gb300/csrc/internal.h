@@ -71,10 +71,9 @@ struct PrefillArgs {
   const float* topk_w;   // GEMM2: routing weights per slot
   void* out;             // GEMM1: h by position (fp16 FP8 / fp32 INT8); GEMM2: y bf16 by slot (weighted)
   int out_ld;
-  uint32_t* hmax;        // INT8 GEMM1: per-position max |h| (bits); INT8 GEMM2 with bh: read, to quantise h
-  const float* bh;       // INT8 GEMM2 quantising h itself: GEMM1's fp32 h [cap, I] by position (else null)
+  uint32_t* hmax;        // INT8 GEMM1: per-position max |h| (bits)
   DeviceStatus* status;
-  __nv_bfloat16* out_bf16;  // GEMM2 (FP8): if set, bf16 output rows out_bf16[slot] (unweighted), not y
+  __nv_bfloat16* out_bf16;  // GEMM2: if set, bf16 output rows out_bf16[slot] (unweighted), not y
   // power-of-two frames of the fp16 operands (FP8 and INT4 weights)
   int x_by_pos;          // GEMM1: sx is indexed by position (masked layout), else by token
   uint32_t* hexp;        // GEMM1: per position, the largest biased frame exponent of its h blocks (atomicMax)
