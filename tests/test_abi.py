@@ -80,6 +80,21 @@ def test_host_side_argument_errors(lib):
     assert lib.moe_align_block_size(None, 4, 2, 8, 512, None, None, None, None, None) == 2
 
 
+def test_decode_path_token_limit_and_size_guard(lib):
+    dec = gbmoe.MOE_PATH_DECODE
+    limit = gbmoe.MOE_MAX_DECODE_TOKENS
+    assert _call_fp8(lib, M=limit, flags=dec) == 3              # at the limit: valid, fails on the workspace
+    assert _call_fp8(lib, M=limit + 1, flags=dec) == 2          # one past it
+    assert b"MOE_MAX_DECODE_TOKENS" in lib.moe_last_error()
+    assert _call_fp8(lib, M=limit + 1) == 3                     # MOE_PATH_AUTO takes the tcgen05 path there
+    p = ctypes.c_void_p(16)
+    assert lib.fused_moe_int8(p, p, p, p, p, p, p, limit + 1, 256, 128, 8, 2, dec, p, p, 0, None) == 2
+    # slots M * topk above 2^30 are refused before any size is computed from them
+    assert _call_fp8(lib, M=1 << 26, topk=32) == 2
+    assert b"too large" in lib.moe_last_error()
+    assert _call_fp8(lib, M=1 << 25, topk=32) == 3              # 2^30 slots exactly: still accepted
+
+
 def test_fp8_activation_flag_host_checks(lib):
     a8 = gbmoe.MOE_ACT_FP8_1X128
     assert _call_fp8(lib, flags=a8 | gbmoe.MOE_PATH_DECODE) == 2   # FP8 x FP8 runs on tcgen05 only
