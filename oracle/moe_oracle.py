@@ -30,6 +30,9 @@ computes, in float64 numpy over dequantised weights:
 * the optional FP8 x FP8 ("A8") mode of the FP8 layer, in which the
   activations and the intermediate h are quantised to E4M3 in groups of 1 x 128
   (a reading: the pages keep FP8 activations in BF16, see quant_fp8_1x128);
+* the same mode with power-of-two ("UE8M0") scales, the scale format of the
+  tensor cores' block-scaled MMA: not on the pages, every scale rounded up to a
+  power of two (a reading, see ue8m0_ceil);
 * the router's gating functions that produce topk_ids / topk_weights from
   logits (softmax top-k renormalised; sigmoid with a selection bias and
   group-limited top-k).  The pages take the router's output as given; these
@@ -38,9 +41,11 @@ computes, in float64 numpy over dequantised weights:
 Precision: float64 accumulation everywhere, except that every decision that
 turns a float into an integer code (activation quantisation) is taken in
 float32 with IEEE division and round-half-to-even, the same precision the
-GPU kernels use for that decision.  The gating functions rank in float64:
-their results are exact rankings, and the GPU gate (which ranks in float32)
-is compared with them only where the ranking margin exceeds float32 error.
+GPU kernels use for that decision; re-quantising stored weights to
+power-of-two scales rounds each exact product decode(q) * s / s' once.  The
+gating functions rank in float64: their results are exact rankings, and the
+GPU gate (which ranks in float32) is compared with them only where the
+ranking margin exceeds float32 error.
 """
 from __future__ import annotations
 
@@ -83,7 +88,12 @@ def e4m3_encode_satfinite(v) -> np.ndarray:
     the midpoints between neighbouring grid points.  On a tie the code with an
     even mantissa (even code) wins.  NaN input -> 0x7F.
     """
-    v = np.asarray(v, dtype=np.float32).astype(np.float64)
+    return _e4m3_round_satfinite(np.asarray(v, dtype=np.float32).astype(np.float64))
+
+
+def _e4m3_round_satfinite(v) -> np.ndarray:
+    """float64 values -> E4M3 codes, each exact value rounded once (the rule of e4m3_encode_satfinite)."""
+    v = np.asarray(v, dtype=np.float64)
     grid = _e4m3_positive_grid()
     a = np.minimum(np.abs(v), FP8_MAX)
     lo = np.clip(np.searchsorted(grid, a, side="right") - 1, 0, 126)
@@ -211,6 +221,71 @@ def dequant_fp8_1x128(codes, scale) -> np.ndarray:
     a = _e4m3_table()[codes].reshape(R, C // QBLOCK, QBLOCK)
     a = a * np.asarray(scale, dtype=np.float64)[..., None]
     return a.reshape(R, C)
+
+
+# ----------------------------------------------------------------------------
+# Power-of-two (UE8M0) scales.  Not on the pages: the pages' FP8 scales are
+# fp32, and the block-scaled MMA of the tensor cores takes its scales as UE8M0
+# exponents (the OCP Microscaling format's E8M0: an unsigned 8-bit exponent,
+# bias 127, value 2^(code - 127), codes 0..254; 255 is NaN).  The reading taken
+# here: every fp32 scale is replaced by the smallest power of two not below it,
+# so that no code overflows; activations are quantised against that scale, and
+# stored weights are re-quantised from their exact values decode(q) * s.  One
+# scale still covers 1 x 128 activations and 128 x 128 weights (a 32-wide MX
+# scale block would repeat it four times).
+# ----------------------------------------------------------------------------
+
+UE8M0_MIN_EXP = -127
+UE8M0_MAX_EXP = 127
+
+
+def ue8m0_ceil(s):
+    """Positive scales -> (float64 2^e, uint8 UE8M0 codes e + 127), e the smallest integer with 2^e >= s,
+    clamped to [-127, 127]."""
+    s = np.asarray(s, dtype=np.float64)
+    if np.any(~(s > 0)) or np.any(~np.isfinite(s)):
+        raise ValueError("UE8M0 scales need positive finite inputs")
+    m, e = np.frexp(s)                       # s = m * 2^e with m in [0.5, 1)
+    e = np.where(m == 0.5, e - 1, e)         # s is 2^(e-1) exactly
+    e = np.clip(e, UE8M0_MIN_EXP, UE8M0_MAX_EXP)
+    return np.ldexp(1.0, e), (e + 127).astype(np.uint8)
+
+
+def quant_fp8_1x128_ue8m0(a):
+    """float32 rows [R, C] -> (E4M3 codes uint8 [R, C], float32 power-of-two scales [R, C/128]).
+
+    As quant_fp8_1x128, with the group's scale amax / 448 (float32, 1 for an
+    all-zero group) replaced by ue8m0_ceil of it; the division by a power of
+    two is exact, so each code is the once-rounded value of the element over
+    its scale.
+    """
+    a = np.asarray(a, dtype=np.float32)
+    R, C = a.shape
+    if C % QBLOCK:
+        raise ValueError("columns must be a multiple of 128")
+    g = a.reshape(R, C // QBLOCK, QBLOCK)
+    amax = np.max(np.abs(g), axis=-1) if R else np.zeros((0, C // QBLOCK), np.float32)
+    s = np.where(amax > 0, np.divide(amax, np.float32(FP8_MAX), dtype=np.float32), np.float32(1.0))
+    s = ue8m0_ceil(s.astype(np.float32))[0].astype(np.float32)
+    q = e4m3_encode_satfinite(np.divide(g, s[..., None], dtype=np.float32))
+    return q.reshape(R, C), s
+
+
+def requant_fp8_block_ue8m0(codes, scale):
+    """Stored FP8 block weights (codes uint8 [R, C], fp32 scale [R/128, C/128]) -> the same weights with
+    power-of-two block scales: (codes uint8 [R, C], float32 scales [R/128, C/128]).
+
+    Per block: s' = ue8m0_ceil(s); every code becomes the E4M3 rounding
+    (ties to even) of the exact value decode(q) * s / s', which lies within
+    +-448 because s / s' is in (1/2, 1].
+    """
+    codes = np.asarray(codes, dtype=np.uint8)
+    scale = np.asarray(scale, dtype=np.float32)
+    R, C = codes.shape
+    s2 = ue8m0_ceil(scale)[0]
+    ratio = scale.astype(np.float64) / s2                    # exact: a division by a power of two
+    v = _e4m3_table()[codes].reshape(R // QBLOCK, QBLOCK, C // QBLOCK, QBLOCK) * ratio[:, None, :, None]
+    return _e4m3_round_satfinite(v).reshape(R, C), s2.astype(np.float32)
 
 
 # ----------------------------------------------------------------------------
@@ -347,12 +422,14 @@ def fused_moe_fp8(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, exper
     act="a16" (the pages' weight-only scheme): activations keep their bf16
     values.  act="fp8_1x128": x is replaced by dequant(quant_fp8_1x128(x)), and
     the intermediate h of every (token, expert) pair, rounded to float32, by
-    dequant(quant_fp8_1x128(h)) before the down projection.
+    dequant(quant_fp8_1x128(h)) before the down projection.  act="fp8_ue8m0":
+    the same with every scale a power of two -- quant_fp8_1x128_ue8m0 for x and
+    h, and both weight tensors re-quantised by requant_fp8_block_ue8m0.
 
     `experts` restricts the loop to a subset (for sampling large layers);
     contributions of other experts are then left out.
     """
-    if act not in ("a16", "fp8_1x128"):
+    if act not in ("a16", "fp8_1x128", "fp8_ue8m0"):
         raise ValueError(act)
     return _naive_moe(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, "fp8", experts, act)
 
@@ -384,8 +461,9 @@ def _naive_moe(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, kind, ex
     Y = np.zeros(ids.shape + (H,), dtype=np.float64)  # Y[t, k] = expert output of slot (t, k)
     if kind == "int8":
         qx, sx = quant_int8_per_row(x)
-    a8 = kind == "fp8" and act == "fp8_1x128"
-    xa = dequant_fp8_1x128(*quant_fp8_1x128(x)) if a8 else x.astype(np.float64)
+    a8 = kind == "fp8" and act in ("fp8_1x128", "fp8_ue8m0")
+    quant_act = quant_fp8_1x128_ue8m0 if act == "fp8_ue8m0" else quant_fp8_1x128
+    xa = dequant_fp8_1x128(*quant_act(x)) if a8 else x.astype(np.float64)
     for e in (range(E) if experts is None else experts):
         tok, slot = np.nonzero(ids == e)  # the mask of this expert
         if tok.size == 0:
@@ -394,12 +472,15 @@ def _naive_moe(x, topk_ids, topk_weights, w13, w13_scale, w2, w2_scale, kind, ex
         q13, s13, q2, s2 = (_as_np(a[e]) for a in (w13, w13_scale, w2, w2_scale))
         if kind in ("fp8", "int4"):
             deq = dequant_fp8_block if kind == "fp8" else dequant_int4_group
+            if kind == "fp8" and act == "fp8_ue8m0":
+                q13, s13 = requant_fp8_block_ue8m0(q13, s13)
+                q2, s2 = requant_fp8_block_ue8m0(q2, s2)
             W13 = deq(q13, s13)                                    # [2I, H]
             W2 = deq(q2, s2)                                       # [H, I]
             C = xa[tok] @ W13.T                                    # A x [B1, B2] = [C1, C2]
             h = silu(C[:, :I]) * C[:, I:]                          # SiLU(C1) * C2
             if a8:
-                h = dequant_fp8_1x128(*quant_fp8_1x128(h.astype(np.float32)))
+                h = dequant_fp8_1x128(*quant_act(h.astype(np.float32)))
             y = h @ W2.T
         else:
             acc = qx[tok].astype(np.int64) @ q13.astype(np.int64).T

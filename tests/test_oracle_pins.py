@@ -461,6 +461,154 @@ def test_a8_layer_close_to_a16():
 
 
 # ----------------------------------------------------------------------------
+# Power-of-two (UE8M0) scales.  Pins: exhaustive search over exponents, the OCP
+# E8M0 code values, equality with the 1 x 128 quantiser wherever its scale is
+# already a power of two, torch's E4M3 cast of the exact quotients, and
+# hand-worked re-quantisations of stored weights (ties included).
+# ----------------------------------------------------------------------------
+
+
+def test_ue8m0_ceil_is_the_smallest_power_of_two_not_below():
+    rng = np.random.default_rng(31)
+    s = np.concatenate([np.exp2(rng.uniform(-135.0, 135.0, 400)), np.exp2(np.arange(-127.0, 128.0)),
+                        [1.0, np.nextafter(1.0, 2.0), np.nextafter(1.0, 0.0), 448.0 / 448.0, 3.0 / 448.0, 0.75]])
+    v, c = oracle.ue8m0_ceil(s)
+    assert v.dtype == np.float64 and c.dtype == np.uint8
+    for si, vi, ci in zip(s, v, c):
+        e = -127
+        while e < 127 and math.ldexp(1.0, e) < si:  # search upwards; the format stops at 2^127
+            e += 1
+        assert vi == math.ldexp(1.0, e) and int(ci) == e + 127, si
+    # OCP E8M0 codes: 127 is 1.0, 0 is 2^-127, 254 is 2^127
+    assert oracle.ue8m0_ceil([1.0, 2.0 ** -127, 2.0 ** 127])[1].tolist() == [127, 0, 254]
+    assert oracle.ue8m0_ceil([1.5])[0][0] == 2.0 and oracle.ue8m0_ceil([0.75])[0][0] == 1.0
+    for bad in (0.0, -1.0, np.inf, np.nan):
+        with pytest.raises(ValueError):
+            oracle.ue8m0_ceil([bad])
+
+
+def test_fp8_1x128_ue8m0_equals_the_1x128_quantiser_on_power_of_two_scales():
+    """Groups whose amax is 448 * 2^j have the scale 2^j already: both quantisers give the same codes and scales."""
+    rng = np.random.default_rng(32)
+    R, G = 5, 4
+    codes = rng.choice(_finite_e4m3_codes(), size=(R, G, 128)).astype(np.uint8)
+    codes[:, :, 7] = np.where(rng.random((R, G)) < 0.5, 0x7E, 0xFE)
+    j = rng.integers(-30, 31, size=(R, G))
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy() * np.exp2(j)[..., None]
+    a = vals.astype(np.float32).reshape(R, G * 128)
+    q8, s8 = oracle.quant_fp8_1x128(a)
+    qu, su = oracle.quant_fp8_1x128_ue8m0(a)
+    assert su.dtype == np.float32 and np.array_equal(su, s8) and np.array_equal(qu, q8)
+    assert np.array_equal(qu, codes.reshape(R, -1))
+
+
+def test_fp8_1x128_ue8m0_scales_and_torch_codes():
+    rng = np.random.default_rng(33)
+    R, G = 12, 5
+    a = (rng.standard_normal((R, G * 128)) * np.exp2(rng.integers(-12, 13, size=(R, 1)))).astype(np.float32)
+    a[4, 128:256] = 0.0                                   # an all-zero group: scale 1, codes 0
+    q, s = oracle.quant_fp8_1x128_ue8m0(a)
+    g = a.reshape(R, G, 128)
+    amax = np.abs(g).max(-1)
+    s32 = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    m, _ = np.frexp(s.astype(np.float64))
+    assert np.all(m == 0.5)                               # powers of two
+    assert np.all(s.astype(np.float64) / 2 < s32) and np.all(s32 <= s)
+    assert s[4, 1] == 1.0 and not q.reshape(R, G, 128)[4, 1].any()
+    # every code is torch's round-to-nearest-even E4M3 cast of the element over its (power-of-two) scale,
+    # a quotient that float32 holds exactly
+    quot = g.astype(np.float64) / s.astype(np.float64)[..., None]
+    assert np.array_equal(quot.astype(np.float32).astype(np.float64), quot)
+    want = torch.from_numpy(quot.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(q.reshape(R, G, 128), want)
+
+
+def test_requant_fp8_block_ue8m0_hand_worked():
+    codes = np.full((128, 256), 0x38, np.uint8)        # E4M3 1.0 everywhere
+    codes[0, 0] = 0x7E                                  # 448
+    codes[0, 1] = 0xB8                                  # -1.0
+    codes[2, 3], codes[2, 4], codes[2, 5] = 0x01, 0x02, 0x03   # subnormals 2^-9, 2^-8, 3 * 2^-9
+    codes[5, 130] = 0x01
+    scale = np.array([[0.75 * 2.0 ** -3, 2.0 ** -5]], np.float32)  # block 0: not a power of two; block 1: one
+    q, s = oracle.requant_fp8_block_ue8m0(codes, scale)
+    assert s.dtype == np.float32 and s.tolist() == [[2.0 ** -3, 2.0 ** -5]]
+    # block 0: every value times 0.75
+    assert q[1, 0] == 0x34                              # 1.0 -> 0.75 = 1.5 * 2^-1
+    assert q[0, 0] == 0x7A                              # 448 -> 336, halfway between 320 and 352 -> 320 (even)
+    assert q[0, 1] == 0xB4                              # -1.0 -> -0.75
+    assert q[2, 3] == 0x01                              # 0.75 * 2^-9 -> 2^-9 (nearest)
+    assert q[2, 4] == 0x02                              # 1.5 * 2^-9, halfway between 2^-9 and 2^-8 -> 2^-8 (even)
+    assert q[2, 5] == 0x02                              # 2.25 * 2^-9 -> 2^-8
+    # block 1 already has a power-of-two scale: its codes stay
+    assert np.array_equal(q[:, 128:], codes[:, 128:])
+
+
+def test_requant_fp8_block_ue8m0_error_bound():
+    rng = np.random.default_rng(34)
+    codes = rng.choice(_finite_e4m3_codes(), size=(256, 384)).astype(np.uint8)
+    scale = (np.exp2(rng.uniform(-20.0, 4.0, size=(2, 3)))).astype(np.float32)
+    scale[1, 2] = np.float32(2.0 ** -7)
+    q, s = oracle.requant_fp8_block_ue8m0(codes, scale)
+    before = oracle.dequant_fp8_block(codes, scale)
+    after = oracle.dequant_fp8_block(q, s)
+    sc = np.repeat(np.repeat(s.astype(np.float64), 128, 0), 128, 1)
+    err = np.abs(after - before)
+    normal = np.abs(before) >= 2.0 ** -6 * sc
+    assert np.all(err[normal] <= 2.0 ** -4 * np.abs(before)[normal])
+    assert np.all(err[~normal] <= 2.0 ** -10 * sc[~normal])
+    assert np.array_equal(q[128:, 256:], codes[128:, 256:])   # the power-of-two block
+
+
+def test_ue8m0_layer_top1_closed_form():
+    """Top-1 routing, weight 1: out = dequant(quant(h)) @ W2'^T with power-of-two scales throughout, h from the
+    re-quantised W13' and the power-of-two quantisation of x (W13', W2' re-quantised from the stored blocks)."""
+    shape = synth.LayerShape("ue", 5, 256, 256, 2, 1, "fp8", "softmax")
+    d = synth.make_layer(shape, seed=35)
+    rng = np.random.default_rng(35)
+    ids = torch.from_numpy(rng.integers(0, 2, size=(5, 1)).astype(np.int32))
+    out = oracle.fused_moe_fp8(d["x"], ids, torch.ones(5, 1), d["w13"], d["w13_scale"], d["w2"], d["w2_scale"],
+                               act="fp8_ue8m0")
+
+    def deq(a):
+        q, s = oracle.quant_fp8_1x128_ue8m0(np.asarray(a, np.float32))
+        v = torch.from_numpy(q).view(torch.float8_e4m3fn).double().numpy().reshape(len(q), -1, 128)
+        return (v * s.astype(np.float64)[..., None]).reshape(len(q), -1)
+
+    a = torch.from_numpy(deq(d["x"].float().numpy()))
+    for t in range(5):
+        e = int(ids[t, 0])
+        q13, s13 = oracle.requant_fp8_block_ue8m0(d["w13"][e].numpy(), d["w13_scale"][e].numpy())
+        q2, s2 = oracle.requant_fp8_block_ue8m0(d["w2"][e].numpy(), d["w2_scale"][e].numpy())
+        W13 = _torch_dequant_fp8(torch.from_numpy(q13), torch.from_numpy(s13))
+        W2 = _torch_dequant_fp8(torch.from_numpy(q2), torch.from_numpy(s2))
+        h = torch.nn.functional.silu(a[t:t + 1] @ W13[:256].T) * (a[t:t + 1] @ W13[256:].T)
+        want = torch.from_numpy(deq(h.numpy())) @ W2.T
+        np.testing.assert_allclose(out[t], want[0].numpy(), rtol=1e-10, atol=1e-12 * np.abs(want.numpy()).max())
+    # both weight tensors were really re-quantised (synthetic block scales are not powers of two), and the
+    # down projection is not the a8 one
+    for w, sc in (("w13", "w13_scale"), ("w2", "w2_scale")):
+        assert not np.array_equal(oracle.requant_fp8_block_ue8m0(d[w][0].numpy(), d[sc][0].numpy())[0], d[w][0].numpy())
+    a8 = oracle.fused_moe_fp8(d["x"], ids, torch.ones(5, 1), d["w13"], d["w13_scale"], d["w2"], d["w2_scale"],
+                              act="fp8_1x128")
+    assert np.abs(out - a8).max() > 0
+
+
+def test_ue8m0_layer_close_to_a8_and_a16():
+    shape = synth.LayerShape("ue", 24, 512, 256, 8, 3, "fp8", "softmax")
+    d = synth.make_layer(shape, seed=24)
+    a16 = oracle.fused_moe_fp8(**d)
+    a8 = oracle.fused_moe_fp8(**d, act="fp8_1x128")
+    ue = oracle.fused_moe_fp8(**d, act="fp8_ue8m0")
+    rel = lambda u, v: np.linalg.norm(u - v) / np.linalg.norm(v)  # noqa: E731
+    assert 1e-3 < rel(ue, a16) < 8e-2 and 1e-3 < rel(ue, a8) < 8e-2
+    # power-of-two scales leave up to a factor 2 of each group's range unused: never a smaller error than A8
+    # by much, on average a larger one
+    assert rel(ue, a16) > 0.8 * rel(a8, a16)
+    sub = oracle.fused_moe_rows(**d, kind="fp8", tokens=[0, 23], act="fp8_ue8m0")
+    np.testing.assert_allclose(sub, ue[[0, 23]], rtol=1e-11, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------
 # Gating.  Pins: the selection against exhaustive search over expert subsets on
 # integer-valued logits (exact sums, planted ties), torch.topk on tie-free
 # inputs, closed forms of the weights, and the group rule checked as an
