@@ -1,7 +1,8 @@
 """CPU oracle of the fused MoE layer -- test infrastructure only.
 
-Imported by the tests, by the package smoke check and by the CPU-baseline
-leg of the benchmark; never by the product path.  See moe_oracle.py.
+Imported by the tests, by the package smoke check, by the CPU-baseline leg
+of the benchmark and by the report script numerics_delta.py; never by the
+product path.  See moe_oracle.py.
 """
 from .moe_oracle import *  # noqa: F401,F403
 from .moe_oracle import (  # noqa: F401

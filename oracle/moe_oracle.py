@@ -1,8 +1,9 @@
 """CPU oracle for the fused MoE (sparse FFN) layer -- TEST INFRASTRUCTURE ONLY.
 
-Only the test suite, the package's smoke check and the CPU-baseline leg of
-the benchmark may import this module.  The product path (the CUDA library
-and its Python binding) never calls it and shares no code with it.
+Only the test suite, the package's smoke check, the CPU-baseline leg of the
+benchmark and the report script beside it (numerics_delta.py) may import this
+module.  The product path (the CUDA library and its Python binding) never
+calls it and shares no code with it.
 
 It is a plain, slow, obviously correct restatement of what the layer
 computes, in float64 numpy over dequantised weights:
