@@ -543,6 +543,16 @@ def test_requant_fp8_block_ue8m0_hand_worked():
     assert np.array_equal(q[:, 128:], codes[:, 128:])
 
 
+def test_requant_fp8_block_ue8m0_rounds_the_exact_product_once():
+    """1.5 * r with r the float32 just above 1.0625 / 1.5 lies just above the E4M3 midpoint 1.0625 (between 1.0
+    and 1.125), so it rounds to 1.125; its float32 product is 1.0625 exactly, which would tie to 1.0."""
+    r = np.nextafter(np.float32(1.0625 / 1.5), np.float32(1.0))
+    assert 1.5 * float(r) > 1.0625 and float(np.float32(1.5) * r) == 1.0625
+    codes = np.full((128, 128), 0x3C, np.uint8)                 # 1.5
+    q, s = oracle.requant_fp8_block_ue8m0(codes, np.array([[r * np.float32(0.125)]], np.float32))
+    assert s.tolist() == [[0.125]] and np.all(q == 0x39)        # 1.125
+
+
 def test_requant_fp8_block_ue8m0_error_bound():
     rng = np.random.default_rng(34)
     codes = rng.choice(_finite_e4m3_codes(), size=(256, 384)).astype(np.uint8)
